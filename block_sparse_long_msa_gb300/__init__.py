@@ -1,0 +1,196 @@
+"""MiniMax Sparse Attention (MSA) for GB300: Python binding of libmsa (include/msa.h).
+
+Argument marshalling only: every step of the operator runs in the CUDA kernels of libmsa.so.
+torch supplies device memory (outputs, workspace) and the current stream.  If the library has
+not been built, every call raises; there is no CPU fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libmsa.so")
+
+MSA_OK, MSA_ERR_INVALID_ARG, MSA_ERR_UNSUPPORTED, MSA_ERR_WORKSPACE = 0, 1, 2, 3
+MSA_ERR_CUDA, MSA_ERR_DEVICE_TIMEOUT, MSA_ERR_DEVICE_BOUNDS = 4, 5, 6
+WS_HEADER_BYTES = 256
+
+EXPORTS = ("msa_index_select_workspace", "msa_index_select", "msa_attn_prefill_workspace",
+           "msa_attn_prefill", "msa_attn_decode_workspace", "msa_attn_decode",
+           "msa_get_device_status", "msa_reset_device_status", "msa_status_string")
+
+
+class MsaConfig(ctypes.Structure):
+    _fields_ = [("num_groups", ctypes.c_int32), ("heads_per_group", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("index_dim", ctypes.c_int32),
+                ("block_size", ctypes.c_int32), ("topk", ctypes.c_int32),
+                ("softmax_scale", ctypes.c_float), ("reserved", ctypes.c_int32),
+                ("wait_limit_ns", ctypes.c_int64)]
+
+
+class MsaPagedKV(ctypes.Structure):
+    _fields_ = [("k_idx_pool", ctypes.c_void_p), ("k_pool", ctypes.c_void_p),
+                ("v_pool", ctypes.c_void_p), ("page_table", ctypes.c_void_p),
+                ("seq_lens", ctypes.c_void_p), ("batch", ctypes.c_int32),
+                ("max_pages", ctypes.c_int32), ("num_pages", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
+
+
+class MsaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libmsa.so; raises if it has not been built (no fallback exists)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libmsa.so is not built ({LIB_PATH}); run "
+                               "`python -m block_sparse_long_msa_gb300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        P, i64, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t
+        cfgp, pagedp = ctypes.POINTER(MsaConfig), ctypes.POINTER(MsaPagedKV)
+        L.msa_index_select_workspace.argtypes = [cfgp, i64, i64, pagedp]
+        L.msa_index_select_workspace.restype = sz
+        L.msa_index_select.argtypes = [cfgp, P, P, i64, pagedp, P, P, P, sz, P]
+        L.msa_attn_prefill_workspace.argtypes = [cfgp, i64]
+        L.msa_attn_prefill_workspace.restype = sz
+        L.msa_attn_prefill.argtypes = [cfgp, P, P, P, i64, P, P, P, P, sz, P]
+        L.msa_attn_decode_workspace.argtypes = [cfgp, pagedp]
+        L.msa_attn_decode_workspace.restype = sz
+        L.msa_attn_decode.argtypes = [cfgp, P, pagedp, P, P, P, P, sz, P]
+        L.msa_get_device_status.argtypes = [P, P]
+        L.msa_reset_device_status.argtypes = [P, P]
+        L.msa_status_string.argtypes = [ctypes.c_int]
+        L.msa_status_string.restype = ctypes.c_char_p
+        for name in ("msa_index_select", "msa_attn_prefill", "msa_attn_decode",
+                     "msa_get_device_status", "msa_reset_device_status"):
+            getattr(L, name).restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    try:
+        return lib().msa_status_string(status).decode()
+    except RuntimeError:
+        return f"status {status}"
+
+
+def config(num_groups: int, heads_per_group: int, topk: int, softmax_scale: float | None = None,
+           head_dim: int = 128, index_dim: int = 128, block_size: int = 128,
+           wait_limit_ns: int = 0) -> MsaConfig:
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(head_dim)
+    return MsaConfig(num_groups, heads_per_group, head_dim, index_dim, block_size, topk,
+                     softmax_scale, 0, wait_limit_ns)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(st: int, where: str):
+    if st != MSA_OK:
+        raise MsaError(st, where)
+
+
+def _workspace(nbytes: int, device, ws):
+    import torch
+    if ws is None:
+        ws = torch.zeros(max(nbytes, WS_HEADER_BYTES), dtype=torch.uint8, device=device)
+    if ws.numel() * ws.element_size() < nbytes:
+        raise MsaError(MSA_ERR_WORKSPACE, "workspace")
+    return ws
+
+
+def paged_kv(k_idx_pool, k_pool, v_pool, page_table, seq_lens) -> MsaPagedKV:
+    batch, max_pages = page_table.shape
+    return MsaPagedKV(k_idx_pool.data_ptr(), k_pool.data_ptr() if k_pool is not None else None,
+                      v_pool.data_ptr() if v_pool is not None else None, page_table.data_ptr(),
+                      seq_lens.data_ptr(), batch, max_pages, k_idx_pool.shape[0], 0)
+
+
+def msa_index_select_workspace(cfg: MsaConfig, num_queries: int, num_keys: int,
+                               paged: MsaPagedKV | None = None) -> int:
+    return int(lib().msa_index_select_workspace(ctypes.byref(cfg), num_queries, num_keys,
+                                                ctypes.byref(paged) if paged else None))
+
+
+def msa_index_select(cfg: MsaConfig, q_idx, k_idx=None, paged: MsaPagedKV | None = None,
+                     sel=None, sel_score=None, want_score: bool = False, ws=None, stream=None):
+    """Index branch.  Returns sel int32 [G][T][k] (and sel_score fp32 if asked)."""
+    import torch
+    T = q_idx.shape[0]
+    L = 0 if paged is not None else k_idx.shape[0]
+    G, k = cfg.num_groups, cfg.topk
+    if sel is None:
+        sel = torch.empty((G, T, k), dtype=torch.int32, device=q_idx.device)
+    if want_score and sel_score is None:
+        sel_score = torch.empty((G, T, k), dtype=torch.float32, device=q_idx.device)
+    ws = _workspace(msa_index_select_workspace(cfg, T, L, paged), q_idx.device, ws)
+    st = lib().msa_index_select(ctypes.byref(cfg), _ptr(q_idx), _ptr(k_idx), L,
+                                ctypes.byref(paged) if paged is not None else None, _ptr(sel),
+                                _ptr(sel_score), _ptr(ws), ws.numel(), _stream(stream))
+    _check(st, "msa_index_select")
+    return (sel, sel_score) if want_score else sel
+
+
+def msa_attn_prefill_workspace(cfg: MsaConfig, L: int) -> int:
+    return int(lib().msa_attn_prefill_workspace(ctypes.byref(cfg), L))
+
+
+def msa_attn_prefill(cfg: MsaConfig, q, k, v, sel, o=None, lse=None, ws=None, stream=None):
+    """Main branch, prefill.  Returns o bf16 [L][Hq][d] and lse fp32 [Hq][L]."""
+    import torch
+    L, Hq, d = q.shape
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((Hq, L), dtype=torch.float32, device=q.device)
+    ws = _workspace(msa_attn_prefill_workspace(cfg, L), q.device, ws)
+    st = lib().msa_attn_prefill(ctypes.byref(cfg), _ptr(q), _ptr(k), _ptr(v), L, _ptr(sel),
+                                _ptr(o), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream))
+    _check(st, "msa_attn_prefill")
+    return o, lse
+
+
+def msa_attn_decode_workspace(cfg: MsaConfig, paged: MsaPagedKV) -> int:
+    return int(lib().msa_attn_decode_workspace(ctypes.byref(cfg), ctypes.byref(paged)))
+
+
+def msa_attn_decode(cfg: MsaConfig, q, paged: MsaPagedKV, sel, o=None, lse=None, ws=None,
+                    stream=None):
+    """Main branch, paged decode.  Returns o bf16 [batch][Hq][d] and lse fp32 [Hq][batch]."""
+    import torch
+    batch, Hq, d = q.shape
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((Hq, batch), dtype=torch.float32, device=q.device)
+    ws = _workspace(msa_attn_decode_workspace(cfg, paged), q.device, ws)
+    st = lib().msa_attn_decode(ctypes.byref(cfg), _ptr(q), ctypes.byref(paged), _ptr(sel),
+                               _ptr(o), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream))
+    _check(st, "msa_attn_decode")
+    return o, lse
+
+
+def msa_get_device_status(ws, stream=None) -> int:
+    return int(lib().msa_get_device_status(_ptr(ws), _stream(stream)))
+
+
+def msa_reset_device_status(ws, stream=None) -> None:
+    _check(lib().msa_reset_device_status(_ptr(ws), _stream(stream)), "msa_reset_device_status")

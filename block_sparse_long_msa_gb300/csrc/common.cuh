@@ -1,0 +1,103 @@
+// Shared constants and small helpers of the MSA kernels.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "ptx.cuh"
+
+namespace msa {
+
+constexpr int kBlock = 128;     // B: tokens per block / page
+constexpr int kDim = 128;       // d = d_i
+constexpr int kTopMax = 16;     // largest k supported
+constexpr int kListMax = 15;    // non-local slots kept while scanning (k - 1 <= 15)
+
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;  // 2 s
+
+// (score desc, block asc): does (sa, ba) rank before (sb, bb)?
+__device__ __forceinline__ bool ranks_before(float sa, int32_t ba, float sb, int32_t bb) {
+  return sa > sb || (sa == sb && ba < bb);
+}
+
+// Register-resident top-kListMax list, kept sorted by rank.  Empty slots hold (-inf, INT_MAX).
+struct TopList {
+  float s[kListMax];
+  int32_t b[kListMax];
+
+  __device__ __forceinline__ void clear() {
+#pragma unroll
+    for (int p = 0; p < kListMax; ++p) {
+      s[p] = -__int_as_float(0x7f800000);
+      b[p] = 0x7fffffff;
+    }
+  }
+  // Insert (score, block) if it ranks before the current last entry.
+  __device__ __forceinline__ void insert(float score, int32_t block) {
+    if (!ranks_before(score, block, s[kListMax - 1], b[kListMax - 1])) return;
+    float cs = score;
+    int32_t cb = block;
+#pragma unroll
+    for (int p = 0; p < kListMax; ++p) {
+      if (ranks_before(cs, cb, s[p], b[p])) {
+        const float ts = s[p];
+        const int32_t tb = b[p];
+        s[p] = cs;
+        b[p] = cb;
+        cs = ts;
+        cb = tb;
+      }
+    }
+  }
+  // Keep the first `keep` entries (by rank), then sort them by ascending block id; entries past
+  // `keep` become (-inf, INT_MAX) and sort to the end.
+  __device__ __forceinline__ void truncate_and_sort_by_block(int keep) {
+#pragma unroll
+    for (int p = 0; p < kListMax; ++p)
+      if (p >= keep) {
+        s[p] = -__int_as_float(0x7f800000);
+        b[p] = 0x7fffffff;
+      }
+    // odd-even transposition sort on block id
+#pragma unroll
+    for (int round = 0; round < kListMax; ++round) {
+#pragma unroll
+      for (int p = (round & 1); p + 1 < kListMax; p += 2) {
+        if (b[p] > b[p + 1]) {
+          const float ts = s[p];
+          const int32_t tb = b[p];
+          s[p] = s[p + 1];
+          b[p] = b[p + 1];
+          s[p + 1] = ts;
+          b[p + 1] = tb;
+        }
+      }
+    }
+  }
+};
+
+// Write one selection row: the n non-local ids (ascending, in list.b[0..n)), then the local
+// block, then -1 padding up to k.  Scores: pooled score, +inf for local, -inf for padding.
+__device__ __forceinline__ void write_sel_row(const TopList& list, int n, int32_t local, int k,
+                                              int32_t* sel_row, float* score_row) {
+#pragma unroll
+  for (int r = 0; r < kTopMax; ++r) {
+    if (r >= k) break;
+    int32_t id;
+    float sc;
+    if (r < n) {
+      id = list.b[r < kListMax ? r : kListMax - 1];
+      sc = list.s[r < kListMax ? r : kListMax - 1];
+    } else if (r == n) {
+      id = local;
+      sc = __int_as_float(0x7f800000);
+    } else {
+      id = -1;
+      sc = -__int_as_float(0x7f800000);
+    }
+    sel_row[r] = id;
+    if (score_row) score_row[r] = sc;
+  }
+}
+
+}  // namespace msa

@@ -1,0 +1,184 @@
+// C ABI of libmsa (declared in include/msa.h): argument checks, workspace carving, tensor-map
+// encoding and kernel launches.  Nothing here allocates device memory or synchronizes, except
+// msa_get_device_status, which reads the status word back.
+#include <mutex>
+
+#include "../../include/msa.h"
+#include "common.cuh"
+#include "launch.h"
+
+namespace {
+
+using msa::kBlock;
+using msa::kDim;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// bf16 tensor map with 128-byte swizzle; dims/strides innermost first (strides in bytes, one
+// fewer than dims); box of 64 elements innermost.
+bool make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
+              const uint64_t* strides, const uint32_t* box) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t d[5], s[4];
+  cuuint32_t b[5], es[5];
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    b[i] = box[i];
+    es[i] = 1;
+  }
+  for (int i = 0; i + 1 < rank; ++i) s[i] = strides[i];
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), d, s, b, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+msa_status_t check_config(const msa_config_t* c) {
+  if (!c) return MSA_ERR_INVALID_ARG;
+  if (c->num_groups < 1 || c->heads_per_group < 1 || c->topk < 1 || c->reserved != 0 ||
+      c->wait_limit_ns < 0 || !(c->softmax_scale == c->softmax_scale))
+    return MSA_ERR_INVALID_ARG;
+  if (c->head_dim != kDim || c->index_dim != kDim || c->block_size != kBlock ||
+      c->topk > msa::kTopMax)
+    return MSA_ERR_UNSUPPORTED;
+  return MSA_OK;
+}
+
+uint64_t wait_ns(const msa_config_t* c) {
+  return c->wait_limit_ns > 0 ? static_cast<uint64_t>(c->wait_limit_ns) : msa::kDefaultWaitNs;
+}
+
+int32_t* status_word(void* ws) { return reinterpret_cast<int32_t*>(ws); }
+
+}  // namespace
+
+extern "C" {
+
+const char* msa_status_string(msa_status_t s) {
+  switch (s) {
+    case MSA_OK: return "ok";
+    case MSA_ERR_INVALID_ARG: return "invalid argument";
+    case MSA_ERR_UNSUPPORTED: return "unsupported size or configuration";
+    case MSA_ERR_WORKSPACE: return "workspace too small";
+    case MSA_ERR_CUDA: return "CUDA error";
+    case MSA_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    case MSA_ERR_DEVICE_BOUNDS: return "device index out of range";
+  }
+  return "unknown status";
+}
+
+msa_status_t msa_reset_device_status(void* ws, cudaStream_t stream) {
+  if (!ws) return MSA_ERR_INVALID_ARG;
+  return cudaMemsetAsync(ws, 0, sizeof(int32_t), stream) == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+}
+
+msa_status_t msa_get_device_status(const void* ws, cudaStream_t stream) {
+  if (!ws) return MSA_ERR_INVALID_ARG;
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, ws, sizeof v, cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess)
+    return MSA_ERR_CUDA;
+  if (v == 0) return MSA_OK;
+  if (v == MSA_ERR_DEVICE_TIMEOUT || v == MSA_ERR_DEVICE_BOUNDS) return static_cast<msa_status_t>(v);
+  return MSA_ERR_CUDA;
+}
+
+size_t msa_index_select_workspace(const msa_config_t* cfg, int64_t num_queries, int64_t num_keys,
+                                  const msa_paged_kv_t* paged) {
+  (void)num_keys;
+  if (check_config(cfg) != MSA_OK) return 0;
+  size_t bytes = MSA_WS_HEADER_BYTES;
+  if (paged) {
+    // pooled block scores [batch][G][max_pages] fp32
+    bytes += align_up(static_cast<size_t>(num_queries) * cfg->num_groups *
+                          static_cast<size_t>(paged->max_pages) * sizeof(float),
+                      256);
+  }
+  return bytes;
+}
+
+msa_status_t msa_index_select(const msa_config_t* cfg, const void* q_idx, const void* k_idx,
+                              int64_t L, const msa_paged_kv_t* paged, int32_t* sel,
+                              float* sel_score, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  msa_status_t st = check_config(cfg);
+  if (st != MSA_OK) return st;
+  if (!q_idx || !sel || !ws || !aligned16(q_idx)) return MSA_ERR_INVALID_ARG;
+  const int G = cfg->num_groups;
+  if (paged) return MSA_ERR_UNSUPPORTED;  // paged decode selection: not built yet
+  if (!k_idx || !aligned16(k_idx) || L < 0) return MSA_ERR_INVALID_ARG;
+  if (G != 1 && G != 2 && G != 4) return MSA_ERR_UNSUPPORTED;
+  if (L > (static_cast<int64_t>(1) << 31) - kBlock) return MSA_ERR_UNSUPPORTED;
+  if (ws_bytes < msa_index_select_workspace(cfg, L, L, nullptr)) return MSA_ERR_WORKSPACE;
+  if (L == 0) return MSA_OK;
+  CUtensorMap mq, mk;
+  {
+    const uint64_t dims[3] = {kDim, static_cast<uint64_t>(G), static_cast<uint64_t>(L)};
+    const uint64_t strides[2] = {kDim * 2, static_cast<uint64_t>(G) * kDim * 2};
+    const uint32_t box[3] = {64, 1, kBlock};
+    if (!make_map(&mq, q_idx, 3, dims, strides, box)) return MSA_ERR_CUDA;
+  }
+  {
+    const uint64_t dims[2] = {kDim, static_cast<uint64_t>(L)};
+    const uint64_t strides[1] = {kDim * 2};
+    const uint32_t box[2] = {64, kBlock};
+    if (!make_map(&mk, k_idx, 2, dims, strides, box)) return MSA_ERR_CUDA;
+  }
+  cudaError_t e = msa::launch_index_select_prefill(mq, mk, L, G, cfg->topk, sel, sel_score,
+                                                   status_word(ws), wait_ns(cfg), stream);
+  return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+}
+
+size_t msa_attn_prefill_workspace(const msa_config_t* cfg, int64_t L) {
+  (void)L;
+  if (check_config(cfg) != MSA_OK) return 0;
+  return MSA_WS_HEADER_BYTES;
+}
+
+msa_status_t msa_attn_prefill(const msa_config_t* cfg, const void* q, const void* k,
+                              const void* v, int64_t L, const int32_t* sel, void* o, float* lse,
+                              void* ws, size_t ws_bytes, cudaStream_t stream) {
+  (void)q; (void)k; (void)v; (void)L; (void)sel; (void)o; (void)lse; (void)ws; (void)ws_bytes;
+  (void)stream;
+  msa_status_t st = check_config(cfg);
+  if (st != MSA_OK) return st;
+  return MSA_ERR_UNSUPPORTED;
+}
+
+size_t msa_attn_decode_workspace(const msa_config_t* cfg, const msa_paged_kv_t* paged) {
+  (void)paged;
+  if (check_config(cfg) != MSA_OK) return 0;
+  return MSA_WS_HEADER_BYTES;
+}
+
+msa_status_t msa_attn_decode(const msa_config_t* cfg, const void* q, const msa_paged_kv_t* paged,
+                             const int32_t* sel, void* o, float* lse, void* ws, size_t ws_bytes,
+                             cudaStream_t stream) {
+  (void)q; (void)paged; (void)sel; (void)o; (void)lse; (void)ws; (void)ws_bytes; (void)stream;
+  msa_status_t st = check_config(cfg);
+  if (st != MSA_OK) return st;
+  return MSA_ERR_UNSUPPORTED;
+}
+
+}  // extern "C"

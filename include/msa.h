@@ -1,0 +1,147 @@
+/*
+ * msa.h — C ABI of libmsa, the MiniMax Sparse Attention (MSA) operator for GB300 (sm_103a).
+ *
+ * MSA is defined on the page "MiniMax M3 算力省 20 倍" (mizuki-eaf.pages.dev), section 二:
+ *   - Index Branch: each GQA group has one index-query head, all groups share one index-key head.
+ *     Index scores are raw query·key dot products over the causal window, max-pooled into
+ *     B-token block scores; every group picks its own top-k blocks; the query's own (local)
+ *     block is always picked (section 三 item 4: it keeps a reserved slot, so it counts in k).
+ *   - Main Branch: exact softmax attention over the tokens of the selected blocks only,
+ *     causal inside the local block.  Deployment: B = 128, k = 16 (2048 keys per query).
+ * Decode over a paged KV cache is named on the page "MiniMax M3 的采用瓶颈，会卡在 serving 生态"
+ * (paragraph on Together AI: paged MSA decode, KV-block-major sparse attention).
+ *
+ * Conventions for every call:
+ *   - All tensor pointers are DEVICE pointers, owned by the caller; the library never allocates
+ *     and never frees.  Tensors are dense, row-major, in the layouts stated per argument.
+ *   - bf16 means IEEE bfloat16 bits (uint16).  Pointers passed to TMA-fed kernels must be
+ *     16-byte aligned (q, k, v, q_idx, k_idx and the pools); violations return INVALID_ARG.
+ *   - Every call is asynchronous on `stream` and never synchronizes, except
+ *     msa_get_device_status.  Calls are stateless and thread-safe; concurrent calls must not
+ *     share a workspace.
+ *   - `ws` is caller-owned device scratch of at least the size the matching *_workspace()
+ *     query returns (never less than MSA_WS_HEADER_BYTES).  Its first MSA_WS_HEADER_BYTES hold a
+ *     device status word: zero it once before first use (msa_reset_device_status or a memset);
+ *     kernels record the first device-side error there (a bounded wait that ran out, an index
+ *     out of range) and it stays set until reset.  Device-side errors never trap: the kernel
+ *     skips the offending access and finishes.
+ *   - Host-side argument errors return before anything is enqueued.  Launch failures return
+ *     MSA_ERR_CUDA.
+ *   - v1 supports head_dim = index_dim = block_size = 128, 1 <= topk <= 16, num_groups <= 4 for
+ *     prefill index selection; other values return MSA_ERR_UNSUPPORTED.
+ */
+#ifndef MSA_H_
+#define MSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MSA_WS_HEADER_BYTES 256
+
+typedef enum {
+  MSA_OK = 0,
+  MSA_ERR_INVALID_ARG = 1,    /* null/misaligned pointer, bad size, inconsistent config */
+  MSA_ERR_UNSUPPORTED = 2,    /* a size this build does not implement */
+  MSA_ERR_WORKSPACE = 3,      /* ws_bytes smaller than the *_workspace() query */
+  MSA_ERR_CUDA = 4,           /* a CUDA runtime call or launch failed */
+  MSA_ERR_DEVICE_TIMEOUT = 5, /* device status: a bounded wait ran out */
+  MSA_ERR_DEVICE_BOUNDS = 6   /* device status: a page id or block id was out of range */
+} msa_status_t;
+
+typedef struct {
+  int32_t num_groups;      /* G: KV heads = GQA groups = index-query heads */
+  int32_t heads_per_group; /* query heads per group; Hq = G * heads_per_group */
+  int32_t head_dim;        /* d of q/k/v (128) */
+  int32_t index_dim;       /* d_i of the index query/key heads (128) */
+  int32_t block_size;      /* B (128) */
+  int32_t topk;            /* k, the local block included (1..16) */
+  float softmax_scale;     /* multiplies q.k in the main branch (1/sqrt(d) in the tests) */
+  int32_t reserved;        /* must be 0 */
+  int64_t wait_limit_ns;   /* bound on every device-side wait; 0 selects 2 seconds */
+} msa_config_t;
+
+/* A paged KV cache of B-token pages shared by `batch` sequences.  Logical block b of sequence s
+ * lives in physical page page_table[s*max_pages + b]. */
+typedef struct {
+  const void* k_idx_pool;    /* bf16 [num_pages][B][d_i]: index keys */
+  const void* k_pool;        /* bf16 [num_pages][G][B][d]: keys, head-major inside a page */
+  const void* v_pool;        /* bf16 [num_pages][G][B][d]: values, same layout */
+  const int32_t* page_table; /* int32 [batch][max_pages], device */
+  const int32_t* seq_lens;   /* int32 [batch], device: context length n >= 1 per sequence; the
+                                query is the token at n-1, already written to the cache */
+  int32_t batch;
+  int32_t max_pages;         /* row length of page_table; n <= max_pages * B is required */
+  int32_t num_pages;         /* pool size; page ids must lie in [0, num_pages) */
+  int32_t reserved;          /* must be 0 */
+} msa_paged_kv_t;
+
+/* Workspace bytes for msa_index_select: num_queries = L for prefill (paged == NULL), the batch
+ * for decode (paged != NULL, num_keys ignored). */
+size_t msa_index_select_workspace(const msa_config_t* cfg, int64_t num_queries, int64_t num_keys,
+                                  const msa_paged_kv_t* paged);
+
+/*
+ * Index branch: block scores, max-pooling, per-group top-k with the forced local block.
+ *   Prefill (paged == NULL): q_idx bf16 [L][G][d_i] (query i is the token at position i),
+ *     k_idx bf16 [L][d_i].  Output rows: T = L.
+ *   Decode (paged != NULL, k_idx and L ignored): q_idx bf16 [batch][G][d_i], one query per
+ *     sequence at position seq_lens[s]-1; index keys read from paged->k_idx_pool.  T = batch.
+ *   sel (out) int32 [G][T][k]: selected block ids, ascending, padded with -1 when fewer than k
+ *     blocks exist.  Ranking is by raw score (higher first), ties to the lower block id.
+ *   sel_score (out, optional, may be NULL) fp32 [G][T][k]: the pooled score of each selected
+ *     block; +inf for the local block (it is never scored), -inf for padding.
+ */
+msa_status_t msa_index_select(const msa_config_t* cfg, const void* q_idx, const void* k_idx,
+                              int64_t L, const msa_paged_kv_t* paged, int32_t* sel,
+                              float* sel_score, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Workspace bytes for msa_attn_prefill over L tokens. */
+size_t msa_attn_prefill_workspace(const msa_config_t* cfg, int64_t L);
+
+/*
+ * Main branch, prefill: exact softmax attention of every query head over the tokens of its
+ * group's selected blocks, causal inside the local block (KV-outer order with a two-phase
+ * log-sum-exp combine; results do not depend on scheduling).
+ *   q bf16 [L][Hq][d]; k, v bf16 [L][G][d]; sel int32 [G][L][k] as msa_index_select writes it.
+ *   o (out) bf16 [L][Hq][d]; lse (out) fp32 [Hq][L], natural log of the softmax denominator of
+ *   the scaled logits.  Ids in sel outside [0, block of the query] are skipped and flagged as
+ *   MSA_ERR_DEVICE_BOUNDS in the status word.
+ */
+msa_status_t msa_attn_prefill(const msa_config_t* cfg, const void* q, const void* k,
+                              const void* v, int64_t L, const int32_t* sel, void* o, float* lse,
+                              void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Workspace bytes for msa_attn_decode on this cache shape. */
+size_t msa_attn_decode_workspace(const msa_config_t* cfg, const msa_paged_kv_t* paged);
+
+/*
+ * Main branch, paged decode: one query token per sequence at position seq_lens[s]-1.
+ *   q bf16 [batch][Hq][d]; sel int32 [G][batch][k] (logical block ids, as msa_index_select
+ *   writes them).  o (out) bf16 [batch][Hq][d]; lse (out) fp32 [Hq][batch].
+ *   Page ids outside [0, num_pages) and block ids outside [0, block of the query] are skipped
+ *   and flagged as MSA_ERR_DEVICE_BOUNDS.
+ */
+msa_status_t msa_attn_decode(const msa_config_t* cfg, const void* q,
+                             const msa_paged_kv_t* paged, const int32_t* sel, void* o,
+                             float* lse, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Synchronizes `stream`, then returns the device status recorded in ws (MSA_OK if none). */
+msa_status_t msa_get_device_status(const void* ws, cudaStream_t stream);
+
+/* Enqueues a clear of the device status word in ws on `stream`. */
+msa_status_t msa_reset_device_status(void* ws, cudaStream_t stream);
+
+/* Static description of a status code. */
+const char* msa_status_string(msa_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MSA_H_ */

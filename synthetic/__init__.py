@@ -210,17 +210,18 @@ def _planted_index(w: Workload, q_int: torch.Tensor, k_int: torch.Tensor, device
             q_int[rows, g, :] = torch.clamp(q_int[rows, g, :] + 4 * s, -8, 8)
 
 
-def prefill_inputs(w: Workload, device="cpu", L: int | None = None) -> dict:
+def prefill_inputs(w: Workload, device="cpu", L: int | None = None,
+                   index_only: bool = False) -> dict:
     """q [L][Hq][d], k/v [L][G][d], q_idx [L][G][di], k_idx [L][di]; all bf16."""
     assert w.kind == "prefill"
     if L is not None:
         w = Workload(**{**w.__dict__, "L": L})
     L = w.L
-    out = {
-        "q": normal_bf16(w.seed, STREAM_Q, (L, w.Hq, w.d), device),
-        "k": normal_bf16(w.seed, STREAM_K, (L, w.G, w.d), device),
-        "v": normal_bf16(w.seed, STREAM_V, (L, w.G, w.d), device),
-    }
+    out = {}
+    if not index_only:
+        out["q"] = normal_bf16(w.seed, STREAM_Q, (L, w.Hq, w.d), device)
+        out["k"] = normal_bf16(w.seed, STREAM_K, (L, w.G, w.d), device)
+        out["v"] = normal_bf16(w.seed, STREAM_V, (L, w.G, w.d), device)
     if w.planted == "none":
         out["q_idx"] = int8th(w.seed, STREAM_QI, (L, w.G, w.di), device)
         out["k_idx"] = int8th(w.seed, STREAM_KI, (L, w.di), device)

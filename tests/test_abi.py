@@ -1,0 +1,71 @@
+"""The C-ABI library builds, loads and exports every entry point include/msa.h declares; host
+argument checks answer without touching a GPU."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from block_sparse_long_msa_gb300 import build
+    build.build()
+    import block_sparse_long_msa_gb300 as msa
+    return msa.lib()
+
+
+def _declared():
+    names = []
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if h.endswith(".h"):
+            txt = open(os.path.join(ROOT, "include", h)).read()
+            names += re.findall(r"^\s*(?:const\s+)?[\w\s\*]+?\b(msa_\w+)\s*\(", txt, re.M)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    declared = _declared()
+    assert len(declared) >= 9
+    out = subprocess.run(["nm", "-D", "--defined-only", lib._name], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT\s+(msa_\w+)", out))
+    missing = [n for n in declared if n not in exported]
+    assert not missing, missing
+    import block_sparse_long_msa_gb300 as msa
+    assert set(msa.EXPORTS) <= exported
+
+
+def test_status_strings(lib):
+    import block_sparse_long_msa_gb300 as msa
+    for s in range(7):
+        assert msa.status_string(s)
+    assert msa.status_string(0) == "ok"
+
+
+def test_host_argument_checks(lib):
+    import block_sparse_long_msa_gb300 as msa
+    cfg = msa.config(4, 16, 16)
+    # config errors return before any CUDA work
+    bad = msa.config(4, 16, 17)
+    assert lib.msa_index_select(ctypes.byref(bad), None, None, 0, None, None, None, None, 0,
+                                None) == msa.MSA_ERR_UNSUPPORTED
+    bad = msa.config(4, 16, 0)
+    assert lib.msa_index_select(ctypes.byref(bad), None, None, 0, None, None, None, None, 0,
+                                None) == msa.MSA_ERR_INVALID_ARG
+    bad = msa.config(4, 16, 16, head_dim=64)
+    assert lib.msa_attn_prefill(ctypes.byref(bad), None, None, None, 0, None, None, None, None,
+                                0, None) == msa.MSA_ERR_UNSUPPORTED
+    # null pointers
+    assert lib.msa_index_select(ctypes.byref(cfg), None, None, 16, None, None, None, None, 0,
+                                None) == msa.MSA_ERR_INVALID_ARG
+    # misaligned pointer (never dereferenced: the check happens first)
+    assert lib.msa_index_select(ctypes.byref(cfg), ctypes.c_void_p(0x1002),
+                                ctypes.c_void_p(0x2000), 16, None, ctypes.c_void_p(0x3000), None,
+                                ctypes.c_void_p(0x4000), 1 << 20, None) == msa.MSA_ERR_INVALID_ARG
+    # workspace queries are pure host arithmetic
+    assert msa.msa_index_select_workspace(cfg, 32768, 32768) >= msa.WS_HEADER_BYTES
+    assert lib.msa_index_select_workspace(ctypes.byref(bad), 1, 1, None) == 0

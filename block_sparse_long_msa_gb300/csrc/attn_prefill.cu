@@ -1,0 +1,748 @@
+// Main branch for prefill, KV-outer ("MiniMax M3 算力省 20 倍", section 四: the outer loop runs
+// over KV blocks; the queries that selected a block are gathered into 128-row tensor-core tiles;
+// hot blocks are pre-split along the query dimension over many CTAs; partial results are merged
+// by a two-phase combine without atomics).  Exactness per section 二: softmax over exactly the
+// selected tokens, causal inside the local block.
+//
+// Per query chunk [q0, q1) (chunks bound the partial-output workspace):
+//   1. sched_hist   per (group, query block): which tokens chose which block (bitmask in shared
+//                   memory), per-block counts -> hist[g][b][qb]
+//   2. sched_scan   per (group, block): exclusive prefix of hist over query blocks, list length
+//   3. sched_bases  one CTA: list offsets and work-item offsets over all (group, block)
+//   4. sched_items  per (group, block): work items of at most kItemTokens tokens
+//   5. sched_fill   per (group, query block): every (token, slot) lands at its place, lists stay
+//                   in ascending token order (deterministic, no global atomics)
+//   6. attn_kv_outer persistent tcgen05 kernel over work items (see below)
+//   7. combine      per (token, group): fixed slot order, LSE-weighted merge
+#include <algorithm>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace msa {
+
+namespace {
+
+constexpr int kTileTokens = 8;                            // 8 tokens x 16 heads = 128 MMA rows
+constexpr int kHeadsPerGroup = 16;
+constexpr int kItemTiles = 16;                            // tiles sharing one K/V staging
+constexpr int kItemTokens = kItemTiles * kTileTokens;     // 128
+constexpr uint32_t kPanel = 16384;
+
+// ------------------------------------------------------------------------------------------
+// Scheduling
+// ------------------------------------------------------------------------------------------
+struct SchedArgs {
+  const int32_t* sel;  // [G][L][k]
+  int64_t L;
+  int32_t G, k;
+  int32_t q0;          // first query of the chunk (multiple of 128)
+  int32_t nbq;         // query blocks in the chunk
+  int32_t nbk;         // key blocks referenced by the chunk (= last query block + 1)
+  int32_t* hist;       // [G][nbk][nbq]
+  int32_t* cnt;        // [G*nbk]
+  int32_t* list_base;  // [G*nbk]
+  int32_t* item_base;  // [G*nbk]
+  int32_t* n_items;    // [1]
+  int4* items;         // {g, b, start, count}
+  int32_t* list;       // (token << 4) | slot
+  int32_t* status;
+};
+
+// Shared-memory bitmask of the (up to 128) tokens of query block qb that selected block b.
+// Returns false (and flags the status word) for ids outside [0, qb].
+__device__ __forceinline__ void build_block_mask(const SchedArgs& a, int g, int qb,
+                                                 uint32_t* mask) {
+  const int t = threadIdx.x;
+  for (int w = t; w < (qb + 1) * 4; w += blockDim.x) mask[w] = 0;
+  __syncthreads();
+  const int64_t i = static_cast<int64_t>(qb) * kBlock + t;
+  if (t < kBlock && i < a.L) {
+    const int32_t* row = a.sel + (static_cast<size_t>(g) * a.L + i) * a.k;
+    for (int s = 0; s < a.k; ++s) {
+      const int32_t b = row[s];
+      if (b < 0) continue;
+      if (b > qb) {
+        report_status(a.status, kStatusBounds);
+        continue;
+      }
+      atomicOr(&mask[b * 4 + (t >> 5)], 1u << (t & 31));
+    }
+  }
+  __syncthreads();
+}
+
+__global__ void sched_hist_kernel(SchedArgs a) {
+  extern __shared__ uint32_t mask[];
+  const int qbl = blockIdx.x, g = blockIdx.y;
+  const int qb = a.q0 / kBlock + qbl;
+  build_block_mask(a, g, qb, mask);
+  for (int b = threadIdx.x; b <= qb; b += blockDim.x) {
+    const int c = __popc(mask[b * 4]) + __popc(mask[b * 4 + 1]) + __popc(mask[b * 4 + 2]) +
+                  __popc(mask[b * 4 + 3]);
+    a.hist[(static_cast<size_t>(g) * a.nbk + b) * a.nbq + qbl] = c;
+  }
+}
+
+// One warp per (group, block): exclusive prefix over the query blocks that can choose b.
+__global__ void sched_scan_kernel(SchedArgs a) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (warp >= a.G * a.nbk) return;
+  const int b = warp % a.nbk;
+  const int qb0 = a.q0 / kBlock;
+  int32_t* h = a.hist + static_cast<size_t>(warp) * a.nbq;
+  const int first = b > qb0 ? b - qb0 : 0;
+  int run = 0;
+  for (int base = first; base < a.nbq; base += 32) {
+    const int q = base + lane;
+    const int v = q < a.nbq ? h[q] : 0;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += n;
+    }
+    if (q < a.nbq) h[q] = run + incl - v;
+    run += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  if (lane == 0) a.cnt[warp] = run;
+}
+
+__device__ __forceinline__ int items_of(int c) {
+  return (c + kItemTokens - 1) / kItemTokens;
+}
+
+// One CTA: exclusive scans of the list lengths and the item counts over all (group, block).
+__global__ void __launch_bounds__(1024) sched_bases_kernel(SchedArgs a) {
+  __shared__ int32_t warp_sums[2][32];
+  __shared__ int32_t carry[2];
+  const int n = a.G * a.nbk, t = threadIdx.x, lane = t & 31, w = t >> 5;
+  if (t == 0) carry[0] = carry[1] = 0;
+  __syncthreads();
+  for (int base = 0; base < n; base += 1024) {
+    const int idx = base + t;
+    const int c = idx < n ? a.cnt[idx] : 0;
+    int v[2] = {c, items_of(c)};
+    int incl[2] = {v[0], v[1]};
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int x = __shfl_up_sync(0xffffffffu, incl[q], o);
+        if (lane >= o) incl[q] += x;
+      }
+    }
+    if (lane == 31) {
+      warp_sums[0][w] = incl[0];
+      warp_sums[1][w] = incl[1];
+    }
+    __syncthreads();
+    if (w == 0) {
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int s = warp_sums[q][lane];
+        int x = s;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, x, o);
+          if (lane >= o) x += y;
+        }
+        warp_sums[q][lane] = x - s;  // exclusive over warps
+      }
+    }
+    __syncthreads();
+    if (idx < n) {
+      a.list_base[idx] = carry[0] + warp_sums[0][w] + incl[0] - v[0];
+      a.item_base[idx] = carry[1] + warp_sums[1][w] + incl[1] - v[1];
+    }
+    __syncthreads();
+    if (t == 1023) {
+      carry[0] += warp_sums[0][w] + incl[0];
+      carry[1] += warp_sums[1][w] + incl[1];
+    }
+    __syncthreads();
+  }
+  if (t == 0) *a.n_items = carry[1];
+}
+
+__global__ void sched_items_kernel(SchedArgs a) {
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= a.G * a.nbk) return;
+  const int g = idx / a.nbk, b = idx % a.nbk;
+  const int c = a.cnt[idx], base = a.list_base[idx], ib = a.item_base[idx];
+  for (int q = 0; q * kItemTokens < c; ++q)
+    a.items[ib + q] = make_int4(g, b, base + q * kItemTokens, min(kItemTokens, c - q * kItemTokens));
+}
+
+__global__ void sched_fill_kernel(SchedArgs a) {
+  extern __shared__ uint32_t mask[];
+  const int qbl = blockIdx.x, g = blockIdx.y;
+  const int qb = a.q0 / kBlock + qbl;
+  build_block_mask(a, g, qb, mask);
+  const int t = threadIdx.x;
+  const int64_t i = static_cast<int64_t>(qb) * kBlock + t;
+  if (t >= kBlock || i >= a.L) return;
+  const int32_t* row = a.sel + (static_cast<size_t>(g) * a.L + i) * a.k;
+  const int w = t >> 5;
+  const uint32_t below = (1u << (t & 31)) - 1u;
+  for (int s = 0; s < a.k; ++s) {
+    const int32_t b = row[s];
+    if (b < 0 || b > qb) continue;
+    int rank = __popc(mask[b * 4 + w] & below);
+    for (int q = 0; q < w; ++q) rank += __popc(mask[b * 4 + q]);
+    const int gb = g * a.nbk + b;
+    const int pos = a.list_base[gb] + a.hist[static_cast<size_t>(gb) * a.nbq + qbl] + rank;
+    a.list[pos] = static_cast<int32_t>((i << 4) | s);
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// KV-outer attention.  One persistent CTA per SM walks the work items; per item it stages
+// K_b and V_b of group g (TMA, double-buffered across items), then for every tile of 8 tokens
+// gathers their 16 query heads (TMA, 16 rows per token) and runs
+//   S = Q K^T (tcgen05, fp32 in TMEM) -> softmax rows (causal limit only in the local block)
+//   -> P (bf16, shared memory) -> O = P V (tcgen05, TMEM) -> unnormalised partial O (bf16) +
+//   row max m and log-sum-exp per (token, head, slot).
+// Roles: warp 0 TMA producer, warp 1 TMEM owner + MMA issuer, warps 4-7 softmax, 8-11 epilogue.
+// ------------------------------------------------------------------------------------------
+struct AttnArgs {
+  const int4* items;
+  const int32_t* n_items;
+  const int32_t* list;
+  int32_t G, k, q0;
+  float scale_log2;       // softmax scale * log2(e)
+  __half* po;             // [(il*G + g)*k + s][16][128] unnormalised partial O (fp16)
+  float* pm;              // [(il*G + g)*k + s][16] row max (natural-log units)
+  float* plse;            // same, log-sum-exp
+  int32_t* status;
+  uint64_t wait_ns;
+};
+
+constexpr uint32_t kSmemKV = 0;             // 2 x (K 32 KB + V 32 KB)
+constexpr uint32_t kSmemQ = 131072;         // 2 x 32 KB
+constexpr uint32_t kSmemP = 196608;         // 32 KB
+constexpr uint32_t kSmemBar = 229376;
+constexpr uint32_t kAttnSmem = kSmemBar + 256 + 1024;
+constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, false, false);
+constexpr uint32_t kIdescPV = idesc_f16_f32(128, 128, false, true);  // P, V in fp16
+
+__global__ void __launch_bounds__(384, 1)
+    attn_kv_outer_kernel(const __grid_constant__ CUtensorMap map_q,
+                         const __grid_constant__ CUtensorMap map_k,
+                         const __grid_constant__ CUtensorMap map_v, AttnArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t base = smem_u32(smem);
+  const uint32_t bars = base + kSmemBar;
+  auto kv_full = [&](int s) { return bars + 8 * s; };
+  auto kv_empty = [&](int s) { return bars + 16 + 8 * s; };
+  auto q_full = [&](int s) { return bars + 32 + 8 * s; };
+  auto q_empty = [&](int s) { return bars + 48 + 8 * s; };
+  auto s_full = [&](int s) { return bars + 64 + 8 * s; };
+  auto s_empty = [&](int s) { return bars + 80 + 8 * s; };
+  const uint32_t p_full = bars + 96, p_empty = bars + 104;
+  auto o_full = [&](int s) { return bars + 112 + 8 * s; };
+  auto o_empty = [&](int s) { return bars + 128 + 8 * s; };
+  const uint32_t drain_bar = bars + 144;
+  auto v_ready = [&](int s) { return bars + 152 + 8 * s; };
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + kSmemBar + 168);
+  volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + kSmemBar + 172);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_items = *a.n_items;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(kv_full(s), 1);
+      mbar_init(kv_empty(s), 1);
+      mbar_init(q_full(s), 1);
+      mbar_init(q_empty(s), 1);
+      mbar_init(s_full(s), 1);
+      mbar_init(s_empty(s), 128);
+      mbar_init(o_full(s), 1);
+      mbar_init(o_empty(s), 128);
+      mbar_init(v_ready(s), 64);
+    }
+    mbar_init(p_full, 128);
+    mbar_init(p_empty, 1);
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;  // columns [0,256): S slots, [256,512): O slots
+
+  if (warp == 0) {
+    // ------------------------------- producer -------------------------------
+    if (lane == 0) {
+      tma_prefetch_map(&map_q);
+      tma_prefetch_map(&map_k);
+      tma_prefetch_map(&map_v);
+      int T = 0, nit = 0;
+      int kv_issued = 0, q_issued = 0;
+      bool ok = true;
+      for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x, ++nit) {
+        const int4 item = a.items[it];
+        const int g = item.x, b = item.y, start = item.z, count = item.w;
+        const int kvs = nit & 1;
+        if (*abort_flag || !mbar_wait(kv_empty(kvs), ((nit >> 1) & 1) ^ 1, a.wait_ns)) {
+          ok = false;
+          break;
+        }
+        const uint32_t kb = base + kSmemKV + kvs * 65536u;
+        mbar_arrive_expect_tx(kv_full(kvs), 65536);
+        tma_load_3d(kb, &map_k, kv_full(kvs), 0, g, b * kBlock);
+        tma_load_3d(kb + kPanel, &map_k, kv_full(kvs), 64, g, b * kBlock);
+        tma_load_3d(kb + 32768, &map_v, kv_full(kvs), 0, g, b * kBlock);
+        tma_load_3d(kb + 32768 + kPanel, &map_v, kv_full(kvs), 64, g, b * kBlock);
+        ++kv_issued;
+        for (int t0 = 0; t0 < count; t0 += kTileTokens, ++T) {
+          const int qs = T & 1;
+          if (*abort_flag || !mbar_wait(q_empty(qs), ((T >> 1) & 1) ^ 1, a.wait_ns)) {
+            ok = false;
+            break;
+          }
+          const int n = min(kTileTokens, count - t0);
+          const uint32_t qb = base + kSmemQ + qs * 32768u;
+          mbar_arrive_expect_tx(q_full(qs), n * 4096);
+          for (int tk = 0; tk < n; ++tk) {
+            const int32_t e = a.list[start + t0 + tk];
+            const int i = e >> 4;
+            tma_load_3d(qb + tk * 2048, &map_q, q_full(qs), 0, g * kHeadsPerGroup, i);
+            tma_load_3d(qb + kPanel + tk * 2048, &map_q, q_full(qs), 64, g * kHeadsPerGroup, i);
+          }
+          ++q_issued;
+        }
+      }
+      if (!ok) {
+        report_status(a.status, kStatusTimeout);
+        *abort_flag = 1;
+        // let in-flight copies land before the CTA can exit (at most one per stage)
+        for (int x = (kv_issued > 2 ? kv_issued - 2 : 0); x < kv_issued; ++x)
+          mbar_wait(kv_full(x & 1), (x >> 1) & 1, a.wait_ns);
+        for (int x = (q_issued > 2 ? q_issued - 2 : 0); x < q_issued; ++x)
+          mbar_wait(q_full(x & 1), (x >> 1) & 1, a.wait_ns);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------- MMA issuer -------------------------------
+    if (lane == 0) {
+      bool ok = true;
+      int T = 0, nit = 0;
+      int pend_T = -1, pend_kvs = 0, pend_nit = 0;
+      bool pend_last = false, pend_first = false;
+      auto issue_pv = [&](int Tp, int kvs, int nitp, bool first_of_item,
+                          bool last_of_item) -> bool {
+        // V of this stage has been converted to fp16 in place before its first use
+        if (first_of_item && !mbar_wait(v_ready(kvs), (nitp >> 1) & 1, a.wait_ns)) return false;
+        if (!mbar_wait(p_full, Tp & 1, a.wait_ns)) return false;
+        if (!mbar_wait(o_empty(Tp & 1), ((Tp >> 1) & 1) ^ 1, a.wait_ns)) return false;
+        tc_fence_after();
+        const uint32_t d = tmem + 256 + (Tp & 1) * 128;
+        const uint32_t vb = base + kSmemKV + kvs * 65536u + 32768;
+        const uint32_t pb = base + kSmemP;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t ad = sdesc_sw128(pb + (kk >> 2) * kPanel + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw128(vb + kk * 2048, kPanel, 1024);
+          mma_bf16_ss(d, ad, bd, kIdescPV, kk > 0);
+        }
+        mma_commit(o_full(Tp & 1));
+        mma_commit(p_empty);
+        if (last_of_item) mma_commit(kv_empty(kvs));
+        return true;
+      };
+      for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x, ++nit) {
+        const int count = a.items[it].w;
+        const int kvs = nit & 1;
+        if (*abort_flag || !mbar_wait(kv_full(kvs), (nit >> 1) & 1, a.wait_ns)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t kb = base + kSmemKV + kvs * 65536u;
+        for (int t0 = 0; t0 < count; t0 += kTileTokens, ++T) {
+          const int qs = T & 1;
+          if (*abort_flag || !mbar_wait(q_full(qs), (T >> 1) & 1, a.wait_ns) ||
+              !mbar_wait(s_empty(T & 1), ((T >> 1) & 1) ^ 1, a.wait_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d = tmem + (T & 1) * 128;
+          const uint32_t qb = base + kSmemQ + qs * 32768u;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 32;
+            mma_bf16_ss(d, sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
+                        kIdescQK, kk > 0);
+          }
+          mma_commit(s_full(T & 1));
+          mma_commit(q_empty(qs));
+          // PV of the previous tile overlaps the softmax of this one
+          if (pend_T >= 0 && !issue_pv(pend_T, pend_kvs, pend_nit, pend_first, pend_last)) {
+            ok = false;
+            break;
+          }
+          pend_T = T;
+          pend_kvs = kvs;
+          pend_nit = nit;
+          pend_first = (t0 == 0);
+          pend_last = (t0 + kTileTokens >= count);
+        }
+      }
+      if (ok && pend_T >= 0) ok = issue_pv(pend_T, pend_kvs, pend_nit, pend_first, pend_last);
+      if (!ok) {
+        report_status(a.status, kStatusTimeout);
+        *abort_flag = 1;
+      }
+      mma_commit(drain_bar);
+      mbar_wait(drain_bar, 0, a.wait_ns);
+    }
+  } else if (warp == 2 || warp == 3) {
+    // ------------------------- V converter: bf16 -> fp16 in place -------------------------
+    // Exact for N(0,1)-range values (bf16 carries 8 significant bits, fp16 11); lets P be
+    // rounded to fp16 instead of bf16 for the P.V product.
+    const int t = (warp - 2) * 32 + lane;
+    int nit = 0;
+    bool ok = true;
+    for (int it = blockIdx.x; it < n_items; it += gridDim.x, ++nit) {
+      const int kvs = nit & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(kv_full(kvs), (nit >> 1) & 1, a.wait_ns))) {
+        ok = false;
+        break;
+      }
+      const uint32_t vb = base + kSmemKV + kvs * 65536u + 32768;
+#pragma unroll 4
+      for (int c = t; c < 2048; c += 64) {
+        uint4 x = ld_shared_v4(vb + c * 16);
+        x.x = bf16x2_to_f16x2(x.x);
+        x.y = bf16x2_to_f16x2(x.y);
+        x.z = bf16x2_to_f16x2(x.z);
+        x.w = bf16x2_to_f16x2(x.w);
+        st_shared_v4(vb + c * 16, x.x, x.y, x.z, x.w);
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(v_ready(kvs));
+    }
+    if (!ok) {
+      report_status(a.status, kStatusTimeout);
+      *abort_flag = 1;
+    }
+  } else if (warp >= 4 && warp < 8) {
+    // ------------------------------- softmax -------------------------------
+    const int row = (warp - 4) * 32 + lane;  // TMEM lane = MMA row
+    const int tk = row >> 4, hh = row & 15;
+    const uint32_t lane_base = static_cast<uint32_t>((warp - 4) * 32) << 16;
+    const uint32_t pb = base + kSmemP;
+    int T = 0;
+    bool ok = true;
+    for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
+      const int4 item = a.items[it];
+      const int g = item.x, b = item.y, start = item.z, count = item.w;
+      for (int t0 = 0; t0 < count; t0 += kTileTokens, ++T) {
+        const int slot = T & 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(s_full(slot), (T >> 1) & 1, a.wait_ns))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const bool valid = t0 + tk < count;
+        int i = 0, s = 0;
+        if (valid) {
+          const int32_t e = a.list[start + t0 + tk];
+          i = e >> 4;
+          s = e & 15;
+        }
+        const int lim = valid ? min(i - b * kBlock, kBlock - 1) : kBlock - 1;
+        const uint32_t sa = tmem + lane_base + slot * 128;
+        // pass 1: row max of the scaled logits (log2 units)
+        float m2 = -__int_as_float(0x7f800000);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          tmem_ld32(sa + c * 32, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int q = 0; q < 32; ++q)
+            if (c * 32 + q <= lim) m2 = fmaxf(m2, __uint_as_float(v[q]) * a.scale_log2);
+        }
+        // the P buffer is free once the previous tile's PV has finished
+        if (T > 0 && !__all_sync(0xffffffffu, mbar_wait(p_empty, (T - 1) & 1, a.wait_ns))) {
+          ok = false;
+          break;
+        }
+        // pass 2: p = exp2(t - m2), row sum, bf16 P row into the swizzled operand tile
+        float l = 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          tmem_ld32(sa + c * 32, v);
+          tmem_ld_wait();
+          uint32_t pk[16];
+#pragma unroll
+          for (int q = 0; q < 32; q += 2) {
+            const float p0 = (c * 32 + q <= lim)
+                                 ? exp2f(__uint_as_float(v[q]) * a.scale_log2 - m2) : 0.f;
+            const float p1 = (c * 32 + q + 1 <= lim)
+                                 ? exp2f(__uint_as_float(v[q + 1]) * a.scale_log2 - m2) : 0.f;
+            l += p0 + p1;
+            pk[q >> 1] = pack_f16x2(p0, p1);
+          }
+          if (valid) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              st_shared_v4(pb + sw128_offset(row, c * 32 + u * 8, 128), pk[4 * u], pk[4 * u + 1],
+                           pk[4 * u + 2], pk[4 * u + 3]);
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(s_empty(slot));
+        fence_proxy_async_smem();
+        mbar_arrive(p_full);
+        if (valid) {
+          const size_t u = (static_cast<size_t>(i - a.q0) * a.G + g) * a.k + s;
+          const float ln2 = 0.6931471805599453f;
+          a.pm[u * kHeadsPerGroup + hh] = m2 * ln2;
+          a.plse[u * kHeadsPerGroup + hh] = (m2 + __log2f(l)) * ln2;
+        }
+      }
+    }
+    if (!ok) {
+      report_status(a.status, kStatusTimeout);
+      *abort_flag = 1;
+    }
+  } else if (warp >= 8) {
+    // ------------------------------- epilogue -------------------------------
+    const int row = (warp - 8) * 32 + lane;
+    const int tk = row >> 4, hh = row & 15;
+    const uint32_t lane_base = static_cast<uint32_t>((warp - 8) * 32) << 16;
+    int T = 0;
+    bool ok = true;
+    for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
+      const int4 item = a.items[it];
+      const int g = item.x, start = item.z, count = item.w;
+      for (int t0 = 0; t0 < count; t0 += kTileTokens, ++T) {
+        const int slot = T & 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(o_full(slot), (T >> 1) & 1, a.wait_ns))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const bool valid = t0 + tk < count;
+        __half* dst = nullptr;
+        if (valid) {
+          const int32_t e = a.list[start + t0 + tk];
+          const int i = e >> 4, s = e & 15;
+          const size_t u = (static_cast<size_t>(i - a.q0) * a.G + g) * a.k + s;
+          dst = a.po + (u * kHeadsPerGroup + hh) * kDim;
+        }
+        const uint32_t oa = tmem + lane_base + 256 + slot * 128;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          tmem_ld32(oa + c * 32, v);
+          tmem_ld_wait();
+          if (valid) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+            for (int u4 = 0; u4 < 4; ++u4) {
+              uint4 w;
+              w.x = pack_f16x2(__uint_as_float(v[8 * u4 + 0]), __uint_as_float(v[8 * u4 + 1]));
+              w.y = pack_f16x2(__uint_as_float(v[8 * u4 + 2]), __uint_as_float(v[8 * u4 + 3]));
+              w.z = pack_f16x2(__uint_as_float(v[8 * u4 + 4]), __uint_as_float(v[8 * u4 + 5]));
+              w.w = pack_f16x2(__uint_as_float(v[8 * u4 + 6]), __uint_as_float(v[8 * u4 + 7]));
+              d4[u4] = w;
+            }
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(o_empty(slot));
+      }
+    }
+    if (!ok) {
+      report_status(a.status, kStatusTimeout);
+      *abort_flag = 1;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// Combine: per (token, group), 128 threads; thread t covers head t/8, dims (t%8)*16 .. +16.
+//   M = max_s lse_s, den = sum_s exp(lse_s - M), o = sum_s exp(m_s - M) * O~_s / den,
+//   lse = M + ln(den).  Slots in fixed ascending order; padding (-1) skipped.
+// ------------------------------------------------------------------------------------------
+struct CombineArgs {
+  const int32_t* sel;          // [G][L][k]
+  const __half* po;
+  const float* pm;
+  const float* plse;
+  int64_t L;                   // rows of sel / o / lse
+  int32_t G, k, q0, nrows;     // rows q0 .. q0+nrows-1
+  __nv_bfloat16* o;            // [L][G*16][128]
+  float* lse;                  // [G*16][L]
+};
+
+__global__ void __launch_bounds__(128) combine_kernel(CombineArgs a) {
+  const int il = blockIdx.x, g = blockIdx.y;
+  const int64_t i = static_cast<int64_t>(a.q0) + il;
+  const int t = threadIdx.x, hh = t >> 3, d0 = (t & 7) * 16;
+  const int32_t* srow = a.sel + (static_cast<size_t>(g) * a.L + i) * a.k;
+  const size_t u0 = (static_cast<size_t>(il) * a.G + g) * a.k;
+  const int32_t bi = static_cast<int32_t>(i / kBlock);
+  float M = -__int_as_float(0x7f800000);
+  for (int s = 0; s < a.k; ++s)
+    if (srow[s] >= 0 && srow[s] <= bi) M = fmaxf(M, a.plse[(u0 + s) * kHeadsPerGroup + hh]);
+  float acc[16];
+#pragma unroll
+  for (int q = 0; q < 16; ++q) acc[q] = 0.f;
+  float den = 0.f;
+  for (int s = 0; s < a.k; ++s) {
+    if (srow[s] < 0 || srow[s] > bi) continue;  // padding; out-of-range ids were flagged
+    const size_t r = (u0 + s) * kHeadsPerGroup + hh;
+    den += __expf(a.plse[r] - M);
+    const float w = __expf(a.pm[r] - M);
+    const uint4* src = reinterpret_cast<const uint4*>(a.po + r * kDim + d0);
+#pragma unroll
+    for (int h2 = 0; h2 < 2; ++h2) {
+      const uint4 x = src[h2];
+      const uint32_t wd[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&wd[q]));
+        acc[h2 * 8 + 2 * q] += w * f.x;
+        acc[h2 * 8 + 2 * q + 1] += w * f.y;
+      }
+    }
+  }
+  const float inv = 1.f / den;
+  const int h = g * kHeadsPerGroup + hh;
+  uint4* dst = reinterpret_cast<uint4*>(a.o + (static_cast<size_t>(i) * a.G * kHeadsPerGroup + h) * kDim + d0);
+#pragma unroll
+  for (int h2 = 0; h2 < 2; ++h2) {
+    uint4 w;
+    w.x = pack_bf16x2(acc[h2 * 8 + 0] * inv, acc[h2 * 8 + 1] * inv);
+    w.y = pack_bf16x2(acc[h2 * 8 + 2] * inv, acc[h2 * 8 + 3] * inv);
+    w.z = pack_bf16x2(acc[h2 * 8 + 4] * inv, acc[h2 * 8 + 5] * inv);
+    w.w = pack_bf16x2(acc[h2 * 8 + 6] * inv, acc[h2 * 8 + 7] * inv);
+    dst[h2] = w;
+  }
+  if ((t & 7) == 0) a.lse[static_cast<size_t>(h) * a.L + i] = M + __logf(den);
+}
+
+}  // namespace
+
+PrefillWorkspace prefill_workspace_layout(int64_t L, int G, int k, int64_t chunk) {
+  PrefillWorkspace w{};
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  const int64_t nbk = (L + kBlock - 1) / kBlock;
+  const int64_t nbq = (chunk + kBlock - 1) / kBlock;
+  const int64_t units = chunk * G * k;
+  const int64_t max_items = G * nbk + (units + kItemTokens - 1) / kItemTokens;
+  size_t off = 256;  // status header
+  w.hist = off;      off += up(sizeof(int32_t) * G * nbk * nbq);
+  w.cnt = off;       off += up(sizeof(int32_t) * G * nbk);
+  w.list_base = off; off += up(sizeof(int32_t) * G * nbk);
+  w.item_base = off; off += up(sizeof(int32_t) * G * nbk);
+  w.n_items = off;   off += 256;
+  w.items = off;     off += up(sizeof(int4) * max_items);
+  w.list = off;      off += up(sizeof(int32_t) * units);
+  w.pm = off;        off += up(sizeof(float) * units * kHeadsPerGroup);
+  w.plse = off;      off += up(sizeof(float) * units * kHeadsPerGroup);
+  w.po = off;        off += up(sizeof(__half) * units * kHeadsPerGroup * kDim);
+  w.total = off;
+  w.chunk = chunk;
+  w.max_items = max_items;
+  return w;
+}
+
+cudaError_t launch_attn_prefill_chunk(const CUtensorMap& map_q, const CUtensorMap& map_k,
+                                      const CUtensorMap& map_v, const int32_t* sel, int64_t L,
+                                      int G, int k, float scale, int64_t q0, int64_t q1,
+                                      uint8_t* ws, const PrefillWorkspace& w, void* o, float* lse,
+                                      uint64_t wait_ns, int num_sms, cudaStream_t stream) {
+  SchedArgs s{};
+  s.sel = sel;
+  s.L = L;
+  s.G = G;
+  s.k = k;
+  s.q0 = static_cast<int32_t>(q0);
+  s.nbq = static_cast<int32_t>((q1 - q0 + kBlock - 1) / kBlock);
+  s.nbk = static_cast<int32_t>((q1 + kBlock - 1) / kBlock);
+  s.hist = reinterpret_cast<int32_t*>(ws + w.hist);
+  s.cnt = reinterpret_cast<int32_t*>(ws + w.cnt);
+  s.list_base = reinterpret_cast<int32_t*>(ws + w.list_base);
+  s.item_base = reinterpret_cast<int32_t*>(ws + w.item_base);
+  s.n_items = reinterpret_cast<int32_t*>(ws + w.n_items);
+  s.items = reinterpret_cast<int4*>(ws + w.items);
+  s.list = reinterpret_cast<int32_t*>(ws + w.list);
+  s.status = reinterpret_cast<int32_t*>(ws);
+  const size_t mask_smem = static_cast<size_t>(s.nbk) * 16;
+  cudaError_t e;
+  if (mask_smem > 48 * 1024) {
+    if ((e = cudaFuncSetAttribute(sched_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  static_cast<int>(mask_smem))) != cudaSuccess)
+      return e;
+    if ((e = cudaFuncSetAttribute(sched_fill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  static_cast<int>(mask_smem))) != cudaSuccess)
+      return e;
+  }
+  const dim3 qgrid(s.nbq, G);
+  sched_hist_kernel<<<qgrid, kBlock, mask_smem, stream>>>(s);
+  const int pairs = G * s.nbk;
+  sched_scan_kernel<<<(pairs * 32 + 255) / 256, 256, 0, stream>>>(s);
+  sched_bases_kernel<<<1, 1024, 0, stream>>>(s);
+  sched_items_kernel<<<(pairs + 255) / 256, 256, 0, stream>>>(s);
+  sched_fill_kernel<<<qgrid, kBlock, mask_smem, stream>>>(s);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+
+  AttnArgs a{};
+  a.items = s.items;
+  a.n_items = s.n_items;
+  a.list = s.list;
+  a.G = G;
+  a.k = k;
+  a.q0 = s.q0;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.po = reinterpret_cast<__half*>(ws + w.po);
+  a.pm = reinterpret_cast<float*>(ws + w.pm);
+  a.plse = reinterpret_cast<float*>(ws + w.plse);
+  a.status = s.status;
+  a.wait_ns = wait_ns;
+  if ((e = cudaFuncSetAttribute(attn_kv_outer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kAttnSmem)) != cudaSuccess)
+    return e;
+  const int grid = static_cast<int>(std::min<int64_t>(w.max_items, num_sms));
+  attn_kv_outer_kernel<<<grid, 384, kAttnSmem, stream>>>(map_q, map_k, map_v, a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+
+  CombineArgs c{};
+  c.sel = sel;
+  c.po = a.po;
+  c.pm = a.pm;
+  c.plse = a.plse;
+  c.L = L;
+  c.G = G;
+  c.k = k;
+  c.q0 = s.q0;
+  c.nrows = static_cast<int32_t>(q1 - q0);
+  c.o = reinterpret_cast<__nv_bfloat16*>(o);
+  c.lse = lse;
+  combine_kernel<<<dim3(c.nrows, G), 128, 0, stream>>>(c);
+  return cudaGetLastError();
+}
+
+}  // namespace msa

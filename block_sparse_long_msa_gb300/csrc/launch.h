@@ -14,4 +14,16 @@ cudaError_t launch_index_select_prefill(const CUtensorMap& map_q, const CUtensor
                                         int64_t L, int G, int k, int32_t* sel, float* sel_score,
                                         int32_t* status, uint64_t wait_ns, cudaStream_t stream);
 
+// Byte offsets of the prefill main-branch workspace (after the 256-byte status header).
+struct PrefillWorkspace {
+  size_t hist, cnt, list_base, item_base, n_items, items, list, pm, plse, po, total;
+  int64_t chunk, max_items;
+};
+PrefillWorkspace prefill_workspace_layout(int64_t L, int G, int k, int64_t chunk);
+cudaError_t launch_attn_prefill_chunk(const CUtensorMap& map_q, const CUtensorMap& map_k,
+                                      const CUtensorMap& map_v, const int32_t* sel, int64_t L,
+                                      int G, int k, float scale, int64_t q0, int64_t q1,
+                                      uint8_t* ws, const PrefillWorkspace& w, void* o, float* lse,
+                                      uint64_t wait_ns, int num_sms, cudaStream_t stream);
+
 }  // namespace msa

@@ -72,6 +72,18 @@ uint64_t wait_ns(const msa_config_t* c) {
 
 int32_t* status_word(void* ws) { return reinterpret_cast<int32_t*>(ws); }
 
+// Queries per prefill main-branch pass: bounds the partial-output workspace (G*k*16*128 bf16 per
+// token, 256 KiB at G = 4, k = 16) to 16 GiB at most.
+constexpr int64_t kPrefillChunk = 65536;
+// The scheduler keeps a 16-byte token mask per key block in shared memory, and list entries
+// pack the token index above a 4-bit slot.
+constexpr int64_t kMaxPrefillTokens = 1536 * 1024;
+
+int64_t prefill_chunk(int64_t L) {
+  const int64_t rounded = (L + kBlock - 1) / kBlock * kBlock;
+  return rounded < kPrefillChunk ? rounded : kPrefillChunk;
+}
+
 }  // namespace
 
 extern "C" {
@@ -151,19 +163,53 @@ msa_status_t msa_index_select(const msa_config_t* cfg, const void* q_idx, const 
 }
 
 size_t msa_attn_prefill_workspace(const msa_config_t* cfg, int64_t L) {
-  (void)L;
-  if (check_config(cfg) != MSA_OK) return 0;
-  return MSA_WS_HEADER_BYTES;
+  if (check_config(cfg) != MSA_OK || L < 0) return 0;
+  if (L == 0) return MSA_WS_HEADER_BYTES;
+  return msa::prefill_workspace_layout(L, cfg->num_groups, cfg->topk, prefill_chunk(L)).total;
 }
 
 msa_status_t msa_attn_prefill(const msa_config_t* cfg, const void* q, const void* k,
                               const void* v, int64_t L, const int32_t* sel, void* o, float* lse,
                               void* ws, size_t ws_bytes, cudaStream_t stream) {
-  (void)q; (void)k; (void)v; (void)L; (void)sel; (void)o; (void)lse; (void)ws; (void)ws_bytes;
-  (void)stream;
   msa_status_t st = check_config(cfg);
   if (st != MSA_OK) return st;
-  return MSA_ERR_UNSUPPORTED;
+  if (!q || !k || !v || !sel || !o || !lse || !ws || L < 0) return MSA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return MSA_ERR_INVALID_ARG;
+  const int G = cfg->num_groups;
+  if (cfg->heads_per_group != 16) return MSA_ERR_UNSUPPORTED;
+  if (L > kMaxPrefillTokens) return MSA_ERR_UNSUPPORTED;
+  if (ws_bytes < msa_attn_prefill_workspace(cfg, L)) return MSA_ERR_WORKSPACE;
+  if (L == 0) return MSA_OK;
+  const int Hq = G * cfg->heads_per_group;
+  CUtensorMap mq, mk, mv;
+  {
+    const uint64_t dims[3] = {kDim, static_cast<uint64_t>(Hq), static_cast<uint64_t>(L)};
+    const uint64_t strides[2] = {kDim * 2, static_cast<uint64_t>(Hq) * kDim * 2};
+    const uint32_t box[3] = {64, 16, 1};
+    if (!make_map(&mq, q, 3, dims, strides, box)) return MSA_ERR_CUDA;
+  }
+  {
+    const uint64_t dims[3] = {kDim, static_cast<uint64_t>(G), static_cast<uint64_t>(L)};
+    const uint64_t strides[2] = {kDim * 2, static_cast<uint64_t>(G) * kDim * 2};
+    const uint32_t box[3] = {64, 1, kBlock};
+    if (!make_map(&mk, k, 3, dims, strides, box)) return MSA_ERR_CUDA;
+    if (!make_map(&mv, v, 3, dims, strides, box)) return MSA_ERR_CUDA;
+  }
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return MSA_ERR_CUDA;
+  const int64_t chunk = prefill_chunk(L);
+  const msa::PrefillWorkspace w = msa::prefill_workspace_layout(L, G, cfg->topk, chunk);
+  for (int64_t q0 = 0; q0 < L; q0 += chunk) {
+    const int64_t q1 = q0 + chunk < L ? q0 + chunk : L;
+    cudaError_t e = msa::launch_attn_prefill_chunk(mq, mk, mv, sel, L, G, cfg->topk,
+                                                   cfg->softmax_scale, q0, q1,
+                                                   static_cast<uint8_t*>(ws), w, o, lse,
+                                                   wait_ns(cfg), sms, stream);
+    if (e != cudaSuccess) return MSA_ERR_CUDA;
+  }
+  return MSA_OK;
 }
 
 size_t msa_attn_decode_workspace(const msa_config_t* cfg, const msa_paged_kv_t* paged) {

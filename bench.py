@@ -1,0 +1,427 @@
+#!/usr/bin/env python
+"""Benchmark of the MSA operator on GB300: prefill tokens/s with per-kernel roofline.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl msa|reference] [--workload NAME]
+
+A step is one full pass of the hot path over one batch of synthetic input resident in HBM:
+index selection (score + max-pool + top-k) followed by the main branch (scheduling, KV-outer
+attention, combine) on the 64/4-head, L = 32768 prefill workload.  Prints ONE JSON line (rank 0).
+
+The path has no exchange step, so N > 1 runs N independent replicas (one per GPU, weak scaling)
+with a barrier and the max over ranks around the timed region.
+``--impl reference`` times the CPU oracle (the only reference there is) on bounded samples.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import synthetic  # noqa: E402
+from block_sparse_long_msa_gb300 import accounting as acc  # noqa: E402
+
+METRIC = "MSA prefill tokens/s and decode tokens/s at 1 GB300; % tensor/HBM roofline"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=60)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="msa", choices=["msa", "reference"])
+    p.add_argument("--workload", default="prefill_L32K")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--e2e-steps", type=int, default=5)
+    p.add_argument("--L", type=int, default=0, help="override the workload length (profiling)")
+    return p.parse_args()
+
+
+def workload(args):
+    w = synthetic.WORKLOADS[args.workload]
+    if args.L:
+        w = synthetic.Workload(**{**w.__dict__, "L": args.L, "name": f"{w.name}@L{args.L}"})
+    return w
+
+
+# ------------------------------------------------------------------------------------------
+# distributed plumbing (replicas only: no collective touches the data path)
+# ------------------------------------------------------------------------------------------
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() and args.impl == "msa" else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return world, rank
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ------------------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = [r for r in csv.reader(io.StringIO(self.out or "")) if len(r) >= 9]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["clocks unavailable"],
+                    "samples": 0}
+        sm = [float(r[1]) for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if "Active" in v
+                          and "Not" not in v})
+        power = []
+        for r in rows:
+            try:
+                power.append(float(r[3]))
+            except ValueError:
+                pass
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][2]),
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(power) if power else None}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+# ------------------------------------------------------------------------------------------
+# algorithmic work of each kernel (bytes / FLOPs per launch)
+# ------------------------------------------------------------------------------------------
+def prefill_work(w, sel_counts=None):
+    L, G, k, B, Hq, d, di = w.L, w.G, w.k, w.B, w.Hq, w.d, w.di
+    nb = (L + B - 1) // B
+    units = acc.units_prefill(L, G, B, k)
+    hpg = Hq // G
+    return {
+        "index_flops": acc.index_flops_prefill(L, G, di, B),
+        "attn_flops": acc.attn_flops_prefill(L, Hq, d, B, k),
+        "units": units,
+        # attention: gather the 16 query heads of every (token, group, block) unit, write its
+        # fp16 partial O and (m, lse); K and V of every (group, block) once
+        "attn_bytes": units * (hpg * d * 2 + hpg * d * 2 + hpg * 8) + G * nb * B * d * 2 * 2,
+        # combine: read every partial and its (m, lse), the selection; write O and LSE
+        "combine_bytes": units * (hpg * d * 2 + hpg * 8) + G * L * k * 4 + L * Hq * (d * 2 + 4),
+    }
+
+
+# ------------------------------------------------------------------------------------------
+# MSA arm
+# ------------------------------------------------------------------------------------------
+def run_msa(args, world, rank):
+    import block_sparse_long_msa_gb300 as msa
+    msa.lib()
+    w = workload(args)
+    assert w.kind == "prefill", "the bench step is the prefill pass"
+    dev = torch.device("cuda", torch.cuda.current_device())
+    inp = synthetic.prefill_inputs(w, device=dev)
+    cfg = msa.config(w.G, w.hpg, w.k, w.scale)
+    L = w.L
+    sel = torch.empty((w.G, L, w.k), dtype=torch.int32, device=dev)
+    o = torch.empty((L, w.Hq, w.d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.Hq, L), dtype=torch.float32, device=dev)
+    ws_bytes = max(msa.msa_attn_prefill_workspace(cfg, L),
+                   msa.msa_index_select_workspace(cfg, L, L))
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+    nchunks = -(-L // msa.msa_prefill_chunk_tokens(cfg, L))
+    launches_per_step = 1 + 7 * nchunks
+    stream = torch.cuda.current_stream()
+
+    def ev():
+        e = torch.cuda.Event(enable_timing=True)
+        e.record(stream)  # materialise the handle
+        return e
+
+    nmarks = 3 * nchunks + 1
+
+    def step(marks=None, start=None):
+        if start is not None:
+            start.record(stream)
+        msa.msa_index_select(cfg, inp["q_idx"], inp["k_idx"], sel=sel, ws=ws)
+        msa.msa_attn_prefill(cfg, inp["q"], inp["k"], inp["v"], sel, o=o, lse=lse, ws=ws,
+                             marks=marks)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    status = msa.msa_get_device_status(ws)
+    if status != 0:
+        raise RuntimeError(f"device status {status} after warm-up")
+
+    starts = [ev() for _ in range(args.steps)]
+    marks = [[ev() for _ in range(nmarks)] for _ in range(args.steps)]
+    t0, t1 = ev(), ev()
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clocks:
+        barrier(world)
+        torch.cuda.synchronize()
+        t0.record(stream)
+        for s in range(args.steps):
+            step(marks[s], starts[s])
+        t1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    total_ms = t0.elapsed_time(t1)
+    total_ms = max_over_ranks(total_ms, world)
+
+    phase = {"index": 0.0, "schedule": 0.0, "attention": 0.0, "combine": 0.0}
+    for s in range(args.steps):
+        m = marks[s]
+        phase["index"] += starts[s].elapsed_time(m[0])
+        for c in range(nchunks):
+            phase["schedule"] += m[3 * c].elapsed_time(m[3 * c + 1])
+            phase["attention"] += m[3 * c + 1].elapsed_time(m[3 * c + 2])
+            phase["combine"] += m[3 * c + 2].elapsed_time(m[3 * c + 3])
+    per_launch_ms = {"index": phase["index"] / args.steps,
+                     "schedule": phase["schedule"] / args.steps,
+                     "attention": phase["attention"] / (args.steps * nchunks),
+                     "combine": phase["combine"] / (args.steps * nchunks)}
+
+    work = prefill_work(w)
+    peaks = load_peaks()
+    tensor_peak = peaks["bf16_tflops"]
+    roof = {
+        "index": ("tensor", work["index_flops"] / (per_launch_ms["index"] * 1e-3) / 1e12,
+                  tensor_peak, "TFLOP/s"),
+        "attention": ("hbm", work["attn_bytes"] / nchunks / (per_launch_ms["attention"] * 1e-3)
+                      / 1e9, peaks["hbm_gbs"], "GB/s"),
+        "combine": ("hbm", work["combine_bytes"] / nchunks / (per_launch_ms["combine"] * 1e-3)
+                    / 1e9, peaks["hbm_gbs"], "GB/s"),
+    }
+    dominant = max(("index", "attention", "combine"), key=lambda n: phase[n])
+    bound, achieved, peak, unit = roof[dominant]
+    traffic = None  # filled from an ncu capture of the same kernel (see profiles/)
+
+    # ---------------- end-to-end through the public API from pinned host buffers ------------
+    host_in = {k: inp[k].cpu().pin_memory() for k in ("q", "k", "v", "q_idx", "k_idx")}
+    host_o = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    host_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    host_sel = torch.empty(sel.shape, dtype=sel.dtype).pin_memory()
+    dev_in = {k: torch.empty_like(inp[k]) for k in host_in}
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in (host_o, host_lse, host_sel))
+
+    def e2e_step():
+        for k_, t in host_in.items():
+            dev_in[k_].copy_(t, non_blocking=True)
+        msa.msa_index_select(cfg, dev_in["q_idx"], dev_in["k_idx"], sel=sel, ws=ws)
+        msa.msa_attn_prefill(cfg, dev_in["q"], dev_in["k"], dev_in["v"], sel, o=o, lse=lse,
+                             ws=ws)
+        host_o.copy_(o, non_blocking=True)
+        host_lse.copy_(lse, non_blocking=True)
+        host_sel.copy_(sel, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = ev(), ev()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    status = msa.msa_get_device_status(ws)
+    if status != 0:
+        raise RuntimeError(f"device status {status} after timed region")
+
+    cpu_base = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu_base = cpu_baseline(w, {k: inp[k].cpu() for k in ("q", "k", "v", "q_idx", "k_idx")},
+                                target_s=15.0)
+
+    ms_per_step = total_ms / args.steps
+    value = world * L * args.steps / (total_ms * 1e-3)
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded SplitMix64; N(0,1) q/k/v, integer/8 index q/k)",
+        "config": {"workload": w.name, "L": L, "Hq": w.Hq, "G": w.G, "d": w.d, "B": w.B,
+                   "k": w.k, "parallelism": f"replicas x{world}",
+                   "step": "index select + prefill main branch over all L queries",
+                   "l2": "inputs larger than L2 (q 512 MiB) and ~8.6 GiB of partials per step"},
+        "phases_ms_per_step": {k: v / args.steps for k, v in phase.items()},
+        "gpu_launches": launches_per_step * args.steps,
+        "roofline": {"bound": bound, "kernel": dominant, "achieved": achieved, "peak": peak,
+                     "unit": unit, "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": peaks["source"]},
+        "kernel_rooflines": {n: {"bound": r[0], "achieved": r[1], "peak": r[2], "unit": r[3],
+                                 "frac": r[1] / r[2], "ms_per_launch": per_launch_ms[n]}
+                             for n, r in roof.items()},
+        "tensor_frac_main_branch": work["attn_flops"] / ((phase["attention"] + phase["combine"]
+                                                          + phase["schedule"]) / args.steps
+                                                         * 1e-3) / 1e12 / tensor_peak,
+        "e2e": {"value": world * L * args.e2e_steps / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "clocks": clocks.summary(),
+        "cpu_baseline": cpu_base,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------------------------
+# CPU oracle timing (the reference arm, and the cpu_baseline of the MSA arm)
+# ------------------------------------------------------------------------------------------
+def _oracle_rows(w, inp, rows):
+    import oracle
+    t = time.perf_counter()
+    sel = oracle.select_prefill(inp["q_idx"], inp["k_idx"], w.B, w.k, rows=rows)
+    oracle.attn_prefill(inp["q"], inp["k"], inp["v"], sel, w.B, w.k, w.scale, rows=rows)
+    return time.perf_counter() - t
+
+
+def _strided_rows(L, n, phase=0):
+    import numpy as np
+    n = max(1, min(L, n))
+    return (np.arange(n, dtype=np.int64) * L // n + phase) % L
+
+
+def cpu_baseline(w, inp, target_s=15.0):
+    import oracle
+    oracle.build()
+    n = 64
+    dt = _oracle_rows(w, inp, _strided_rows(w.L, n))
+    n2 = int(min(w.L, max(n, n * target_s / max(dt, 1e-3))))
+    rows = _strided_rows(w.L, n2, 1)
+    dt2 = _oracle_rows(w, inp, rows)
+    return {"value": len(rows) / dt2, "unit": "tokens/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"{len(rows)} evenly strided query rows of the L={w.L} workload "
+                      f"(index selection + attention for all {w.G} groups / {w.Hq} heads), "
+                      f"{dt2:.1f} s"}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    w = workload(args)
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    inp = {k: v.cpu() for k, v in synthetic.prefill_inputs(w, device=dev).items()
+           if isinstance(v, torch.Tensor)}
+    budget_s = 150.0
+    cal = _oracle_rows(w, inp, _strided_rows(w.L, 16))
+    per_row = cal / 16
+    rows_per_step = int(max(4, min(2048, budget_s / (args.steps + args.warmup) / per_row)))
+    for s in range(args.warmup):
+        _oracle_rows(w, inp, _strided_rows(w.L, rows_per_step, s + 1))
+    total, n = 0.0, 0
+    for s in range(args.steps):
+        rows = _strided_rows(w.L, rows_per_step, args.warmup + s + 1)
+        total += _oracle_rows(w, inp, rows)
+        n += len(rows)
+    value = n / total
+    cb = {"value": value, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+          "sample": f"{rows_per_step} evenly strided query rows per step of the L={w.L} "
+                    "workload (index selection + attention, all groups and heads)"}
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "L": w.L, "Hq": w.Hq, "G": w.G, "d": w.d, "B": w.B,
+                   "k": w.k, "parallelism": "cpu oracle (rank 0 only)"},
+        "impl": "reference", "cpu_baseline": cb,
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    world, rank = dist_setup(args)
+    if args.gpus != world and world > 1:
+        raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE {world}")
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_msa(args, world, rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

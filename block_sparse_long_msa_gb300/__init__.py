@@ -18,7 +18,8 @@ MSA_ERR_CUDA, MSA_ERR_DEVICE_TIMEOUT, MSA_ERR_DEVICE_BOUNDS = 4, 5, 6
 WS_HEADER_BYTES = 256
 
 EXPORTS = ("msa_index_select_workspace", "msa_index_select", "msa_attn_prefill_workspace",
-           "msa_attn_prefill", "msa_attn_decode_workspace", "msa_attn_decode",
+           "msa_attn_prefill", "msa_attn_prefill_marked", "msa_prefill_chunk_tokens",
+           "msa_attn_decode_workspace", "msa_attn_decode",
            "msa_get_device_status", "msa_reset_device_status", "msa_status_string")
 
 
@@ -63,6 +64,10 @@ def lib() -> ctypes.CDLL:
         L.msa_attn_prefill_workspace.argtypes = [cfgp, i64]
         L.msa_attn_prefill_workspace.restype = sz
         L.msa_attn_prefill.argtypes = [cfgp, P, P, P, i64, P, P, P, P, sz, P]
+        L.msa_attn_prefill_marked.argtypes = [cfgp, P, P, P, i64, P, P, P, P, sz, P, P,
+                                              ctypes.c_int32]
+        L.msa_prefill_chunk_tokens.argtypes = [cfgp, i64]
+        L.msa_prefill_chunk_tokens.restype = i64
         L.msa_attn_decode_workspace.argtypes = [cfgp, pagedp]
         L.msa_attn_decode_workspace.restype = sz
         L.msa_attn_decode.argtypes = [cfgp, P, pagedp, P, P, P, P, sz, P]
@@ -70,7 +75,8 @@ def lib() -> ctypes.CDLL:
         L.msa_reset_device_status.argtypes = [P, P]
         L.msa_status_string.argtypes = [ctypes.c_int]
         L.msa_status_string.restype = ctypes.c_char_p
-        for name in ("msa_index_select", "msa_attn_prefill", "msa_attn_decode",
+        for name in ("msa_index_select", "msa_attn_prefill", "msa_attn_prefill_marked",
+                     "msa_attn_decode",
                      "msa_get_device_status", "msa_reset_device_status"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
@@ -153,8 +159,17 @@ def msa_attn_prefill_workspace(cfg: MsaConfig, L: int) -> int:
     return int(lib().msa_attn_prefill_workspace(ctypes.byref(cfg), L))
 
 
-def msa_attn_prefill(cfg: MsaConfig, q, k, v, sel, o=None, lse=None, ws=None, stream=None):
-    """Main branch, prefill.  Returns o bf16 [L][Hq][d] and lse fp32 [Hq][L]."""
+def msa_prefill_chunk_tokens(cfg: MsaConfig, L: int) -> int:
+    return int(lib().msa_prefill_chunk_tokens(ctypes.byref(cfg), L))
+
+
+def msa_attn_prefill(cfg: MsaConfig, q, k, v, sel, o=None, lse=None, ws=None, stream=None,
+                     marks=None):
+    """Main branch, prefill.  Returns o bf16 [L][Hq][d] and lse fp32 [Hq][L].
+
+    marks: optional list of recorded torch.cuda.Event(enable_timing=True); see
+    msa_attn_prefill_marked in include/msa.h for where each is recorded.
+    """
     import torch
     L, Hq, d = q.shape
     if o is None:
@@ -162,8 +177,14 @@ def msa_attn_prefill(cfg: MsaConfig, q, k, v, sel, o=None, lse=None, ws=None, st
     if lse is None:
         lse = torch.empty((Hq, L), dtype=torch.float32, device=q.device)
     ws = _workspace(msa_attn_prefill_workspace(cfg, L), q.device, ws)
-    st = lib().msa_attn_prefill(ctypes.byref(cfg), _ptr(q), _ptr(k), _ptr(v), L, _ptr(sel),
-                                _ptr(o), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream))
+    if marks:
+        arr = (ctypes.c_void_p * len(marks))(*[m.cuda_event for m in marks])
+        st = lib().msa_attn_prefill_marked(ctypes.byref(cfg), _ptr(q), _ptr(k), _ptr(v), L,
+                                           _ptr(sel), _ptr(o), _ptr(lse), _ptr(ws), ws.numel(),
+                                           _stream(stream), arr, len(marks))
+    else:
+        st = lib().msa_attn_prefill(ctypes.byref(cfg), _ptr(q), _ptr(k), _ptr(v), L, _ptr(sel),
+                                    _ptr(o), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream))
     _check(st, "msa_attn_prefill")
     return o, lse
 

@@ -198,12 +198,14 @@ __global__ void sched_fill_kernel(SchedArgs a) {
 
 // ------------------------------------------------------------------------------------------
 // KV-outer attention.  One persistent CTA per SM walks the work items; per item it stages
-// K_b and V_b of group g (TMA, double-buffered across items), then for every tile of 8 tokens
-// gathers their 16 query heads (TMA, 16 rows per token) and runs
+// K_b and V_b of group g (TMA, double-buffered across items) and the item's token list, then
+// for every tile of 8 tokens gathers their 16 query heads (TMA, 16 rows per token) and runs
 //   S = Q K^T (tcgen05, fp32 in TMEM) -> softmax rows (causal limit only in the local block)
-//   -> P (bf16, shared memory) -> O = P V (tcgen05, TMEM) -> unnormalised partial O (bf16) +
-//   row max m and log-sum-exp per (token, head, slot).
-// Roles: warp 0 TMA producer, warp 1 TMEM owner + MMA issuer, warps 4-7 softmax, 8-11 epilogue.
+//   -> P (fp16, written back into the same TMEM columns) -> O = P V (tcgen05, A from TMEM)
+//   -> unnormalised partial O (fp16) + row max m and log-sum-exp per (token, head, slot).
+// Roles (16 warps): 0 TMA producer + token-list staging, 1 TMEM owner + MMA issuer,
+// 2-3 V converter (bf16 -> fp16 in place), 4-7 softmax of even tiles, 8-11 softmax of odd
+// tiles, 12-15 epilogue.  TMEM: columns [0,256) two S/P slots, [256,512) two O slots.
 // ------------------------------------------------------------------------------------------
 struct AttnArgs {
   const int4* items;
@@ -218,15 +220,28 @@ struct AttnArgs {
   uint64_t wait_ns;
 };
 
-constexpr uint32_t kSmemKV = 0;             // 2 x (K 32 KB + V 32 KB)
-constexpr uint32_t kSmemQ = 131072;         // 2 x 32 KB
-constexpr uint32_t kSmemP = 196608;         // 32 KB
-constexpr uint32_t kSmemBar = 229376;
+struct ItemMeta {
+  int32_t g, b, count, pad;
+  int32_t tok[kItemTokens];  // (token << 4) | slot
+};
+
+constexpr int kQStages = 3;
+constexpr uint32_t kSmemKV = 0;                          // 2 x (K 32 KB + V 32 KB)
+constexpr uint32_t kSmemQ = 131072;                      // 3 x 32 KB
+constexpr uint32_t kSmemMeta = kSmemQ + kQStages * 32768;  // 2 x ItemMeta
+constexpr uint32_t kSmemBar = kSmemMeta + 2 * sizeof(ItemMeta);
 constexpr uint32_t kAttnSmem = kSmemBar + 256 + 1024;
+static_assert(kAttnSmem <= 232448, "attention kernel shared memory");
 constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, false, false);
 constexpr uint32_t kIdescPV = idesc_f16_f32(128, 128, false, true);  // P, V in fp16
 
-__global__ void __launch_bounds__(384, 1)
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__global__ void __launch_bounds__(512, 1)
     attn_kv_outer_kernel(const __grid_constant__ CUtensorMap map_q,
                          const __grid_constant__ CUtensorMap map_k,
                          const __grid_constant__ CUtensorMap map_v, AttnArgs a) {
@@ -237,17 +252,19 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t bars = base + kSmemBar;
   auto kv_full = [&](int s) { return bars + 8 * s; };
   auto kv_empty = [&](int s) { return bars + 16 + 8 * s; };
-  auto q_full = [&](int s) { return bars + 32 + 8 * s; };
-  auto q_empty = [&](int s) { return bars + 48 + 8 * s; };
-  auto s_full = [&](int s) { return bars + 64 + 8 * s; };
-  auto s_empty = [&](int s) { return bars + 80 + 8 * s; };
-  const uint32_t p_full = bars + 96, p_empty = bars + 104;
-  auto o_full = [&](int s) { return bars + 112 + 8 * s; };
-  auto o_empty = [&](int s) { return bars + 128 + 8 * s; };
-  const uint32_t drain_bar = bars + 144;
-  auto v_ready = [&](int s) { return bars + 152 + 8 * s; };
-  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + kSmemBar + 168);
-  volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + kSmemBar + 172);
+  auto meta_empty = [&](int s) { return bars + 32 + 8 * s; };
+  auto v_ready = [&](int s) { return bars + 48 + 8 * s; };
+  auto q_full = [&](int s) { return bars + 64 + 8 * s; };
+  auto q_empty = [&](int s) { return bars + 88 + 8 * s; };
+  auto s_full = [&](int s) { return bars + 112 + 8 * s; };
+  auto p_full = [&](int s) { return bars + 128 + 8 * s; };
+  auto sp_free = [&](int s) { return bars + 144 + 8 * s; };
+  auto o_full = [&](int s) { return bars + 160 + 8 * s; };
+  auto o_empty = [&](int s) { return bars + 176 + 8 * s; };
+  const uint32_t drain_bar = bars + 192;
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + kSmemBar + 200);
+  volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + kSmemBar + 204);
+  ItemMeta* meta = reinterpret_cast<ItemMeta*>(smem + kSmemMeta);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_items = *a.n_items;
@@ -256,16 +273,18 @@ __global__ void __launch_bounds__(384, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(kv_full(s), 1);
       mbar_init(kv_empty(s), 1);
-      mbar_init(q_full(s), 1);
-      mbar_init(q_empty(s), 1);
+      mbar_init(meta_empty(s), 128);
+      mbar_init(v_ready(s), 64);
       mbar_init(s_full(s), 1);
-      mbar_init(s_empty(s), 128);
+      mbar_init(p_full(s), 128);
+      mbar_init(sp_free(s), 1);
       mbar_init(o_full(s), 1);
       mbar_init(o_empty(s), 128);
-      mbar_init(v_ready(s), 64);
     }
-    mbar_init(p_full, 128);
-    mbar_init(p_empty, 1);
+    for (int s = 0; s < kQStages; ++s) {
+      mbar_init(q_full(s), 1);
+      mbar_init(q_empty(s), 1);
+    }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -277,58 +296,73 @@ __global__ void __launch_bounds__(384, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;  // columns [0,256): S slots, [256,512): O slots
+  const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
     // ------------------------------- producer -------------------------------
+    int T = 0, nit = 0, kv_issued = 0, q_issued = 0;
+    bool ok = true;
     if (lane == 0) {
       tma_prefetch_map(&map_q);
       tma_prefetch_map(&map_k);
       tma_prefetch_map(&map_v);
-      int T = 0, nit = 0;
-      int kv_issued = 0, q_issued = 0;
-      bool ok = true;
-      for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x, ++nit) {
-        const int4 item = a.items[it];
-        const int g = item.x, b = item.y, start = item.z, count = item.w;
-        const int kvs = nit & 1;
-        if (*abort_flag || !mbar_wait(kv_empty(kvs), ((nit >> 1) & 1) ^ 1, a.wait_ns)) {
+    }
+    for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x, ++nit) {
+      const int kvs = nit & 1, par = ((nit >> 1) & 1) ^ 1;
+      const bool free_ok = !*abort_flag && mbar_wait(kv_empty(kvs), par, a.wait_ns) &&
+                           mbar_wait(meta_empty(kvs), par, a.wait_ns);
+      if (!__all_sync(0xffffffffu, free_ok)) {
+        ok = false;
+        break;
+      }
+      const int4 item = a.items[it];
+      ItemMeta& m = meta[kvs];
+      for (int j = lane; j < item.w; j += 32) m.tok[j] = a.list[item.z + j];
+      if (lane == 0) {
+        m.g = item.x;
+        m.b = item.y;
+        m.count = item.w;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        const uint32_t kb = base + kSmemKV + kvs * 65536u;
+        mbar_arrive_expect_tx(kv_full(kvs), 65536);
+        tma_load_3d(kb, &map_k, kv_full(kvs), 0, item.x, item.y * kBlock);
+        tma_load_3d(kb + kPanel, &map_k, kv_full(kvs), 64, item.x, item.y * kBlock);
+        tma_load_3d(kb + 32768, &map_v, kv_full(kvs), 0, item.x, item.y * kBlock);
+        tma_load_3d(kb + 32768 + kPanel, &map_v, kv_full(kvs), 64, item.x, item.y * kBlock);
+      }
+      ++kv_issued;
+      for (int t0 = 0; t0 < item.w; t0 += kTileTokens, ++T) {
+        const int qs = T % kQStages;
+        if (!__all_sync(0xffffffffu, !*abort_flag && mbar_wait(q_empty(qs),
+                                                               ((T / kQStages) & 1) ^ 1,
+                                                               a.wait_ns))) {
           ok = false;
           break;
         }
-        const uint32_t kb = base + kSmemKV + kvs * 65536u;
-        mbar_arrive_expect_tx(kv_full(kvs), 65536);
-        tma_load_3d(kb, &map_k, kv_full(kvs), 0, g, b * kBlock);
-        tma_load_3d(kb + kPanel, &map_k, kv_full(kvs), 64, g, b * kBlock);
-        tma_load_3d(kb + 32768, &map_v, kv_full(kvs), 0, g, b * kBlock);
-        tma_load_3d(kb + 32768 + kPanel, &map_v, kv_full(kvs), 64, g, b * kBlock);
-        ++kv_issued;
-        for (int t0 = 0; t0 < count; t0 += kTileTokens, ++T) {
-          const int qs = T & 1;
-          if (*abort_flag || !mbar_wait(q_empty(qs), ((T >> 1) & 1) ^ 1, a.wait_ns)) {
-            ok = false;
-            break;
-          }
-          const int n = min(kTileTokens, count - t0);
-          const uint32_t qb = base + kSmemQ + qs * 32768u;
-          mbar_arrive_expect_tx(q_full(qs), n * 4096);
-          for (int tk = 0; tk < n; ++tk) {
-            const int32_t e = a.list[start + t0 + tk];
-            const int i = e >> 4;
-            tma_load_3d(qb + tk * 2048, &map_q, q_full(qs), 0, g * kHeadsPerGroup, i);
-            tma_load_3d(qb + kPanel + tk * 2048, &map_q, q_full(qs), 64, g * kHeadsPerGroup, i);
-          }
-          ++q_issued;
+        const int n = min(kTileTokens, item.w - t0);
+        const uint32_t qb = base + kSmemQ + qs * 32768u;
+        if (lane == 0) mbar_arrive_expect_tx(q_full(qs), n * 4096);
+        __syncwarp();
+        if (lane < 2 * n) {  // lanes 0..2n-1: token lane/2, 64-column half lane%2
+          const int tk = lane >> 1, half = lane & 1;
+          const int i = m.tok[t0 + tk] >> 4;
+          tma_load_3d(qb + half * kPanel + tk * 2048, &map_q, q_full(qs), half * 64,
+                      item.x * kHeadsPerGroup, i);
         }
+        ++q_issued;
       }
-      if (!ok) {
-        report_status(a.status, kStatusTimeout);
-        *abort_flag = 1;
-        // let in-flight copies land before the CTA can exit (at most one per stage)
+    }
+    if (!ok) {
+      if (lane == 0) report_status(a.status, kStatusTimeout);
+      *abort_flag = 1;
+      // let in-flight copies land before the CTA can exit (at most one per stage)
+      if (lane == 0) {
         for (int x = (kv_issued > 2 ? kv_issued - 2 : 0); x < kv_issued; ++x)
           mbar_wait(kv_full(x & 1), (x >> 1) & 1, a.wait_ns);
-        for (int x = (q_issued > 2 ? q_issued - 2 : 0); x < q_issued; ++x)
-          mbar_wait(q_full(x & 1), (x >> 1) & 1, a.wait_ns);
+        for (int x = (q_issued > kQStages ? q_issued - kQStages : 0); x < q_issued; ++x)
+          mbar_wait(q_full(x % kQStages), (x / kQStages) & 1, a.wait_ns);
       }
     }
   } else if (warp == 1) {
@@ -338,45 +372,46 @@ __global__ void __launch_bounds__(384, 1)
       int T = 0, nit = 0;
       int pend_T = -1, pend_kvs = 0, pend_nit = 0;
       bool pend_last = false, pend_first = false;
-      auto issue_pv = [&](int Tp, int kvs, int nitp, bool first_of_item,
-                          bool last_of_item) -> bool {
+      // O[slot] = P[slot] . V (PV of tile Tp); frees the S/P slot, and the K/V stage after the
+      // last tile of its item
+      auto issue_pv = [bars, tmem, base](int Tp, int kvs, int nitp, bool first_of_item,
+                                         bool last_of_item, uint64_t wait_ns) -> bool {
+        const int slot = Tp & 1, use = Tp >> 1;
         // V of this stage has been converted to fp16 in place before its first use
-        if (first_of_item && !mbar_wait(v_ready(kvs), (nitp >> 1) & 1, a.wait_ns)) return false;
-        if (!mbar_wait(p_full, Tp & 1, a.wait_ns)) return false;
-        if (!mbar_wait(o_empty(Tp & 1), ((Tp >> 1) & 1) ^ 1, a.wait_ns)) return false;
+        if (first_of_item && !mbar_wait(bars + 48 + 8 * kvs, (nitp >> 1) & 1, wait_ns))
+          return false;
+        if (!mbar_wait(bars + 128 + 8 * slot, use & 1, wait_ns)) return false;         // p_full
+        if (!mbar_wait(bars + 176 + 8 * slot, (use & 1) ^ 1, wait_ns)) return false;   // o_empty
         tc_fence_after();
-        const uint32_t d = tmem + 256 + (Tp & 1) * 128;
+        const uint32_t d = tmem + 256 + slot * 128;
+        const uint32_t pa = tmem + slot * 128;
         const uint32_t vb = base + kSmemKV + kvs * 65536u + 32768;
-        const uint32_t pb = base + kSmemP;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t ad = sdesc_sw128(pb + (kk >> 2) * kPanel + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(vb + kk * 2048, kPanel, 1024);
-          mma_bf16_ss(d, ad, bd, kIdescPV, kk > 0);
-        }
-        mma_commit(o_full(Tp & 1));
-        mma_commit(p_empty);
-        if (last_of_item) mma_commit(kv_empty(kvs));
+        for (int kk = 0; kk < 8; ++kk)
+          mma_f16_ts(d, pa + kk * 8, sdesc_sw128(vb + kk * 2048, kPanel, 1024), kIdescPV, kk > 0);
+        mma_commit(bars + 160 + 8 * slot);  // o_full
+        mma_commit(bars + 144 + 8 * slot);  // sp_free
+        if (last_of_item) mma_commit(bars + 16 + 8 * kvs);  // kv_empty
         return true;
       };
       for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x, ++nit) {
-        const int count = a.items[it].w;
         const int kvs = nit & 1;
         if (*abort_flag || !mbar_wait(kv_full(kvs), (nit >> 1) & 1, a.wait_ns)) {
           ok = false;
           break;
         }
         tc_fence_after();
+        const int count = meta[kvs].count;
         const uint32_t kb = base + kSmemKV + kvs * 65536u;
         for (int t0 = 0; t0 < count; t0 += kTileTokens, ++T) {
-          const int qs = T & 1;
-          if (*abort_flag || !mbar_wait(q_full(qs), (T >> 1) & 1, a.wait_ns) ||
-              !mbar_wait(s_empty(T & 1), ((T >> 1) & 1) ^ 1, a.wait_ns)) {
+          const int qs = T % kQStages, slot = T & 1, use = T >> 1;
+          if (*abort_flag || !mbar_wait(q_full(qs), (T / kQStages) & 1, a.wait_ns) ||
+              !mbar_wait(sp_free(slot), (use & 1) ^ 1, a.wait_ns)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t d = tmem + (T & 1) * 128;
+          const uint32_t d = tmem + slot * 128;
           const uint32_t qb = base + kSmemQ + qs * 32768u;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
@@ -384,10 +419,11 @@ __global__ void __launch_bounds__(384, 1)
             mma_bf16_ss(d, sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
                         kIdescQK, kk > 0);
           }
-          mma_commit(s_full(T & 1));
+          mma_commit(s_full(slot));
           mma_commit(q_empty(qs));
           // PV of the previous tile overlaps the softmax of this one
-          if (pend_T >= 0 && !issue_pv(pend_T, pend_kvs, pend_nit, pend_first, pend_last)) {
+          if (pend_T >= 0 &&
+              !issue_pv(pend_T, pend_kvs, pend_nit, pend_first, pend_last, a.wait_ns)) {
             ok = false;
             break;
           }
@@ -398,7 +434,8 @@ __global__ void __launch_bounds__(384, 1)
           pend_last = (t0 + kTileTokens >= count);
         }
       }
-      if (ok && pend_T >= 0) ok = issue_pv(pend_T, pend_kvs, pend_nit, pend_first, pend_last);
+      if (ok && pend_T >= 0)
+        ok = issue_pv(pend_T, pend_kvs, pend_nit, pend_first, pend_last, a.wait_ns);
       if (!ok) {
         report_status(a.status, kStatusTimeout);
         *abort_flag = 1;
@@ -436,20 +473,27 @@ __global__ void __launch_bounds__(384, 1)
       report_status(a.status, kStatusTimeout);
       *abort_flag = 1;
     }
-  } else if (warp >= 4 && warp < 8) {
+  } else if (warp >= 4 && warp < 12) {
     // ------------------------------- softmax -------------------------------
-    const int row = (warp - 4) * 32 + lane;  // TMEM lane = MMA row
+    const int wg = (warp - 4) >> 2;          // handles tiles with (T & 1) == wg
+    const int row = (warp & 3) * 32 + lane;  // TMEM lane = MMA row
     const int tk = row >> 4, hh = row & 15;
-    const uint32_t lane_base = static_cast<uint32_t>((warp - 4) * 32) << 16;
-    const uint32_t pb = base + kSmemP;
-    int T = 0;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t sa = tmem + lane_base + wg * 128;
+    int T = 0, nit = 0;
     bool ok = true;
-    for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
-      const int4 item = a.items[it];
-      const int g = item.x, b = item.y, start = item.z, count = item.w;
+    for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x, ++nit) {
+      const int kvs = nit & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(kv_full(kvs), (nit >> 1) & 1, a.wait_ns))) {
+        ok = false;
+        break;
+      }
+      const ItemMeta& m = meta[kvs];
+      const int count = m.count, g = m.g, b = m.b;
       for (int t0 = 0; t0 < count; t0 += kTileTokens, ++T) {
-        const int slot = T & 1;
-        if (!__all_sync(0xffffffffu, mbar_wait(s_full(slot), (T >> 1) & 1, a.wait_ns))) {
+        if ((T & 1) != wg) continue;
+        const int use = T >> 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(s_full(wg), use & 1, a.wait_ns))) {
           ok = false;
           break;
         }
@@ -457,12 +501,11 @@ __global__ void __launch_bounds__(384, 1)
         const bool valid = t0 + tk < count;
         int i = 0, s = 0;
         if (valid) {
-          const int32_t e = a.list[start + t0 + tk];
+          const int32_t e = m.tok[t0 + tk];
           i = e >> 4;
           s = e & 15;
         }
         const int lim = valid ? min(i - b * kBlock, kBlock - 1) : kBlock - 1;
-        const uint32_t sa = tmem + lane_base + slot * 128;
         // pass 1: row max of the scaled logits (log2 units)
         float m2 = -__int_as_float(0x7f800000);
 #pragma unroll
@@ -474,39 +517,30 @@ __global__ void __launch_bounds__(384, 1)
           for (int q = 0; q < 32; ++q)
             if (c * 32 + q <= lim) m2 = fmaxf(m2, __uint_as_float(v[q]) * a.scale_log2);
         }
-        // the P buffer is free once the previous tile's PV has finished
-        if (T > 0 && !__all_sync(0xffffffffu, mbar_wait(p_empty, (T - 1) & 1, a.wait_ns))) {
-          ok = false;
-          break;
-        }
-        // pass 2: p = exp2(t - m2), row sum, bf16 P row into the swizzled operand tile
+        // pass 2: p = exp2(t - m2) -> fp16 pairs; keys [32c, 32c+32) go to columns
+        // [16c, 16c+16), which hold S values this thread has already read
         float l = 0.f;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          uint32_t v[32];
+          uint32_t v[32], pk[16];
           tmem_ld32(sa + c * 32, v);
           tmem_ld_wait();
-          uint32_t pk[16];
 #pragma unroll
           for (int q = 0; q < 32; q += 2) {
-            const float p0 = (c * 32 + q <= lim)
-                                 ? exp2f(__uint_as_float(v[q]) * a.scale_log2 - m2) : 0.f;
-            const float p1 = (c * 32 + q + 1 <= lim)
-                                 ? exp2f(__uint_as_float(v[q + 1]) * a.scale_log2 - m2) : 0.f;
+            const int j = c * 32 + q;
+            const float p0 =
+                j <= lim ? fast_exp2(fmaf(__uint_as_float(v[q]), a.scale_log2, -m2)) : 0.f;
+            const float p1 =
+                j + 1 <= lim ? fast_exp2(fmaf(__uint_as_float(v[q + 1]), a.scale_log2, -m2))
+                             : 0.f;
             l += p0 + p1;
             pk[q >> 1] = pack_f16x2(p0, p1);
           }
-          if (valid) {
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-              st_shared_v4(pb + sw128_offset(row, c * 32 + u * 8, 128), pk[4 * u], pk[4 * u + 1],
-                           pk[4 * u + 2], pk[4 * u + 3]);
-          }
+          tmem_st16(sa + c * 16, pk);
         }
+        tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(s_empty(slot));
-        fence_proxy_async_smem();
-        mbar_arrive(p_full);
+        mbar_arrive(p_full(wg));
         if (valid) {
           const size_t u = (static_cast<size_t>(i - a.q0) * a.G + g) * a.k + s;
           const float ln2 = 0.6931471805599453f;
@@ -519,19 +553,24 @@ __global__ void __launch_bounds__(384, 1)
       report_status(a.status, kStatusTimeout);
       *abort_flag = 1;
     }
-  } else if (warp >= 8) {
+  } else {
     // ------------------------------- epilogue -------------------------------
-    const int row = (warp - 8) * 32 + lane;
+    const int row = (warp & 3) * 32 + lane;
     const int tk = row >> 4, hh = row & 15;
-    const uint32_t lane_base = static_cast<uint32_t>((warp - 8) * 32) << 16;
-    int T = 0;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    int T = 0, nit = 0;
     bool ok = true;
-    for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
-      const int4 item = a.items[it];
-      const int g = item.x, start = item.z, count = item.w;
+    for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x, ++nit) {
+      const int kvs = nit & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(kv_full(kvs), (nit >> 1) & 1, a.wait_ns))) {
+        ok = false;
+        break;
+      }
+      const ItemMeta& m = meta[kvs];
+      const int count = m.count, g = m.g;
       for (int t0 = 0; t0 < count; t0 += kTileTokens, ++T) {
-        const int slot = T & 1;
-        if (!__all_sync(0xffffffffu, mbar_wait(o_full(slot), (T >> 1) & 1, a.wait_ns))) {
+        const int slot = T & 1, use = T >> 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(o_full(slot), use & 1, a.wait_ns))) {
           ok = false;
           break;
         }
@@ -539,7 +578,7 @@ __global__ void __launch_bounds__(384, 1)
         const bool valid = t0 + tk < count;
         __half* dst = nullptr;
         if (valid) {
-          const int32_t e = a.list[start + t0 + tk];
+          const int32_t e = m.tok[t0 + tk];
           const int i = e >> 4, s = e & 15;
           const size_t u = (static_cast<size_t>(i - a.q0) * a.G + g) * a.k + s;
           dst = a.po + (u * kHeadsPerGroup + hh) * kDim;
@@ -550,22 +589,24 @@ __global__ void __launch_bounds__(384, 1)
           uint32_t v[32];
           tmem_ld32(oa + c * 32, v);
           tmem_ld_wait();
+          if (c == 3) {  // all of O is in registers: the slot can take the next tile
+            tc_fence_before();
+            mbar_arrive(o_empty(slot));
+          }
           if (valid) {
             uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
 #pragma unroll
-            for (int u4 = 0; u4 < 4; ++u4) {
-              uint4 w;
-              w.x = pack_f16x2(__uint_as_float(v[8 * u4 + 0]), __uint_as_float(v[8 * u4 + 1]));
-              w.y = pack_f16x2(__uint_as_float(v[8 * u4 + 2]), __uint_as_float(v[8 * u4 + 3]));
-              w.z = pack_f16x2(__uint_as_float(v[8 * u4 + 4]), __uint_as_float(v[8 * u4 + 5]));
-              w.w = pack_f16x2(__uint_as_float(v[8 * u4 + 6]), __uint_as_float(v[8 * u4 + 7]));
-              d4[u4] = w;
-            }
+            for (int u4 = 0; u4 < 4; ++u4)
+              d4[u4] = make_uint4(
+                  pack_f16x2(__uint_as_float(v[8 * u4 + 0]), __uint_as_float(v[8 * u4 + 1])),
+                  pack_f16x2(__uint_as_float(v[8 * u4 + 2]), __uint_as_float(v[8 * u4 + 3])),
+                  pack_f16x2(__uint_as_float(v[8 * u4 + 4]), __uint_as_float(v[8 * u4 + 5])),
+                  pack_f16x2(__uint_as_float(v[8 * u4 + 6]), __uint_as_float(v[8 * u4 + 7])));
           }
         }
-        tc_fence_before();
-        mbar_arrive(o_empty(slot));
       }
+      if (!ok) break;
+      mbar_arrive(meta_empty(kvs));
     }
     if (!ok) {
       report_status(a.status, kStatusTimeout);
@@ -673,7 +714,8 @@ cudaError_t launch_attn_prefill_chunk(const CUtensorMap& map_q, const CUtensorMa
                                       const CUtensorMap& map_v, const int32_t* sel, int64_t L,
                                       int G, int k, float scale, int64_t q0, int64_t q1,
                                       uint8_t* ws, const PrefillWorkspace& w, void* o, float* lse,
-                                      uint64_t wait_ns, int num_sms, cudaStream_t stream) {
+                                      uint64_t wait_ns, int num_sms, cudaStream_t stream,
+                                      cudaEvent_t* marks) {
   SchedArgs s{};
   s.sel = sel;
   s.L = L;
@@ -701,6 +743,7 @@ cudaError_t launch_attn_prefill_chunk(const CUtensorMap& map_q, const CUtensorMa
       return e;
   }
   const dim3 qgrid(s.nbq, G);
+  if (marks && marks[0]) cudaEventRecord(marks[0], stream);
   sched_hist_kernel<<<qgrid, kBlock, mask_smem, stream>>>(s);
   const int pairs = G * s.nbk;
   sched_scan_kernel<<<(pairs * 32 + 255) / 256, 256, 0, stream>>>(s);
@@ -726,7 +769,8 @@ cudaError_t launch_attn_prefill_chunk(const CUtensorMap& map_q, const CUtensorMa
                                 kAttnSmem)) != cudaSuccess)
     return e;
   const int grid = static_cast<int>(std::min<int64_t>(w.max_items, num_sms));
-  attn_kv_outer_kernel<<<grid, 384, kAttnSmem, stream>>>(map_q, map_k, map_v, a);
+  if (marks && marks[1]) cudaEventRecord(marks[1], stream);
+  attn_kv_outer_kernel<<<grid, 512, kAttnSmem, stream>>>(map_q, map_k, map_v, a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   CombineArgs c{};
@@ -741,6 +785,7 @@ cudaError_t launch_attn_prefill_chunk(const CUtensorMap& map_q, const CUtensorMa
   c.nrows = static_cast<int32_t>(q1 - q0);
   c.o = reinterpret_cast<__nv_bfloat16*>(o);
   c.lse = lse;
+  if (marks && marks[2]) cudaEventRecord(marks[2], stream);
   combine_kernel<<<dim3(c.nrows, G), 128, 0, stream>>>(c);
   return cudaGetLastError();
 }

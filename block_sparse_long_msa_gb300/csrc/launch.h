@@ -24,6 +24,7 @@ cudaError_t launch_attn_prefill_chunk(const CUtensorMap& map_q, const CUtensorMa
                                       const CUtensorMap& map_v, const int32_t* sel, int64_t L,
                                       int G, int k, float scale, int64_t q0, int64_t q1,
                                       uint8_t* ws, const PrefillWorkspace& w, void* o, float* lse,
-                                      uint64_t wait_ns, int num_sms, cudaStream_t stream);
+                                      uint64_t wait_ns, int num_sms, cudaStream_t stream,
+                                      cudaEvent_t* marks);
 
 }  // namespace msa

@@ -168,9 +168,21 @@ size_t msa_attn_prefill_workspace(const msa_config_t* cfg, int64_t L) {
   return msa::prefill_workspace_layout(L, cfg->num_groups, cfg->topk, prefill_chunk(L)).total;
 }
 
+int64_t msa_prefill_chunk_tokens(const msa_config_t* cfg, int64_t L) {
+  if (check_config(cfg) != MSA_OK || L <= 0) return 0;
+  return prefill_chunk(L);
+}
+
 msa_status_t msa_attn_prefill(const msa_config_t* cfg, const void* q, const void* k,
                               const void* v, int64_t L, const int32_t* sel, void* o, float* lse,
                               void* ws, size_t ws_bytes, cudaStream_t stream) {
+  return msa_attn_prefill_marked(cfg, q, k, v, L, sel, o, lse, ws, ws_bytes, stream, nullptr, 0);
+}
+
+msa_status_t msa_attn_prefill_marked(const msa_config_t* cfg, const void* q, const void* k,
+                                     const void* v, int64_t L, const int32_t* sel, void* o,
+                                     float* lse, void* ws, size_t ws_bytes, cudaStream_t stream,
+                                     cudaEvent_t* marks, int32_t n_marks) {
   msa_status_t st = check_config(cfg);
   if (st != MSA_OK) return st;
   if (!q || !k || !v || !sel || !o || !lse || !ws || L < 0) return MSA_ERR_INVALID_ARG;
@@ -201,14 +213,21 @@ msa_status_t msa_attn_prefill(const msa_config_t* cfg, const void* q, const void
     return MSA_ERR_CUDA;
   const int64_t chunk = prefill_chunk(L);
   const msa::PrefillWorkspace w = msa::prefill_workspace_layout(L, G, cfg->topk, chunk);
-  for (int64_t q0 = 0; q0 < L; q0 += chunk) {
+  int32_t c = 0;
+  for (int64_t q0 = 0; q0 < L; q0 += chunk, ++c) {
     const int64_t q1 = q0 + chunk < L ? q0 + chunk : L;
+    cudaEvent_t m3[3] = {nullptr, nullptr, nullptr};
+    for (int j = 0; j < 3; ++j)
+      if (marks && 3 * c + j < n_marks) m3[j] = marks[3 * c + j];
     cudaError_t e = msa::launch_attn_prefill_chunk(mq, mk, mv, sel, L, G, cfg->topk,
                                                    cfg->softmax_scale, q0, q1,
                                                    static_cast<uint8_t*>(ws), w, o, lse,
-                                                   wait_ns(cfg), sms, stream);
+                                                   wait_ns(cfg), sms, stream, m3);
     if (e != cudaSuccess) return MSA_ERR_CUDA;
   }
+  if (marks && 3 * c < n_marks && marks[3 * c] &&
+      cudaEventRecord(marks[3 * c], stream) != cudaSuccess)
+    return MSA_ERR_CUDA;
   return MSA_OK;
 }
 

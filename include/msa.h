@@ -117,6 +117,21 @@ msa_status_t msa_attn_prefill(const msa_config_t* cfg, const void* q, const void
                               const void* v, int64_t L, const int32_t* sel, void* o, float* lse,
                               void* ws, size_t ws_bytes, cudaStream_t stream);
 
+/*
+ * Instrumented form of msa_attn_prefill, for timing its phases; results are identical.
+ * marks (may be NULL) are caller-created CUDA events (timing enabled).  On `stream` the call
+ * records, for query chunk c: marks[3c] before the scheduling kernels, marks[3c+1] before the
+ * attention kernel, marks[3c+2] before the combine kernel, and marks[3*chunks] after the last
+ * combine.  Recording stops after n_marks events.  Chunks are msa_prefill_chunk_tokens() long.
+ */
+msa_status_t msa_attn_prefill_marked(const msa_config_t* cfg, const void* q, const void* k,
+                                     const void* v, int64_t L, const int32_t* sel, void* o,
+                                     float* lse, void* ws, size_t ws_bytes, cudaStream_t stream,
+                                     cudaEvent_t* marks, int32_t n_marks);
+
+/* Query tokens per main-branch pass of msa_attn_prefill (its workspace covers one pass). */
+int64_t msa_prefill_chunk_tokens(const msa_config_t* cfg, int64_t L);
+
 /* Workspace bytes for msa_attn_decode on this cache shape. */
 size_t msa_attn_decode_workspace(const msa_config_t* cfg, const msa_paged_kv_t* paged);
 

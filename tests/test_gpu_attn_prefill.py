@@ -50,6 +50,7 @@ def compare(w, inp, sel, o, lse, rows=None):
     assert err.max() <= MAX_ABS and err.mean() <= MEAN_ABS, msg
     assert lerr.max() <= MAX_ABS and lerr.mean() <= MEAN_ABS, msg
     assert np.isfinite(o).all() and np.isfinite(lse).all()
+    print(f"[parity {w.name} L={w.L}] {msg}")
     return err.max(), err.mean()
 
 

@@ -516,18 +516,19 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
           for (int q = 0; q < 32; ++q)
             if (c * 32 + q <= lim) m2 = fmaxf(m2, __uint_as_float(v[q]) * a.scale_log2);
+          asm volatile("" : "+f"(m2));  // finish this chunk before the next TMEM load
         }
-        // pass 2: p = exp2(t - m2) -> fp16 pairs; keys [32c, 32c+32) go to columns
-        // [16c, 16c+16), which hold S values this thread has already read
+        // pass 2: p = exp2(t - m2) -> fp16 pairs; keys [16c, 16c+16) go to columns
+        // [8c, 8c+8), which hold S values this thread has already read
         float l = 0.f;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t v[32], pk[16];
-          tmem_ld32(sa + c * 32, v);
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          uint32_t v[16], pk[8];
+          tmem_ld16(sa + c * 16, v);
           tmem_ld_wait();
 #pragma unroll
-          for (int q = 0; q < 32; q += 2) {
-            const int j = c * 32 + q;
+          for (int q = 0; q < 16; q += 2) {
+            const int j = c * 16 + q;
             const float p0 =
                 j <= lim ? fast_exp2(fmaf(__uint_as_float(v[q]), a.scale_log2, -m2)) : 0.f;
             const float p1 =
@@ -536,7 +537,7 @@ __global__ void __launch_bounds__(512, 1)
             l += p0 + p1;
             pk[q >> 1] = pack_f16x2(p0, p1);
           }
-          tmem_st16(sa + c * 16, pk);
+          tmem_st8(sa + c * 8, pk);
         }
         tmem_st_wait();
         tc_fence_before();

@@ -132,6 +132,38 @@ msa_status_t msa_attn_prefill_marked(const msa_config_t* cfg, const void* q, con
 /* Query tokens per main-branch pass of msa_attn_prefill (its workspace covers one pass). */
 int64_t msa_prefill_chunk_tokens(const msa_config_t* cfg, int64_t L);
 
+/*
+ * msa_attn_prefill_noalloc — msa_attn_prefill for callers that cannot allocate device memory.
+ * (The paper has no counterpart: this is a deployment convenience of this library.)
+ *
+ * Some callers are handed only their input and output tensors and are not allowed to allocate:
+ * a plugin or callback inside another framework's memory pool, code on a latency-critical path
+ * where cudaMalloc (which can synchronize the device) is forbidden, or an engine whose device
+ * memory budget is fixed ahead of time.  This entry point needs no workspace from them: its
+ * scratch is a library-owned static device array of MSA_NOALLOC_SCRATCH_BYTES (64 MiB), which
+ * every GPU that loads libmsa holds until the process exits.  The call itself allocates nothing
+ * (no cudaMalloc, no cudaFree, no allocating library routine).
+ *
+ *   Arguments are those of msa_attn_prefill without ws/ws_bytes; outputs are identical.
+ *   device_status (optional, device pointer to one int32): receives the device status word of
+ *     this call (0, MSA_ERR_DEVICE_TIMEOUT or MSA_ERR_DEVICE_BOUNDS) when the call's work has run.
+ *   Queries are processed in passes sized to fit the scratch (128 queries per pass at G = 4,
+ *     k = 16), so long prefills run slower than msa_attn_prefill with a full workspace.
+ *   Sizes beyond what the scratch or the kernels can take (L above 1,572,864 tokens, or a
+ *     configuration whose 128-query pass would not fit) return MSA_ERR_UNSUPPORTED before
+ *     anything is enqueued.
+ *   The first call on each device looks up the device address of the scratch array
+ *     (cudaGetSymbolAddress, with that device current); make that first call before any stream
+ *     capture.
+ *   All calls share the one array, which keeps the last call's contents; the call clears what
+ *     must start at zero.  Calls that overlap on the GPU (different streams, concurrent host
+ *     threads) race on it: issue them in order on one stream.
+ */
+#define MSA_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+msa_status_t msa_attn_prefill_noalloc(const msa_config_t* cfg, const void* q, const void* k,
+                                      const void* v, int64_t L, const int32_t* sel, void* o,
+                                      float* lse, int32_t* device_status, cudaStream_t stream);
+
 /* Workspace bytes for msa_attn_decode on this cache shape. */
 size_t msa_attn_decode_workspace(const msa_config_t* cfg, const msa_paged_kv_t* paged);
 

@@ -1,0 +1,68 @@
+"""msa_attn_prefill_noalloc, the entry point for callers that cannot allocate device memory
+(they are handed only inputs and outputs), must give the same result as msa_attn_prefill with a
+caller workspace.  It is called through the C ABI twice in a row: the second call reuses the
+library's static scratch that the first one left behind.
+
+This file sorts last so that a run stopping at the first failure has run every other test.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import synthetic
+
+pytestmark = pytest.mark.gpu
+
+MAX_ABS, MEAN_ABS = 1e-2, 1e-3  # the tolerance of the other prefill parity tests
+
+
+def _p(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def test_noalloc_matches_workspace_entry_point_twice():
+    import block_sparse_long_msa_gb300 as msa
+    lib = msa.lib()
+    fn = lib.msa_attn_prefill_noalloc
+    fn.argtypes = [ctypes.POINTER(msa.MsaConfig)] + [ctypes.c_void_p] * 3 + [ctypes.c_int64] + \
+        [ctypes.c_void_p] * 5
+    fn.restype = ctypes.c_int
+    base = synthetic.WORKLOADS["prefill_L32K"]
+    # several 128-query passes per call, a ragged tail, and two different inputs in a row
+    for call, (L, seed) in enumerate([(1100, 501), (777, 502)]):
+        w = synthetic.Workload(**{**base.__dict__, "L": L, "seed": seed})
+        inp = synthetic.prefill_inputs(w, device="cuda")
+        cfg = msa.config(w.G, w.hpg, w.k, w.scale)
+        sel = msa.msa_index_select(cfg, inp["q_idx"], inp["k_idx"])
+        o_ref, lse_ref = msa.msa_attn_prefill(cfg, inp["q"], inp["k"], inp["v"], sel)
+        o = torch.full_like(o_ref, float("nan"))
+        lse = torch.full_like(lse_ref, float("nan"))
+        status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+        stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        rc = fn(ctypes.byref(cfg), _p(inp["q"]), _p(inp["k"]), _p(inp["v"]), L, _p(sel), _p(o),
+                _p(lse), _p(status), stream)
+        assert rc == msa.MSA_OK, msa.status_string(rc)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0, f"call {call}: device status {int(status.item())}"
+        err = (o.float() - o_ref.float()).abs()
+        lerr = (lse - lse_ref).abs()
+        assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
+        assert err.max().item() <= MAX_ABS and err.mean().item() <= MEAN_ABS, (call, err.max())
+        assert lerr.max().item() <= MAX_ABS and lerr.mean().item() <= MEAN_ABS, (call, lerr.max())
+
+
+def test_noalloc_rejects_oversized_problem():
+    import block_sparse_long_msa_gb300 as msa
+    lib = msa.lib()
+    fn = lib.msa_attn_prefill_noalloc
+    fn.argtypes = [ctypes.POINTER(msa.MsaConfig)] + [ctypes.c_void_p] * 3 + [ctypes.c_int64] + \
+        [ctypes.c_void_p] * 5
+    fn.restype = ctypes.c_int
+    cfg = msa.config(4, 16, 16)
+    x = torch.zeros(64, dtype=torch.int32, device="cuda")  # never read: rejected on the host
+    rc = fn(ctypes.byref(cfg), _p(x), _p(x), _p(x), 2 * 1536 * 1024, _p(x), _p(x), _p(x), None,
+            None)
+    assert rc == msa.MSA_ERR_UNSUPPORTED
+    assert np.isfinite(1.0)

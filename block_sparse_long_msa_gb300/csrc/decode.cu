@@ -1,0 +1,710 @@
+// Paged decode: one query per sequence at position n-1 over a cache of 128-token pages.
+//
+//   index branch ("MiniMax M3 算力省 20 倍", section 二; paged decode as named on the page about
+//   serving MSA): every index-key page strictly before the query's page is scored against the
+//   sequence's G index queries and max-pooled, then each (sequence, group) keeps its top-(k-1)
+//   blocks plus the local block (section 四: exp-free top-k, lanes each stream 1/32 of the row
+//   and their lists are merged with warp shuffles).
+//   main branch: exact softmax attention of the 16 query heads of a group over the selected
+//   pages (causal inside the local page), one partial per (sequence, group, slot), merged by a
+//   log-sum-exp combine.
+//
+// The scan is the dominant stream of this step (every index key of every sequence, 32 KiB per
+// page); it is fed by TMA into a deep shared-memory ring and scored by tcgen05 with the page as
+// the 128-row A operand, so the SM's issue slots stay free for the max-pool.
+#include <algorithm>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace msa {
+
+namespace {
+
+constexpr int kHeads = 16;  // query heads per group
+constexpr int kPagesPerChunk = 16;
+constexpr int kScanStages = 6;
+constexpr uint32_t kScanStage = 32768 + 4096;  // 128 keys x 128 bf16 + the 16-row query tile
+constexpr int kScanSlots = 8;                  // TMEM accumulators of 16 columns
+// barrier block after the stages: full[6], empty[6], acc_full[8], acc_empty[8], drain, then the
+// TMEM base address and the abort flag
+constexpr uint32_t kScanBarFull = 0, kScanBarEmpty = 64, kScanBarAccFull = 128,
+                   kScanBarAccEmpty = 192, kScanBarDrain = 256, kScanTmemSlot = 264,
+                   kScanAbort = 268, kScanBarBytes = 512;
+static_assert(kScanBarFull + 8 * kScanStages <= kScanBarEmpty, "scan barriers");
+static_assert(kScanBarEmpty + 8 * kScanStages <= kScanBarAccFull, "scan barriers");
+static_assert(kScanBarAccFull + 8 * kScanSlots <= kScanBarAccEmpty, "scan barriers");
+static_assert(kScanBarAccEmpty + 8 * kScanSlots <= kScanBarDrain, "scan barriers");
+static_assert(kScanAbort + 4 <= kScanBarBytes, "scan barriers");
+constexpr uint32_t kScanSmem = kScanStages * kScanStage + kScanBarBytes + 1024;
+static_assert(kScanSmem <= 232448, "scan shared memory");
+constexpr uint32_t kIdescScan = idesc_bf16_f32(128, 16, false, false);
+constexpr uint32_t kPanel = 16384;
+
+struct ScanArgs {
+  const int32_t* page_table;
+  const int32_t* seq_lens;
+  int32_t batch, max_pages, num_pages, G;
+  int32_t cps;       // chunks of kPagesPerChunk pages per sequence
+  int32_t n_chunks;  // batch * cps
+  float4* scores;    // [batch][G][max_pages]: per-warp maxima of the 4 epilogue warps
+  int32_t* status;
+  uint64_t wait_ns;
+};
+
+// The page sequence every role of a CTA walks identically: chunks blockIdx.x, +gridDim.x, ...;
+// inside a chunk the pages that lie strictly before the query's page.
+struct PageWalk {
+  int chunk, b, bend, s;
+  __device__ __forceinline__ void init() {
+    chunk = static_cast<int>(blockIdx.x) - static_cast<int>(gridDim.x);
+    b = bend = 0;
+    s = 0;
+  }
+  // Advances to the next page; returns its logical block id, or -1 at the end.
+  __device__ __forceinline__ int next(const ScanArgs& a) {
+    while (b >= bend) {
+      chunk += gridDim.x;
+      if (chunk >= a.n_chunks) return -1;
+      s = chunk / a.cps;
+      const int b0 = (chunk % a.cps) * kPagesPerChunk;
+      const int n = a.seq_lens[s];
+      int bi = n > 0 ? (n - 1) / kBlock : 0;
+      bi = min(bi, a.max_pages);
+      b = b0;
+      bend = min(b0 + kPagesPerChunk, bi);
+    }
+    return b++;
+  }
+};
+
+__global__ void __launch_bounds__(256, 1)
+    decode_scan_kernel(const __grid_constant__ CUtensorMap map_k,
+                       const __grid_constant__ CUtensorMap map_q, ScanArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t base = smem_u32(smem);
+  const uint32_t bars = base + kScanStages * kScanStage;
+  auto full = [&](int s) { return bars + kScanBarFull + 8 * s; };
+  auto empty = [&](int s) { return bars + kScanBarEmpty + 8 * s; };
+  auto acc_full = [&](int t) { return bars + kScanBarAccFull + 8 * t; };
+  auto acc_empty = [&](int t) { return bars + kScanBarAccEmpty + 8 * t; };
+  const uint32_t drain_bar = bars + kScanBarDrain;
+  volatile uint32_t* tmem_slot =
+      reinterpret_cast<volatile uint32_t*>(smem + kScanStages * kScanStage + kScanTmemSlot);
+  volatile int32_t* abort_flag =
+      reinterpret_cast<volatile int32_t*>(smem + kScanStages * kScanStage + kScanAbort);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // rows G..15 of every stage's query tile stay zero (TMA writes rows 0..G-1 only)
+  for (int st = 0; st < kScanStages; ++st) {
+    uint32_t* qt = reinterpret_cast<uint32_t*>(smem + st * kScanStage + 32768);
+    for (int w = threadIdx.x; w < 1024; w += blockDim.x) qt[w] = 0;
+  }
+  fence_proxy_async_smem();
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kScanStages; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+    }
+    for (int t = 0; t < kScanSlots; ++t) {
+      mbar_init(acc_full(t), 1);
+      mbar_init(acc_empty(t), 128);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), 128);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_map(&map_k);
+      tma_prefetch_map(&map_q);
+      PageWalk w;
+      w.init();
+      int p = 0;
+      for (int b = w.next(a); b >= 0; b = w.next(a), ++p) {
+        const int st = p % kScanStages;
+        if (*abort_flag || !mbar_wait(empty(st), ((p / kScanStages) & 1) ^ 1, a.wait_ns)) {
+          report_status(a.status, kStatusTimeout);
+          *abort_flag = 1;
+          break;
+        }
+        int page = a.page_table[static_cast<size_t>(w.s) * a.max_pages + b];
+        if (page < 0 || page >= a.num_pages) {
+          report_status(a.status, kStatusBounds);
+          page = 0;  // keep the pipeline in step; the status word marks the result invalid
+        }
+        const uint32_t sb = base + st * kScanStage;
+        mbar_arrive_expect_tx(full(st), 32768 + a.G * 256);
+        tma_load_2d(sb, &map_k, full(st), 0, page * kBlock);
+        tma_load_2d(sb + kPanel, &map_k, full(st), 64, page * kBlock);
+        tma_load_2d(sb + 32768, &map_q, full(st), 0, w.s * a.G);
+        tma_load_2d(sb + 32768 + 2048, &map_q, full(st), 64, w.s * a.G);
+      }
+      if (*abort_flag) {
+        for (int x = (p > kScanStages ? p - kScanStages : 0); x < p; ++x)
+          mbar_wait(full(x % kScanStages), (x / kScanStages) & 1, a.wait_ns);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      PageWalk w;
+      w.init();
+      int p = 0;
+      bool ok = true;
+      for (int b = w.next(a); b >= 0; b = w.next(a), ++p) {
+        const int st = p % kScanStages, slot = p % kScanSlots;
+        if (*abort_flag || !mbar_wait(full(st), (p / kScanStages) & 1, a.wait_ns) ||
+            !mbar_wait(acc_empty(slot), ((p / kScanSlots) & 1) ^ 1, a.wait_ns)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sb = base + st * kScanStage;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t ad = sdesc_sw128(sb + (kk >> 2) * kPanel + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd =
+              sdesc_sw128(sb + 32768 + (kk >> 2) * 2048 + (kk & 3) * 32, 16, 1024);
+          mma_bf16_ss(tmem + slot * 16, ad, bd, kIdescScan, kk > 0);
+        }
+        mma_commit(acc_full(slot));
+        mma_commit(empty(st));
+      }
+      if (!ok) {
+        report_status(a.status, kStatusTimeout);
+        *abort_flag = 1;
+      }
+      mma_commit(drain_bar);
+      mbar_wait(drain_bar, 0, a.wait_ns);
+    }
+  } else if (warp >= 4) {
+    // epilogue: thread = key of the page; the warp's max over its 32 keys per group
+    const int ew = warp - 4;
+    const uint32_t lane_base = static_cast<uint32_t>(ew * 32) << 16;
+    PageWalk w;
+    w.init();
+    int p = 0;
+    for (int b = w.next(a); b >= 0; b = w.next(a), ++p) {
+      const int slot = p % kScanSlots;
+      if (!__all_sync(0xffffffffu, mbar_wait(acc_full(slot), (p / kScanSlots) & 1, a.wait_ns))) {
+        report_status(a.status, kStatusTimeout);
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      uint32_t v[4];
+      tmem_ld4(tmem + lane_base + slot * 16, v);
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(acc_empty(slot));
+      float m[4];
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        m[g] = __uint_as_float(v[g]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m[g] = fmaxf(m[g], __shfl_xor_sync(0xffffffffu, m[g], o));
+      }
+      if (lane < a.G) {
+        float* dst = reinterpret_cast<float*>(
+            a.scores + (static_cast<size_t>(w.s) * a.G + lane) * a.max_pages + b);
+        dst[ew] = lane == 0 ? m[0] : lane == 1 ? m[1] : lane == 2 ? m[2] : m[3];
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 128);
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// Top-k: one warp per (sequence, group).  Lane l streams blocks l, l+32, ... (ascending, so the
+// strict rank test keeps the tie rule), then k-1 rounds of a warp arg-max pop the winners.
+// ------------------------------------------------------------------------------------------
+struct TopkArgs {
+  const float4* scores;
+  const int32_t* seq_lens;
+  int32_t batch, max_pages, G, k;
+  int32_t* sel;       // [G][batch][k]
+  float* sel_score;   // optional, same shape
+  int32_t* status;
+};
+
+__global__ void __launch_bounds__(128) decode_topk_kernel(TopkArgs a) {
+  const int wg = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (wg >= a.batch * a.G) return;
+  const int s = wg / a.G, g = wg % a.G;
+  const int n = a.seq_lens[s];
+  int32_t* out = a.sel + (static_cast<size_t>(g) * a.batch + s) * a.k;
+  float* out_s = a.sel_score ? a.sel_score + (static_cast<size_t>(g) * a.batch + s) * a.k : nullptr;
+  if (n <= 0 || (n - 1) / kBlock >= a.max_pages) {
+    if (lane == 0) report_status(a.status, kStatusBounds);
+    for (int r = lane; r < a.k; r += 32) {
+      out[r] = -1;
+      if (out_s) out_s[r] = -__int_as_float(0x7f800000);
+    }
+    return;
+  }
+  const int bi = (n - 1) / kBlock;
+  TopList list;
+  list.clear();
+  const float4* row = a.scores + (static_cast<size_t>(s) * a.G + g) * a.max_pages;
+  for (int b = lane; b < bi; b += 32) {
+    const float4 v = row[b];
+    list.insert(fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)), b);
+  }
+  const int take = min(a.k - 1, bi);
+  int my_id = 0x7fffffff;
+  float my_sc = 0.f;
+  for (int r = 0; r < take; ++r) {
+    float bs = list.s[0];
+    int bb = list.b[0];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float os = __shfl_xor_sync(0xffffffffu, bs, o);
+      const int ob = __shfl_xor_sync(0xffffffffu, bb, o);
+      if (ranks_before(os, ob, bs, bb)) {
+        bs = os;
+        bb = ob;
+      }
+    }
+    if (list.b[0] == bb) {  // the winner pops its head (block ids are unique)
+#pragma unroll
+      for (int q = 0; q + 1 < kListMax; ++q) {
+        list.s[q] = list.s[q + 1];
+        list.b[q] = list.b[q + 1];
+      }
+      list.s[kListMax - 1] = -__int_as_float(0x7f800000);
+      list.b[kListMax - 1] = 0x7fffffff;
+    }
+    if (lane == r) {
+      my_id = bb;
+      my_sc = bs;
+    }
+  }
+  // lanes 0..take-1 hold the winners; place each at its rank by block id
+  int rank = 0;
+  for (int q = 0; q < take; ++q) {
+    const int other = __shfl_sync(0xffffffffu, my_id, q);
+    rank += other < my_id;
+  }
+  if (lane < take) {
+    out[rank] = my_id;
+    if (out_s) out_s[rank] = my_sc;
+  }
+  for (int r = take + lane; r < a.k; r += 32) {
+    out[r] = r == take ? bi : -1;
+    if (out_s) out_s[r] = r == take ? __int_as_float(0x7f800000) : -__int_as_float(0x7f800000);
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// Decode attention: one unit per (sequence, group, slot).  A persistent CTA takes a contiguous
+// range of units; warp 0 stages each unit's K and V page tiles (TMA, 128-byte swizzle), warps
+// 1-4 each take 32 keys: S = q K^T and O = P V with m16n8k16 MMAs (M = the group's 16 heads),
+// then the four warps' partial softmax states are merged in shared memory.
+// ------------------------------------------------------------------------------------------
+struct DecAttnArgs {
+  const __nv_bfloat16* q;  // [batch][G*16][128]
+  const int32_t* sel;      // [G][batch][k]
+  const int32_t* page_table;
+  const int32_t* seq_lens;
+  int32_t batch, max_pages, num_pages, G, k;
+  int32_t units, per_cta;
+  float scale_log2;
+  float* po;    // [unit][16][128] normalised partial O
+  float* plse;  // [unit][16] log-sum-exp (-inf for empty units)
+  int32_t* status;
+  uint64_t wait_ns;
+};
+
+constexpr int kDecStages = 2;
+constexpr uint32_t kDecStage = 65536;
+constexpr uint32_t kDecRed = kDecStages * kDecStage;          // 4 warps x 16 x 128 fp32
+constexpr uint32_t kDecML = kDecRed + 4 * kHeads * kDim * 4;  // 4 warps x 16 x (m, l)
+constexpr uint32_t kDecBar = kDecML + 4 * kHeads * 8;
+constexpr uint32_t kDecSmem = kDecBar + 128 + 1024;
+
+struct UnitInfo {
+  int s, g, b, page, lim;
+  bool valid;
+};
+
+__device__ __forceinline__ UnitInfo unit_info(const DecAttnArgs& a, int u, bool flag) {
+  UnitInfo x;
+  x.s = u / (a.G * a.k);
+  x.g = (u / a.k) % a.G;
+  const int t = u % a.k;
+  x.b = a.sel[(static_cast<size_t>(x.g) * a.batch + x.s) * a.k + t];
+  const int n = a.seq_lens[x.s];
+  const int bi = n > 0 ? (n - 1) / kBlock : -1;
+  x.valid = x.b >= 0 && x.b <= bi && x.b < a.max_pages;
+  x.page = 0;
+  if (x.valid) {
+    x.page = a.page_table[static_cast<size_t>(x.s) * a.max_pages + x.b];
+    if (x.page < 0 || x.page >= a.num_pages) x.valid = false;
+  }
+  if (flag && !x.valid && x.b >= 0) report_status(a.status, kStatusBounds);
+  x.lim = x.valid ? min(n - 1 - x.b * kBlock, kBlock - 1) : -1;
+  return x;
+}
+
+__device__ __forceinline__ uint32_t swz(uint32_t tile, int row, int chunk) {
+  return tile + (chunk >> 3) * kPanel + row * 128 + (((chunk & 7) ^ (row & 7)) << 4);
+}
+
+__global__ void __launch_bounds__(160, 1)
+    decode_attn_kernel(const __grid_constant__ CUtensorMap map_kp,
+                       const __grid_constant__ CUtensorMap map_vp, DecAttnArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t base = smem_u32(smem);
+  const uint32_t bars = base + kDecBar;
+  auto full = [&](int s) { return bars + 8 * s; };
+  auto empty = [&](int s) { return bars + 16 + 8 * s; };
+  volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + kDecBar + 32);
+  float* red = reinterpret_cast<float*>(smem + kDecRed);
+  float* ml = reinterpret_cast<float*>(smem + kDecML);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int u0 = blockIdx.x * a.per_cta, u1 = min(a.units, u0 + a.per_cta);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kDecStages; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 4);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_map(&map_kp);
+      tma_prefetch_map(&map_vp);
+      int p = 0;
+      for (int u = u0; u < u1; ++u) {
+        const UnitInfo x = unit_info(a, u, true);
+        if (!x.valid) continue;
+        const int st = p % kDecStages;
+        if (*abort_flag || !mbar_wait(empty(st), ((p / kDecStages) & 1) ^ 1, a.wait_ns)) {
+          report_status(a.status, kStatusTimeout);
+          *abort_flag = 1;
+          break;
+        }
+        const uint32_t sb = base + st * kDecStage;
+        const int row0 = (x.page * a.G + x.g) * kBlock;
+        mbar_arrive_expect_tx(full(st), kDecStage);
+        tma_load_2d(sb, &map_kp, full(st), 0, row0);
+        tma_load_2d(sb + kPanel, &map_kp, full(st), 64, row0);
+        tma_load_2d(sb + 32768, &map_vp, full(st), 0, row0);
+        tma_load_2d(sb + 32768 + kPanel, &map_vp, full(st), 64, row0);
+        ++p;
+      }
+      if (*abort_flag) {
+        for (int x = (p > kDecStages ? p - kDecStages : 0); x < p; ++x)
+          mbar_wait(full(x % kDecStages), (x / kDecStages) & 1, a.wait_ns);
+      }
+    }
+    return;  // the producer takes no part in the compute warps' named barriers
+  }
+
+  // ------------------------------ compute warps 1..4 ------------------------------
+  const int w = warp - 1;
+  const int gid = lane >> 2, tq = lane & 3;
+  uint32_t qa[8][4];
+  int cur_sg = -1;
+  int p = 0;
+  for (int u = u0; u < u1; ++u) {
+    const UnitInfo x = unit_info(a, u, false);
+    if (!x.valid) {
+      if (w == 0 && lane < kHeads)
+        a.plse[static_cast<size_t>(u) * kHeads + lane] = -__int_as_float(0x7f800000);
+      continue;
+    }
+    const int sg = x.s * a.G + x.g;
+    if (sg != cur_sg) {  // query fragments of this (sequence, group), straight from global
+      const uint32_t* q32 = reinterpret_cast<const uint32_t*>(a.q + static_cast<size_t>(sg) *
+                                                                        kHeads * kDim);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        qa[kk][0] = q32[(gid * kDim + kk * 16 + tq * 2) >> 1];
+        qa[kk][1] = q32[((gid + 8) * kDim + kk * 16 + tq * 2) >> 1];
+        qa[kk][2] = q32[(gid * kDim + kk * 16 + 8 + tq * 2) >> 1];
+        qa[kk][3] = q32[((gid + 8) * kDim + kk * 16 + 8 + tq * 2) >> 1];
+      }
+      cur_sg = sg;
+    }
+    const int st = p % kDecStages;
+    bool ok = !*abort_flag && mbar_wait(full(st), (p / kDecStages) & 1, a.wait_ns);
+    if (!__all_sync(0xffffffffu, ok)) {
+      if (lane == 0) report_status(a.status, kStatusTimeout);
+      *abort_flag = 1;  // keep going with whatever is in the buffer: every warp still meets
+                        // the same barriers, and the status word marks the output invalid
+    }
+    const uint32_t kt = base + st * kDecStage, vt = kt + 32768;
+    // S = q K^T over this warp's 32 keys: 4 n-tiles of 8 keys
+    float sacc[4][4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sacc[j][e] = 0.f;
+      const int key = w * 32 + j * 8 + (lane & 7);
+#pragma unroll
+      for (int kk = 0; kk < 8; kk += 2) {
+        uint32_t r[4];
+        ldmatrix_x4(swz(kt, key, 2 * kk + (lane >> 3)), r);
+        mma_m16n8k16_bf16(sacc[j], qa[kk], r[0], r[1]);
+        mma_m16n8k16_bf16(sacc[j], qa[kk + 1], r[2], r[3]);
+      }
+    }
+    // scale, causal limit, row max (rows gid and gid+8), quad reduction
+    float m0 = -__int_as_float(0x7f800000), m1 = m0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int key = w * 32 + j * 8 + tq * 2 + (e & 1);
+        const float z = key <= x.lim ? sacc[j][e] * a.scale_log2 : -__int_as_float(0x7f800000);
+        sacc[j][e] = z;
+        if (e < 2) m0 = fmaxf(m0, z);
+        else m1 = fmaxf(m1, z);
+      }
+    }
+    m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 1));
+    m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 2));
+    m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 1));
+    m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 2));
+    const float b0 = m0 == -__int_as_float(0x7f800000) ? 0.f : m0;
+    const float b1 = m1 == -__int_as_float(0x7f800000) ? 0.f : m1;
+    float l0 = 0.f, l1 = 0.f;
+    uint32_t pa[2][4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float p0 = exp2f(sacc[j][0] - b0), p1 = exp2f(sacc[j][1] - b0);
+      const float p2 = exp2f(sacc[j][2] - b1), p3 = exp2f(sacc[j][3] - b1);
+      l0 += p0 + p1;
+      l1 += p2 + p3;
+      pa[j >> 1][(j & 1) * 2 + 0] = pack_bf16x2(p0, p1);
+      pa[j >> 1][(j & 1) * 2 + 1] = pack_bf16x2(p2, p3);
+    }
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    // O = P V over this warp's 32 keys: 16 n-tiles of 8 dims
+    float oacc[16][4];
+#pragma unroll
+    for (int nt = 0; nt < 16; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) oacc[nt][e] = 0.f;
+#pragma unroll
+    for (int kk2 = 0; kk2 < 2; ++kk2) {
+      const int mtx = lane >> 3;
+      const int key = w * 32 + kk2 * 16 + (mtx & 1) * 8 + (lane & 7);
+#pragma unroll
+      for (int nt = 0; nt < 16; nt += 2) {
+        uint32_t r[4];
+        ldmatrix_x4_trans(swz(vt, key, nt + (mtx >> 1)), r);
+        mma_m16n8k16_bf16(oacc[nt], pa[kk2], r[0], r[1]);
+        mma_m16n8k16_bf16(oacc[nt + 1], pa[kk2], r[2], r[3]);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty(st));
+    ++p;
+    // merge the four warps' states: (m, l) per row and O in shared memory
+    if (tq == 0) {
+      ml[(w * kHeads + gid) * 2] = m0;
+      ml[(w * kHeads + gid) * 2 + 1] = l0;
+      ml[(w * kHeads + gid + 8) * 2] = m1;
+      ml[(w * kHeads + gid + 8) * 2 + 1] = l1;
+    }
+#pragma unroll
+    for (int nt = 0; nt < 16; ++nt) {
+      float* r0 = red + (w * kHeads + gid) * kDim + nt * 8 + tq * 2;
+      float* r1 = red + (w * kHeads + gid + 8) * kDim + nt * 8 + tq * 2;
+      *reinterpret_cast<float2*>(r0) = make_float2(oacc[nt][0], oacc[nt][1]);
+      *reinterpret_cast<float2*>(r1) = make_float2(oacc[nt][2], oacc[nt][3]);
+    }
+    named_barrier(1, 128);
+    {
+      const int t = threadIdx.x - 32, h = t >> 3, d0 = (t & 7) * 16;
+      float mw[4], wt[4], M = -__int_as_float(0x7f800000);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        mw[q] = ml[(q * kHeads + h) * 2];
+        M = fmaxf(M, mw[q]);
+      }
+      float Lsum = 0.f;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        // a warp whose keys were all masked contributes nothing
+        wt[q] = mw[q] == -__int_as_float(0x7f800000) ? 0.f : exp2f(mw[q] - M);
+        Lsum += wt[q] * ml[(q * kHeads + h) * 2 + 1];
+      }
+      const float inv = 1.f / Lsum;
+      float* dst = a.po + (static_cast<size_t>(u) * kHeads + h) * kDim + d0;
+#pragma unroll
+      for (int c = 0; c < 16; c += 4) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float4 r = *reinterpret_cast<const float4*>(red + (q * kHeads + h) * kDim + d0 + c);
+          acc.x += wt[q] * r.x;
+          acc.y += wt[q] * r.y;
+          acc.z += wt[q] * r.z;
+          acc.w += wt[q] * r.w;
+        }
+        *reinterpret_cast<float4*>(dst + c) =
+            make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+      }
+      if ((t & 7) == 0)
+        a.plse[static_cast<size_t>(u) * kHeads + h] = (M + __log2f(Lsum)) * 0.6931471805599453f;
+    }
+    named_barrier(1, 128);
+  }
+}
+
+// Combine of the k slot partials of each (sequence, head): fixed slot order, no atomics.
+struct DecCombineArgs {
+  const float* po;
+  const float* plse;
+  int32_t batch, G, k;
+  __nv_bfloat16* o;  // [batch][G*16][128]
+  float* lse;        // [G*16][batch]
+};
+
+__global__ void __launch_bounds__(128) decode_combine_kernel(DecCombineArgs a) {
+  const int s = blockIdx.x, g = blockIdx.y, t = threadIdx.x, hh = t >> 3, d0 = (t & 7) * 16;
+  const size_t u0 = (static_cast<size_t>(s) * a.G + g) * a.k;
+  float M = -__int_as_float(0x7f800000);
+  for (int j = 0; j < a.k; ++j) M = fmaxf(M, a.plse[(u0 + j) * kHeads + hh]);
+  float acc[16];
+#pragma unroll
+  for (int q = 0; q < 16; ++q) acc[q] = 0.f;
+  float den = 0.f;
+  for (int j = 0; j < a.k; ++j) {
+    const float l = a.plse[(u0 + j) * kHeads + hh];
+    if (l == -__int_as_float(0x7f800000)) continue;
+    const float wgt = __expf(l - M);
+    den += wgt;
+    const float4* src = reinterpret_cast<const float4*>(a.po + ((u0 + j) * kHeads + hh) * kDim + d0);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const float4 x = src[c];
+      acc[4 * c] += wgt * x.x;
+      acc[4 * c + 1] += wgt * x.y;
+      acc[4 * c + 2] += wgt * x.z;
+      acc[4 * c + 3] += wgt * x.w;
+    }
+  }
+  const float inv = 1.f / den;
+  const int h = g * kHeads + hh;
+  uint4* dst = reinterpret_cast<uint4*>(a.o + (static_cast<size_t>(s) * a.G * kHeads + h) * kDim + d0);
+#pragma unroll
+  for (int c = 0; c < 2; ++c)
+    dst[c] = make_uint4(pack_bf16x2(acc[8 * c] * inv, acc[8 * c + 1] * inv),
+                        pack_bf16x2(acc[8 * c + 2] * inv, acc[8 * c + 3] * inv),
+                        pack_bf16x2(acc[8 * c + 4] * inv, acc[8 * c + 5] * inv),
+                        pack_bf16x2(acc[8 * c + 6] * inv, acc[8 * c + 7] * inv));
+  if ((t & 7) == 0) a.lse[static_cast<size_t>(h) * a.batch + s] = M + __logf(den);
+}
+
+}  // namespace
+
+size_t decode_select_workspace_bytes(int batch, int G, int max_pages) {
+  return static_cast<size_t>(batch) * G * max_pages * sizeof(float4);
+}
+
+cudaError_t launch_decode_select(const CUtensorMap& map_k, const CUtensorMap& map_q,
+                                 const int32_t* page_table, const int32_t* seq_lens, int batch,
+                                 int max_pages, int num_pages, int G, int k, float* scores,
+                                 int32_t* sel, float* sel_score, int32_t* status,
+                                 uint64_t wait_ns, int num_sms, cudaStream_t stream) {
+  ScanArgs a{};
+  a.page_table = page_table;
+  a.seq_lens = seq_lens;
+  a.batch = batch;
+  a.max_pages = max_pages;
+  a.num_pages = num_pages;
+  a.G = G;
+  a.cps = (max_pages + kPagesPerChunk - 1) / kPagesPerChunk;
+  a.n_chunks = batch * a.cps;
+  a.scores = reinterpret_cast<float4*>(scores);
+  a.status = status;
+  a.wait_ns = wait_ns;
+  cudaError_t e = cudaFuncSetAttribute(decode_scan_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kScanSmem);
+  if (e != cudaSuccess) return e;
+  const int grid = std::max(1, std::min(num_sms, a.n_chunks));
+  decode_scan_kernel<<<grid, 256, kScanSmem, stream>>>(map_k, map_q, a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  TopkArgs t{};
+  t.scores = a.scores;
+  t.seq_lens = seq_lens;
+  t.batch = batch;
+  t.max_pages = max_pages;
+  t.G = G;
+  t.k = k;
+  t.sel = sel;
+  t.sel_score = sel_score;
+  t.status = status;
+  decode_topk_kernel<<<(batch * G * 32 + 127) / 128, 128, 0, stream>>>(t);
+  return cudaGetLastError();
+}
+
+size_t decode_attn_workspace_bytes(int batch, int G, int k) {
+  const size_t units = static_cast<size_t>(batch) * G * k;
+  return units * kHeads * kDim * sizeof(float) + units * kHeads * sizeof(float);
+}
+
+cudaError_t launch_decode_attn(const CUtensorMap& map_kp, const CUtensorMap& map_vp,
+                               const void* q, const int32_t* sel, const int32_t* page_table,
+                               const int32_t* seq_lens, int batch, int max_pages, int num_pages,
+                               int G, int k, float scale, uint8_t* scratch, void* o, float* lse,
+                               int32_t* status, uint64_t wait_ns, int num_sms,
+                               cudaStream_t stream) {
+  DecAttnArgs a{};
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.sel = sel;
+  a.page_table = page_table;
+  a.seq_lens = seq_lens;
+  a.batch = batch;
+  a.max_pages = max_pages;
+  a.num_pages = num_pages;
+  a.G = G;
+  a.k = k;
+  a.units = batch * G * k;
+  const int grid = std::max(1, std::min(num_sms, a.units));
+  a.per_cta = (a.units + grid - 1) / grid;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.po = reinterpret_cast<float*>(scratch);
+  a.plse = reinterpret_cast<float*>(scratch + static_cast<size_t>(a.units) * kHeads * kDim * 4);
+  a.status = status;
+  a.wait_ns = wait_ns;
+  cudaError_t e = cudaFuncSetAttribute(decode_attn_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kDecSmem);
+  if (e != cudaSuccess) return e;
+  decode_attn_kernel<<<grid, 160, kDecSmem, stream>>>(map_kp, map_vp, a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  DecCombineArgs c{a.po, a.plse, batch, G, k, static_cast<__nv_bfloat16*>(o), lse};
+  decode_combine_kernel<<<dim3(batch, G), 128, 0, stream>>>(c);
+  return cudaGetLastError();
+}
+
+}  // namespace msa

@@ -27,4 +27,18 @@ cudaError_t launch_attn_prefill_chunk(const CUtensorMap& map_q, const CUtensorMa
                                       uint64_t wait_ns, int num_sms, cudaStream_t stream,
                                       cudaEvent_t* marks);
 
+size_t decode_select_workspace_bytes(int batch, int G, int max_pages);
+cudaError_t launch_decode_select(const CUtensorMap& map_k, const CUtensorMap& map_q,
+                                 const int32_t* page_table, const int32_t* seq_lens, int batch,
+                                 int max_pages, int num_pages, int G, int k, float* scores,
+                                 int32_t* sel, float* sel_score, int32_t* status,
+                                 uint64_t wait_ns, int num_sms, cudaStream_t stream);
+size_t decode_attn_workspace_bytes(int batch, int G, int k);
+cudaError_t launch_decode_attn(const CUtensorMap& map_kp, const CUtensorMap& map_vp,
+                               const void* q, const int32_t* sel, const int32_t* page_table,
+                               const int32_t* seq_lens, int batch, int max_pages, int num_pages,
+                               int G, int k, float scale, uint8_t* scratch, void* o, float* lse,
+                               int32_t* status, uint64_t wait_ns, int num_sms,
+                               cudaStream_t stream);
+
 }  // namespace msa

@@ -84,6 +84,56 @@ int64_t prefill_chunk(int64_t L) {
   return rounded < kPrefillChunk ? rounded : kPrefillChunk;
 }
 
+msa_status_t check_paged(const msa_paged_kv_t* p, bool need_kv) {
+  if (!p || !p->k_idx_pool || !p->page_table || !p->seq_lens || p->batch < 0 ||
+      p->max_pages < 1 || p->num_pages < 1 || p->reserved != 0 || !aligned16(p->k_idx_pool))
+    return MSA_ERR_INVALID_ARG;
+  if (need_kv && (!p->k_pool || !p->v_pool || !aligned16(p->k_pool) || !aligned16(p->v_pool)))
+    return MSA_ERR_INVALID_ARG;
+  // page rows are addressed with 32-bit TMA coordinates
+  if (static_cast<int64_t>(p->num_pages) * kBlock * 4 >= (static_cast<int64_t>(1) << 31))
+    return MSA_ERR_UNSUPPORTED;
+  return MSA_OK;
+}
+
+bool sm_count(int* sms) {
+  int dev = 0;
+  return cudaGetDevice(&dev) == cudaSuccess &&
+         cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess;
+}
+
+msa_status_t index_select_paged(const msa_config_t* cfg, const void* q_idx,
+                                const msa_paged_kv_t* paged, int32_t* sel, float* sel_score,
+                                void* ws, size_t ws_bytes, cudaStream_t stream) {
+  msa_status_t st = check_paged(paged, false);
+  if (st != MSA_OK) return st;
+  const int G = cfg->num_groups;
+  if (G > 4) return MSA_ERR_UNSUPPORTED;
+  if (ws_bytes < msa_index_select_workspace(cfg, paged->batch, 0, paged)) return MSA_ERR_WORKSPACE;
+  if (paged->batch == 0) return MSA_OK;
+  CUtensorMap mk, mq;
+  {
+    const uint64_t dims[2] = {kDim, static_cast<uint64_t>(paged->num_pages) * kBlock};
+    const uint64_t strides[1] = {kDim * 2};
+    const uint32_t box[2] = {64, kBlock};
+    if (!make_map(&mk, paged->k_idx_pool, 2, dims, strides, box)) return MSA_ERR_CUDA;
+  }
+  {
+    const uint64_t dims[2] = {kDim, static_cast<uint64_t>(paged->batch) * G};
+    const uint64_t strides[1] = {kDim * 2};
+    const uint32_t box[2] = {64, static_cast<uint32_t>(G)};
+    if (!make_map(&mq, q_idx, 2, dims, strides, box)) return MSA_ERR_CUDA;
+  }
+  int sms = 0;
+  if (!sm_count(&sms)) return MSA_ERR_CUDA;
+  float* scores = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + MSA_WS_HEADER_BYTES);
+  cudaError_t e = msa::launch_decode_select(mk, mq, paged->page_table, paged->seq_lens,
+                                            paged->batch, paged->max_pages, paged->num_pages, G,
+                                            cfg->topk, scores, sel, sel_score, status_word(ws),
+                                            wait_ns(cfg), sms, stream);
+  return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
@@ -123,9 +173,10 @@ size_t msa_index_select_workspace(const msa_config_t* cfg, int64_t num_queries, 
   if (check_config(cfg) != MSA_OK) return 0;
   size_t bytes = MSA_WS_HEADER_BYTES;
   if (paged) {
-    // pooled block scores [batch][G][max_pages] fp32
-    bytes += align_up(static_cast<size_t>(num_queries) * cfg->num_groups *
-                          static_cast<size_t>(paged->max_pages) * sizeof(float),
+    if (num_queries < 0 || paged->max_pages < 0) return 0;
+    // per-page pooled scores of the scan: [batch][G][max_pages] x 4 partial maxima
+    bytes += align_up(msa::decode_select_workspace_bytes(static_cast<int>(num_queries),
+                                                         cfg->num_groups, paged->max_pages),
                       256);
   }
   return bytes;
@@ -138,7 +189,7 @@ msa_status_t msa_index_select(const msa_config_t* cfg, const void* q_idx, const 
   if (st != MSA_OK) return st;
   if (!q_idx || !sel || !ws || !aligned16(q_idx)) return MSA_ERR_INVALID_ARG;
   const int G = cfg->num_groups;
-  if (paged) return MSA_ERR_UNSUPPORTED;  // paged decode selection: not built yet
+  if (paged) return index_select_paged(cfg, q_idx, paged, sel, sel_score, ws, ws_bytes, stream);
   if (!k_idx || !aligned16(k_idx) || L < 0) return MSA_ERR_INVALID_ARG;
   if (G != 1 && G != 2 && G != 4) return MSA_ERR_UNSUPPORTED;
   if (L > (static_cast<int64_t>(1) << 31) - kBlock) return MSA_ERR_UNSUPPORTED;
@@ -232,18 +283,39 @@ msa_status_t msa_attn_prefill_marked(const msa_config_t* cfg, const void* q, con
 }
 
 size_t msa_attn_decode_workspace(const msa_config_t* cfg, const msa_paged_kv_t* paged) {
-  (void)paged;
-  if (check_config(cfg) != MSA_OK) return 0;
-  return MSA_WS_HEADER_BYTES;
+  if (check_config(cfg) != MSA_OK || !paged || paged->batch < 0) return 0;
+  return MSA_WS_HEADER_BYTES +
+         align_up(msa::decode_attn_workspace_bytes(paged->batch, cfg->num_groups, cfg->topk),
+                  256);
 }
 
 msa_status_t msa_attn_decode(const msa_config_t* cfg, const void* q, const msa_paged_kv_t* paged,
                              const int32_t* sel, void* o, float* lse, void* ws, size_t ws_bytes,
                              cudaStream_t stream) {
-  (void)q; (void)paged; (void)sel; (void)o; (void)lse; (void)ws; (void)ws_bytes; (void)stream;
   msa_status_t st = check_config(cfg);
   if (st != MSA_OK) return st;
-  return MSA_ERR_UNSUPPORTED;
+  if ((st = check_paged(paged, true)) != MSA_OK) return st;
+  if (!q || !sel || !o || !lse || !ws || !aligned16(q) || !aligned16(o)) return MSA_ERR_INVALID_ARG;
+  if (cfg->heads_per_group != 16) return MSA_ERR_UNSUPPORTED;
+  if (ws_bytes < msa_attn_decode_workspace(cfg, paged)) return MSA_ERR_WORKSPACE;
+  if (paged->batch == 0) return MSA_OK;
+  const int G = cfg->num_groups;
+  CUtensorMap mk, mv;
+  {
+    const uint64_t dims[2] = {kDim, static_cast<uint64_t>(paged->num_pages) * G * kBlock};
+    const uint64_t strides[1] = {kDim * 2};
+    const uint32_t box[2] = {64, kBlock};
+    if (!make_map(&mk, paged->k_pool, 2, dims, strides, box)) return MSA_ERR_CUDA;
+    if (!make_map(&mv, paged->v_pool, 2, dims, strides, box)) return MSA_ERR_CUDA;
+  }
+  int sms = 0;
+  if (!sm_count(&sms)) return MSA_ERR_CUDA;
+  cudaError_t e = msa::launch_decode_attn(
+      mk, mv, q, sel, paged->page_table, paged->seq_lens, paged->batch, paged->max_pages,
+      paged->num_pages, G, cfg->topk, cfg->softmax_scale,
+      static_cast<uint8_t*>(ws) + MSA_WS_HEADER_BYTES, o, lse, status_word(ws), wait_ns(cfg), sms,
+      stream);
+  return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
 }
 
 }  // extern "C"

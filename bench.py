@@ -41,6 +41,9 @@ def parse():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="msa", choices=["msa", "reference"])
     p.add_argument("--workload", default="prefill_L32K")
+    p.add_argument("--decode-workload", default="decode_b64_16K_256K")
+    p.add_argument("--decode-batch", type=int, default=0, help="override (profiling)")
+    p.add_argument("--decode-nmax", type=int, default=0, help="override (profiling)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=5)
     p.add_argument("--L", type=int, default=0, help="override the workload length (profiling)")
@@ -174,6 +177,16 @@ def prefill_work(w, sel_counts=None):
     }
 
 
+def decode_work(w, seq_lens):
+    """Algorithmic bytes of one decode step: the scan reads every index key strictly before each
+    query's page (plus the index queries); the attention reads K and V of the selected pages
+    (the local page up to n) plus q and o."""
+    lens = [int(n) for n in seq_lens]
+    scan = acc.decode_index_bytes(lens, w.B, w.di, w.G)
+    attn = acc.decode_attn_bytes(lens, w.B, w.d, w.G, w.Hq, w.k)
+    return {"scan_bytes": scan, "attn_bytes": attn}
+
+
 # ------------------------------------------------------------------------------------------
 # MSA arm
 # ------------------------------------------------------------------------------------------
@@ -203,22 +216,47 @@ def run_msa(args, world, rank):
 
     nmarks = 3 * nchunks + 1
 
-    def step(marks=None, start=None):
+    # ---- decode: one new token for each of the 64 sequences of the paged workload ----
+    dw0 = synthetic.WORKLOADS[args.decode_workload]
+    dinp = synthetic.decode_inputs(dw0, device=dev, batch=args.decode_batch or None,
+                                   n_hi=args.decode_nmax or None)
+    dw = dinp["workload"]
+    dcfg = msa.config(dw.G, dw.hpg, dw.k, dw.scale)
+    paged = msa.paged_kv(dinp["k_idx_pool"], dinp["k_pool"], dinp["v_pool"], dinp["page_table"],
+                         dinp["seq_lens"])
+    dsel = torch.empty((dw.G, dw.batch, dw.k), dtype=torch.int32, device=dev)
+    do = torch.empty((dw.batch, dw.Hq, dw.d), dtype=torch.bfloat16, device=dev)
+    dlse = torch.empty((dw.Hq, dw.batch), dtype=torch.float32, device=dev)
+    dws = torch.zeros(max(msa.msa_index_select_workspace(dcfg, dw.batch, 0, paged),
+                          msa.msa_attn_decode_workspace(dcfg, paged)), dtype=torch.uint8,
+                      device=dev)
+    dec_launches = 4
+
+    def step(marks=None, start=None, dmarks=None):
         if start is not None:
             start.record(stream)
         msa.msa_index_select(cfg, inp["q_idx"], inp["k_idx"], sel=sel, ws=ws)
         msa.msa_attn_prefill(cfg, inp["q"], inp["k"], inp["v"], sel, o=o, lse=lse, ws=ws,
                              marks=marks)
+        if dmarks is not None:
+            dmarks[0].record(stream)
+        msa.msa_index_select(dcfg, dinp["q_idx"], paged=paged, sel=dsel, ws=dws)
+        if dmarks is not None:
+            dmarks[1].record(stream)
+        msa.msa_attn_decode(dcfg, dinp["q"], paged, dsel, o=do, lse=dlse, ws=dws)
+        if dmarks is not None:
+            dmarks[2].record(stream)
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
-    status = msa.msa_get_device_status(ws)
+    status = msa.msa_get_device_status(ws) or msa.msa_get_device_status(dws)
     if status != 0:
         raise RuntimeError(f"device status {status} after warm-up")
 
     starts = [ev() for _ in range(args.steps)]
     marks = [[ev() for _ in range(nmarks)] for _ in range(args.steps)]
+    dmarks = [[ev() for _ in range(3)] for _ in range(args.steps)]
     t0, t1 = ev(), ev()
     torch.cuda.synchronize()
     with ClockSampler(torch.cuda.current_device()) as clocks:
@@ -226,7 +264,7 @@ def run_msa(args, world, rank):
         torch.cuda.synchronize()
         t0.record(stream)
         for s in range(args.steps):
-            step(marks[s], starts[s])
+            step(marks[s], starts[s], dmarks[s])
         t1.record(stream)
         torch.cuda.synchronize()
         barrier(world)
@@ -241,6 +279,10 @@ def run_msa(args, world, rank):
             phase["schedule"] += m[3 * c].elapsed_time(m[3 * c + 1])
             phase["attention"] += m[3 * c + 1].elapsed_time(m[3 * c + 2])
             phase["combine"] += m[3 * c + 2].elapsed_time(m[3 * c + 3])
+    dec_sel_ms = sum(d[0].elapsed_time(d[1]) for d in dmarks) / args.steps
+    dec_attn_ms = sum(d[1].elapsed_time(d[2]) for d in dmarks) / args.steps
+    prefill_ms = sum(starts[s].elapsed_time(marks[s][-1]) for s in range(args.steps)) / args.steps
+    dec_ms = dec_sel_ms + dec_attn_ms
     per_launch_ms = {"index": phase["index"] / args.steps,
                      "schedule": phase["schedule"] / args.steps,
                      "attention": phase["attention"] / (args.steps * nchunks),
@@ -270,6 +312,12 @@ def run_msa(args, world, rank):
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
     d2h = sum(t.numel() * t.element_size() for t in (host_o, host_lse, host_sel))
 
+    dhost_in = {k: dinp[k].cpu().pin_memory() for k in ("q", "q_idx", "seq_lens", "page_table")}
+    ddev_in = {k: dinp[k] for k in dhost_in}
+    dhost_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (do, dlse, dsel)]
+    h2d += sum(t.numel() * t.element_size() for t in dhost_in.values())
+    d2h += sum(t.numel() * t.element_size() for t in dhost_out)
+
     def e2e_step():
         for k_, t in host_in.items():
             dev_in[k_].copy_(t, non_blocking=True)
@@ -279,6 +327,12 @@ def run_msa(args, world, rank):
         host_o.copy_(o, non_blocking=True)
         host_lse.copy_(lse, non_blocking=True)
         host_sel.copy_(sel, non_blocking=True)
+        for k_, t in dhost_in.items():
+            ddev_in[k_].copy_(t, non_blocking=True)
+        msa.msa_index_select(dcfg, ddev_in["q_idx"], paged=paged, sel=dsel, ws=dws)
+        msa.msa_attn_decode(dcfg, ddev_in["q"], paged, dsel, o=do, lse=dlse, ws=dws)
+        for hd, t in zip(dhost_out, (do, dlse, dsel)):
+            hd.copy_(t, non_blocking=True)
 
     e2e_step()
     torch.cuda.synchronize()
@@ -296,12 +350,39 @@ def run_msa(args, world, rank):
         raise RuntimeError(f"device status {status} after timed region")
 
     cpu_base = None
+    dec_cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu_base = cpu_baseline(w, {k: inp[k].cpu() for k in ("q", "k", "v", "q_idx", "k_idx")},
                                 target_s=15.0)
+        dec_cpu = decode_cpu_baseline(dw, dinp)
 
     ms_per_step = total_ms / args.steps
-    value = world * L * args.steps / (total_ms * 1e-3)
+    prefill_ms = max_over_ranks(prefill_ms, world)
+    dec_ms = max_over_ranks(dec_ms, world)
+    value = world * L / (prefill_ms * 1e-3)
+    dwork = decode_work(dw, dinp["seq_lens"].tolist())
+    dec_scan_gbs = dwork["scan_bytes"] / (dec_sel_ms * 1e-3) / 1e9
+    dec_attn_gbs = dwork["attn_bytes"] / (dec_attn_ms * 1e-3) / 1e9
+    dec_step_gbs = (dwork["scan_bytes"] + dwork["attn_bytes"]) / (dec_ms * 1e-3) / 1e9
+    decode = {
+        "metric": "MSA paged decode tokens/s (one new token per sequence per step)",
+        "value": world * dw.batch / (dec_ms * 1e-3), "unit": "tokens/s",
+        "ms_per_step": dec_ms,
+        "config": {"workload": dw.name, "batch": dw.batch, "n_min": dw.n_lo, "n_max": dw.n_hi,
+                   "context_tokens": int(dinp["seq_lens"].sum().item()), "Hq": dw.Hq,
+                   "G": dw.G, "k": dw.k, "pages": dinp["num_pages"]},
+        "phases_ms_per_step": {"index_select": dec_sel_ms, "attention": dec_attn_ms},
+        "roofline": {"bound": "hbm", "kernel": "index page scan (+ top-k merge)",
+                     "achieved": dec_scan_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": dec_scan_gbs / peaks["hbm_gbs"], "traffic": None,
+                     "peak_source": peaks["source"]},
+        "attention_roofline": {"bound": "hbm", "achieved": dec_attn_gbs, "peak": peaks["hbm_gbs"],
+                               "unit": "GB/s", "frac": dec_attn_gbs / peaks["hbm_gbs"]},
+        "step_hbm_frac": dec_step_gbs / peaks["hbm_gbs"],
+        "algorithmic_bytes": dwork,
+        "gpu_launches": dec_launches * args.steps,
+        "cpu_baseline": None,
+    }
     line = {
         "metric": METRIC,
         "value": value,
@@ -317,10 +398,12 @@ def run_msa(args, world, rank):
         "data": "synthetic (seeded SplitMix64; N(0,1) q/k/v, integer/8 index q/k)",
         "config": {"workload": w.name, "L": L, "Hq": w.Hq, "G": w.G, "d": w.d, "B": w.B,
                    "k": w.k, "parallelism": f"replicas x{world}",
-                   "step": "index select + prefill main branch over all L queries",
+                   "step": "prefill (index select + main branch over all L queries) + one paged "
+                           "decode step of the 64-sequence workload; value = prefill tokens/s",
                    "l2": "inputs larger than L2 (q 512 MiB) and ~8.6 GiB of partials per step"},
         "phases_ms_per_step": {k: v / args.steps for k, v in phase.items()},
-        "gpu_launches": launches_per_step * args.steps,
+        "prefill_ms_per_step": prefill_ms,
+        "gpu_launches": (launches_per_step + dec_launches) * args.steps,
         "roofline": {"bound": bound, "kernel": dominant, "achieved": achieved, "peak": peak,
                      "unit": unit, "frac": achieved / peak, "traffic": traffic,
                      "peak_source": peaks["source"]},
@@ -331,10 +414,15 @@ def run_msa(args, world, rank):
                                                           + phase["schedule"]) / args.steps
                                                          * 1e-3) / 1e12 / tensor_peak,
         "e2e": {"value": world * L * args.e2e_steps / (e2e_ms * 1e-3), "unit": "tokens/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "note": "prefill tokens over the whole step (prefill + decode) with inputs copied "
+                        "from pinned host memory and outputs copied back each step; the decode "
+                        "KV cache is resident state"},
         "clocks": clocks.summary(),
         "cpu_baseline": cpu_base,
+        "decode": decode,
     }
+    line["decode"]["cpu_baseline"] = dec_cpu
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -369,6 +457,33 @@ def cpu_baseline(w, inp, target_s=15.0):
             "sample": f"{len(rows)} evenly strided query rows of the L={w.L} workload "
                       f"(index selection + attention for all {w.G} groups / {w.Hq} heads), "
                       f"{dt2:.1f} s"}
+
+
+def decode_cpu_baseline(w, dinp, n_seq=4):
+    """Oracle decode of a few sequences of the workload (their pages copied to the host)."""
+    import oracle
+    oracle.build()
+    idx = torch.arange(n_seq) * (w.batch // n_seq)
+    pt = dinp["page_table"][idx.to(dinp["page_table"].device)].cpu()
+    seq = dinp["seq_lens"][idx.to(dinp["seq_lens"].device)].cpu()
+    used = sorted({int(p) for p in pt.flatten().tolist() if p >= 0})
+    remap = torch.full((dinp["num_pages"],), 0, dtype=torch.int32)
+    remap[torch.tensor(used)] = torch.arange(len(used), dtype=torch.int32)
+    ui = torch.tensor(used, device=dinp["k_pool"].device)
+    kip = dinp["k_idx_pool"].index_select(0, ui).cpu()
+    kp = dinp["k_pool"].index_select(0, ui).cpu()
+    vp = dinp["v_pool"].index_select(0, ui).cpu()
+    pt2 = torch.where(pt >= 0, remap[pt.clamp(min=0).long()], torch.zeros_like(pt))
+    q = dinp["q"][idx.to(dinp["q"].device)].cpu()
+    qi = dinp["q_idx"][idx.to(dinp["q_idx"].device)].cpu()
+    t = time.perf_counter()
+    sel = oracle.select_decode(qi, kip, pt2, seq, w.B, w.k)
+    oracle.attn_decode(q, kp, vp, pt2, seq, sel, w.B, w.k, w.scale)
+    dt = time.perf_counter() - t
+    return {"value": n_seq / dt, "unit": "tokens/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"{n_seq} of the {w.batch} sequences ({int(seq.sum())} context tokens), "
+                      f"{dt:.2f} s"}
 
 
 def run_reference(args, world, rank):

@@ -145,6 +145,35 @@ class ClockSampler:
                 "power_w_max": max(power) if power else None}
 
 
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu capture
+# of the named kernel (profiles/ has the capture summaries).  A figure is reported only while the
+# kernel's sources still hash to the value recorded with it; otherwise the traffic is null.
+CSRC = os.path.join(ROOT, "block_sparse_long_msa_gb300", "csrc")
+KERNEL_SOURCES = {
+    "attention": ["attn_prefill.cu", "common.cuh", "ptx.cuh"],
+    "combine": ["attn_prefill.cu", "common.cuh", "ptx.cuh"],
+    "index": ["index_prefill.cu", "common.cuh", "ptx.cuh"],
+    "decode_scan": ["decode.cu", "common.cuh", "ptx.cuh"],
+}
+NCU_TRAFFIC = {}
+
+
+def sources_sha256(kernel: str) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def measured_traffic(kernel: str):
+    t = NCU_TRAFFIC.get(kernel)
+    if not t or t["sources_sha256"] != sources_sha256(kernel):
+        return None
+    return t["bytes_per_launch"]
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -301,7 +330,7 @@ def run_msa(args, world, rank):
     }
     dominant = max(("index", "attention", "combine"), key=lambda n: phase[n])
     bound, achieved, peak, unit = roof[dominant]
-    traffic = None  # filled from an ncu capture of the same kernel (see profiles/)
+    traffic = measured_traffic(dominant)
 
     # ---------------- end-to-end through the public API from pinned host buffers ------------
     host_in = {k: inp[k].cpu().pin_memory() for k in ("q", "k", "v", "q_idx", "k_idx")}
@@ -374,7 +403,8 @@ def run_msa(args, world, rank):
         "phases_ms_per_step": {"index_select": dec_sel_ms, "attention": dec_attn_ms},
         "roofline": {"bound": "hbm", "kernel": "index page scan (+ top-k merge)",
                      "achieved": dec_scan_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": dec_scan_gbs / peaks["hbm_gbs"], "traffic": None,
+                     "frac": dec_scan_gbs / peaks["hbm_gbs"],
+                     "traffic": measured_traffic("decode_scan"),
                      "peak_source": peaks["source"]},
         "attention_roofline": {"bound": "hbm", "achieved": dec_attn_gbs, "peak": peaks["hbm_gbs"],
                                "unit": "GB/s", "frac": dec_attn_gbs / peaks["hbm_gbs"]},

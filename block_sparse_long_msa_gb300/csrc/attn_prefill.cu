@@ -18,6 +18,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "tmap.h"
 
 namespace msa {
 
@@ -225,10 +226,11 @@ struct ItemMeta {
   int32_t tok[kItemTokens];  // (token << 4) | slot
 };
 
-constexpr int kQStages = 3;
-constexpr uint32_t kSmemKV = 0;                          // 2 x (K 32 KB + V 32 KB)
-constexpr uint32_t kSmemQ = 131072;                      // 3 x 32 KB
-constexpr uint32_t kSmemMeta = kSmemQ + kQStages * 32768;  // 2 x ItemMeta
+constexpr int kQStages = 2;
+constexpr uint32_t kSmemKV = 0;                            // 2 x (K 32 KB + V 32 KB)
+constexpr uint32_t kSmemQ = 131072;                        // 2 x 32 KB
+constexpr uint32_t kSmemO = kSmemQ + kQStages * 32768;     // O staging tile for TMA stores
+constexpr uint32_t kSmemMeta = kSmemO + 32768;             // 2 x ItemMeta
 constexpr uint32_t kSmemBar = kSmemMeta + 2 * sizeof(ItemMeta);
 constexpr uint32_t kAttnSmem = kSmemBar + 256 + 1024;
 static_assert(kAttnSmem <= 232448, "attention kernel shared memory");
@@ -241,10 +243,22 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  uint64_t ra, rb, rc, rd;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(ra) : "f"(a.x), "f"(a.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(rb) : "f"(b.x), "f"(b.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(rc) : "f"(c.x), "f"(c.y));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(rd) : "l"(ra), "l"(rb), "l"(rc));
+  float2 d;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(rd));
+  return d;
+}
+
 __global__ void __launch_bounds__(512, 1)
     attn_kv_outer_kernel(const __grid_constant__ CUtensorMap map_q,
                          const __grid_constant__ CUtensorMap map_k,
-                         const __grid_constant__ CUtensorMap map_v, AttnArgs a) {
+                         const __grid_constant__ CUtensorMap map_v,
+                         const __grid_constant__ CUtensorMap map_po, AttnArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -506,39 +520,56 @@ __global__ void __launch_bounds__(512, 1)
           s = e & 15;
         }
         const int lim = valid ? min(i - b * kBlock, kBlock - 1) : kBlock - 1;
-        // pass 1: row max of the scaled logits (log2 units)
-        float m2 = -__int_as_float(0x7f800000);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t v[32];
-          tmem_ld32(sa + c * 32, v);
-          tmem_ld_wait();
-#pragma unroll
-          for (int q = 0; q < 32; ++q)
-            if (c * 32 + q <= lim) m2 = fmaxf(m2, __uint_as_float(v[q]) * a.scale_log2);
-          asm volatile("" : "+f"(m2));  // finish this chunk before the next TMEM load
-        }
-        // pass 2: p = exp2(t - m2) -> fp16 pairs; keys [16c, 16c+16) go to columns
-        // [8c, 8c+8), which hold S values this thread has already read
-        float l = 0.f;
+        // tiles of non-local tokens (all but the first 16 of a block's list) need no mask
+        const bool unmasked = __all_sync(0xffffffffu, lim >= kBlock - 1);
+        // pass 1: row max of the scaled logits (log2 units); two TMEM loads per wait
+        float mraw = -__int_as_float(0x7f800000);
 #pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
-          uint32_t v[16], pk[8];
-          tmem_ld16(sa + c * 16, v);
+        for (int c = 0; c < 4; c += 2) {
+          uint32_t v0[32], v1[32];
+          tmem_ld32(sa + c * 32, v0);
+          tmem_ld32(sa + c * 32 + 32, v1);
+          tmem_ld_wait();
+          if (unmasked) {
+#pragma unroll
+            for (int q = 0; q < 32; ++q)
+              mraw = fmaxf(mraw, fmaxf(__uint_as_float(v0[q]), __uint_as_float(v1[q])));
+          } else {
+#pragma unroll
+            for (int q = 0; q < 32; ++q) {
+              if (c * 32 + q <= lim) mraw = fmaxf(mraw, __uint_as_float(v0[q]));
+              if (c * 32 + 32 + q <= lim) mraw = fmaxf(mraw, __uint_as_float(v1[q]));
+            }
+          }
+        }
+        const float m2 = mraw * a.scale_log2;  // the scale is positive
+        // pass 2: p = exp2(s * scale - m2) -> fp16 pairs; keys [16c, 16c+16) go to columns
+        // [8c, 8c+8), which hold S values this thread has already read
+        float2 l2 = make_float2(0.f, 0.f);
+        const float2 sc2 = make_float2(a.scale_log2, a.scale_log2), nm2 = make_float2(-m2, -m2);
+#pragma unroll 1
+        for (int c = 0; c < 8; c += 2) {
+          uint32_t v[32], pk[16];
+          tmem_ld16(sa + c * 16, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+          tmem_ld16(sa + c * 16 + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
           tmem_ld_wait();
 #pragma unroll
-          for (int q = 0; q < 16; q += 2) {
-            const int j = c * 16 + q;
-            const float p0 =
-                j <= lim ? fast_exp2(fmaf(__uint_as_float(v[q]), a.scale_log2, -m2)) : 0.f;
-            const float p1 =
-                j + 1 <= lim ? fast_exp2(fmaf(__uint_as_float(v[q + 1]), a.scale_log2, -m2))
-                             : 0.f;
-            l += p0 + p1;
+          for (int q = 0; q < 32; q += 2) {
+            float2 t = ffma2(make_float2(__uint_as_float(v[q]), __uint_as_float(v[q + 1])), sc2,
+                             nm2);
+            float p0 = fast_exp2(t.x), p1 = fast_exp2(t.y);
+            if (!unmasked) {
+              const int j = c * 16 + q;
+              p0 = j <= lim ? p0 : 0.f;
+              p1 = j + 1 <= lim ? p1 : 0.f;
+            }
+            l2.x += p0;
+            l2.y += p1;
             pk[q >> 1] = pack_f16x2(p0, p1);
           }
-          tmem_st8(sa + c * 8, pk);
+          tmem_st16(sa + c * 8, pk);
         }
+        const float l = l2.x + l2.y;
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(p_full(wg));
@@ -556,63 +587,66 @@ __global__ void __launch_bounds__(512, 1)
     }
   } else {
     // ------------------------------- epilogue -------------------------------
+    // O (fp32, TMEM) -> fp16 rows in a 128-byte-swizzled staging tile -> one TMA store per
+    // (token, 64-column half): each token's 16 heads are 4 KB contiguous in the partial buffer.
+    // Every epilogue thread runs the same loop, so the named barriers always pair up; after an
+    // abort the waits are skipped and nothing more is stored.
+    const int et = threadIdx.x - 384;
     const int row = (warp & 3) * 32 + lane;
-    const int tk = row >> 4, hh = row & 15;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t stg = base + kSmemO;
     int T = 0, nit = 0;
-    bool ok = true;
-    for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x, ++nit) {
+    for (int it = blockIdx.x; it < n_items; it += gridDim.x, ++nit) {
       const int kvs = nit & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(kv_full(kvs), (nit >> 1) & 1, a.wait_ns))) {
-        ok = false;
-        break;
+      const bool okv = !*abort_flag && mbar_wait(kv_full(kvs), (nit >> 1) & 1, a.wait_ns);
+      if (!__all_sync(0xffffffffu, okv)) {
+        report_status(a.status, kStatusTimeout);
+        *abort_flag = 1;
       }
       const ItemMeta& m = meta[kvs];
-      const int count = m.count, g = m.g;
+      const int count = min(max(m.count, 0), kItemTokens), g = m.g;
       for (int t0 = 0; t0 < count; t0 += kTileTokens, ++T) {
         const int slot = T & 1, use = T >> 1;
-        if (!__all_sync(0xffffffffu, mbar_wait(o_full(slot), use & 1, a.wait_ns))) {
-          ok = false;
-          break;
+        const bool oko = !*abort_flag && mbar_wait(o_full(slot), use & 1, a.wait_ns);
+        if (!__all_sync(0xffffffffu, oko)) {
+          report_status(a.status, kStatusTimeout);
+          *abort_flag = 1;
         }
         tc_fence_after();
-        const bool valid = t0 + tk < count;
-        __half* dst = nullptr;
-        if (valid) {
-          const int32_t e = m.tok[t0 + tk];
-          const int i = e >> 4, s = e & 15;
-          const size_t u = (static_cast<size_t>(i - a.q0) * a.G + g) * a.k + s;
-          dst = a.po + (u * kHeadsPerGroup + hh) * kDim;
-        }
+        if (et < 16) bulk_wait_read0();  // the previous tile's stores have read the staging tile
+        named_barrier(1, 128);
         const uint32_t oa = tmem + lane_base + 256 + slot * 128;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t v[32];
           tmem_ld32(oa + c * 32, v);
           tmem_ld_wait();
-          if (c == 3) {  // all of O is in registers: the slot can take the next tile
-            tc_fence_before();
-            mbar_arrive(o_empty(slot));
-          }
-          if (valid) {
-            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
 #pragma unroll
-            for (int u4 = 0; u4 < 4; ++u4)
-              d4[u4] = make_uint4(
-                  pack_f16x2(__uint_as_float(v[8 * u4 + 0]), __uint_as_float(v[8 * u4 + 1])),
-                  pack_f16x2(__uint_as_float(v[8 * u4 + 2]), __uint_as_float(v[8 * u4 + 3])),
-                  pack_f16x2(__uint_as_float(v[8 * u4 + 4]), __uint_as_float(v[8 * u4 + 5])),
-                  pack_f16x2(__uint_as_float(v[8 * u4 + 6]), __uint_as_float(v[8 * u4 + 7])));
+          for (int u4 = 0; u4 < 4; ++u4)
+            st_shared_v4(stg + sw128_offset(row, c * 32 + u4 * 8, 128),
+                         pack_f16x2(__uint_as_float(v[8 * u4 + 0]), __uint_as_float(v[8 * u4 + 1])),
+                         pack_f16x2(__uint_as_float(v[8 * u4 + 2]), __uint_as_float(v[8 * u4 + 3])),
+                         pack_f16x2(__uint_as_float(v[8 * u4 + 4]), __uint_as_float(v[8 * u4 + 5])),
+                         pack_f16x2(__uint_as_float(v[8 * u4 + 6]), __uint_as_float(v[8 * u4 + 7])));
+        }
+        tc_fence_before();
+        mbar_arrive(o_empty(slot));
+        fence_proxy_async_smem();
+        named_barrier(1, 128);
+        if (et < 16) {
+          const int tk = et >> 1, h = et & 1;
+          if (t0 + tk < count && !*abort_flag) {
+            const int32_t e = m.tok[t0 + tk];
+            const int i = e >> 4, s = e & 15;
+            const int u = ((i - a.q0) * a.G + g) * a.k + s;
+            tma_store_2d(&map_po, stg + h * kPanel + tk * 2048, h * 64, u * kHeadsPerGroup);
           }
+          bulk_commit();
         }
       }
-      if (!ok) break;
       mbar_arrive(meta_empty(kvs));
     }
-    if (!ok) {
-      report_status(a.status, kStatusTimeout);
-      *abort_flag = 1;
-    }
+    if (et < 16) bulk_wait0();
   }
   tc_fence_before();
   __syncthreads();
@@ -769,9 +803,19 @@ cudaError_t launch_attn_prefill_chunk(const CUtensorMap& map_q, const CUtensorMa
   if ((e = cudaFuncSetAttribute(attn_kv_outer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 kAttnSmem)) != cudaSuccess)
     return e;
+  // partial O as a 2-D fp16 tensor [units * 16 rows][128]: the epilogue's TMA stores
+  CUtensorMap map_po;
+  {
+    const uint64_t dims[2] = {static_cast<uint64_t>(kDim),
+                              static_cast<uint64_t>(w.chunk) * G * k * kHeadsPerGroup};
+    const uint64_t strides[1] = {kDim * 2};
+    const uint32_t box[2] = {64, kHeadsPerGroup};
+    if (!encode_tmap(&map_po, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.po, 2, dims, strides, box))
+      return cudaErrorInvalidValue;
+  }
   const int grid = static_cast<int>(std::min<int64_t>(w.max_items, num_sms));
   if (marks && marks[1]) cudaEventRecord(marks[1], stream);
-  attn_kv_outer_kernel<<<grid, 512, kAttnSmem, stream>>>(map_q, map_k, map_v, a);
+  attn_kv_outer_kernel<<<grid, 512, kAttnSmem, stream>>>(map_q, map_k, map_v, map_po, a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   CombineArgs c{};

@@ -262,9 +262,22 @@ __global__ void __launch_bounds__(128) decode_topk_kernel(TopkArgs a) {
   TopList list;
   list.clear();
   const float4* row = a.scores + (static_cast<size_t>(s) * a.G + g) * a.max_pages;
-  for (int b = lane; b < bi; b += 32) {
-    const float4 v = row[b];
-    list.insert(fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)), b);
+  // eight loads in flight per lane, then eight inserts (blocks stay ascending per lane)
+  for (int b0 = 0; b0 < bi; b0 += 8 * 32) {
+    float sc[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int b = b0 + q * 32 + lane;
+      if (b < bi) {
+        const float4 v = row[b];
+        sc[q] = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int b = b0 + q * 32 + lane;
+      if (b < bi) list.insert(sc[q], b);
+    }
   }
   const int take = min(a.k - 1, bi);
   int my_id = 0x7fffffff;

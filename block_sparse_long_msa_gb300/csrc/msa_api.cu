@@ -1,54 +1,21 @@
 // C ABI of libmsa (declared in include/msa.h): argument checks, workspace carving, tensor-map
 // encoding and kernel launches.  Nothing here allocates device memory or synchronizes, except
 // msa_get_device_status, which reads the status word back.
-#include <mutex>
-
 #include "../../include/msa.h"
 #include "common.cuh"
 #include "launch.h"
+#include "tmap.h"
 
 namespace {
 
 using msa::kBlock;
 using msa::kDim;
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  });
-  return fn;
-}
-
 // bf16 tensor map with 128-byte swizzle; dims/strides innermost first (strides in bytes, one
 // fewer than dims); box of 64 elements innermost.
 bool make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
               const uint64_t* strides, const uint32_t* box) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return false;
-  cuuint64_t d[5], s[4];
-  cuuint32_t b[5], es[5];
-  for (int i = 0; i < rank; ++i) {
-    d[i] = dims[i];
-    b[i] = box[i];
-    es[i] = 1;
-  }
-  for (int i = 0; i + 1 < rank; ++i) s[i] = strides[i];
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), d, s, b, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return msa::encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, rank, dims, strides, box);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

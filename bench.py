@@ -155,7 +155,18 @@ KERNEL_SOURCES = {
     "index": ["index_prefill.cu", "common.cuh", "ptx.cuh"],
     "decode_scan": ["decode.cu", "common.cuh", "ptx.cuh"],
 }
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # prefill L=32768, 64/4 heads, k=16 (profiles/dram_prefill_L32K_decode_b64.md)
+    "attention": {"bytes_per_launch": 3140837120 + 8547729920,
+                  "sources_sha256": "0fba90eeaca37c9f537b85afeec60b347cbb306fe01a773fe4955fb15057355a"},
+    "combine": {"bytes_per_launch": 8622441984 + 540351488,
+                "sources_sha256": "0fba90eeaca37c9f537b85afeec60b347cbb306fe01a773fe4955fb15057355a"},
+    "index": {"bytes_per_launch": 41820160 + 16384,
+              "sources_sha256": "ba46e6dc27fdf2dbe0eae8db725358e962ca15fa074a392a0248472322a39eab"},
+    # decode, 64 sequences of 16K-256K tokens
+    "decode_scan": {"bytes_per_launch": 2080732928 + 7241216,
+                    "sources_sha256": "cde950c8ec201b6a80ca88fd24b39d3bb13304dd82137808726d802d94dfed68"},
+}
 
 
 def sources_sha256(kernel: str) -> str:

@@ -8,8 +8,12 @@
 //   1. sched_hist   per (group, query block): which tokens chose which block (bitmask in shared
 //                   memory), per-block counts -> hist[g][b][qb]
 //   2. sched_scan   per (group, block): exclusive prefix of hist over query blocks, list length
-//   3. sched_bases  one CTA: list offsets and work-item offsets over all (group, block)
-//   4. sched_items  per (group, block): work items of at most kItemTokens tokens
+//   3. sched_bases  one CTA: list offsets over (group, block), work-item offsets over
+//                   (query range, group, block)
+//   4. sched_items  per (query range, group, block): work items of at most kItemTokens tokens.
+//                   Items are ordered query-range-major, so the CTAs working at any moment
+//                   gather the queries of one range (a few tens of MB) and L2 serves the
+//                   repeated gathers of each query for its k blocks.
 //   5. sched_fill   per (group, query block): every (token, slot) lands at its place, lists stay
 //                   in ascending token order (deterministic, no global atomics)
 //   6. attn_kv_outer persistent tcgen05 kernel over work items (see below)
@@ -29,6 +33,7 @@ constexpr int kHeadsPerGroup = 16;
 constexpr int kItemTiles = 16;                            // tiles sharing one K/V staging
 constexpr int kItemTokens = kItemTiles * kTileTokens;     // 128
 constexpr uint32_t kPanel = 16384;
+constexpr int kMaxRanges = 16;
 
 // ------------------------------------------------------------------------------------------
 // Scheduling
@@ -40,10 +45,13 @@ struct SchedArgs {
   int32_t q0;          // first query of the chunk (multiple of 128)
   int32_t nbq;         // query blocks in the chunk
   int32_t nbk;         // key blocks referenced by the chunk (= last query block + 1)
+  int32_t rq, nr;      // query blocks per query range, number of ranges (<= kMaxRanges)
   int32_t* hist;       // [G][nbk][nbq]
   int32_t* cnt;        // [G*nbk]
   int32_t* list_base;  // [G*nbk]
-  int32_t* item_base;  // [G*nbk]
+  int32_t* rstart;     // [nr][G][nbk]: offset of the range's first token in the (g, b) list
+  int32_t* rcnt;       // [nr][G][nbk]: tokens of the range in the (g, b) list
+  int32_t* item_base;  // [nr][G][nbk]
   int32_t* n_items;    // [1]
   int4* items;         // {g, b, start, count}
   int32_t* list;       // (token << 4) | slot
@@ -107,70 +115,83 @@ __global__ void sched_scan_kernel(SchedArgs a) {
     run += __shfl_sync(0xffffffffu, incl, 31);
   }
   if (lane == 0) a.cnt[warp] = run;
+  __syncwarp();
+  // where each query range starts in this (g, b) list; ranges before the first query block
+  // that can choose b start at 0
+  int start = run;
+  if (lane < a.nr) {
+    const int q = lane * a.rq;
+    start = q < first ? 0 : h[q];
+  }
+  const int next = __shfl_down_sync(0xffffffffu, start, 1);
+  if (lane < a.nr) {
+    const size_t idx = static_cast<size_t>(lane) * a.G * a.nbk + warp;
+    a.rstart[idx] = start;
+    a.rcnt[idx] = (lane + 1 < a.nr ? next : run) - start;
+  }
 }
 
 __device__ __forceinline__ int items_of(int c) {
   return (c + kItemTokens - 1) / kItemTokens;
 }
 
-// One CTA: exclusive scans of the list lengths and the item counts over all (group, block).
-__global__ void __launch_bounds__(1024) sched_bases_kernel(SchedArgs a) {
-  __shared__ int32_t warp_sums[2][32];
-  __shared__ int32_t carry[2];
-  const int n = a.G * a.nbk, t = threadIdx.x, lane = t & 31, w = t >> 5;
-  if (t == 0) carry[0] = carry[1] = 0;
+// Exclusive scan of n values (val(i)) by one CTA of 1024 threads into out; returns the total.
+template <typename F>
+__device__ int block_exclusive_scan(int n, F val, int32_t* out, int32_t* warp_sums,
+                                    int32_t* carry) {
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  if (t == 0) *carry = 0;
   __syncthreads();
   for (int base = 0; base < n; base += 1024) {
     const int idx = base + t;
-    const int c = idx < n ? a.cnt[idx] : 0;
-    int v[2] = {c, items_of(c)};
-    int incl[2] = {v[0], v[1]};
+    const int v = idx < n ? val(idx) : 0;
+    int incl = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const int x = __shfl_up_sync(0xffffffffu, incl[q], o);
-        if (lane >= o) incl[q] += x;
-      }
+      const int x = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += x;
     }
-    if (lane == 31) {
-      warp_sums[0][w] = incl[0];
-      warp_sums[1][w] = incl[1];
-    }
+    if (lane == 31) warp_sums[w] = incl;
     __syncthreads();
     if (w == 0) {
+      const int s = warp_sums[lane];
+      int x = s;
 #pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const int s = warp_sums[q][lane];
-        int x = s;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int y = __shfl_up_sync(0xffffffffu, x, o);
-          if (lane >= o) x += y;
-        }
-        warp_sums[q][lane] = x - s;  // exclusive over warps
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
       }
+      warp_sums[lane] = x - s;
     }
     __syncthreads();
-    if (idx < n) {
-      a.list_base[idx] = carry[0] + warp_sums[0][w] + incl[0] - v[0];
-      a.item_base[idx] = carry[1] + warp_sums[1][w] + incl[1] - v[1];
-    }
+    if (idx < n) out[idx] = *carry + warp_sums[w] + incl - v;
     __syncthreads();
-    if (t == 1023) {
-      carry[0] += warp_sums[0][w] + incl[0];
-      carry[1] += warp_sums[1][w] + incl[1];
-    }
+    if (t == 1023) *carry += warp_sums[w] + incl;
     __syncthreads();
   }
-  if (t == 0) *a.n_items = carry[1];
+  return *carry;
+}
+
+// One CTA: list offsets over (group, block), item offsets over (range, group, block).
+__global__ void __launch_bounds__(1024) sched_bases_kernel(SchedArgs a) {
+  __shared__ int32_t warp_sums[32];
+  __shared__ int32_t carry;
+  const int32_t* cnt = a.cnt;
+  const int32_t* rcnt = a.rcnt;
+  block_exclusive_scan(a.G * a.nbk, [cnt](int i) { return cnt[i]; }, a.list_base, warp_sums,
+                       &carry);
+  const int total = block_exclusive_scan(
+      a.nr * a.G * a.nbk, [rcnt](int i) { return items_of(rcnt[i]); }, a.item_base, warp_sums,
+      &carry);
+  if (threadIdx.x == 0) *a.n_items = total;
 }
 
 __global__ void sched_items_kernel(SchedArgs a) {
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= a.G * a.nbk) return;
-  const int g = idx / a.nbk, b = idx % a.nbk;
-  const int c = a.cnt[idx], base = a.list_base[idx], ib = a.item_base[idx];
+  if (idx >= a.nr * a.G * a.nbk) return;
+  const int gb = idx % (a.G * a.nbk);
+  const int g = gb / a.nbk, b = gb % a.nbk;
+  const int c = a.rcnt[idx], base = a.list_base[gb] + a.rstart[idx], ib = a.item_base[idx];
   for (int q = 0; q * kItemTokens < c; ++q)
     a.items[ib + q] = make_int4(g, b, base + q * kItemTokens, min(kItemTokens, c - q * kItemTokens));
 }
@@ -727,12 +748,14 @@ PrefillWorkspace prefill_workspace_layout(int64_t L, int G, int k, int64_t chunk
   const int64_t nbk = (L + kBlock - 1) / kBlock;
   const int64_t nbq = (chunk + kBlock - 1) / kBlock;
   const int64_t units = chunk * G * k;
-  const int64_t max_items = G * nbk + (units + kItemTokens - 1) / kItemTokens;
+  const int64_t max_items = kMaxRanges * G * nbk + (units + kItemTokens - 1) / kItemTokens;
   size_t off = 256;  // status header
   w.hist = off;      off += up(sizeof(int32_t) * G * nbk * nbq);
   w.cnt = off;       off += up(sizeof(int32_t) * G * nbk);
   w.list_base = off; off += up(sizeof(int32_t) * G * nbk);
-  w.item_base = off; off += up(sizeof(int32_t) * G * nbk);
+  w.rstart = off;    off += up(sizeof(int32_t) * kMaxRanges * G * nbk);
+  w.rcnt = off;      off += up(sizeof(int32_t) * kMaxRanges * G * nbk);
+  w.item_base = off; off += up(sizeof(int32_t) * kMaxRanges * G * nbk);
   w.n_items = off;   off += 256;
   w.items = off;     off += up(sizeof(int4) * max_items);
   w.list = off;      off += up(sizeof(int32_t) * units);
@@ -763,6 +786,10 @@ cudaError_t launch_attn_prefill_chunk(const CUtensorMap& map_q, const CUtensorMa
   s.cnt = reinterpret_cast<int32_t*>(ws + w.cnt);
   s.list_base = reinterpret_cast<int32_t*>(ws + w.list_base);
   s.item_base = reinterpret_cast<int32_t*>(ws + w.item_base);
+  s.rstart = reinterpret_cast<int32_t*>(ws + w.rstart);
+  s.rcnt = reinterpret_cast<int32_t*>(ws + w.rcnt);
+  s.rq = std::max(16, (s.nbq + kMaxRanges - 1) / kMaxRanges);
+  s.nr = (s.nbq + s.rq - 1) / s.rq;
   s.n_items = reinterpret_cast<int32_t*>(ws + w.n_items);
   s.items = reinterpret_cast<int4*>(ws + w.items);
   s.list = reinterpret_cast<int32_t*>(ws + w.list);
@@ -783,7 +810,7 @@ cudaError_t launch_attn_prefill_chunk(const CUtensorMap& map_q, const CUtensorMa
   const int pairs = G * s.nbk;
   sched_scan_kernel<<<(pairs * 32 + 255) / 256, 256, 0, stream>>>(s);
   sched_bases_kernel<<<1, 1024, 0, stream>>>(s);
-  sched_items_kernel<<<(pairs + 255) / 256, 256, 0, stream>>>(s);
+  sched_items_kernel<<<(s.nr * pairs + 255) / 256, 256, 0, stream>>>(s);
   sched_fill_kernel<<<qgrid, kBlock, mask_smem, stream>>>(s);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 

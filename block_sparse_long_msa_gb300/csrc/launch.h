@@ -16,7 +16,8 @@ cudaError_t launch_index_select_prefill(const CUtensorMap& map_q, const CUtensor
 
 // Byte offsets of the prefill main-branch workspace (after the 256-byte status header).
 struct PrefillWorkspace {
-  size_t hist, cnt, list_base, item_base, n_items, items, list, pm, plse, po, total;
+  size_t hist, cnt, list_base, rstart, rcnt, item_base, n_items, items, list, pm, plse, po,
+      total;
   int64_t chunk, max_items;
 };
 PrefillWorkspace prefill_workspace_layout(int64_t L, int G, int k, int64_t chunk);

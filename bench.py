@@ -344,19 +344,21 @@ def run_msa(args, world, rank):
     traffic = measured_traffic(dominant)
 
     # ---------------- end-to-end through the public API from pinned host buffers ------------
-    host_in = {k: inp[k].cpu().pin_memory() for k in ("q", "k", "v", "q_idx", "k_idx")}
-    host_o = torch.empty(o.shape, dtype=o.dtype).pin_memory()
-    host_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    host_sel = torch.empty(sel.shape, dtype=sel.dtype).pin_memory()
-    dev_in = {k: torch.empty_like(inp[k]) for k in host_in}
-    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
-    d2h = sum(t.numel() * t.element_size() for t in (host_o, host_lse, host_sel))
+    e2e_on = args.e2e_steps > 0
+    pin = (lambda t: t.cpu().pin_memory()) if e2e_on else (lambda t: t[:0].cpu())
+    host_in = {k: pin(inp[k]) for k in ("q", "k", "v", "q_idx", "k_idx")}
+    host_o = pin(o)
+    host_lse = pin(lse)
+    host_sel = pin(sel)
+    dev_in = {k: torch.empty_like(inp[k]) if e2e_on else inp[k] for k in host_in}
+    h2d = sum(inp[k].numel() * inp[k].element_size() for k in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in (o, lse, sel))
 
-    dhost_in = {k: dinp[k].cpu().pin_memory() for k in ("q", "q_idx", "seq_lens", "page_table")}
+    dhost_in = {k: pin(dinp[k]) for k in ("q", "q_idx", "seq_lens", "page_table")}
     ddev_in = {k: dinp[k] for k in dhost_in}
-    dhost_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (do, dlse, dsel)]
-    h2d += sum(t.numel() * t.element_size() for t in dhost_in.values())
-    d2h += sum(t.numel() * t.element_size() for t in dhost_out)
+    dhost_out = [pin(t) for t in (do, dlse, dsel)]
+    h2d += sum(dinp[k].numel() * dinp[k].element_size() for k in dhost_in)
+    d2h += sum(t.numel() * t.element_size() for t in (do, dlse, dsel))
 
     def e2e_step():
         for k_, t in host_in.items():
@@ -374,17 +376,19 @@ def run_msa(args, world, rank):
         for hd, t in zip(dhost_out, (do, dlse, dsel)):
             hd.copy_(t, non_blocking=True)
 
-    e2e_step()
-    torch.cuda.synchronize()
-    e0, e1 = ev(), ev()
-    barrier(world)
-    torch.cuda.synchronize()
-    e0.record(stream)
-    for _ in range(args.e2e_steps):
+    e2e_ms = None
+    if args.e2e_steps > 0:
         e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+        torch.cuda.synchronize()
+        e0, e1 = ev(), ev()
+        barrier(world)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
     status = msa.msa_get_device_status(ws)
     if status != 0:
         raise RuntimeError(f"device status {status} after timed region")
@@ -454,7 +458,8 @@ def run_msa(args, world, rank):
         "tensor_frac_main_branch": work["attn_flops"] / ((phase["attention"] + phase["combine"]
                                                           + phase["schedule"]) / args.steps
                                                          * 1e-3) / 1e12 / tensor_peak,
-        "e2e": {"value": world * L * args.e2e_steps / (e2e_ms * 1e-3), "unit": "tokens/s",
+        "e2e": None if e2e_ms is None else {
+                "value": world * L * args.e2e_steps / (e2e_ms * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "note": "prefill tokens over the whole step (prefill + decode) with inputs copied "
                         "from pinned host memory and outputs copied back each step; the decode "

@@ -788,8 +788,15 @@ cudaError_t launch_attn_prefill_chunk(const CUtensorMap& map_q, const CUtensorMa
   s.item_base = reinterpret_cast<int32_t*>(ws + w.item_base);
   s.rstart = reinterpret_cast<int32_t*>(ws + w.rstart);
   s.rcnt = reinterpret_cast<int32_t*>(ws + w.rcnt);
-  s.rq = std::max(16, (s.nbq + kMaxRanges - 1) / kMaxRanges);
-  s.nr = (s.nbq + s.rq - 1) / s.rq;
+  // query ranges: as many as keep the expected (group, block) list of a range at one full work
+  // item or more (ranges that cut lists shorter would pad tiles and reload K/V per item)
+  {
+    const int64_t per_list = (q1 - q0) * k / std::max(1, s.nbk);  // tokens per (g, b) list
+    const int nr_want = static_cast<int>(std::min<int64_t>(kMaxRanges,
+                                                           std::max<int64_t>(1, per_list / kItemTokens)));
+    s.rq = (s.nbq + nr_want - 1) / nr_want;
+    s.nr = (s.nbq + s.rq - 1) / s.rq;
+  }
   s.n_items = reinterpret_cast<int32_t*>(ws + w.n_items);
   s.items = reinterpret_cast<int4*>(ws + w.items);
   s.list = reinterpret_cast<int32_t*>(ws + w.list);

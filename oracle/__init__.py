@@ -41,7 +41,7 @@ def _load():
         i64, i32, f64 = ctypes.c_int64, ctypes.c_int, ctypes.c_double
         lib.oracle_select_prefill.argtypes = [P, P, i64, i32, i32, i32, i32, P, i64, P, P]
         lib.oracle_attn_prefill.argtypes = [P, P, P, i64, i32, i32, i32, i32, i32, f64, P, P, i64,
-                                            P, P]
+                                            P, P, i32]
         lib.oracle_select_decode.argtypes = [P, P, P, i64, P, i64, i32, i32, i32, i32, P, P]
         lib.oracle_attn_decode.argtypes = [P, P, P, P, i64, P, i64, i32, i32, i32, i32, i32, f64,
                                            P, P, P]
@@ -92,21 +92,27 @@ def select_prefill(q_idx, k_idx, B: int, k: int, rows=None, want_score: bool = F
     return (sel, score) if want_score else sel
 
 
-def attn_prefill(q, kk, vv, sel, B: int, k: int, scale: float, rows=None):
-    """Main branch for prefill.  q [L][Hq][d], kk/vv [L][G][d], sel [G][nrows][k] for `rows`.
+def attn_prefill(q, kk, vv, sel, B: int, k: int, scale: float, rows=None, q_compact=False):
+    """Main branch for prefill.  q [L][Hq][d] (or [nrows][Hq][d] holding just `rows` when
+    q_compact), kk/vv [L][G][d], sel [G][nrows][k] for `rows`.
 
     Returns o float64 [nrows][Hq][d] and lse float64 [Hq][nrows] (natural log).
     """
     qb, kb, vb = _bits(q), _bits(kk), _bits(vv)
-    L, Hq, d = qb.shape
-    G = kb.shape[1]
+    L, G, d = kb.shape
+    Hq = qb.shape[1]
     rows = np.arange(L, dtype=np.int64) if rows is None else np.ascontiguousarray(rows, np.int64)
+    if q_compact:
+        assert qb.shape[0] == len(rows)
+    else:
+        assert qb.shape[0] == L
     s = _i32(sel)
     assert s.shape == (G, len(rows), k), (s.shape, G, len(rows), k)
     o = np.empty((len(rows), Hq, d), np.float64)
     lse = np.empty((Hq, len(rows)), np.float64)
     _load().oracle_attn_prefill(_ptr(qb), _ptr(kb), _ptr(vb), L, Hq, G, d, B, k, float(scale),
-                                _ptr(s), _ptr(rows), len(rows), _ptr(o), _ptr(lse))
+                                _ptr(s), _ptr(rows), len(rows), _ptr(o), _ptr(lse),
+                                1 if q_compact else 0)
     return o, lse
 
 

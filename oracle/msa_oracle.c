@@ -158,13 +158,15 @@ static void attend_one(const uint16_t* q, const uint16_t* const* krows,
 }
 
 /*
- * Prefill main branch.  q [L][Hq][d], k/v [L][G][d].  For the nrows positions rows[r] and every
- * head h, with sel [G][nrows][k] the selection of those positions (the layout the index branch
- * above writes for the same rows): o[(r*Hq + h)*d + .] and lse[h*nrows + r].
+ * Prefill main branch.  q [L][Hq][d] (or, when q_compact is set, [nrows][Hq][d] holding only
+ * the listed rows), k/v [L][G][d].  For the nrows positions rows[r] and every head h, with
+ * sel [G][nrows][k] the selection of those positions (the layout the index branch above writes
+ * for the same rows): o[(r*Hq + h)*d + .] and lse[h*nrows + r].
  */
 void oracle_attn_prefill(const uint16_t* q, const uint16_t* kk, const uint16_t* vv, int64_t L,
                          int Hq, int G, int d, int B, int k, double scale, const int32_t* sel,
-                         const int64_t* rows, int64_t nrows, double* o, double* lse) {
+                         const int64_t* rows, int64_t nrows, double* o, double* lse,
+                         int q_compact) {
     const int hpg = Hq / G;
     const int64_t cap = (int64_t)k * B;
     (void)L;
@@ -191,7 +193,8 @@ void oracle_attn_prefill(const uint16_t* q, const uint16_t* kk, const uint16_t* 
                     ++n;
                 }
             }
-            attend_one(q + ((size_t)i * Hq + h) * d, kr, vr, n, d, scale, z,
+            const int64_t qi = q_compact ? r : i;  /* compact q holds only the listed rows */
+            attend_one(q + ((size_t)qi * Hq + h) * d, kr, vr, n, d, scale, z,
                        o + ((size_t)r * Hq + h) * d, lse + (size_t)h * nrows + r);
         }
         free(kr);

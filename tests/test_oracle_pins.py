@@ -337,3 +337,18 @@ def test_index_scores_exact_in_fp32():
     assert torch.equal(f32_fwd.double(), exact) and torch.equal(f32_rev.double(), exact)
     ones = torch.ones(128, dtype=torch.float64)
     assert float(ones @ ones) == 128.0
+
+
+def test_compact_query_rows_match_full():
+    L, B, Hq, G, d, di, k = 80, 8, 4, 2, 16, 8, 3
+    q = synthetic.normal_bf16(31, 1, (L, Hq, d))
+    kk = synthetic.normal_bf16(31, 2, (L, G, d))
+    vv = synthetic.normal_bf16(31, 3, (L, G, d))
+    rows = np.array([0, 7, 8, 40, 79])
+    sel = oracle.select_prefill(synthetic.int8th(31, 4, (L, G, di)),
+                                synthetic.int8th(31, 5, (L, di)), B, k, rows=rows)
+    o1, l1 = oracle.attn_prefill(q, kk, vv, sel, B, k, 0.3, rows=rows)
+    o2, l2 = oracle.attn_prefill(q[torch.tensor(rows)], kk, vv, sel, B, k, 0.3, rows=rows,
+                                 q_compact=True)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)

@@ -219,15 +219,20 @@ __global__ void sched_fill_kernel(SchedArgs a) {
 }
 
 // ------------------------------------------------------------------------------------------
-// KV-outer attention.  One persistent CTA per SM walks the work items; per item it stages
-// K_b and V_b of group g (TMA, double-buffered across items) and the item's token list, then
-// for every tile of 8 tokens gathers their 16 query heads (TMA, 16 rows per token) and runs
+// KV-outer attention.  One persistent CTA per SM walks its work items; per item it stages K_b
+// and V_b of group g (TMA; V converted to fp16 in place) and the item's token list, then for
+// every tile of 8 tokens gathers their 16 query heads (TMA, 16 rows per token) and runs
 //   S = Q K^T (tcgen05, fp32 in TMEM) -> softmax rows (causal limit only in the local block)
 //   -> P (fp16, written back into the same TMEM columns) -> O = P V (tcgen05, A from TMEM)
-//   -> unnormalised partial O (fp16) + row max m and log-sum-exp per (token, head, slot).
-// Roles (16 warps): 0 TMA producer + token-list staging, 1 TMEM owner + MMA issuer,
-// 2-3 V converter (bf16 -> fp16 in place), 4-7 softmax of even tiles, 8-11 softmax of odd
-// tiles, 12-15 epilogue.  TMEM: columns [0,256) two S/P slots, [256,512) two O slots.
+//   -> unnormalised partial O (fp16, staged and stored with TMA) + row max m and log-sum-exp.
+// Roles (16 warps): 0 query-gather producer + token-list staging, 1 TMEM owner + MMA issuer,
+// 2 K loader, 3 V loader + fp16 converter, 4-7 softmax of even tiles, 8-11 softmax of odd
+// tiles, 12-15 epilogue.
+// TMEM: columns [0,384) three S/P slots (tile T uses slot T % 3), [384,512) the O accumulator.
+// The MMA issuer keeps two tiles ahead: S of tile T+2 is issued before P.V of tile T, so a
+// softmax warpgroup finds its next S ready when it finishes a tile.  K and V are single-buffered
+// with separate loaders (K paced by the QK^T cursor, V by the P.V cursor), which frees shared
+// memory for a three-deep query ring that covers the gather latency.
 // ------------------------------------------------------------------------------------------
 struct AttnArgs {
   const int4* items;
@@ -247,16 +252,35 @@ struct ItemMeta {
   int32_t tok[kItemTokens];  // (token << 4) | slot
 };
 
-constexpr int kQStages = 2;
-constexpr uint32_t kSmemKV = 0;                            // 2 x (K 32 KB + V 32 KB)
-constexpr uint32_t kSmemQ = 131072;                        // 2 x 32 KB
+constexpr int kQStages = 3;
+constexpr int kMetaRing = 4;  // > items that can be in flight between the gather and the epilogue
+constexpr uint32_t kSmemK = 0;                             // K of the current item (32 KB)
+constexpr uint32_t kSmemV = 32768;                         // V of the current item (32 KB)
+constexpr uint32_t kSmemQ = 65536;                         // 3 x 32 KB
 constexpr uint32_t kSmemO = kSmemQ + kQStages * 32768;     // O staging tile for TMA stores
-constexpr uint32_t kSmemMeta = kSmemO + 32768;             // 2 x ItemMeta
-constexpr uint32_t kSmemBar = kSmemMeta + 2 * sizeof(ItemMeta);
-constexpr uint32_t kAttnSmem = kSmemBar + 256 + 1024;
+constexpr uint32_t kSmemMeta = kSmemO + 32768;             // 4 x ItemMeta
+constexpr uint32_t kSmemBar = kSmemMeta + kMetaRing * sizeof(ItemMeta);
+constexpr uint32_t kAttnBarBytes = 512;
+constexpr uint32_t kAttnSmem = kSmemBar + kAttnBarBytes + 1024;
 static_assert(kAttnSmem <= 232448, "attention kernel shared memory");
 constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, false, false);
 constexpr uint32_t kIdescPV = idesc_f16_f32(128, 128, false, true);  // P, V in fp16
+
+// barrier block offsets (bytes from kSmemBar)
+constexpr uint32_t kBMetaFull = 0;     // [4]
+constexpr uint32_t kBMetaEmpty = 32;   // [4]
+constexpr uint32_t kBKFull = 64, kBKEmpty = 72, kBVFull = 80, kBVEmpty = 88, kBVReady = 96;
+constexpr uint32_t kBQFull = 104;      // [3]
+constexpr uint32_t kBQEmpty = 128;     // [3]
+constexpr uint32_t kBSFull = 152;      // [6]: slot * 2 + softmax warpgroup
+constexpr uint32_t kBPFull = 200;      // [6]
+constexpr uint32_t kBSPFree = 248;     // [3]
+constexpr uint32_t kBOFull = 272, kBOEmpty = 280, kBDrain = 288;
+constexpr uint32_t kTmemSlot = 296, kAbort = 300;
+static_assert(kBQFull + 8 * kQStages <= kBQEmpty && kBQEmpty + 8 * kQStages <= kBSFull, "bars");
+static_assert(kBSFull + 48 <= kBPFull && kBPFull + 48 <= kBSPFree && kBSPFree + 24 <= kBOFull,
+              "bars");
+static_assert(kAbort + 4 <= kAttnBarBytes, "bars");
 
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
@@ -285,41 +309,45 @@ __global__ void __launch_bounds__(512, 1)
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t base = smem_u32(smem);
   const uint32_t bars = base + kSmemBar;
-  auto kv_full = [&](int s) { return bars + 8 * s; };
-  auto kv_empty = [&](int s) { return bars + 16 + 8 * s; };
-  auto meta_empty = [&](int s) { return bars + 32 + 8 * s; };
-  auto v_ready = [&](int s) { return bars + 48 + 8 * s; };
-  auto q_full = [&](int s) { return bars + 64 + 8 * s; };
-  auto q_empty = [&](int s) { return bars + 88 + 8 * s; };
-  auto s_full = [&](int s) { return bars + 112 + 8 * s; };
-  auto p_full = [&](int s) { return bars + 128 + 8 * s; };
-  auto sp_free = [&](int s) { return bars + 144 + 8 * s; };
-  auto o_full = [&](int s) { return bars + 160 + 8 * s; };
-  auto o_empty = [&](int s) { return bars + 176 + 8 * s; };
-  const uint32_t drain_bar = bars + 192;
-  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + kSmemBar + 200);
-  volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + kSmemBar + 204);
+  auto meta_full = [&](int r) { return bars + kBMetaFull + 8 * r; };
+  auto meta_empty = [&](int r) { return bars + kBMetaEmpty + 8 * r; };
+  const uint32_t k_full = bars + kBKFull, k_empty = bars + kBKEmpty;
+  const uint32_t v_full = bars + kBVFull, v_empty = bars + kBVEmpty, v_ready = bars + kBVReady;
+  auto q_full = [&](int s) { return bars + kBQFull + 8 * s; };
+  auto q_empty = [&](int s) { return bars + kBQEmpty + 8 * s; };
+  auto s_full = [&](int sw) { return bars + kBSFull + 8 * sw; };
+  auto p_full = [&](int sw) { return bars + kBPFull + 8 * sw; };
+  auto sp_free = [&](int s) { return bars + kBSPFree + 8 * s; };
+  const uint32_t o_full = bars + kBOFull, o_empty = bars + kBOEmpty;
+  const uint32_t drain_bar = bars + kBDrain;
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + kSmemBar + kTmemSlot);
+  volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + kSmemBar + kAbort);
   ItemMeta* meta = reinterpret_cast<ItemMeta*>(smem + kSmemMeta);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_items = *a.n_items;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(kv_full(s), 1);
-      mbar_init(kv_empty(s), 1);
-      mbar_init(meta_empty(s), 128);
-      mbar_init(v_ready(s), 64);
-      mbar_init(s_full(s), 1);
-      mbar_init(p_full(s), 128);
-      mbar_init(sp_free(s), 1);
-      mbar_init(o_full(s), 1);
-      mbar_init(o_empty(s), 128);
+    for (int r = 0; r < kMetaRing; ++r) {
+      mbar_init(meta_full(r), 1);
+      mbar_init(meta_empty(r), 128);
     }
-    for (int s = 0; s < kQStages; ++s) {
-      mbar_init(q_full(s), 1);
-      mbar_init(q_empty(s), 1);
+    mbar_init(k_full, 1);
+    mbar_init(k_empty, 1);
+    mbar_init(v_full, 1);
+    mbar_init(v_empty, 1);
+    mbar_init(v_ready, 32);
+    for (int q = 0; q < kQStages; ++q) {
+      mbar_init(q_full(q), 1);
+      mbar_init(q_empty(q), 1);
     }
+    for (int sw = 0; sw < 6; ++sw) {
+      mbar_init(s_full(sw), 1);
+      mbar_init(p_full(sw), 128);
+    }
+    for (int q = 0; q < 3; ++q) mbar_init(sp_free(q), 1);
+    mbar_init(o_full, 1);
+    mbar_init(o_empty, 128);
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -334,24 +362,20 @@ __global__ void __launch_bounds__(512, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
-    // ------------------------------- producer -------------------------------
-    int T = 0, nit = 0, kv_issued = 0, q_issued = 0;
+    // --------------------- token lists + query gathers ---------------------
+    int T = 0, q_issued = 0;
     bool ok = true;
-    if (lane == 0) {
-      tma_prefetch_map(&map_q);
-      tma_prefetch_map(&map_k);
-      tma_prefetch_map(&map_v);
-    }
-    for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x, ++nit) {
-      const int kvs = nit & 1, par = ((nit >> 1) & 1) ^ 1;
-      const bool free_ok = !*abort_flag && mbar_wait(kv_empty(kvs), par, a.wait_ns) &&
-                           mbar_wait(meta_empty(kvs), par, a.wait_ns);
-      if (!__all_sync(0xffffffffu, free_ok)) {
+    if (lane == 0) tma_prefetch_map(&map_q);
+    for (int it = blockIdx.x, n = 0; ok && it < n_items; it += gridDim.x, ++n) {
+      const int r = n % kMetaRing;
+      if (!__all_sync(0xffffffffu, !*abort_flag && mbar_wait(meta_empty(r),
+                                                             ((n / kMetaRing) & 1) ^ 1,
+                                                             a.wait_ns))) {
         ok = false;
         break;
       }
       const int4 item = a.items[it];
-      ItemMeta& m = meta[kvs];
+      ItemMeta& m = meta[r];
       for (int j = lane; j < item.w; j += 32) m.tok[j] = a.list[item.z + j];
       if (lane == 0) {
         m.g = item.x;
@@ -359,15 +383,7 @@ __global__ void __launch_bounds__(512, 1)
         m.count = item.w;
       }
       __syncwarp();
-      if (lane == 0) {
-        const uint32_t kb = base + kSmemKV + kvs * 65536u;
-        mbar_arrive_expect_tx(kv_full(kvs), 65536);
-        tma_load_3d(kb, &map_k, kv_full(kvs), 0, item.x, item.y * kBlock);
-        tma_load_3d(kb + kPanel, &map_k, kv_full(kvs), 64, item.x, item.y * kBlock);
-        tma_load_3d(kb + 32768, &map_v, kv_full(kvs), 0, item.x, item.y * kBlock);
-        tma_load_3d(kb + 32768 + kPanel, &map_v, kv_full(kvs), 64, item.x, item.y * kBlock);
-      }
-      ++kv_issued;
+      if (lane == 0) mbar_arrive(meta_full(r));
       for (int t0 = 0; t0 < item.w; t0 += kTileTokens, ++T) {
         const int qs = T % kQStages;
         if (!__all_sync(0xffffffffu, !*abort_flag && mbar_wait(q_empty(qs),
@@ -376,11 +392,11 @@ __global__ void __launch_bounds__(512, 1)
           ok = false;
           break;
         }
-        const int n = min(kTileTokens, item.w - t0);
+        const int nt = min(kTileTokens, item.w - t0);
         const uint32_t qb = base + kSmemQ + qs * 32768u;
-        if (lane == 0) mbar_arrive_expect_tx(q_full(qs), n * 4096);
+        if (lane == 0) mbar_arrive_expect_tx(q_full(qs), nt * 4096);
         __syncwarp();
-        if (lane < 2 * n) {  // lanes 0..2n-1: token lane/2, 64-column half lane%2
+        if (lane < 2 * nt) {  // lanes 0..2n-1: token lane/2, 64-column half lane%2
           const int tk = lane >> 1, half = lane & 1;
           const int i = m.tok[t0 + tk] >> 4;
           tma_load_3d(qb + half * kPanel + tk * 2048, &map_q, q_full(qs), half * 64,
@@ -392,108 +408,161 @@ __global__ void __launch_bounds__(512, 1)
     if (!ok) {
       if (lane == 0) report_status(a.status, kStatusTimeout);
       *abort_flag = 1;
-      // let in-flight copies land before the CTA can exit (at most one per stage)
-      if (lane == 0) {
-        for (int x = (kv_issued > 2 ? kv_issued - 2 : 0); x < kv_issued; ++x)
-          mbar_wait(kv_full(x & 1), (x >> 1) & 1, a.wait_ns);
+      if (lane == 0)  // let in-flight gathers land before the CTA can exit
         for (int x = (q_issued > kQStages ? q_issued - kQStages : 0); x < q_issued; ++x)
-          mbar_wait(q_full(x % kQStages), (x / kQStages) & 1, a.wait_ns);
-      }
+          mbar_wait(q_full(x % kQStages), (x / kQStages) & 1, kDefaultWaitNs);
     }
   } else if (warp == 1) {
     // ------------------------------- MMA issuer -------------------------------
     if (lane == 0) {
       bool ok = true;
-      int T = 0, nit = 0;
-      int pend_T = -1, pend_kvs = 0, pend_nit = 0;
-      bool pend_last = false, pend_first = false;
-      // O[slot] = P[slot] . V (PV of tile Tp); frees the S/P slot, and the K/V stage after the
-      // last tile of its item
-      auto issue_pv = [bars, tmem, base](int Tp, int kvs, int nitp, bool first_of_item,
-                                         bool last_of_item, uint64_t wait_ns) -> bool {
-        const int slot = Tp & 1, use = Tp >> 1;
-        // V of this stage has been converted to fp16 in place before its first use
-        if (first_of_item && !mbar_wait(bars + 48 + 8 * kvs, (nitp >> 1) & 1, wait_ns))
-          return false;
-        if (!mbar_wait(bars + 128 + 8 * slot, use & 1, wait_ns)) return false;         // p_full
-        if (!mbar_wait(bars + 176 + 8 * slot, (use & 1) ^ 1, wait_ns)) return false;   // o_empty
-        tc_fence_after();
-        const uint32_t d = tmem + 256 + slot * 128;
-        const uint32_t pa = tmem + slot * 128;
-        const uint32_t vb = base + kSmemKV + kvs * 65536u + 32768;
+      // cursor A issues S = Q K^T, cursor B issues O = P V, two tiles behind A
+      int a_it = blockIdx.x, a_n = 0, a_t0 = 0, a_cnt = -1, a_T = 0;
+      int b_it = blockIdx.x, b_n = 0, b_t0 = 0, b_cnt = -1, b_T = 0;
+      // Non-blocking scheduler: each pass issues the next S if its slot, query tile and K are
+      // ready, and the next P.V if its P and the O accumulator are; neither cursor waits for the
+      // other, so the tensor pipe sees work as soon as any of it is ready.  Each chain is
+      // committed on its own: a commit covers every MMA issued before it, so grouping the K-steps
+      // of several tiles would hold back the softmax and the O drain until the whole group is done
+      // (measured slower, although interleaved chains use the tensor pipe better).
+      uint64_t idle_since = 0;
+      bool idle = false;
+      while (ok && b_it < n_items) {
+        bool progressed = false;
+        // ---- S = Q K^T for tile a_T (at most three tiles ahead: one per S/P slot) ----
+        if (a_it < n_items && a_T - b_T < 3) {
+          if (a_cnt < 0 && mbar_try_wait(meta_full(a_n % kMetaRing), (a_n / kMetaRing) & 1) &&
+              mbar_try_wait(k_full, a_n & 1)) {
+            a_cnt = meta[a_n % kMetaRing].count;
+            a_t0 = 0;
+          }
+          const int qs = a_T % kQStages, s3 = a_T % 3;
+          if (a_cnt >= 0 && mbar_try_wait(q_full(qs), (a_T / kQStages) & 1) &&
+              mbar_try_wait(sp_free(s3), ((a_T / 3) & 1) ^ 1)) {
+            tc_fence_after();
+            const uint32_t d = tmem + s3 * 128;
+            const uint32_t qb = base + kSmemQ + qs * 32768u, kb = base + kSmemK;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_f16_ts(d, pa + kk * 8, sdesc_sw128(vb + kk * 2048, kPanel, 1024), kIdescPV, kk > 0);
-        mma_commit(bars + 160 + 8 * slot);  // o_full
-        mma_commit(bars + 144 + 8 * slot);  // sp_free
-        if (last_of_item) mma_commit(bars + 16 + 8 * kvs);  // kv_empty
-        return true;
-      };
-      for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x, ++nit) {
-        const int kvs = nit & 1;
-        if (*abort_flag || !mbar_wait(kv_full(kvs), (nit >> 1) & 1, a.wait_ns)) {
-          ok = false;
-          break;
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 32;
+              mma_bf16_ss(d, sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
+                          kIdescQK, kk > 0);
+            }
+            mma_commit(s_full(s3 * 2 + (a_T & 1)));
+            mma_commit(q_empty(qs));
+            ++a_T;
+            a_t0 += kTileTokens;
+            if (a_t0 >= a_cnt) {  // the item's last S: K may be replaced once these are done
+              mma_commit(k_empty);
+              a_it += gridDim.x;
+              ++a_n;
+              a_cnt = -1;
+            }
+            progressed = true;
+          }
         }
-        tc_fence_after();
-        const int count = meta[kvs].count;
-        const uint32_t kb = base + kSmemKV + kvs * 65536u;
-        for (int t0 = 0; t0 < count; t0 += kTileTokens, ++T) {
-          const int qs = T % kQStages, slot = T & 1, use = T >> 1;
-          if (*abort_flag || !mbar_wait(q_full(qs), (T / kQStages) & 1, a.wait_ns) ||
-              !mbar_wait(sp_free(slot), (use & 1) ^ 1, a.wait_ns)) {
-            ok = false;
-            break;
+        // ---- O = P V for tile b_T ----
+        if (b_T < a_T) {
+          if (b_cnt < 0 && mbar_try_wait(v_ready, b_n & 1)) {  // cursor A opened the item
+            b_cnt = meta[b_n % kMetaRing].count;
+            b_t0 = 0;
           }
-          tc_fence_after();
-          const uint32_t d = tmem + slot * 128;
-          const uint32_t qb = base + kSmemQ + qs * 32768u;
+          const int s3 = b_T % 3;
+          if (b_cnt >= 0 && mbar_try_wait(p_full(s3 * 2 + (b_T & 1)), (b_T / 6) & 1) &&
+              mbar_try_wait(o_empty, (b_T & 1) ^ 1)) {
+            tc_fence_after();
+            const uint32_t pa = tmem + s3 * 128, vb = base + kSmemV;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 32;
-            mma_bf16_ss(d, sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
-                        kIdescQK, kk > 0);
+            for (int kk = 0; kk < 8; ++kk)
+              mma_f16_ts(tmem + 384, pa + kk * 8, sdesc_sw128(vb + kk * 2048, kPanel, 1024),
+                         kIdescPV, kk > 0);
+            mma_commit(o_full);
+            mma_commit(sp_free(s3));
+            ++b_T;
+            b_t0 += kTileTokens;
+            if (b_t0 >= b_cnt) {  // the item's last P.V: V may be replaced once it is done
+              mma_commit(v_empty);
+              b_it += gridDim.x;
+              ++b_n;
+              b_cnt = -1;
+            }
+            progressed = true;
           }
-          mma_commit(s_full(slot));
-          mma_commit(q_empty(qs));
-          // PV of the previous tile overlaps the softmax of this one
-          if (pend_T >= 0 &&
-              !issue_pv(pend_T, pend_kvs, pend_nit, pend_first, pend_last, a.wait_ns)) {
+        }
+        if (progressed) {
+          idle = false;
+        } else {
+          const uint64_t now = globaltimer_ns();
+          if (!idle) {
+            idle = true;
+            idle_since = now;
+          } else if (now - idle_since > a.wait_ns || *abort_flag) {
             ok = false;
-            break;
           }
-          pend_T = T;
-          pend_kvs = kvs;
-          pend_nit = nit;
-          pend_first = (t0 == 0);
-          pend_last = (t0 + kTileTokens >= count);
+          __nanosleep(32);
         }
       }
-      if (ok && pend_T >= 0)
-        ok = issue_pv(pend_T, pend_kvs, pend_nit, pend_first, pend_last, a.wait_ns);
       if (!ok) {
         report_status(a.status, kStatusTimeout);
         *abort_flag = 1;
       }
       mma_commit(drain_bar);
-      mbar_wait(drain_bar, 0, a.wait_ns);
+      mbar_wait(drain_bar, 0, kDefaultWaitNs);
     }
-  } else if (warp == 2 || warp == 3) {
-    // ------------------------- V converter: bf16 -> fp16 in place -------------------------
+  } else if (warp == 2) {
+    // ------------------------------- K loader -------------------------------
+    if (lane == 0) {
+      tma_prefetch_map(&map_k);
+      int issued = 0;
+      bool ok = true;
+      for (int it = blockIdx.x, n = 0; it < n_items; it += gridDim.x, ++n) {
+        const int r = n % kMetaRing;
+        if (*abort_flag || !mbar_wait(meta_full(r), (n / kMetaRing) & 1, a.wait_ns) ||
+            !mbar_wait(k_empty, (n & 1) ^ 1, a.wait_ns)) {
+          ok = false;
+          break;
+        }
+        const int g = meta[r].g, b = meta[r].b;
+        mbar_arrive_expect_tx(k_full, 32768);
+        tma_load_3d(base + kSmemK, &map_k, k_full, 0, g, b * kBlock);
+        tma_load_3d(base + kSmemK + kPanel, &map_k, k_full, 64, g, b * kBlock);
+        ++issued;
+      }
+      if (!ok) {
+        report_status(a.status, kStatusTimeout);
+        *abort_flag = 1;
+        if (issued > 0) mbar_wait(k_full, (issued - 1) & 1, kDefaultWaitNs);
+      }
+    }
+  } else if (warp == 3) {
+    // ------------- V loader + converter: bf16 -> fp16 in place -------------
     // Exact for N(0,1)-range values (bf16 carries 8 significant bits, fp16 11); lets P be
     // rounded to fp16 instead of bf16 for the P.V product.
-    const int t = (warp - 2) * 32 + lane;
-    int nit = 0;
+    if (lane == 0) tma_prefetch_map(&map_v);
+    int issued = 0;
     bool ok = true;
-    for (int it = blockIdx.x; it < n_items; it += gridDim.x, ++nit) {
-      const int kvs = nit & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(kv_full(kvs), (nit >> 1) & 1, a.wait_ns))) {
+    for (int it = blockIdx.x, n = 0; it < n_items; it += gridDim.x, ++n) {
+      const int r = n % kMetaRing;
+      const bool okw = !*abort_flag && mbar_wait(meta_full(r), (n / kMetaRing) & 1, a.wait_ns) &&
+                       mbar_wait(v_empty, (n & 1) ^ 1, a.wait_ns);
+      if (!__all_sync(0xffffffffu, okw)) {
         ok = false;
         break;
       }
-      const uint32_t vb = base + kSmemKV + kvs * 65536u + 32768;
+      if (lane == 0) {
+        const int g = meta[r].g, b = meta[r].b;
+        mbar_arrive_expect_tx(v_full, 32768);
+        tma_load_3d(base + kSmemV, &map_v, v_full, 0, g, b * kBlock);
+        tma_load_3d(base + kSmemV + kPanel, &map_v, v_full, 64, g, b * kBlock);
+      }
+      ++issued;
+      if (!__all_sync(0xffffffffu, mbar_wait(v_full, n & 1, a.wait_ns))) {
+        ok = false;
+        break;
+      }
+      const uint32_t vb = base + kSmemV;
 #pragma unroll 4
-      for (int c = t; c < 2048; c += 64) {
+      for (int c = lane; c < 2048; c += 32) {
         uint4 x = ld_shared_v4(vb + c * 16);
         x.x = bf16x2_to_f16x2(x.x);
         x.y = bf16x2_to_f16x2(x.y);
@@ -502,11 +571,12 @@ __global__ void __launch_bounds__(512, 1)
         st_shared_v4(vb + c * 16, x.x, x.y, x.z, x.w);
       }
       fence_proxy_async_smem();
-      mbar_arrive(v_ready(kvs));
+      mbar_arrive(v_ready);
     }
     if (!ok) {
-      report_status(a.status, kStatusTimeout);
+      if (lane == 0) report_status(a.status, kStatusTimeout);
       *abort_flag = 1;
+      if (lane == 0 && issued > 0) mbar_wait(v_full, (issued - 1) & 1, kDefaultWaitNs);
     }
   } else if (warp >= 4 && warp < 12) {
     // ------------------------------- softmax -------------------------------
@@ -514,21 +584,21 @@ __global__ void __launch_bounds__(512, 1)
     const int row = (warp & 3) * 32 + lane;  // TMEM lane = MMA row
     const int tk = row >> 4, hh = row & 15;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t sa = tmem + lane_base + wg * 128;
-    int T = 0, nit = 0;
+    int T = 0;
     bool ok = true;
-    for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x, ++nit) {
-      const int kvs = nit & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(kv_full(kvs), (nit >> 1) & 1, a.wait_ns))) {
+    for (int it = blockIdx.x, n = 0; ok && it < n_items; it += gridDim.x, ++n) {
+      const int r = n % kMetaRing;
+      if (!__all_sync(0xffffffffu, mbar_wait(meta_full(r), (n / kMetaRing) & 1, a.wait_ns))) {
         ok = false;
         break;
       }
-      const ItemMeta& m = meta[kvs];
+      const ItemMeta& m = meta[r];
       const int count = m.count, g = m.g, b = m.b;
       for (int t0 = 0; t0 < count; t0 += kTileTokens, ++T) {
         if ((T & 1) != wg) continue;
-        const int use = T >> 1;
-        if (!__all_sync(0xffffffffu, mbar_wait(s_full(wg), use & 1, a.wait_ns))) {
+        const int s3 = T % 3;
+        const uint32_t sa = tmem + lane_base + s3 * 128;
+        if (!__all_sync(0xffffffffu, mbar_wait(s_full(s3 * 2 + wg), (T / 6) & 1, a.wait_ns))) {
           ok = false;
           break;
         }
@@ -593,7 +663,7 @@ __global__ void __launch_bounds__(512, 1)
         const float l = l2.x + l2.y;
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(p_full(wg));
+        mbar_arrive(p_full(s3 * 2 + wg));
         if (valid) {
           const size_t u = (static_cast<size_t>(i - a.q0) * a.G + g) * a.k + s;
           const float ln2 = 0.6931471805599453f;
@@ -616,42 +686,49 @@ __global__ void __launch_bounds__(512, 1)
     const int row = (warp & 3) * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t stg = base + kSmemO;
-    int T = 0, nit = 0;
-    for (int it = blockIdx.x; it < n_items; it += gridDim.x, ++nit) {
-      const int kvs = nit & 1;
-      const bool okv = !*abort_flag && mbar_wait(kv_full(kvs), (nit >> 1) & 1, a.wait_ns);
-      if (!__all_sync(0xffffffffu, okv)) {
+    int T = 0;
+    for (int it = blockIdx.x, n = 0; it < n_items; it += gridDim.x, ++n) {
+      const int r = n % kMetaRing;
+      const bool okm = !*abort_flag && mbar_wait(meta_full(r), (n / kMetaRing) & 1, a.wait_ns);
+      if (!__all_sync(0xffffffffu, okm)) {
         report_status(a.status, kStatusTimeout);
         *abort_flag = 1;
       }
-      const ItemMeta& m = meta[kvs];
+      const ItemMeta& m = meta[r];
       const int count = min(max(m.count, 0), kItemTokens), g = m.g;
       for (int t0 = 0; t0 < count; t0 += kTileTokens, ++T) {
-        const int slot = T & 1, use = T >> 1;
-        const bool oko = !*abort_flag && mbar_wait(o_full(slot), use & 1, a.wait_ns);
+        if (et < 16) bulk_wait_read0();  // the previous tile's stores have read the staging tile
+        named_barrier(1, 128);
+        const bool oko = !*abort_flag && mbar_wait(o_full, T & 1, a.wait_ns);
         if (!__all_sync(0xffffffffu, oko)) {
           report_status(a.status, kStatusTimeout);
           *abort_flag = 1;
         }
         tc_fence_after();
-        if (et < 16) bulk_wait_read0();  // the previous tile's stores have read the staging tile
-        named_barrier(1, 128);
-        const uint32_t oa = tmem + lane_base + 256 + slot * 128;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t v[32];
-          tmem_ld32(oa + c * 32, v);
+        for (int h = 0; h < 2; ++h) {
+          uint32_t v0[32], v1[32];
+          tmem_ld32(tmem + lane_base + 384 + h * 64, v0);
+          tmem_ld32(tmem + lane_base + 384 + h * 64 + 32, v1);
           tmem_ld_wait();
+          if (h == 1) {  // all of O is in registers or staged: the next tile's P.V may start
+            tc_fence_before();
+            mbar_arrive(o_empty);
+          }
 #pragma unroll
-          for (int u4 = 0; u4 < 4; ++u4)
-            st_shared_v4(stg + sw128_offset(row, c * 32 + u4 * 8, 128),
-                         pack_f16x2(__uint_as_float(v[8 * u4 + 0]), __uint_as_float(v[8 * u4 + 1])),
-                         pack_f16x2(__uint_as_float(v[8 * u4 + 2]), __uint_as_float(v[8 * u4 + 3])),
-                         pack_f16x2(__uint_as_float(v[8 * u4 + 4]), __uint_as_float(v[8 * u4 + 5])),
-                         pack_f16x2(__uint_as_float(v[8 * u4 + 6]), __uint_as_float(v[8 * u4 + 7])));
+          for (int u4 = 0; u4 < 4; ++u4) {
+            st_shared_v4(stg + sw128_offset(row, h * 64 + u4 * 8, 128),
+                         pack_f16x2(__uint_as_float(v0[8 * u4 + 0]), __uint_as_float(v0[8 * u4 + 1])),
+                         pack_f16x2(__uint_as_float(v0[8 * u4 + 2]), __uint_as_float(v0[8 * u4 + 3])),
+                         pack_f16x2(__uint_as_float(v0[8 * u4 + 4]), __uint_as_float(v0[8 * u4 + 5])),
+                         pack_f16x2(__uint_as_float(v0[8 * u4 + 6]), __uint_as_float(v0[8 * u4 + 7])));
+            st_shared_v4(stg + sw128_offset(row, h * 64 + 32 + u4 * 8, 128),
+                         pack_f16x2(__uint_as_float(v1[8 * u4 + 0]), __uint_as_float(v1[8 * u4 + 1])),
+                         pack_f16x2(__uint_as_float(v1[8 * u4 + 2]), __uint_as_float(v1[8 * u4 + 3])),
+                         pack_f16x2(__uint_as_float(v1[8 * u4 + 4]), __uint_as_float(v1[8 * u4 + 5])),
+                         pack_f16x2(__uint_as_float(v1[8 * u4 + 6]), __uint_as_float(v1[8 * u4 + 7])));
+          }
         }
-        tc_fence_before();
-        mbar_arrive(o_empty(slot));
         fence_proxy_async_smem();
         named_barrier(1, 128);
         if (et < 16) {
@@ -665,7 +742,7 @@ __global__ void __launch_bounds__(512, 1)
           bulk_commit();
         }
       }
-      mbar_arrive(meta_empty(kvs));
+      mbar_arrive(meta_empty(r));
     }
     if (et < 16) bulk_wait0();
   }

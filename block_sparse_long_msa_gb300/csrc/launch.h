@@ -9,7 +9,9 @@
 
 namespace msa {
 
-size_t index_prefill_smem_bytes(int G, int ns);
+// Keys per tile of the prefill index kernel (two blocks): the box height of its key tensor map.
+constexpr int kIndexKeyTile = 256;
+size_t index_prefill_smem_bytes(int gpc, int ns);
 cudaError_t launch_index_select_prefill(const CUtensorMap& map_q, const CUtensorMap& map_k,
                                         int64_t L, int G, int k, int32_t* sel, float* sel_score,
                                         int32_t* status, uint64_t wait_ns, cudaStream_t stream);

@@ -172,7 +172,7 @@ msa_status_t msa_index_select(const msa_config_t* cfg, const void* q_idx, const 
   {
     const uint64_t dims[2] = {kDim, static_cast<uint64_t>(L)};
     const uint64_t strides[1] = {kDim * 2};
-    const uint32_t box[2] = {64, kBlock};
+    const uint32_t box[2] = {64, msa::kIndexKeyTile};
     if (!make_map(&mk, k_idx, 2, dims, strides, box)) return MSA_ERR_CUDA;
   }
   cudaError_t e = msa::launch_index_select_prefill(mq, mk, L, G, cfg->topk, sel, sel_score,

@@ -33,22 +33,23 @@ struct TopList {
       b[p] = 0x7fffffff;
     }
   }
-  // Insert (score, block) if it ranks before the current last entry.
+  // Insert (score, block) if it ranks before the current last entry.  Branch-free: walking from
+  // the tail, entry p takes entry p-1 when the new pair ranks before p-1, the new pair when it
+  // ranks before p only, and stays otherwise (the list is sorted, so these tests are monotone).
+  // The warp skips the walk when none of its lanes has anything to insert.
   __device__ __forceinline__ void insert(float score, int32_t block) {
-    if (!ranks_before(score, block, s[kListMax - 1], b[kListMax - 1])) return;
-    float cs = score;
-    int32_t cb = block;
+    const bool any = ranks_before(score, block, s[kListMax - 1], b[kListMax - 1]);
+    if (!__any_sync(__activemask(), any)) return;
+    bool c_here = any;  // the new pair ranks before entry p (p = kListMax - 1 first)
 #pragma unroll
-    for (int p = 0; p < kListMax; ++p) {
-      if (ranks_before(cs, cb, s[p], b[p])) {
-        const float ts = s[p];
-        const int32_t tb = b[p];
-        s[p] = cs;
-        b[p] = cb;
-        cs = ts;
-        cb = tb;
-      }
+    for (int p = kListMax - 1; p > 0; --p) {
+      const bool c_prev = ranks_before(score, block, s[p - 1], b[p - 1]);
+      s[p] = c_prev ? s[p - 1] : (c_here ? score : s[p]);
+      b[p] = c_prev ? b[p - 1] : (c_here ? block : b[p]);
+      c_here = c_prev;
     }
+    s[0] = c_here ? score : s[0];
+    b[0] = c_here ? block : b[0];
   }
   // Keep the first `keep` entries (by rank), then sort them by ascending block id; entries past
   // `keep` become (-inf, INT_MAX) and sort to the end.

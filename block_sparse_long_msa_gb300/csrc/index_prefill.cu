@@ -199,24 +199,29 @@ __global__ void __launch_bounds__(384, 1)
         break;
       }
       tc_fence_after();
+      // 64-column loads reduced with four independent max chains; the slot is released as soon
+      // as the last load has landed
       float mx[2];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        float m = -__int_as_float(0x7f800000);
+        const float ninf = -__int_as_float(0x7f800000);
+        float m4[4] = {ninf, ninf, ninf, ninf};
 #pragma unroll 1
-        for (int c = 0; c < 4; c += 2) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t v0[32], v1[32];
-          tmem_ld32(acc + h * kBlock + c * 32, v0);
-          tmem_ld32(acc + h * kBlock + c * 32 + 32, v1);
+          tmem_ld32(acc + h * kBlock + c * 64, v0);
+          tmem_ld32(acc + h * kBlock + c * 64 + 32, v1);
           tmem_ld_wait();
+          if (h == 1 && c == 1) {
+            tc_fence_before();
+            mbar_arrive(acc_empty(e));
+          }
 #pragma unroll
           for (int q = 0; q < 32; ++q)
-            m = fmaxf(m, fmaxf(__uint_as_float(v0[q]), __uint_as_float(v1[q])));
+            m4[q & 3] = fmaxf(m4[q & 3], fmaxf(__uint_as_float(v0[q]), __uint_as_float(v1[q])));
         }
-        mx[h] = m;
+        mx[h] = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
       }
-      tc_fence_before();
-      mbar_arrive(acc_empty(e));
       list.insert(mx[0], 2 * t);
       if (2 * t + 1 < nkey) list.insert(mx[1], 2 * t + 1);
     }

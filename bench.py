@@ -157,15 +157,15 @@ KERNEL_SOURCES = {
 }
 NCU_TRAFFIC = {
     # prefill L=32768, 64/4 heads, k=16 (profiles/dram_prefill_L32K_decode_b64.md)
-    "attention": {"bytes_per_launch": 3140837120 + 8547729920,
-                  "sources_sha256": "0fba90eeaca37c9f537b85afeec60b347cbb306fe01a773fe4955fb15057355a"},
-    "combine": {"bytes_per_launch": 8622441984 + 540351488,
-                "sources_sha256": "0fba90eeaca37c9f537b85afeec60b347cbb306fe01a773fe4955fb15057355a"},
-    "index": {"bytes_per_launch": 41820160 + 16384,
-              "sources_sha256": "ba46e6dc27fdf2dbe0eae8db725358e962ca15fa074a392a0248472322a39eab"},
+    "attention": {"bytes_per_launch": 3202479872 + 8546904064,
+                  "sources_sha256": "68df3ccf3ddf94e6580a1d87845fe5d770a4c048db8877e2338a4469c1ce6aa4"},
+    "combine": {"bytes_per_launch": 8622035456 + 540562688,
+                "sources_sha256": "68df3ccf3ddf94e6580a1d87845fe5d770a4c048db8877e2338a4469c1ce6aa4"},
+    "index": {"bytes_per_launch": 41900928 + 0,
+              "sources_sha256": "b67b36e49d74a6877630e328b26f99272e16815b25e578620b481c2d1e912d1f"},
     # decode, 64 sequences of 16K-256K tokens
-    "decode_scan": {"bytes_per_launch": 2080732928 + 7241216,
-                    "sources_sha256": "cde950c8ec201b6a80ca88fd24b39d3bb13304dd82137808726d802d94dfed68"},
+    "decode_scan": {"bytes_per_launch": 2080786816 + 7407104,
+                    "sources_sha256": "e0fbab574ffee4cd8dac665041d72c0e6d11514299c923a681c53a84d1864415"},
 }
 
 

@@ -157,14 +157,15 @@ KERNEL_SOURCES = {
 }
 NCU_TRAFFIC = {
     # prefill L=32768, 64/4 heads, k=16 (profiles/dram_prefill_L32K_decode_b64.md)
-    "attention": {"bytes_per_launch": 3202479872 + 8546904064,
+    "attention": {"bytes_per_launch": 3202479872 + 8546904064, "workload": "prefill_L32K@32768",
                   "sources_sha256": "68df3ccf3ddf94e6580a1d87845fe5d770a4c048db8877e2338a4469c1ce6aa4"},
-    "combine": {"bytes_per_launch": 8622035456 + 540562688,
+    "combine": {"bytes_per_launch": 8622035456 + 540562688, "workload": "prefill_L32K@32768",
                 "sources_sha256": "68df3ccf3ddf94e6580a1d87845fe5d770a4c048db8877e2338a4469c1ce6aa4"},
-    "index": {"bytes_per_launch": 41900928 + 0,
+    "index": {"bytes_per_launch": 41900928 + 0, "workload": "prefill_L32K@32768",
               "sources_sha256": "b67b36e49d74a6877630e328b26f99272e16815b25e578620b481c2d1e912d1f"},
     # decode, 64 sequences of 16K-256K tokens
     "decode_scan": {"bytes_per_launch": 2080786816 + 7407104,
+                    "workload": "decode_b64_16K_256K@64x262144",
                     "sources_sha256": "e0fbab574ffee4cd8dac665041d72c0e6d11514299c923a681c53a84d1864415"},
 }
 
@@ -178,9 +179,11 @@ def sources_sha256(kernel: str) -> str:
     return h.hexdigest()
 
 
-def measured_traffic(kernel: str):
+def measured_traffic(kernel: str, workload: str):
+    """ncu DRAM bytes per launch, or None unless they were taken on this workload with the
+    current kernel sources."""
     t = NCU_TRAFFIC.get(kernel)
-    if not t or t["sources_sha256"] != sources_sha256(kernel):
+    if not t or t["workload"] != workload or t["sources_sha256"] != sources_sha256(kernel):
         return None
     return t["bytes_per_launch"]
 
@@ -341,7 +344,7 @@ def run_msa(args, world, rank):
     }
     dominant = max(("index", "attention", "combine"), key=lambda n: phase[n])
     bound, achieved, peak, unit = roof[dominant]
-    traffic = measured_traffic(dominant)
+    traffic = measured_traffic(dominant, f"{w.name}@{L}")
 
     # ---------------- end-to-end through the public API from pinned host buffers ------------
     e2e_on = args.e2e_steps > 0
@@ -419,7 +422,8 @@ def run_msa(args, world, rank):
         "roofline": {"bound": "hbm", "kernel": "index page scan (+ top-k merge)",
                      "achieved": dec_scan_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": dec_scan_gbs / peaks["hbm_gbs"],
-                     "traffic": measured_traffic("decode_scan"),
+                     "traffic": measured_traffic("decode_scan",
+                                                 f"{dw.name}@{dw.batch}x{dw.n_hi}"),
                      "peak_source": peaks["source"]},
         "attention_roofline": {"bound": "hbm", "achieved": dec_attn_gbs, "peak": peaks["hbm_gbs"],
                                "unit": "GB/s", "frac": dec_attn_gbs / peaks["hbm_gbs"]},
@@ -445,7 +449,9 @@ def run_msa(args, world, rank):
                    "k": w.k, "parallelism": f"replicas x{world}",
                    "step": "prefill (index select + main branch over all L queries) + one paged "
                            "decode step of the 64-sequence workload; value = prefill tokens/s",
-                   "l2": "inputs larger than L2 (q 512 MiB) and ~8.6 GiB of partials per step"},
+                   "l2": f"inputs larger than L2 (q {L * w.Hq * w.d * 2 / 2**20:.0f} MiB) and "
+                         f"{work['units'] * w.hpg * (w.d * 2 + 8) / 2**30:.1f} GiB of partials "
+                         f"per step"},
         "phases_ms_per_step": {k: v / args.steps for k, v in phase.items()},
         "prefill_ms_per_step": prefill_ms,
         "gpu_launches": (launches_per_step + dec_launches) * args.steps,

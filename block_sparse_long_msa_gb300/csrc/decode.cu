@@ -327,8 +327,9 @@ __global__ void __launch_bounds__(128) decode_topk_kernel(TopkArgs a) {
 // ------------------------------------------------------------------------------------------
 // Decode attention: one unit per (sequence, group, slot).  A persistent CTA takes a contiguous
 // range of units; warp 0 stages each unit's K and V page tiles (TMA, 128-byte swizzle), warps
-// 1-4 each take 32 keys: S = q K^T and O = P V with m16n8k16 MMAs (M = the group's 16 heads),
-// then the four warps' partial softmax states are merged in shared memory.
+// 1-4 each score 32 keys (S = q K^T with m16n8k16 MMAs, M = the group's 16 heads), exchange row
+// maxima, sums and their slice of P through shared memory, and then each computes O = P V for 32
+// of the 128 output dimensions over all the page's keys, written straight to the partial.
 // ------------------------------------------------------------------------------------------
 struct DecAttnArgs {
   const __nv_bfloat16* q;  // [batch][G*16][128]
@@ -344,12 +345,21 @@ struct DecAttnArgs {
   uint64_t wait_ns;
 };
 
-constexpr int kDecStages = 2;
+constexpr int kDecStages = 3;
 constexpr uint32_t kDecStage = 65536;
-constexpr uint32_t kDecRed = kDecStages * kDecStage;          // 4 warps x 16 x 128 fp32
-constexpr uint32_t kDecML = kDecRed + 4 * kHeads * kDim * 4;  // 4 warps x 16 x (m, l)
-constexpr uint32_t kDecBar = kDecML + 4 * kHeads * 8;
+// Per unit the four warps exchange their row maxima and row sums and the bf16 P tile (16 rows x
+// 128 keys, 128-byte swizzled panels); two copies, by unit parity, so a warp may start the next
+// unit while another still reads this one's.
+constexpr uint32_t kDecP = kDecStages * kDecStage;  // 2 x 4 KB
+constexpr uint32_t kDecPBytes = kHeads * kBlock * 2;
+constexpr uint32_t kDecML = kDecP + 2 * kDecPBytes;  // 2 x (max, sum) x 4 warps x 16 rows fp32
+constexpr uint32_t kDecBar = kDecML + 2 * 2 * 4 * kHeads * 4;
+constexpr uint32_t kDecBarFull = 0, kDecBarEmpty = 32, kDecAbort = 64;
 constexpr uint32_t kDecSmem = kDecBar + 128 + 1024;
+static_assert(kDecBarFull + 8 * kDecStages <= kDecBarEmpty, "decode attention barriers");
+static_assert(kDecBarEmpty + 8 * kDecStages <= kDecAbort, "decode attention barriers");
+static_assert(kDecAbort + 4 <= 128, "decode attention barriers");
+static_assert(kDecSmem <= 232448, "decode attention shared memory");
 
 struct UnitInfo {
   int s, g, b, page, lim;
@@ -379,6 +389,12 @@ __device__ __forceinline__ uint32_t swz(uint32_t tile, int row, int chunk) {
   return tile + (chunk >> 3) * kPanel + row * 128 + (((chunk & 7) ^ (row & 7)) << 4);
 }
 
+// The 16 x 128 bf16 P tile: two 64-key panels of 16 rows x 128 bytes, 16-byte chunks XOR-swizzled
+// by row, so the stores of a warp and the ldmatrix reads both spread over all banks.
+__device__ __forceinline__ uint32_t dec_p_addr(uint32_t tile, int row, int chunk) {
+  return tile + (chunk >> 3) * (kHeads * 128) + row * 128 + (((chunk & 7) ^ (row & 7)) << 4);
+}
+
 __global__ void __launch_bounds__(160, 1)
     decode_attn_kernel(const __grid_constant__ CUtensorMap map_kp,
                        const __grid_constant__ CUtensorMap map_vp, DecAttnArgs a) {
@@ -387,11 +403,10 @@ __global__ void __launch_bounds__(160, 1)
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t base = smem_u32(smem);
   const uint32_t bars = base + kDecBar;
-  auto full = [&](int s) { return bars + 8 * s; };
-  auto empty = [&](int s) { return bars + 16 + 8 * s; };
-  volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + kDecBar + 32);
-  float* red = reinterpret_cast<float*>(smem + kDecRed);
-  float* ml = reinterpret_cast<float*>(smem + kDecML);
+  auto full = [&](int s) { return bars + kDecBarFull + 8 * s; };
+  auto empty = [&](int s) { return bars + kDecBarEmpty + 8 * s; };
+  volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + kDecBar + kDecAbort);
+  float* mlx = reinterpret_cast<float*>(smem + kDecML);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int u0 = blockIdx.x * a.per_cta, u1 = min(a.units, u0 + a.per_cta);
 
@@ -442,11 +457,12 @@ __global__ void __launch_bounds__(160, 1)
   uint32_t qa[8][4];
   int cur_sg = -1;
   int p = 0;
+  const float ninf = -__int_as_float(0x7f800000);
   for (int u = u0; u < u1; ++u) {
     const UnitInfo x = unit_info(a, u, false);
     if (!x.valid) {
       if (w == 0 && lane < kHeads)
-        a.plse[static_cast<size_t>(u) * kHeads + lane] = -__int_as_float(0x7f800000);
+        a.plse[static_cast<size_t>(u) * kHeads + lane] = ninf;
       continue;
     }
     const int sg = x.s * a.G + x.g;
@@ -470,6 +486,10 @@ __global__ void __launch_bounds__(160, 1)
                         // the same barriers, and the status word marks the output invalid
     }
     const uint32_t kt = base + st * kDecStage, vt = kt + 32768;
+    const int par = p & 1;
+    const uint32_t pt = base + kDecP + par * kDecPBytes;  // this unit's P tile
+    float* mx = mlx + par * (2 * 4 * kHeads);              // [4 warps][16] maxima
+    float* ls = mx + 4 * kHeads;                           // [4 warps][16] sums
     // S = q K^T over this warp's 32 keys: 4 n-tiles of 8 keys
     float sacc[4][4];
 #pragma unroll
@@ -485,14 +505,14 @@ __global__ void __launch_bounds__(160, 1)
         mma_m16n8k16_bf16(sacc[j], qa[kk + 1], r[2], r[3]);
       }
     }
-    // scale, causal limit, row max (rows gid and gid+8), quad reduction
-    float m0 = -__int_as_float(0x7f800000), m1 = m0;
+    // scale, causal limit, this warp's row maxima (rows gid and gid+8) over its 32 keys
+    float m0 = ninf, m1 = ninf;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int key = w * 32 + j * 8 + tq * 2 + (e & 1);
-        const float z = key <= x.lim ? sacc[j][e] * a.scale_log2 : -__int_as_float(0x7f800000);
+        const float z = key <= x.lim ? sacc[j][e] * a.scale_log2 : ninf;
         sacc[j][e] = z;
         if (e < 2) m0 = fmaxf(m0, z);
         else m1 = fmaxf(m1, z);
@@ -502,94 +522,80 @@ __global__ void __launch_bounds__(160, 1)
     m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 2));
     m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 1));
     m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 2));
-    const float b0 = m0 == -__int_as_float(0x7f800000) ? 0.f : m0;
-    const float b1 = m1 == -__int_as_float(0x7f800000) ? 0.f : m1;
+    if (tq == 0) {
+      mx[w * kHeads + gid] = m0;
+      mx[w * kHeads + gid + 8] = m1;
+    }
+    named_barrier(1, 128);
+    // row maxima over the page (key 0 is always in range, so they are finite)
+    float M0 = mx[gid], M1 = mx[gid + 8];
+#pragma unroll
+    for (int q = 1; q < 4; ++q) {
+      M0 = fmaxf(M0, mx[q * kHeads + gid]);
+      M1 = fmaxf(M1, mx[q * kHeads + gid + 8]);
+    }
+    // P = exp2(z - M) for this warp's keys -> bf16 into the shared P tile; partial row sums
     float l0 = 0.f, l1 = 0.f;
-    uint32_t pa[2][4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const float p0 = exp2f(sacc[j][0] - b0), p1 = exp2f(sacc[j][1] - b0);
-      const float p2 = exp2f(sacc[j][2] - b1), p3 = exp2f(sacc[j][3] - b1);
+      const float p0 = exp2f(sacc[j][0] - M0), p1 = exp2f(sacc[j][1] - M0);
+      const float p2 = exp2f(sacc[j][2] - M1), p3 = exp2f(sacc[j][3] - M1);
       l0 += p0 + p1;
       l1 += p2 + p3;
-      pa[j >> 1][(j & 1) * 2 + 0] = pack_bf16x2(p0, p1);
-      pa[j >> 1][(j & 1) * 2 + 1] = pack_bf16x2(p2, p3);
+      const int chunk = w * 4 + j;  // keys [8 chunk, 8 chunk + 8)
+      st_shared_u32(dec_p_addr(pt, gid, chunk) + tq * 4, pack_bf16x2(p0, p1));
+      st_shared_u32(dec_p_addr(pt, gid + 8, chunk) + tq * 4, pack_bf16x2(p2, p3));
     }
     l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
     l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-    // O = P V over this warp's 32 keys: 16 n-tiles of 8 dims
-    float oacc[16][4];
+    if (tq == 0) {
+      ls[w * kHeads + gid] = l0;
+      ls[w * kHeads + gid + 8] = l1;
+    }
+    named_barrier(1, 128);
+    const float L0 = ls[gid] + ls[kHeads + gid] + ls[2 * kHeads + gid] + ls[3 * kHeads + gid];
+    const float L1 = ls[gid + 8] + ls[kHeads + gid + 8] + ls[2 * kHeads + gid + 8] +
+                     ls[3 * kHeads + gid + 8];
+    // O[:, 32w, 32w + 32) = P V over all 128 keys: 8 k-steps x 4 n-tiles of 8 dims
+    float oacc[4][4];
 #pragma unroll
-    for (int nt = 0; nt < 16; ++nt)
+    for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) oacc[nt][e] = 0.f;
+    const int mtx = lane >> 3;
 #pragma unroll
-    for (int kk2 = 0; kk2 < 2; ++kk2) {
-      const int mtx = lane >> 3;
-      const int key = w * 32 + kk2 * 16 + (mtx & 1) * 8 + (lane & 7);
+    for (int kk = 0; kk < 8; ++kk) {
+      uint32_t pa[4];
+      ldmatrix_x4(dec_p_addr(pt, lane & 15, 2 * kk + (lane >> 4)), pa);
+      const int key = kk * 16 + (mtx & 1) * 8 + (lane & 7);
 #pragma unroll
-      for (int nt = 0; nt < 16; nt += 2) {
+      for (int nt = 0; nt < 4; nt += 2) {
         uint32_t r[4];
-        ldmatrix_x4_trans(swz(vt, key, nt + (mtx >> 1)), r);
-        mma_m16n8k16_bf16(oacc[nt], pa[kk2], r[0], r[1]);
-        mma_m16n8k16_bf16(oacc[nt + 1], pa[kk2], r[2], r[3]);
+        ldmatrix_x4_trans(swz(vt, key, w * 4 + nt + (mtx >> 1)), r);
+        mma_m16n8k16_bf16(oacc[nt], pa, r[0], r[1]);
+        mma_m16n8k16_bf16(oacc[nt + 1], pa, r[2], r[3]);
       }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(empty(st));
     ++p;
-    // merge the four warps' states: (m, l) per row and O in shared memory
-    if (tq == 0) {
-      ml[(w * kHeads + gid) * 2] = m0;
-      ml[(w * kHeads + gid) * 2 + 1] = l0;
-      ml[(w * kHeads + gid + 8) * 2] = m1;
-      ml[(w * kHeads + gid + 8) * 2 + 1] = l1;
+    const float i0 = 1.f / L0, i1 = 1.f / L1;
+    float* dst = a.po + static_cast<size_t>(u) * kHeads * kDim;
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+      const int d = (w * 4 + nt) * 8 + tq * 2;
+      *reinterpret_cast<float2*>(dst + gid * kDim + d) =
+          make_float2(oacc[nt][0] * i0, oacc[nt][1] * i0);
+      *reinterpret_cast<float2*>(dst + (gid + 8) * kDim + d) =
+          make_float2(oacc[nt][2] * i1, oacc[nt][3] * i1);
     }
-#pragma unroll
-    for (int nt = 0; nt < 16; ++nt) {
-      float* r0 = red + (w * kHeads + gid) * kDim + nt * 8 + tq * 2;
-      float* r1 = red + (w * kHeads + gid + 8) * kDim + nt * 8 + tq * 2;
-      *reinterpret_cast<float2*>(r0) = make_float2(oacc[nt][0], oacc[nt][1]);
-      *reinterpret_cast<float2*>(r1) = make_float2(oacc[nt][2], oacc[nt][3]);
+    if (w == 0 && tq == 0) {
+      const float ln2 = 0.6931471805599453f;
+      a.plse[static_cast<size_t>(u) * kHeads + gid] = (M0 + __log2f(L0)) * ln2;
+      a.plse[static_cast<size_t>(u) * kHeads + gid + 8] = (M1 + __log2f(L1)) * ln2;
     }
-    named_barrier(1, 128);
-    {
-      const int t = threadIdx.x - 32, h = t >> 3, d0 = (t & 7) * 16;
-      float mw[4], wt[4], M = -__int_as_float(0x7f800000);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        mw[q] = ml[(q * kHeads + h) * 2];
-        M = fmaxf(M, mw[q]);
-      }
-      float Lsum = 0.f;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        // a warp whose keys were all masked contributes nothing
-        wt[q] = mw[q] == -__int_as_float(0x7f800000) ? 0.f : exp2f(mw[q] - M);
-        Lsum += wt[q] * ml[(q * kHeads + h) * 2 + 1];
-      }
-      const float inv = 1.f / Lsum;
-      float* dst = a.po + (static_cast<size_t>(u) * kHeads + h) * kDim + d0;
-#pragma unroll
-      for (int c = 0; c < 16; c += 4) {
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float4 r = *reinterpret_cast<const float4*>(red + (q * kHeads + h) * kDim + d0 + c);
-          acc.x += wt[q] * r.x;
-          acc.y += wt[q] * r.y;
-          acc.z += wt[q] * r.z;
-          acc.w += wt[q] * r.w;
-        }
-        *reinterpret_cast<float4*>(dst + c) =
-            make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-      }
-      if ((t & 7) == 0)
-        a.plse[static_cast<size_t>(u) * kHeads + h] = (M + __log2f(Lsum)) * 0.6931471805599453f;
-    }
-    named_barrier(1, 128);
   }
 }
 

@@ -285,6 +285,10 @@ __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t col, uin
   return panel * rows * 128u + row * 128u + chunk * 16u + (c & 7) * 2u;
 }
 
+__device__ __forceinline__ void st_shared_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));

@@ -22,7 +22,6 @@ namespace msa {
 namespace {
 
 constexpr int kHeads = 16;  // query heads per group
-constexpr int kPagesPerChunk = 16;
 constexpr int kScanStages = 6;
 constexpr uint32_t kScanStage = 32768 + 4096;  // 128 keys x 128 bf16 + the 16-row query tile
 constexpr int kScanSlots = 8;                  // TMEM accumulators of 16 columns
@@ -30,12 +29,13 @@ constexpr int kScanSlots = 8;                  // TMEM accumulators of 16 column
 // TMEM base address and the abort flag
 constexpr uint32_t kScanBarFull = 0, kScanBarEmpty = 64, kScanBarAccFull = 128,
                    kScanBarAccEmpty = 192, kScanBarDrain = 256, kScanTmemSlot = 264,
-                   kScanAbort = 268, kScanBarBytes = 512;
+                   kScanAbort = 268, kScanWalk = 272, kScanBarBytes = 512;
 static_assert(kScanBarFull + 8 * kScanStages <= kScanBarEmpty, "scan barriers");
 static_assert(kScanBarEmpty + 8 * kScanStages <= kScanBarAccFull, "scan barriers");
 static_assert(kScanBarAccFull + 8 * kScanSlots <= kScanBarAccEmpty, "scan barriers");
 static_assert(kScanBarAccEmpty + 8 * kScanSlots <= kScanBarDrain, "scan barriers");
-static_assert(kScanAbort + 4 <= kScanBarBytes, "scan barriers");
+static_assert(kScanAbort + 4 <= kScanWalk, "scan barriers");
+static_assert(kScanWalk + 12 <= kScanBarBytes, "scan barriers");
 constexpr uint32_t kScanSmem = kScanStages * kScanStage + kScanBarBytes + 1024;
 static_assert(kScanSmem <= 232448, "scan shared memory");
 constexpr uint32_t kIdescScan = idesc_bf16_f32(128, 16, false, false);
@@ -45,36 +45,78 @@ struct ScanArgs {
   const int32_t* page_table;
   const int32_t* seq_lens;
   int32_t batch, max_pages, num_pages, G;
-  int32_t cps;       // chunks of kPagesPerChunk pages per sequence
-  int32_t n_chunks;  // batch * cps
   float4* scores;    // [batch][G][max_pages]: per-warp maxima of the 4 epilogue warps
   int32_t* status;
   uint64_t wait_ns;
 };
 
-// The page sequence every role of a CTA walks identically: chunks blockIdx.x, +gridDim.x, ...;
-// inside a chunk the pages that lie strictly before the query's page.
-struct PageWalk {
-  int chunk, b, bend, s;
-  __device__ __forceinline__ void init() {
-    chunk = static_cast<int>(blockIdx.x) - static_cast<int>(gridDim.x);
-    b = bend = 0;
-    s = 0;
+// Index pages scored for sequence s: those strictly before the query's page.
+__device__ __forceinline__ int scan_pages(const ScanArgs& a, int s) {
+  const int n = a.seq_lens[s];
+  return n > 0 ? min((n - 1) / kBlock, a.max_pages) : 0;
+}
+
+// The pages of all sequences, concatenated in (sequence, block) order, are split into equal
+// contiguous ranges, one per CTA.  One warp finds the CTA's first page with warp prefix sums over
+// the sequence lengths; every role then walks the range identically.
+__device__ void scan_range(const ScanArgs& a, int lane, int* out /* s0, b0, count */) {
+  long long total = 0;
+  for (int s0 = 0; s0 < a.batch; s0 += 32) {
+    const int s = s0 + lane;
+    int c = s < a.batch ? scan_pages(a, s) : 0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+    total += c;
   }
-  // Advances to the next page; returns its logical block id, or -1 at the end.
-  __device__ __forceinline__ int next(const ScanArgs& a) {
-    while (b >= bend) {
-      chunk += gridDim.x;
-      if (chunk >= a.n_chunks) return -1;
-      s = chunk / a.cps;
-      const int b0 = (chunk % a.cps) * kPagesPerChunk;
-      const int n = a.seq_lens[s];
-      int bi = n > 0 ? (n - 1) / kBlock : 0;
-      bi = min(bi, a.max_pages);
-      b = b0;
-      bend = min(b0 + kPagesPerChunk, bi);
+  const long long p0 = total * blockIdx.x / gridDim.x;
+  const long long p1 = total * (blockIdx.x + 1) / gridDim.x;
+  long long before = 0;  // pages of the sequences before the current group of 32
+  int s_first = a.batch, b_first = 0;
+  for (int s0 = 0; s0 < a.batch && s_first == a.batch; s0 += 32) {
+    const int s = s0 + lane;
+    const int c = s < a.batch ? scan_pages(a, s) : 0;
+    int incl = c;  // inclusive prefix within the group
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
     }
-    return b++;
+    const long long start = before + incl - c;
+    // the sequence whose pages contain p0 (first lane whose range reaches past it)
+    const unsigned hit = __ballot_sync(0xffffffffu, c > 0 && start <= p0 && p0 < start + c);
+    if (hit) {
+      const int l = __ffs(hit) - 1;
+      s_first = s0 + l;
+      b_first = static_cast<int>(p0 - __shfl_sync(0xffffffffu, start, l));
+    }
+    before += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  if (lane == 0) {
+    out[0] = s_first;
+    out[1] = b_first;
+    out[2] = static_cast<int>(p1 - p0);
+  }
+}
+
+struct PageWalk {
+  int s, b, left, ns;
+  __device__ __forceinline__ void init(const ScanArgs& a, const volatile int* r) {
+    s = r[0];
+    b = r[1] - 1;
+    left = r[2];
+    ns = left > 0 ? scan_pages(a, s) : 0;
+  }
+  // Advances to the next page of the range; returns its logical block id, or -1 at the end.
+  __device__ __forceinline__ int next(const ScanArgs& a) {
+    if (left <= 0) return -1;
+    --left;
+    ++b;
+    while (b >= ns) {  // on to the next sequence that has pages
+      ++s;
+      b = 0;
+      ns = scan_pages(a, s);
+    }
+    return b;
   }
 };
 
@@ -116,6 +158,8 @@ __global__ void __launch_bounds__(256, 1)
     *abort_flag = 0;
     fence_mbar_init();
   }
+  volatile int* walk = reinterpret_cast<volatile int*>(smem + kScanStages * kScanStage + kScanWalk);
+  if (warp == 2) scan_range(a, lane, const_cast<int*>(walk));
   if (warp == 1) {
     tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), 128);
     tmem_relinquish();
@@ -130,7 +174,7 @@ __global__ void __launch_bounds__(256, 1)
       tma_prefetch_map(&map_k);
       tma_prefetch_map(&map_q);
       PageWalk w;
-      w.init();
+      w.init(a, walk);
       int p = 0;
       for (int b = w.next(a); b >= 0; b = w.next(a), ++p) {
         const int st = p % kScanStages;
@@ -159,7 +203,7 @@ __global__ void __launch_bounds__(256, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       PageWalk w;
-      w.init();
+      w.init(a, walk);
       int p = 0;
       bool ok = true;
       for (int b = w.next(a); b >= 0; b = w.next(a), ++p) {
@@ -193,7 +237,7 @@ __global__ void __launch_bounds__(256, 1)
     const int ew = warp - 4;
     const uint32_t lane_base = static_cast<uint32_t>(ew * 32) << 16;
     PageWalk w;
-    w.init();
+    w.init(a, walk);
     int p = 0;
     for (int b = w.next(a); b >= 0; b = w.next(a), ++p) {
       const int slot = p % kScanSlots;
@@ -662,15 +706,14 @@ cudaError_t launch_decode_select(const CUtensorMap& map_k, const CUtensorMap& ma
   a.max_pages = max_pages;
   a.num_pages = num_pages;
   a.G = G;
-  a.cps = (max_pages + kPagesPerChunk - 1) / kPagesPerChunk;
-  a.n_chunks = batch * a.cps;
   a.scores = reinterpret_cast<float4*>(scores);
   a.status = status;
   a.wait_ns = wait_ns;
   cudaError_t e = cudaFuncSetAttribute(decode_scan_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kScanSmem);
   if (e != cudaSuccess) return e;
-  const int grid = std::max(1, std::min(num_sms, a.n_chunks));
+  const int grid = static_cast<int>(
+      std::max<int64_t>(1, std::min<int64_t>(num_sms, static_cast<int64_t>(batch) * max_pages)));
   decode_scan_kernel<<<grid, 256, kScanSmem, stream>>>(map_k, map_q, a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   TopkArgs t{};

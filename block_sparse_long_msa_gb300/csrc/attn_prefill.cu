@@ -55,6 +55,7 @@ struct SchedArgs {
   int32_t* n_items;    // [1]
   int4* items;         // {g, b, start, count}
   int32_t* list;       // (token << 4) | slot
+  int32_t* pos;        // [(il*G + g)*k + s]: list position of the slot's unit, -1 if none
   int32_t* status;
 };
 
@@ -207,14 +208,19 @@ __global__ void sched_fill_kernel(SchedArgs a) {
   const int32_t* row = a.sel + (static_cast<size_t>(g) * a.L + i) * a.k;
   const int w = t >> 5;
   const uint32_t below = (1u << (t & 31)) - 1u;
+  const size_t u0 = (static_cast<size_t>(qbl) * kBlock + t) * a.G * a.k + static_cast<size_t>(g) * a.k;
   for (int s = 0; s < a.k; ++s) {
     const int32_t b = row[s];
-    if (b < 0 || b > qb) continue;
+    if (b < 0 || b > qb) {
+      a.pos[u0 + s] = -1;
+      continue;
+    }
     int rank = __popc(mask[b * 4 + w] & below);
     for (int q = 0; q < w; ++q) rank += __popc(mask[b * 4 + q]);
     const int gb = g * a.nbk + b;
     const int pos = a.list_base[gb] + a.hist[static_cast<size_t>(gb) * a.nbq + qbl] + rank;
     a.list[pos] = static_cast<int32_t>((i << 4) | s);
+    a.pos[u0 + s] = pos;
   }
 }
 
@@ -240,15 +246,15 @@ struct AttnArgs {
   const int32_t* list;
   int32_t G, k, q0;
   float scale_log2;       // softmax scale * log2(e)
-  __half* po;             // [(il*G + g)*k + s][16][128] unnormalised partial O (fp16)
-  float* pm;              // [(il*G + g)*k + s][16] row max (natural-log units)
+  __half* po;             // [list position][16][128] unnormalised partial O (fp16)
+  float* pm;              // [list position][16] row max (natural-log units)
   float* plse;            // same, log-sum-exp
   int32_t* status;
   uint64_t wait_ns;
 };
 
 struct ItemMeta {
-  int32_t g, b, count, pad;
+  int32_t g, b, count, start;  // start: list position of the item's first token
   int32_t tok[kItemTokens];  // (token << 4) | slot
 };
 
@@ -303,7 +309,8 @@ __global__ void __launch_bounds__(512, 1)
     attn_kv_outer_kernel(const __grid_constant__ CUtensorMap map_q,
                          const __grid_constant__ CUtensorMap map_k,
                          const __grid_constant__ CUtensorMap map_v,
-                         const __grid_constant__ CUtensorMap map_po, AttnArgs a) {
+                         const __grid_constant__ CUtensorMap map_po,
+                         const __grid_constant__ CUtensorMap map_po_tok, AttnArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -381,6 +388,7 @@ __global__ void __launch_bounds__(512, 1)
         m.g = item.x;
         m.b = item.y;
         m.count = item.w;
+        m.start = item.z;
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(meta_full(r));
@@ -665,10 +673,10 @@ __global__ void __launch_bounds__(512, 1)
         tc_fence_before();
         mbar_arrive(p_full(s3 * 2 + wg));
         if (valid) {
-          const size_t u = (static_cast<size_t>(i - a.q0) * a.G + g) * a.k + s;
+          const size_t p = static_cast<size_t>(m.start) + t0 + tk;  // list position
           const float ln2 = 0.6931471805599453f;
-          a.pm[u * kHeadsPerGroup + hh] = m2 * ln2;
-          a.plse[u * kHeadsPerGroup + hh] = (m2 + __log2f(l)) * ln2;
+          a.pm[p * kHeadsPerGroup + hh] = m2 * ln2;
+          a.plse[p * kHeadsPerGroup + hh] = (m2 + __log2f(l)) * ln2;
         }
       }
     }
@@ -684,6 +692,10 @@ __global__ void __launch_bounds__(512, 1)
     // abort the waits are skipped and nothing more is stored.
     const int et = threadIdx.x - 384;
     const int row = (warp & 3) * 32 + lane;
+    if (et == 0) {
+      tma_prefetch_map(&map_po);
+      tma_prefetch_map(&map_po_tok);
+    }
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t stg = base + kSmemO;
     int T = 0;
@@ -731,14 +743,15 @@ __global__ void __launch_bounds__(512, 1)
         }
         fence_proxy_async_smem();
         named_barrier(1, 128);
+        // Partials are kept in list order, so a full tile's 8 tokens x 16 heads are 128
+        // consecutive rows: two TMA stores (one per 64-column half).  A short last tile stores
+        // token by token (rows past it belong to the next item).
         if (et < 16) {
-          const int tk = et >> 1, h = et & 1;
-          if (t0 + tk < count && !*abort_flag) {
-            const int32_t e = m.tok[t0 + tk];
-            const int i = e >> 4, s = e & 15;
-            const int u = ((i - a.q0) * a.G + g) * a.k + s;
-            tma_store_2d(&map_po, stg + h * kPanel + tk * 2048, h * 64, u * kHeadsPerGroup);
-          }
+          const bool full = t0 + kTileTokens <= count;
+          const int tk = full ? 0 : et >> 1, h = full ? et : et & 1;
+          if (!*abort_flag && (full ? et < 2 : t0 + tk < count))
+            tma_store_2d(full ? &map_po : &map_po_tok, stg + h * kPanel + tk * 2048, h * 64,
+                         (m.start + t0 + tk) * kHeadsPerGroup);
           bulk_commit();
         }
       }
@@ -760,7 +773,7 @@ __global__ void __launch_bounds__(512, 1)
 //   lse = M + ln(den).  Slots in fixed ascending order; padding (-1) skipped.
 // ------------------------------------------------------------------------------------------
 struct CombineArgs {
-  const int32_t* sel;          // [G][L][k]
+  const int32_t* pos;          // [(il*G + g)*k + s]: list position of each slot, -1 if none
   const __half* po;
   const float* pm;
   const float* plse;
@@ -774,19 +787,17 @@ __global__ void __launch_bounds__(128) combine_kernel(CombineArgs a) {
   const int il = blockIdx.x, g = blockIdx.y;
   const int64_t i = static_cast<int64_t>(a.q0) + il;
   const int t = threadIdx.x, hh = t >> 3, d0 = (t & 7) * 16;
-  const int32_t* srow = a.sel + (static_cast<size_t>(g) * a.L + i) * a.k;
-  const size_t u0 = (static_cast<size_t>(il) * a.G + g) * a.k;
-  const int32_t bi = static_cast<int32_t>(i / kBlock);
+  const int32_t* prow = a.pos + (static_cast<size_t>(il) * a.G + g) * a.k;
   float M = -__int_as_float(0x7f800000);
   for (int s = 0; s < a.k; ++s)
-    if (srow[s] >= 0 && srow[s] <= bi) M = fmaxf(M, a.plse[(u0 + s) * kHeadsPerGroup + hh]);
+    if (prow[s] >= 0) M = fmaxf(M, a.plse[static_cast<size_t>(prow[s]) * kHeadsPerGroup + hh]);
   float acc[16];
 #pragma unroll
   for (int q = 0; q < 16; ++q) acc[q] = 0.f;
   float den = 0.f;
   for (int s = 0; s < a.k; ++s) {
-    if (srow[s] < 0 || srow[s] > bi) continue;  // padding; out-of-range ids were flagged
-    const size_t r = (u0 + s) * kHeadsPerGroup + hh;
+    if (prow[s] < 0) continue;  // padding (and out-of-range ids, which were flagged)
+    const size_t r = static_cast<size_t>(prow[s]) * kHeadsPerGroup + hh;
     den += __expf(a.plse[r] - M);
     const float w = __expf(a.pm[r] - M);
     const uint4* src = reinterpret_cast<const uint4*>(a.po + r * kDim + d0);
@@ -836,6 +847,7 @@ PrefillWorkspace prefill_workspace_layout(int64_t L, int G, int k, int64_t chunk
   w.n_items = off;   off += 256;
   w.items = off;     off += up(sizeof(int4) * max_items);
   w.list = off;      off += up(sizeof(int32_t) * units);
+  w.pos = off;       off += up(sizeof(int32_t) * units);
   w.pm = off;        off += up(sizeof(float) * units * kHeadsPerGroup);
   w.plse = off;      off += up(sizeof(float) * units * kHeadsPerGroup);
   w.po = off;        off += up(sizeof(__half) * units * kHeadsPerGroup * kDim);
@@ -877,6 +889,7 @@ cudaError_t launch_attn_prefill_chunk(const CUtensorMap& map_q, const CUtensorMa
   s.n_items = reinterpret_cast<int32_t*>(ws + w.n_items);
   s.items = reinterpret_cast<int4*>(ws + w.items);
   s.list = reinterpret_cast<int32_t*>(ws + w.list);
+  s.pos = reinterpret_cast<int32_t*>(ws + w.pos);
   s.status = reinterpret_cast<int32_t*>(ws);
   const size_t mask_smem = static_cast<size_t>(s.nbk) * 16;
   cudaError_t e;
@@ -914,23 +927,28 @@ cudaError_t launch_attn_prefill_chunk(const CUtensorMap& map_q, const CUtensorMa
   if ((e = cudaFuncSetAttribute(attn_kv_outer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 kAttnSmem)) != cudaSuccess)
     return e;
-  // partial O as a 2-D fp16 tensor [units * 16 rows][128]: the epilogue's TMA stores
-  CUtensorMap map_po;
+  // partial O as a 2-D fp16 tensor [positions * 16 rows][128]: the epilogue's TMA stores, a
+  // full tile (128 rows) or one token (16 rows) at a time
+  CUtensorMap map_po, map_po_tok;
   {
     const uint64_t dims[2] = {static_cast<uint64_t>(kDim),
                               static_cast<uint64_t>(w.chunk) * G * k * kHeadsPerGroup};
     const uint64_t strides[1] = {kDim * 2};
-    const uint32_t box[2] = {64, kHeadsPerGroup};
-    if (!encode_tmap(&map_po, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.po, 2, dims, strides, box))
+    const uint32_t box[2] = {64, kTileTokens * kHeadsPerGroup};
+    const uint32_t box_tok[2] = {64, kHeadsPerGroup};
+    if (!encode_tmap(&map_po, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.po, 2, dims, strides, box) ||
+        !encode_tmap(&map_po_tok, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.po, 2, dims, strides,
+                     box_tok))
       return cudaErrorInvalidValue;
   }
   const int grid = static_cast<int>(std::min<int64_t>(w.max_items, num_sms));
   if (marks && marks[1]) cudaEventRecord(marks[1], stream);
-  attn_kv_outer_kernel<<<grid, 512, kAttnSmem, stream>>>(map_q, map_k, map_v, map_po, a);
+  attn_kv_outer_kernel<<<grid, 512, kAttnSmem, stream>>>(map_q, map_k, map_v, map_po,
+                                                          map_po_tok, a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   CombineArgs c{};
-  c.sel = sel;
+  c.pos = s.pos;
   c.po = a.po;
   c.pm = a.pm;
   c.plse = a.plse;

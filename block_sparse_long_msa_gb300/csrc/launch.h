@@ -18,7 +18,7 @@ cudaError_t launch_index_select_prefill(const CUtensorMap& map_q, const CUtensor
 
 // Byte offsets of the prefill main-branch workspace (after the 256-byte status header).
 struct PrefillWorkspace {
-  size_t hist, cnt, list_base, rstart, rcnt, item_base, n_items, items, list, pm, plse, po,
+  size_t hist, cnt, list_base, rstart, rcnt, item_base, n_items, items, list, pos, pm, plse, po,
       total;
   int64_t chunk, max_items;
 };

@@ -31,7 +31,8 @@ EncodeTiledFn encode_fn() {
 }  // namespace
 
 bool encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, int rank,
-                 const uint64_t* dims, const uint64_t* strides, const uint32_t* box) {
+                 const uint64_t* dims, const uint64_t* strides, const uint32_t* box,
+                 bool swizzle128) {
   EncodeTiledFn enc = encode_fn();
   if (!enc || rank < 1 || rank > 5) return false;
   cuuint64_t d[5], s[4];
@@ -43,7 +44,8 @@ bool encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, 
   }
   for (int i = 0; i + 1 < rank; ++i) s[i] = strides[i];
   return enc(map, dtype, static_cast<cuuint32_t>(rank), const_cast<void*>(base), d, s, b, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_INTERLEAVE_NONE,
+             swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

@@ -231,14 +231,15 @@ __global__ void sched_fill_kernel(SchedArgs a) {
 //   S = Q K^T (tcgen05, fp32 in TMEM) -> softmax rows (causal limit only in the local block)
 //   -> P (fp16, written back into the same TMEM columns) -> O = P V (tcgen05, A from TMEM)
 //   -> unnormalised partial O (fp16, staged and stored with TMA) + row max m and log-sum-exp.
-// Roles (16 warps): 0 query-gather producer + token-list staging, 1 TMEM owner + MMA issuer,
-// 2 K loader, 3 V loader + fp16 converter, 4-7 softmax of even tiles, 8-11 softmax of odd
+// Roles (16 warps): 0 query-gather producer + token-list staging, 1 S = QK^T issuer, 2 K loader
+// + O = PV issuer, 3 V loader + fp16 converter, 4-7 softmax of even tiles, 8-11 softmax of odd
 // tiles, 12-15 epilogue.
 // TMEM: columns [0,384) three S/P slots (tile T uses slot T % 3), [384,512) the O accumulator.
-// The MMA issuer keeps two tiles ahead: S of tile T+2 is issued before P.V of tile T, so a
-// softmax warpgroup finds its next S ready when it finishes a tile.  K and V are single-buffered
-// with separate loaders (K paced by the QK^T cursor, V by the P.V cursor), which frees shared
-// memory for a three-deep query ring that covers the gather latency.
+// The two MMA chains of a tile come from two threads: a commit covers only its own thread's
+// MMAs, so each chain signals its consumer when it is done while the tensor pipe interleaves
+// them.  K and V are single-buffered (K paced by the S issuer, V by the P.V issuer), which frees
+// shared memory for a three-deep query ring that covers the gather latency.  Partial outputs
+// are kept in work-list order, so a full tile leaves with two TMA stores.
 // ------------------------------------------------------------------------------------------
 struct AttnArgs {
   const int4* items;
@@ -355,7 +356,7 @@ __global__ void __launch_bounds__(512, 1)
     for (int q = 0; q < 3; ++q) mbar_init(sp_free(q), 1);
     mbar_init(o_full, 1);
     mbar_init(o_empty, 128);
-    mbar_init(drain_bar, 1);
+    mbar_init(drain_bar, 2);  // one commit from each MMA issuer
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -421,57 +422,76 @@ __global__ void __launch_bounds__(512, 1)
           mbar_wait(q_full(x % kQStages), (x / kQStages) & 1, kDefaultWaitNs);
     }
   } else if (warp == 1) {
-    // ------------------------------- MMA issuer -------------------------------
+    // ---------------------------- S = Q K^T issuer ----------------------------
+    // S and P.V are issued by two threads (this one and lane 0 of warp 2).  A tcgen05.commit
+    // covers only the MMAs of the thread that issues it, so each chain signals its consumer as
+    // soon as it is done while the tensor pipe interleaves the two threads' independent chains.
     if (lane == 0) {
       bool ok = true;
-      // cursor A issues S = Q K^T, cursor B issues O = P V, two tiles behind A
-      int a_it = blockIdx.x, a_n = 0, a_t0 = 0, a_cnt = -1, a_T = 0;
-      int b_it = blockIdx.x, b_n = 0, b_t0 = 0, b_cnt = -1, b_T = 0;
-      // Non-blocking scheduler: each pass issues the next S if its slot, query tile and K are
-      // ready, and the next P.V if its P and the O accumulator are; neither cursor waits for the
-      // other, so the tensor pipe sees work as soon as any of it is ready.  Each chain is
-      // committed on its own: a commit covers every MMA issued before it, so grouping the K-steps
-      // of several tiles would hold back the softmax and the O drain until the whole group is done
-      // (measured slower, although interleaved chains use the tensor pipe better).
-      uint64_t idle_since = 0;
-      bool idle = false;
-      while (ok && b_it < n_items) {
-        bool progressed = false;
-        // ---- S = Q K^T for tile a_T (at most three tiles ahead: one per S/P slot) ----
-        if (a_it < n_items && a_T - b_T < 3) {
-          if (a_cnt < 0 && mbar_try_wait(meta_full(a_n % kMetaRing), (a_n / kMetaRing) & 1) &&
-              mbar_try_wait(k_full, a_n & 1)) {
-            a_cnt = meta[a_n % kMetaRing].count;
-            a_t0 = 0;
-          }
-          const int qs = a_T % kQStages, s3 = a_T % 3;
-          if (a_cnt >= 0 && mbar_try_wait(q_full(qs), (a_T / kQStages) & 1) &&
-              mbar_try_wait(sp_free(s3), ((a_T / 3) & 1) ^ 1)) {
-            tc_fence_after();
-            const uint32_t d = tmem + s3 * 128;
-            const uint32_t qb = base + kSmemQ + qs * 32768u, kb = base + kSmemK;
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 32;
-              mma_bf16_ss(d, sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
-                          kIdescQK, kk > 0);
-            }
-            mma_commit(s_full(s3 * 2 + (a_T & 1)));
-            mma_commit(q_empty(qs));
-            ++a_T;
-            a_t0 += kTileTokens;
-            if (a_t0 >= a_cnt) {  // the item's last S: K may be replaced once these are done
-              mma_commit(k_empty);
-              a_it += gridDim.x;
-              ++a_n;
-              a_cnt = -1;
-            }
-            progressed = true;
-          }
+      int T = 0;
+      for (int it = blockIdx.x, n = 0; ok && it < n_items; it += gridDim.x, ++n) {
+        const int r = n % kMetaRing;
+        if (*abort_flag || !mbar_wait(meta_full(r), (n / kMetaRing) & 1, a.wait_ns) ||
+            !mbar_wait(k_full, n & 1, a.wait_ns)) {
+          ok = false;
+          break;
         }
-        // ---- O = P V for tile b_T ----
-        if (b_T < a_T) {
-          if (b_cnt < 0 && mbar_try_wait(v_ready, b_n & 1)) {  // cursor A opened the item
+        const int cnt = meta[r].count;
+        for (int t0 = 0; t0 < cnt; t0 += kTileTokens, ++T) {
+          const int qs = T % kQStages, s3 = T % 3;
+          // S(T) reuses the S/P slot of tile T-3: in-order issue keeps the parities unambiguous
+          if (*abort_flag || !mbar_wait(q_full(qs), (T / kQStages) & 1, a.wait_ns) ||
+              !mbar_wait(sp_free(s3), ((T / 3) & 1) ^ 1, a.wait_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d = tmem + s3 * 128;
+          const uint32_t qb = base + kSmemQ + qs * 32768u, kb = base + kSmemK;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 32;
+            mma_bf16_ss(d, sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
+                        kIdescQK, kk > 0);
+          }
+          mma_commit(s_full(s3 * 2 + (T & 1)));
+          mma_commit(q_empty(qs));
+        }
+        if (!ok) break;
+        mma_commit(k_empty);  // the item's last S: K may be replaced once these are done
+      }
+      if (!ok) {
+        report_status(a.status, kStatusTimeout);
+        *abort_flag = 1;
+      }
+      mma_commit(drain_bar);
+      mbar_wait(drain_bar, 0, kDefaultWaitNs);
+    }
+  } else if (warp == 2) {
+    // --------------------- K loader + O = P V issuer (polling) ---------------------
+    if (lane == 0) {
+      tma_prefetch_map(&map_k);
+      const int n_mine = n_items > static_cast<int>(blockIdx.x)
+                             ? (n_items - 1 - static_cast<int>(blockIdx.x)) / gridDim.x + 1
+                             : 0;
+      int nk = 0;                        // items whose K has been requested
+      int b_n = 0, b_cnt = -1, b_t0 = 0, b_T = 0;  // P.V cursor
+      bool ok = true, idle = false;
+      uint64_t idle_since = 0;
+      while (ok && (nk < n_mine || b_n < n_mine)) {
+        bool progressed = false;
+        if (nk < n_mine && mbar_try_wait(meta_full(nk % kMetaRing), (nk / kMetaRing) & 1) &&
+            mbar_try_wait(k_empty, (nk & 1) ^ 1)) {
+          const int r = nk % kMetaRing;
+          const int g = meta[r].g, b = meta[r].b;
+          mbar_arrive_expect_tx(k_full, 32768);
+          tma_load_3d(base + kSmemK, &map_k, k_full, 0, g, b * kBlock);
+          tma_load_3d(base + kSmemK + kPanel, &map_k, k_full, 64, g, b * kBlock);
+          ++nk;
+          progressed = true;
+        }
+        if (b_n < n_mine) {
+          if (b_cnt < 0 && mbar_try_wait(v_ready, b_n & 1)) {  // V of item b_n converted
             b_cnt = meta[b_n % kMetaRing].count;
             b_t0 = 0;
           }
@@ -490,7 +510,6 @@ __global__ void __launch_bounds__(512, 1)
             b_t0 += kTileTokens;
             if (b_t0 >= b_cnt) {  // the item's last P.V: V may be replaced once it is done
               mma_commit(v_empty);
-              b_it += gridDim.x;
               ++b_n;
               b_cnt = -1;
             }
@@ -513,34 +532,10 @@ __global__ void __launch_bounds__(512, 1)
       if (!ok) {
         report_status(a.status, kStatusTimeout);
         *abort_flag = 1;
+        if (nk > 0) mbar_wait(k_full, (nk - 1) & 1, kDefaultWaitNs);
       }
       mma_commit(drain_bar);
       mbar_wait(drain_bar, 0, kDefaultWaitNs);
-    }
-  } else if (warp == 2) {
-    // ------------------------------- K loader -------------------------------
-    if (lane == 0) {
-      tma_prefetch_map(&map_k);
-      int issued = 0;
-      bool ok = true;
-      for (int it = blockIdx.x, n = 0; it < n_items; it += gridDim.x, ++n) {
-        const int r = n % kMetaRing;
-        if (*abort_flag || !mbar_wait(meta_full(r), (n / kMetaRing) & 1, a.wait_ns) ||
-            !mbar_wait(k_empty, (n & 1) ^ 1, a.wait_ns)) {
-          ok = false;
-          break;
-        }
-        const int g = meta[r].g, b = meta[r].b;
-        mbar_arrive_expect_tx(k_full, 32768);
-        tma_load_3d(base + kSmemK, &map_k, k_full, 0, g, b * kBlock);
-        tma_load_3d(base + kSmemK + kPanel, &map_k, k_full, 64, g, b * kBlock);
-        ++issued;
-      }
-      if (!ok) {
-        report_status(a.status, kStatusTimeout);
-        *abort_flag = 1;
-        if (issued > 0) mbar_wait(k_full, (issued - 1) & 1, kDefaultWaitNs);
-      }
     }
   } else if (warp == 3) {
     // ------------- V loader + converter: bf16 -> fp16 in place -------------

@@ -123,32 +123,6 @@ __device__ __forceinline__ void bulk_wait_read0() {
 __device__ __forceinline__ void bulk_wait0() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
-// Wait until at most n (0..16) of this thread's most recent bulk groups are still pending.
-__device__ __forceinline__ void bulk_wait_upto(int n) {
-#define MSA_BULK_WAIT_CASE(N) \
-  case N:                     \
-    asm volatile("cp.async.bulk.wait_group " #N ";" ::: "memory"); \
-    break;
-  switch (n) {
-    MSA_BULK_WAIT_CASE(1) MSA_BULK_WAIT_CASE(2) MSA_BULK_WAIT_CASE(3) MSA_BULK_WAIT_CASE(4)
-    MSA_BULK_WAIT_CASE(5) MSA_BULK_WAIT_CASE(6) MSA_BULK_WAIT_CASE(7) MSA_BULK_WAIT_CASE(8)
-    MSA_BULK_WAIT_CASE(9) MSA_BULK_WAIT_CASE(10) MSA_BULK_WAIT_CASE(11) MSA_BULK_WAIT_CASE(12)
-    MSA_BULK_WAIT_CASE(13) MSA_BULK_WAIT_CASE(14) MSA_BULK_WAIT_CASE(15) MSA_BULK_WAIT_CASE(16)
-    default:
-      asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-  }
-#undef MSA_BULK_WAIT_CASE
-}
-// Order this thread's completed async-proxy global writes before its later generic accesses
-// (and its generic accesses before later async-proxy global reads).
-__device__ __forceinline__ void fence_proxy_async_global() {
-  asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-__device__ __forceinline__ int ld_acquire_gpu(const int32_t* p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
 // Make generic-proxy shared-memory writes visible to the async proxy (tensor core, TMA).
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -332,11 +306,6 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
   return pack_f16x2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
 
-__device__ __forceinline__ uint2 ld_shared_v2(uint32_t addr) {
-  uint2 v;
-  asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr) : "memory");
-  return v;
-}
 __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"

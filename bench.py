@@ -157,16 +157,16 @@ KERNEL_SOURCES = {
 }
 NCU_TRAFFIC = {
     # prefill L=32768, 64/4 heads, k=16 (profiles/dram_prefill_L32K_decode_b64.md)
-    "attention": {"bytes_per_launch": 3202479872 + 8546904064, "workload": "prefill_L32K@32768",
-                  "sources_sha256": "68df3ccf3ddf94e6580a1d87845fe5d770a4c048db8877e2338a4469c1ce6aa4"},
-    "combine": {"bytes_per_launch": 8622035456 + 540562688, "workload": "prefill_L32K@32768",
-                "sources_sha256": "68df3ccf3ddf94e6580a1d87845fe5d770a4c048db8877e2338a4469c1ce6aa4"},
-    "index": {"bytes_per_launch": 41900928 + 0, "workload": "prefill_L32K@32768",
-              "sources_sha256": "b67b36e49d74a6877630e328b26f99272e16815b25e578620b481c2d1e912d1f"},
+    "attention": {"bytes_per_launch": 11706841984, "workload": "prefill_L32K@32768",
+                  "sources_sha256": "4959dfb526429f5ac59cea209119e8d4d15b425d2660f6cbedf911f727319b6e"},
+    "combine": {"bytes_per_launch": 9175326208, "workload": "prefill_L32K@32768",
+                "sources_sha256": "4959dfb526429f5ac59cea209119e8d4d15b425d2660f6cbedf911f727319b6e"},
+    "index": {"bytes_per_launch": 41909760, "workload": "prefill_L32K@32768",
+              "sources_sha256": "0f33ac3c78196a8d50dcacf237c9649b8fb27e4d91625b1c5efcc819bd23e39c"},
     # decode, 64 sequences of 16K-256K tokens
-    "decode_scan": {"bytes_per_launch": 2080786816 + 7407104,
+    "decode_scan": {"bytes_per_launch": 2088155136,
                     "workload": "decode_b64_16K_256K@64x262144",
-                    "sources_sha256": "e0fbab574ffee4cd8dac665041d72c0e6d11514299c923a681c53a84d1864415"},
+                    "sources_sha256": "d32ca51ba84e840ef970e6e870773d2ce0b263594862f789179ffe9eab504635"},
 }
 
 

@@ -704,38 +704,36 @@ __global__ void __launch_bounds__(512, 1)
       const ItemMeta& m = meta[r];
       const int count = min(max(m.count, 0), kItemTokens), g = m.g;
       for (int t0 = 0; t0 < count; t0 += kTileTokens, ++T) {
-        if (et < 16) bulk_wait_read0();  // the previous tile's stores have read the staging tile
-        named_barrier(1, 128);
         const bool oko = !*abort_flag && mbar_wait(o_full, T & 1, a.wait_ns);
         if (!__all_sync(0xffffffffu, oko)) {
           report_status(a.status, kStatusTimeout);
           *abort_flag = 1;
         }
         tc_fence_after();
+        // O -> registers as fp16 pairs; the accumulator is released before the staging tile is
+        // waited for, so the next P.V does not wait on the previous tile's TMA stores
+        uint32_t ph[64];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           uint32_t v0[32], v1[32];
           tmem_ld32(tmem + lane_base + 384 + h * 64, v0);
           tmem_ld32(tmem + lane_base + 384 + h * 64 + 32, v1);
           tmem_ld_wait();
-          if (h == 1) {  // all of O is in registers or staged: the next tile's P.V may start
-            tc_fence_before();
-            mbar_arrive(o_empty);
-          }
 #pragma unroll
-          for (int u4 = 0; u4 < 4; ++u4) {
-            st_shared_v4(stg + sw128_offset(row, h * 64 + u4 * 8, 128),
-                         pack_f16x2(__uint_as_float(v0[8 * u4 + 0]), __uint_as_float(v0[8 * u4 + 1])),
-                         pack_f16x2(__uint_as_float(v0[8 * u4 + 2]), __uint_as_float(v0[8 * u4 + 3])),
-                         pack_f16x2(__uint_as_float(v0[8 * u4 + 4]), __uint_as_float(v0[8 * u4 + 5])),
-                         pack_f16x2(__uint_as_float(v0[8 * u4 + 6]), __uint_as_float(v0[8 * u4 + 7])));
-            st_shared_v4(stg + sw128_offset(row, h * 64 + 32 + u4 * 8, 128),
-                         pack_f16x2(__uint_as_float(v1[8 * u4 + 0]), __uint_as_float(v1[8 * u4 + 1])),
-                         pack_f16x2(__uint_as_float(v1[8 * u4 + 2]), __uint_as_float(v1[8 * u4 + 3])),
-                         pack_f16x2(__uint_as_float(v1[8 * u4 + 4]), __uint_as_float(v1[8 * u4 + 5])),
-                         pack_f16x2(__uint_as_float(v1[8 * u4 + 6]), __uint_as_float(v1[8 * u4 + 7])));
+          for (int q = 0; q < 16; ++q) {
+            ph[h * 32 + q] = pack_f16x2(__uint_as_float(v0[2 * q]), __uint_as_float(v0[2 * q + 1]));
+            ph[h * 32 + 16 + q] =
+                pack_f16x2(__uint_as_float(v1[2 * q]), __uint_as_float(v1[2 * q + 1]));
           }
         }
+        tc_fence_before();
+        mbar_arrive(o_empty);
+        if (et < 16) bulk_wait_read0();  // the previous tile's stores have read the staging tile
+        named_barrier(1, 128);
+#pragma unroll
+        for (int c8 = 0; c8 < 16; ++c8)  // 16-byte chunk c8 = columns [8 c8, 8 c8 + 8)
+          st_shared_v4(stg + sw128_offset(row, c8 * 8, 128), ph[4 * c8], ph[4 * c8 + 1],
+                       ph[4 * c8 + 2], ph[4 * c8 + 3]);
         fence_proxy_async_smem();
         named_barrier(1, 128);
         // Partials are kept in list order, so a full tile's 8 tokens x 16 heads are 128

@@ -45,7 +45,7 @@ def parse():
     p.add_argument("--decode-batch", type=int, default=0, help="override (profiling)")
     p.add_argument("--decode-nmax", type=int, default=0, help="override (profiling)")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--e2e-steps", type=int, default=10)
+    p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--L", type=int, default=0, help="override the workload length (profiling)")
     return p.parse_args()
 
@@ -150,17 +150,12 @@ class ClockSampler:
 # kernel's sources still hash to the value recorded with it; otherwise the traffic is null.
 CSRC = os.path.join(ROOT, "block_sparse_long_msa_gb300", "csrc")
 KERNEL_SOURCES = {
-    "attention": ["attn_prefill.cu", "common.cuh", "ptx.cuh"],
-    "combine": ["attn_prefill.cu", "common.cuh", "ptx.cuh"],
+    "main_branch": ["attn_prefill.cu", "common.cuh", "ptx.cuh"],
     "index": ["index_prefill.cu", "common.cuh", "ptx.cuh"],
     "decode_scan": ["decode.cu", "common.cuh", "ptx.cuh"],
 }
 NCU_TRAFFIC = {
     # prefill L=32768, 64/4 heads, k=16 (profiles/dram_prefill_L32K_decode_b64.md)
-    "attention": {"bytes_per_launch": 11706841984, "workload": "prefill_L32K@32768",
-                  "sources_sha256": "4959dfb526429f5ac59cea209119e8d4d15b425d2660f6cbedf911f727319b6e"},
-    "combine": {"bytes_per_launch": 9175326208, "workload": "prefill_L32K@32768",
-                "sources_sha256": "4959dfb526429f5ac59cea209119e8d4d15b425d2660f6cbedf911f727319b6e"},
     "index": {"bytes_per_launch": 41909760, "workload": "prefill_L32K@32768",
               "sources_sha256": "0f33ac3c78196a8d50dcacf237c9649b8fb27e4d91625b1c5efcc819bd23e39c"},
     # decode, 64 sequences of 16K-256K tokens
@@ -249,7 +244,7 @@ def run_msa(args, world, rank):
                    msa.msa_index_select_workspace(cfg, L, L))
     ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
     nchunks = -(-L // msa.msa_prefill_chunk_tokens(cfg, L))
-    launches_per_step = 1 + 7 * nchunks
+    launches_per_step = 1 + msa.msa_attn_prefill_launches(cfg, L)
     stream = torch.cuda.current_stream()
 
     def ev():
@@ -314,35 +309,35 @@ def run_msa(args, world, rank):
     total_ms = t0.elapsed_time(t1)
     total_ms = max_over_ranks(total_ms, world)
 
-    phase = {"index": 0.0, "schedule": 0.0, "attention": 0.0, "combine": 0.0}
+    # attention_waves: the wave launches (attention of every work item, and the merge of the rows
+    # of all but the last wave on a few SMs); merge_last_wave: the merge of the last wave's rows
+    phase = {"index": 0.0, "schedule": 0.0, "attention_waves": 0.0, "merge_last_wave": 0.0}
     for s in range(args.steps):
         m = marks[s]
         phase["index"] += starts[s].elapsed_time(m[0])
         for c in range(nchunks):
             phase["schedule"] += m[3 * c].elapsed_time(m[3 * c + 1])
-            phase["attention"] += m[3 * c + 1].elapsed_time(m[3 * c + 2])
-            phase["combine"] += m[3 * c + 2].elapsed_time(m[3 * c + 3])
+            phase["attention_waves"] += m[3 * c + 1].elapsed_time(m[3 * c + 2])
+            phase["merge_last_wave"] += m[3 * c + 2].elapsed_time(m[3 * c + 3])
     dec_sel_ms = sum(d[0].elapsed_time(d[1]) for d in dmarks) / args.steps
     dec_attn_ms = sum(d[1].elapsed_time(d[2]) for d in dmarks) / args.steps
     prefill_ms = sum(starts[s].elapsed_time(marks[s][-1]) for s in range(args.steps)) / args.steps
     dec_ms = dec_sel_ms + dec_attn_ms
-    per_launch_ms = {"index": phase["index"] / args.steps,
-                     "schedule": phase["schedule"] / args.steps,
-                     "attention": phase["attention"] / (args.steps * nchunks),
-                     "combine": phase["combine"] / (args.steps * nchunks)}
+    main_ms = (phase["attention_waves"] + phase["merge_last_wave"]) / args.steps
+    per_launch_ms = {"index": phase["index"] / args.steps, "main_branch": main_ms}
 
     work = prefill_work(w)
     peaks = load_peaks()
     tensor_peak = peaks["bf16_tflops"]
+    # the main branch (attention waves + the last merge) as one unit: its attention and merge
+    # kernels share the launches, so their bytes are counted together
     roof = {
         "index": ("tensor", work["index_flops"] / (per_launch_ms["index"] * 1e-3) / 1e12,
                   tensor_peak, "TFLOP/s"),
-        "attention": ("hbm", work["attn_bytes"] / nchunks / (per_launch_ms["attention"] * 1e-3)
-                      / 1e9, peaks["hbm_gbs"], "GB/s"),
-        "combine": ("hbm", work["combine_bytes"] / nchunks / (per_launch_ms["combine"] * 1e-3)
-                    / 1e9, peaks["hbm_gbs"], "GB/s"),
+        "main_branch": ("hbm", (work["attn_bytes"] + work["combine_bytes"]) / (main_ms * 1e-3)
+                        / 1e9, peaks["hbm_gbs"], "GB/s"),
     }
-    dominant = max(("index", "attention", "combine"), key=lambda n: phase[n])
+    dominant = max(("index", "main_branch"), key=lambda n: per_launch_ms[n])
     bound, achieved, peak, unit = roof[dominant]
     traffic = measured_traffic(dominant, f"{w.name}@{L}")
 
@@ -489,9 +484,10 @@ def run_msa(args, world, rank):
                      "unit": unit, "frac": achieved / peak, "traffic": traffic,
                      "peak_source": peaks["source"]},
         "kernel_rooflines": {n: {"bound": r[0], "achieved": r[1], "peak": r[2], "unit": r[3],
-                                 "frac": r[1] / r[2], "ms_per_launch": per_launch_ms[n]}
+                                 "frac": r[1] / r[2], "ms_per_step": per_launch_ms[n]}
                              for n, r in roof.items()},
-        "tensor_frac_main_branch": work["attn_flops"] / ((phase["attention"] + phase["combine"]
+        "tensor_frac_main_branch": work["attn_flops"] / ((phase["attention_waves"]
+                                                          + phase["merge_last_wave"]
                                                           + phase["schedule"]) / args.steps
                                                          * 1e-3) / 1e12 / tensor_peak,
         "e2e": None if e2e_ms is None else {

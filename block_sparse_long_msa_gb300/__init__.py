@@ -19,6 +19,7 @@ WS_HEADER_BYTES = 256
 
 EXPORTS = ("msa_index_select_workspace", "msa_index_select", "msa_attn_prefill_workspace",
            "msa_attn_prefill", "msa_attn_prefill_marked", "msa_prefill_chunk_tokens",
+           "msa_attn_prefill_launches",
            "msa_attn_decode_workspace", "msa_attn_decode",
            "msa_get_device_status", "msa_reset_device_status", "msa_status_string")
 
@@ -68,6 +69,8 @@ def lib() -> ctypes.CDLL:
                                               ctypes.c_int32]
         L.msa_prefill_chunk_tokens.argtypes = [cfgp, i64]
         L.msa_prefill_chunk_tokens.restype = i64
+        L.msa_attn_prefill_launches.argtypes = [cfgp, i64]
+        L.msa_attn_prefill_launches.restype = ctypes.c_int32
         L.msa_attn_decode_workspace.argtypes = [cfgp, pagedp]
         L.msa_attn_decode_workspace.restype = sz
         L.msa_attn_decode.argtypes = [cfgp, P, pagedp, P, P, P, P, sz, P]
@@ -161,6 +164,10 @@ def msa_attn_prefill_workspace(cfg: MsaConfig, L: int) -> int:
 
 def msa_prefill_chunk_tokens(cfg: MsaConfig, L: int) -> int:
     return int(lib().msa_prefill_chunk_tokens(ctypes.byref(cfg), L))
+
+
+def msa_attn_prefill_launches(cfg: MsaConfig, L: int) -> int:
+    return int(lib().msa_attn_prefill_launches(ctypes.byref(cfg), L))
 
 
 def msa_attn_prefill(cfg: MsaConfig, q, k, v, sel, o=None, lse=None, ws=None, stream=None,

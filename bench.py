@@ -45,6 +45,8 @@ def parse():
     p.add_argument("--decode-batch", type=int, default=0, help="override (profiling)")
     p.add_argument("--decode-nmax", type=int, default=0, help="override (profiling)")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e4m3-index", action="store_true",
+                   help="skip timing the e4m3 (FP8) index kernels beside the bf16 step")
     p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--L", type=int, default=0, help="override the workload length (profiling)")
     return p.parse_args()
@@ -215,12 +217,13 @@ def prefill_work(w, sel_counts=None):
     }
 
 
-def decode_work(w, seq_lens):
+def decode_work(w, seq_lens, index_bytes=2):
     """Algorithmic bytes of one decode step: the scan reads every index key strictly before each
     query's page (plus the index queries); the attention reads K and V of the selected pages
-    (the local page up to n) plus q and o."""
+    (the local page up to n) plus q and o.  index_bytes: bytes per index element (2 bf16, 1
+    e4m3)."""
     lens = [int(n) for n in seq_lens]
-    scan = acc.decode_index_bytes(lens, w.B, w.di, w.G)
+    scan = acc.decode_index_bytes(lens, w.B, w.di, w.G) * index_bytes // 2
     attn = acc.decode_attn_bytes(lens, w.B, w.d, w.G, w.Hq, w.k)
     return {"scan_bytes": scan, "attn_bytes": attn}
 
@@ -421,6 +424,60 @@ def run_msa(args, world, rank):
     if status != 0:
         raise RuntimeError(f"device status {status} after timed region")
 
+    # ---- e4m3 index vectors (the FP8 indexer, tcgen05 kind::f8f6f4): the integer/8 index
+    # inputs are exact in e4m3, so the selections must equal the bf16 ones; the two index
+    # kernels are timed alone and the step throughputs recomputed with their times ----
+    e4m3 = None
+    if not args.no_e4m3_index:
+        f8 = torch.float8_e4m3fn
+        q8, k8 = inp["q_idx"].to(f8), inp["k_idx"].to(f8)
+        dq8, dk8 = dinp["q_idx"].to(f8), dinp["k_idx_pool"].to(f8)
+        cfg8 = msa.config(w.G, w.hpg, w.k, w.scale, index_dtype="e4m3")
+        dcfg8 = msa.config(dw.G, dw.hpg, dw.k, dw.scale, index_dtype="e4m3")
+        paged8 = msa.paged_kv(dk8, dinp["k_pool"], dinp["v_pool"], dinp["page_table"],
+                              dinp["seq_lens"])
+        sel8, dsel8 = torch.empty_like(sel), torch.empty_like(dsel)
+
+        def timed(fn, n):
+            for _ in range(max(3, args.warmup)):
+                fn()
+            a0, a1 = ev(), ev()
+            torch.cuda.synchronize()
+            a0.record(stream)
+            for _ in range(n):
+                fn()
+            a1.record(stream)
+            torch.cuda.synchronize()
+            return a0.elapsed_time(a1) / n
+
+        n8 = max(3, args.steps)
+        idx8_ms = timed(lambda: msa.msa_index_select(cfg8, q8, k8, sel=sel8, ws=ws), n8)
+        didx8_ms = timed(lambda: msa.msa_index_select(dcfg8, dq8, paged=paged8, sel=dsel8,
+                                                      ws=dws), n8)
+        msa.msa_index_select(cfg, inp["q_idx"], inp["k_idx"], sel=sel, ws=ws)
+        msa.msa_index_select(dcfg, dinp["q_idx"], paged=paged, sel=dsel, ws=dws)
+        torch.cuda.synchronize()
+        assert torch.equal(sel8, sel) and torch.equal(dsel8, dsel), "e4m3 selection differs"
+        idx16_ms = phase["index"] / args.steps
+        pre8_ms = prefill_ms - idx16_ms + idx8_ms
+        dec8_ms = dec_attn_ms + didx8_ms
+        scan8_bytes = decode_work(dw, dinp["seq_lens"].tolist(), index_bytes=1)["scan_bytes"]
+        e4m3 = {
+            "note": "index vectors in e4m3 (exact for the integer/8 inputs: same selections, "
+                    "asserted); the main branch is unchanged, so the step times below are the "
+                    "measured bf16 steps with the e4m3 index kernels' measured times in place "
+                    "of the bf16 ones",
+            "prefill_index_ms": idx8_ms, "prefill_index_ms_bf16": idx16_ms,
+            "prefill_index_tflops": work["index_flops"] / (idx8_ms * 1e-3) / 1e12,
+            "prefill_index_frac_of_fp8_peak": work["index_flops"] / (idx8_ms * 1e-3) / 1e12
+                                              / (2 * tensor_peak),
+            "prefill_tokens_per_s": world * L / (pre8_ms * 1e-3),
+            "decode_index_ms": didx8_ms, "decode_index_ms_bf16": dec_sel_ms,
+            "decode_scan_gbs": scan8_bytes / (didx8_ms * 1e-3) / 1e9,
+            "decode_tokens_per_s": world * dw.batch / (dec8_ms * 1e-3),
+            "gpu_launches": 3 * n8,
+        }
+
     cpu_base = None
     dec_cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -503,6 +560,7 @@ def run_msa(args, world, rank):
         "decode": decode,
     }
     line["decode"]["cpu_baseline"] = dec_cpu
+    line["e4m3_index"] = e4m3
     if rank == 0:
         print(json.dumps(line), flush=True)
 

@@ -28,7 +28,7 @@ class MsaConfig(ctypes.Structure):
     _fields_ = [("num_groups", ctypes.c_int32), ("heads_per_group", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("index_dim", ctypes.c_int32),
                 ("block_size", ctypes.c_int32), ("topk", ctypes.c_int32),
-                ("softmax_scale", ctypes.c_float), ("reserved", ctypes.c_int32),
+                ("softmax_scale", ctypes.c_float), ("index_dtype", ctypes.c_int32),
                 ("wait_limit_ns", ctypes.c_int64)]
 
 
@@ -93,13 +93,26 @@ def status_string(status: int) -> str:
         return f"status {status}"
 
 
+INDEX_DTYPES = {"bf16": 0, "e4m3": 1}  # msa_index_dtype_t
+
+
 def config(num_groups: int, heads_per_group: int, topk: int, softmax_scale: float | None = None,
            head_dim: int = 128, index_dim: int = 128, block_size: int = 128,
-           wait_limit_ns: int = 0) -> MsaConfig:
+           wait_limit_ns: int = 0, index_dtype: str = "bf16") -> MsaConfig:
+    """index_dtype: element type of q_idx, k_idx and the paged k_idx_pool, "bf16" or "e4m3"
+    (torch.float8_e4m3fn tensors)."""
     if softmax_scale is None:
         softmax_scale = 1.0 / math.sqrt(head_dim)
     return MsaConfig(num_groups, heads_per_group, head_dim, index_dim, block_size, topk,
-                     softmax_scale, 0, wait_limit_ns)
+                     softmax_scale, INDEX_DTYPES[index_dtype], wait_limit_ns)
+
+
+def _index_dtype_ok(cfg: MsaConfig, *tensors):
+    import torch
+    want = torch.float8_e4m3fn if cfg.index_dtype == INDEX_DTYPES["e4m3"] else torch.bfloat16
+    for t in tensors:
+        if t is not None and t.dtype != want:
+            raise MsaError(MSA_ERR_INVALID_ARG, f"index vectors must be {want}, got {t.dtype}")
 
 
 def _ptr(t):
@@ -143,6 +156,7 @@ def msa_index_select(cfg: MsaConfig, q_idx, k_idx=None, paged: MsaPagedKV | None
                      sel=None, sel_score=None, want_score: bool = False, ws=None, stream=None):
     """Index branch.  Returns sel int32 [G][T][k] (and sel_score fp32 if asked)."""
     import torch
+    _index_dtype_ok(cfg, q_idx, k_idx)
     T = q_idx.shape[0]
     L = 0 if paged is not None else k_idx.shape[0]
     G, k = cfg.num_groups, cfg.topk

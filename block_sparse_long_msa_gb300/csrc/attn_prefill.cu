@@ -844,10 +844,12 @@ __global__ void __launch_bounds__(512, 1)
           tmem_ld32(sa + c * 32, v0);
           tmem_ld32(sa + c * 32 + 32, v1);
           tmem_ld_wait();
-          if (unmasked) {
+          if (unmasked) {  // four independent three-input max chains
+            float m4[4] = {mraw, mraw, mraw, mraw};
 #pragma unroll
             for (int q = 0; q < 32; ++q)
-              mraw = fmaxf(mraw, fmaxf(__uint_as_float(v0[q]), __uint_as_float(v1[q])));
+              m4[q & 3] = fmax3(m4[q & 3], __uint_as_float(v0[q]), __uint_as_float(v1[q]));
+            mraw = fmax3(fmaxf(m4[0], m4[1]), m4[2], m4[3]);
           } else {
 #pragma unroll
             for (int q = 0; q < 32; ++q) {

@@ -22,24 +22,44 @@ namespace msa {
 namespace {
 
 constexpr int kHeads = 16;  // query heads per group
-constexpr int kScanStages = 6;
-constexpr uint32_t kScanStage = 32768 + 4096;  // 128 keys x 128 bf16 + the 16-row query tile
+constexpr uint32_t kPanel = 16384;  // 128 rows x 128 bytes: one 128-byte-swizzled panel
+// Scan stage: one index-key page (128 keys, K-major, 128-byte swizzle: two 64-element panels
+// per bf16 row, one per e4m3 row) and a 16-row index-query tile (rows G..15 zero).  Every MMA
+// step covers 32 bytes of K: 8 bf16 steps or 4 e4m3 steps for K = 128.
+template <bool kF8>
+struct ScanTiles {
+  static constexpr uint32_t kEsz = kF8 ? 1 : 2;
+  static constexpr uint32_t kKeys = kBlock * kDim * kEsz;      // 32 KB bf16, 16 KB e4m3
+  static constexpr uint32_t kQRows = 16 * kDim * kEsz;         // 4 KB bf16, 2 KB e4m3
+  static constexpr uint32_t kQPanel = 16 * 128;
+  static constexpr uint32_t kStage = kKeys + kQRows;
+  static constexpr int kPanels = kF8 ? 1 : 2;
+  static constexpr int kSteps = kF8 ? 4 : 8;
+  static constexpr int kStages = kF8 ? 11 : 6;                 // about 200 KB in flight
+  static constexpr uint32_t kIdesc = kF8 ? idesc_e4m3_f32(128, 16)
+                                         : idesc_bf16_f32(128, 16, false, false);
+};
+constexpr int kScanMaxStages = 12;
 constexpr int kScanSlots = 8;                  // TMEM accumulators of 16 columns
-// barrier block after the stages: full[6], empty[6], acc_full[8], acc_empty[8], drain, then the
-// TMEM base address and the abort flag
-constexpr uint32_t kScanBarFull = 0, kScanBarEmpty = 64, kScanBarAccFull = 128,
-                   kScanBarAccEmpty = 192, kScanBarDrain = 256, kScanTmemSlot = 264,
-                   kScanAbort = 268, kScanWalk = 272, kScanBarBytes = 512;
-static_assert(kScanBarFull + 8 * kScanStages <= kScanBarEmpty, "scan barriers");
-static_assert(kScanBarEmpty + 8 * kScanStages <= kScanBarAccFull, "scan barriers");
+// barrier block after the stages: full[], empty[], acc_full[8], acc_empty[8], drain, then the
+// TMEM base address, the abort flag and the CTA's page range
+constexpr uint32_t kScanBarFull = 0, kScanBarEmpty = 96, kScanBarAccFull = 192,
+                   kScanBarAccEmpty = 256, kScanBarDrain = 320, kScanTmemSlot = 328,
+                   kScanAbort = 332, kScanWalk = 336, kScanBarBytes = 512;
+static_assert(kScanBarFull + 8 * kScanMaxStages <= kScanBarEmpty, "scan barriers");
+static_assert(kScanBarEmpty + 8 * kScanMaxStages <= kScanBarAccFull, "scan barriers");
 static_assert(kScanBarAccFull + 8 * kScanSlots <= kScanBarAccEmpty, "scan barriers");
 static_assert(kScanBarAccEmpty + 8 * kScanSlots <= kScanBarDrain, "scan barriers");
 static_assert(kScanAbort + 4 <= kScanWalk, "scan barriers");
 static_assert(kScanWalk + 12 <= kScanBarBytes, "scan barriers");
-constexpr uint32_t kScanSmem = kScanStages * kScanStage + kScanBarBytes + 1024;
-static_assert(kScanSmem <= 232448, "scan shared memory");
-constexpr uint32_t kIdescScan = idesc_bf16_f32(128, 16, false, false);
-constexpr uint32_t kPanel = 16384;
+template <bool kF8>
+constexpr uint32_t scan_smem() {
+  return ScanTiles<kF8>::kStages * ScanTiles<kF8>::kStage + kScanBarBytes + 1024;
+}
+static_assert(ScanTiles<false>::kStages <= kScanMaxStages && scan_smem<false>() <= 232448,
+              "scan shared memory");
+static_assert(ScanTiles<true>::kStages <= kScanMaxStages && scan_smem<true>() <= 232448,
+              "scan shared memory");
 
 struct ScanArgs {
   const int32_t* page_table;
@@ -120,9 +140,13 @@ struct PageWalk {
   }
 };
 
+template <bool kF8>
 __global__ void __launch_bounds__(256, 1)
     decode_scan_kernel(const __grid_constant__ CUtensorMap map_k,
                        const __grid_constant__ CUtensorMap map_q, ScanArgs a) {
+  using T = ScanTiles<kF8>;
+  constexpr int kScanStages = T::kStages;
+  constexpr uint32_t kScanStage = T::kStage;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -141,8 +165,8 @@ __global__ void __launch_bounds__(256, 1)
 
   // rows G..15 of every stage's query tile stay zero (TMA writes rows 0..G-1 only)
   for (int st = 0; st < kScanStages; ++st) {
-    uint32_t* qt = reinterpret_cast<uint32_t*>(smem + st * kScanStage + 32768);
-    for (int w = threadIdx.x; w < 1024; w += blockDim.x) qt[w] = 0;
+    uint32_t* qt = reinterpret_cast<uint32_t*>(smem + st * kScanStage + T::kKeys);
+    for (int w = threadIdx.x; w < static_cast<int>(T::kQRows / 4); w += blockDim.x) qt[w] = 0;
   }
   fence_proxy_async_smem();
   if (threadIdx.x == 0) {
@@ -173,27 +197,57 @@ __global__ void __launch_bounds__(256, 1)
     if (lane == 0) {
       tma_prefetch_map(&map_k);
       tma_prefetch_map(&map_q);
+      // Page ids are read 8 pages ahead (a batch of independent loads while the previous batch
+      // is issued), so the page-table latency stays off the issue path.
       PageWalk w;
       w.init(a, walk);
+      auto fetch8 = [&](int (&pid)[8], int (&sq)[8]) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int b = w.next(a);
+          sq[j] = b >= 0 ? w.s : -1;
+          pid[j] = b >= 0 ? a.page_table[static_cast<size_t>(w.s) * a.max_pages + b] : 0;
+        }
+      };
+      int pa[8], sa[8], pb[8], sb8[8];
+      fetch8(pa, sa);
       int p = 0;
-      for (int b = w.next(a); b >= 0; b = w.next(a), ++p) {
-        const int st = p % kScanStages;
-        if (*abort_flag || !mbar_wait(empty(st), ((p / kScanStages) & 1) ^ 1, a.wait_ns)) {
-          report_status(a.status, kStatusTimeout);
-          *abort_flag = 1;
-          break;
+      bool more = sa[0] >= 0;
+      while (more) {
+        fetch8(pb, sb8);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (sa[j] < 0 || *abort_flag) {
+            more = false;
+            break;
+          }
+          const int st = p % kScanStages;
+          if (!mbar_wait(empty(st), ((p / kScanStages) & 1) ^ 1, a.wait_ns)) {
+            report_status(a.status, kStatusTimeout);
+            *abort_flag = 1;
+            more = false;
+            break;
+          }
+          int page = pa[j];
+          if (page < 0 || page >= a.num_pages) {
+            report_status(a.status, kStatusBounds);
+            page = 0;  // keep the pipeline in step; the status word marks the result invalid
+          }
+          const uint32_t sbase = base + st * kScanStage;
+          mbar_arrive_expect_tx(full(st), T::kKeys + a.G * kDim * T::kEsz);
+          for (int pn = 0; pn < T::kPanels; ++pn) {
+            tma_load_2d(sbase + pn * kPanel, &map_k, full(st), pn * 64, page * kBlock);
+            tma_load_2d(sbase + T::kKeys + pn * T::kQPanel, &map_q, full(st), pn * 64,
+                        sa[j] * a.G);
+          }
+          ++p;
         }
-        int page = a.page_table[static_cast<size_t>(w.s) * a.max_pages + b];
-        if (page < 0 || page >= a.num_pages) {
-          report_status(a.status, kStatusBounds);
-          page = 0;  // keep the pipeline in step; the status word marks the result invalid
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          pa[j] = pb[j];
+          sa[j] = sb8[j];
         }
-        const uint32_t sb = base + st * kScanStage;
-        mbar_arrive_expect_tx(full(st), 32768 + a.G * 256);
-        tma_load_2d(sb, &map_k, full(st), 0, page * kBlock);
-        tma_load_2d(sb + kPanel, &map_k, full(st), 64, page * kBlock);
-        tma_load_2d(sb + 32768, &map_q, full(st), 0, w.s * a.G);
-        tma_load_2d(sb + 32768 + 2048, &map_q, full(st), 64, w.s * a.G);
+        more = more && sa[0] >= 0;
       }
       if (*abort_flag) {
         for (int x = (p > kScanStages ? p - kScanStages : 0); x < p; ++x)
@@ -216,11 +270,14 @@ __global__ void __launch_bounds__(256, 1)
         tc_fence_after();
         const uint32_t sb = base + st * kScanStage;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
+        for (int kk = 0; kk < T::kSteps; ++kk) {
           const uint64_t ad = sdesc_sw128(sb + (kk >> 2) * kPanel + (kk & 3) * 32, 16, 1024);
           const uint64_t bd =
-              sdesc_sw128(sb + 32768 + (kk >> 2) * 2048 + (kk & 3) * 32, 16, 1024);
-          mma_bf16_ss(tmem + slot * 16, ad, bd, kIdescScan, kk > 0);
+              sdesc_sw128(sb + T::kKeys + (kk >> 2) * T::kQPanel + (kk & 3) * 32, 16, 1024);
+          if (kF8)
+            mma_f8_ss(tmem + slot * 16, ad, bd, T::kIdesc, kk > 0);
+          else
+            mma_bf16_ss(tmem + slot * 16, ad, bd, T::kIdesc, kk > 0);
         }
         mma_commit(acc_full(slot));
         mma_commit(empty(st));
@@ -696,8 +753,8 @@ size_t decode_select_workspace_bytes(int batch, int G, int max_pages) {
 
 cudaError_t launch_decode_select(const CUtensorMap& map_k, const CUtensorMap& map_q,
                                  const int32_t* page_table, const int32_t* seq_lens, int batch,
-                                 int max_pages, int num_pages, int G, int k, float* scores,
-                                 int32_t* sel, float* sel_score, int32_t* status,
+                                 int max_pages, int num_pages, int G, int k, bool fp8,
+                                 float* scores, int32_t* sel, float* sel_score, int32_t* status,
                                  uint64_t wait_ns, int num_sms, cudaStream_t stream) {
   ScanArgs a{};
   a.page_table = page_table;
@@ -709,12 +766,22 @@ cudaError_t launch_decode_select(const CUtensorMap& map_k, const CUtensorMap& ma
   a.scores = reinterpret_cast<float4*>(scores);
   a.status = status;
   a.wait_ns = wait_ns;
-  cudaError_t e = cudaFuncSetAttribute(decode_scan_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kScanSmem);
-  if (e != cudaSuccess) return e;
   const int grid = static_cast<int>(
       std::max<int64_t>(1, std::min<int64_t>(num_sms, static_cast<int64_t>(batch) * max_pages)));
-  decode_scan_kernel<<<grid, 256, kScanSmem, stream>>>(map_k, map_q, a);
+  cudaError_t e;
+  if (fp8) {
+    if ((e = cudaFuncSetAttribute(decode_scan_kernel<true>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  scan_smem<true>())) != cudaSuccess)
+      return e;
+    decode_scan_kernel<true><<<grid, 256, scan_smem<true>(), stream>>>(map_k, map_q, a);
+  } else {
+    if ((e = cudaFuncSetAttribute(decode_scan_kernel<false>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  scan_smem<false>())) != cudaSuccess)
+      return e;
+    decode_scan_kernel<false><<<grid, 256, scan_smem<false>(), stream>>>(map_k, map_q, a);
+  }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   TopkArgs t{};
   t.scores = a.scores;

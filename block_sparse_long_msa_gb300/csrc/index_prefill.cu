@@ -25,12 +25,23 @@ namespace msa {
 
 namespace {
 
-constexpr uint32_t kQTile = 32768;   // 128 query rows x 128 bf16
-constexpr uint32_t kQPanel = 16384;  // 128 rows x 64 bf16 (one 128-byte swizzle panel)
-constexpr uint32_t kKTile = 65536;   // kIndexKeyTile keys x 128 bf16
-constexpr uint32_t kKPanel = 32768;  // kIndexKeyTile rows x 64 bf16
-constexpr int kMaxStagesIdx = 3;
-constexpr uint32_t kIdescS = idesc_bf16_f32(128, kIndexKeyTile, false, false);
+// Tiles of index vectors (128 elements), K-major with the 128-byte swizzle: a bf16 row is two
+// 128-byte panels (64 elements each), an e4m3 row one.  Every MMA step covers 32 bytes of K
+// (16 bf16 or 32 e4m3 elements), so K = 128 takes 8 bf16 steps or 4 e4m3 steps.
+template <bool kF8>
+struct IdxTiles {
+  static constexpr uint32_t kEsz = kF8 ? 1 : 2;
+  static constexpr uint32_t kQPanel = 128 * 128;                 // 128 rows x 128 bytes
+  static constexpr uint32_t kQTile = 128 * kDim * kEsz;
+  static constexpr uint32_t kKPanel = kIndexKeyTile * 128;
+  static constexpr uint32_t kKTile = kIndexKeyTile * kDim * kEsz;
+  static constexpr int kPanels = kF8 ? 1 : 2;
+  static constexpr int kSteps = kF8 ? 4 : 8;
+  static constexpr uint32_t kIdesc = kF8 ? idesc_e4m3_f32(128, kIndexKeyTile)
+                                         : idesc_bf16_f32(128, kIndexKeyTile, false, false);
+  static constexpr int kMaxStages = kF8 ? 6 : 3;
+};
+constexpr int kMaxStagesIdx = 6;
 static_assert(kIndexKeyTile == 2 * kBlock, "a key tile is two blocks");
 
 // barrier block (offsets from its start)
@@ -54,10 +65,14 @@ struct IndexPrefillArgs {
   uint64_t wait_ns;
 };
 
-// Shared memory: gpc index-query tiles, ns key stages of 64 KB, then the barrier block.
+// Shared memory: gpc index-query tiles, ns key stages, then the barrier block.
+template <bool kF8>
 __global__ void __launch_bounds__(384, 1)
     index_select_prefill_kernel(const __grid_constant__ CUtensorMap map_q,
                                 const __grid_constant__ CUtensorMap map_k, IndexPrefillArgs a) {
+  using T = IdxTiles<kF8>;
+  constexpr uint32_t kQTile = T::kQTile, kQPanel = T::kQPanel, kKTile = T::kKTile,
+                     kKPanel = T::kKPanel;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -112,10 +127,10 @@ __global__ void __launch_bounds__(384, 1)
       tma_prefetch_map(&map_q);
       tma_prefetch_map(&map_k);
       mbar_arrive_expect_tx(bar_q, gpc * kQTile);
-      for (int gl = 0; gl < gpc; ++gl) {
-        tma_load_3d(sQ + gl * kQTile, &map_q, bar_q, 0, g0 + gl, qb * kBlock);
-        tma_load_3d(sQ + gl * kQTile + kQPanel, &map_q, bar_q, 64, g0 + gl, qb * kBlock);
-      }
+      for (int gl = 0; gl < gpc; ++gl)
+        for (int pn = 0; pn < T::kPanels; ++pn)
+          tma_load_3d(sQ + gl * kQTile + pn * kQPanel, &map_q, bar_q, pn * 64, g0 + gl,
+                      qb * kBlock);
       // The last tile of an odd count also carries block qb (or rows past L, zero-filled);
       // those scores are never read.
       bool ok = true;
@@ -127,8 +142,9 @@ __global__ void __launch_bounds__(384, 1)
           break;
         }
         mbar_arrive_expect_tx(b_full(stage), kKTile);
-        tma_load_2d(sK + stage * kKTile, &map_k, b_full(stage), 0, t * kIndexKeyTile);
-        tma_load_2d(sK + stage * kKTile + kKPanel, &map_k, b_full(stage), 64, t * kIndexKeyTile);
+        for (int pn = 0; pn < T::kPanels; ++pn)
+          tma_load_2d(sK + stage * kKTile + pn * kKPanel, &map_k, b_full(stage), pn * 64,
+                      t * kIndexKeyTile);
         ++issued;
       }
       if (!ok) {
@@ -164,10 +180,14 @@ __global__ void __launch_bounds__(384, 1)
           const uint32_t d = tmem + slot * kIndexKeyTile;
           const uint32_t qt = sQ + gl * kQTile;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
+          for (int kk = 0; kk < T::kSteps; ++kk) {
             const uint32_t col = (kk & 3) * 32;
-            mma_bf16_ss(d, sdesc_sw128(qt + (kk >> 2) * kQPanel + col, 16, 1024),
-                        sdesc_sw128(kst + (kk >> 2) * kKPanel + col, 16, 1024), kIdescS, kk > 0);
+            const uint64_t ad = sdesc_sw128(qt + (kk >> 2) * kQPanel + col, 16, 1024);
+            const uint64_t bd = sdesc_sw128(kst + (kk >> 2) * kKPanel + col, 16, 1024);
+            if (kF8)
+              mma_f8_ss(d, ad, bd, T::kIdesc, kk > 0);
+            else
+              mma_bf16_ss(d, ad, bd, T::kIdesc, kk > 0);
           }
           mma_commit(acc_full(slot));
         }
@@ -218,7 +238,7 @@ __global__ void __launch_bounds__(384, 1)
           }
 #pragma unroll
           for (int q = 0; q < 32; ++q)
-            m4[q & 3] = fmaxf(m4[q & 3], fmaxf(__uint_as_float(v0[q]), __uint_as_float(v1[q])));
+            m4[q & 3] = fmax3(m4[q & 3], __uint_as_float(v0[q]), __uint_as_float(v1[q]));
         }
         mx[h] = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
       }
@@ -265,27 +285,38 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
-}  // namespace
-
-size_t index_prefill_smem_bytes(int gpc, int ns) {
-  return 1024 + static_cast<size_t>(gpc) * kQTile + static_cast<size_t>(ns) * kKTile + kBarBytes;
+template <bool kF8>
+size_t smem_bytes(int gpc, int ns) {
+  return 1024 + static_cast<size_t>(gpc) * IdxTiles<kF8>::kQTile +
+         static_cast<size_t>(ns) * IdxTiles<kF8>::kKTile + kBarBytes;
 }
 
-cudaError_t launch_index_select_prefill(const CUtensorMap& map_q, const CUtensorMap& map_k,
-                                        int64_t L, int G, int k, int32_t* sel, float* sel_score,
-                                        int32_t* status, uint64_t wait_ns, cudaStream_t stream) {
+template <bool kF8>
+cudaError_t launch(const CUtensorMap& map_q, const CUtensorMap& map_k, int64_t L, int G, int k,
+                   int32_t* sel, float* sel_score, int32_t* status, uint64_t wait_ns,
+                   cudaStream_t stream) {
   const int nb = static_cast<int>((L + kBlock - 1) / kBlock);
   const int gpc = (G % 2 == 0) ? 2 : 1;  // groups per CTA
-  int ns = kMaxStagesIdx;                // key stages of 64 KB
-  while (ns > 1 && index_prefill_smem_bytes(gpc, ns) > 232448) --ns;
-  const size_t smem = index_prefill_smem_bytes(gpc, ns);
-  cudaError_t e = cudaFuncSetAttribute(index_select_prefill_kernel,
+  int ns = IdxTiles<kF8>::kMaxStages;    // key stages
+  while (ns > 1 && smem_bytes<kF8>(gpc, ns) > 232448) --ns;
+  const size_t smem = smem_bytes<kF8>(gpc, ns);
+  cudaError_t e = cudaFuncSetAttribute(index_select_prefill_kernel<kF8>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   IndexPrefillArgs a{L, G, gpc, k, nb, ns, sel, sel_score, status, wait_ns};
-  index_select_prefill_kernel<<<nb * (G / gpc), 384, smem, stream>>>(map_q, map_k, a);
+  index_select_prefill_kernel<kF8><<<nb * (G / gpc), 384, smem, stream>>>(map_q, map_k, a);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_index_select_prefill(const CUtensorMap& map_q, const CUtensorMap& map_k,
+                                        int64_t L, int G, int k, bool fp8, int32_t* sel,
+                                        float* sel_score, int32_t* status, uint64_t wait_ns,
+                                        cudaStream_t stream) {
+  return fp8 ? launch<true>(map_q, map_k, L, G, k, sel, sel_score, status, wait_ns, stream)
+             : launch<false>(map_q, map_k, L, G, k, sel, sel_score, status, wait_ns, stream);
 }
 
 }  // namespace msa

@@ -11,10 +11,11 @@ namespace msa {
 
 // Keys per tile of the prefill index kernel (two blocks): the box height of its key tensor map.
 constexpr int kIndexKeyTile = 256;
-size_t index_prefill_smem_bytes(int gpc, int ns);
+// fp8: index vectors are e4m3 (else bf16); the tensor maps' element type must match.
 cudaError_t launch_index_select_prefill(const CUtensorMap& map_q, const CUtensorMap& map_k,
-                                        int64_t L, int G, int k, int32_t* sel, float* sel_score,
-                                        int32_t* status, uint64_t wait_ns, cudaStream_t stream);
+                                        int64_t L, int G, int k, bool fp8, int32_t* sel,
+                                        float* sel_score, int32_t* status, uint64_t wait_ns,
+                                        cudaStream_t stream);
 
 // Byte offsets of the prefill main-branch workspace (after the 256-byte status header).
 struct PrefillWorkspace {
@@ -39,8 +40,8 @@ cudaError_t launch_attn_prefill_chunk(const CUtensorMap& map_q, const CUtensorMa
 size_t decode_select_workspace_bytes(int batch, int G, int max_pages);
 cudaError_t launch_decode_select(const CUtensorMap& map_k, const CUtensorMap& map_q,
                                  const int32_t* page_table, const int32_t* seq_lens, int batch,
-                                 int max_pages, int num_pages, int G, int k, float* scores,
-                                 int32_t* sel, float* sel_score, int32_t* status,
+                                 int max_pages, int num_pages, int G, int k, bool fp8,
+                                 float* scores, int32_t* sel, float* sel_score, int32_t* status,
                                  uint64_t wait_ns, int num_sms, cudaStream_t stream);
 size_t decode_attn_workspace_bytes(int batch, int G, int k);
 cudaError_t launch_decode_attn(const CUtensorMap& map_kp, const CUtensorMap& map_vp,

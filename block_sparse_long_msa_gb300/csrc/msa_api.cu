@@ -18,13 +18,33 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
   return msa::encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, rank, dims, strides, box);
 }
 
+// Tensor map of index vectors (128 elements of the config's index type per row), 128-byte
+// swizzle: dims[0] = 128 elements, strides in elements of the index type (converted to bytes
+// here), box[0] = one 128-byte panel (64 bf16 or 128 e4m3 elements).
+bool make_index_map(CUtensorMap* m, bool fp8, const void* base, int rank, const uint64_t* dims,
+                    const uint64_t* strides_el, const uint32_t* box_rest) {
+  const uint64_t esz = fp8 ? 1 : 2;
+  uint64_t strides[3];
+  uint32_t box[3];
+  box[0] = fp8 ? 128 : 64;
+  for (int r = 1; r < rank; ++r) {
+    strides[r - 1] = strides_el[r - 1] * esz;
+    box[r] = box_rest[r - 1];
+  }
+  return msa::encode_tmap(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                          base, rank, dims, strides, box);
+}
+
+bool index_fp8(const msa_config_t* c) { return c->index_dtype == MSA_INDEX_E4M3; }
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 msa_status_t check_config(const msa_config_t* c) {
   if (!c) return MSA_ERR_INVALID_ARG;
-  if (c->num_groups < 1 || c->heads_per_group < 1 || c->topk < 1 || c->reserved != 0 ||
+  if (c->num_groups < 1 || c->heads_per_group < 1 || c->topk < 1 ||
+      (c->index_dtype != MSA_INDEX_BF16 && c->index_dtype != MSA_INDEX_E4M3) ||
       c->wait_limit_ns < 0 || !(c->softmax_scale == c->softmax_scale))
     return MSA_ERR_INVALID_ARG;
   if (c->head_dim != kDim || c->index_dim != kDim || c->block_size != kBlock ||
@@ -79,24 +99,25 @@ msa_status_t index_select_paged(const msa_config_t* cfg, const void* q_idx,
   if (ws_bytes < msa_index_select_workspace(cfg, paged->batch, 0, paged)) return MSA_ERR_WORKSPACE;
   if (paged->batch == 0) return MSA_OK;
   CUtensorMap mk, mq;
+  const bool fp8 = index_fp8(cfg);
   {
     const uint64_t dims[2] = {kDim, static_cast<uint64_t>(paged->num_pages) * kBlock};
-    const uint64_t strides[1] = {kDim * 2};
-    const uint32_t box[2] = {64, kBlock};
-    if (!make_map(&mk, paged->k_idx_pool, 2, dims, strides, box)) return MSA_ERR_CUDA;
+    const uint64_t strides[1] = {kDim};
+    const uint32_t box[1] = {kBlock};
+    if (!make_index_map(&mk, fp8, paged->k_idx_pool, 2, dims, strides, box)) return MSA_ERR_CUDA;
   }
   {
     const uint64_t dims[2] = {kDim, static_cast<uint64_t>(paged->batch) * G};
-    const uint64_t strides[1] = {kDim * 2};
-    const uint32_t box[2] = {64, static_cast<uint32_t>(G)};
-    if (!make_map(&mq, q_idx, 2, dims, strides, box)) return MSA_ERR_CUDA;
+    const uint64_t strides[1] = {kDim};
+    const uint32_t box[1] = {static_cast<uint32_t>(G)};
+    if (!make_index_map(&mq, fp8, q_idx, 2, dims, strides, box)) return MSA_ERR_CUDA;
   }
   int sms = 0;
   if (!sm_count(&sms)) return MSA_ERR_CUDA;
   float* scores = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + MSA_WS_HEADER_BYTES);
   cudaError_t e = msa::launch_decode_select(mk, mq, paged->page_table, paged->seq_lens,
                                             paged->batch, paged->max_pages, paged->num_pages, G,
-                                            cfg->topk, scores, sel, sel_score, status_word(ws),
+                                            cfg->topk, fp8, scores, sel, sel_score, status_word(ws),
                                             wait_ns(cfg), sms, stream);
   return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
 }
@@ -163,19 +184,20 @@ msa_status_t msa_index_select(const msa_config_t* cfg, const void* q_idx, const 
   if (ws_bytes < msa_index_select_workspace(cfg, L, L, nullptr)) return MSA_ERR_WORKSPACE;
   if (L == 0) return MSA_OK;
   CUtensorMap mq, mk;
+  const bool fp8 = index_fp8(cfg);
   {
     const uint64_t dims[3] = {kDim, static_cast<uint64_t>(G), static_cast<uint64_t>(L)};
-    const uint64_t strides[2] = {kDim * 2, static_cast<uint64_t>(G) * kDim * 2};
-    const uint32_t box[3] = {64, 1, kBlock};
-    if (!make_map(&mq, q_idx, 3, dims, strides, box)) return MSA_ERR_CUDA;
+    const uint64_t strides[2] = {kDim, static_cast<uint64_t>(G) * kDim};
+    const uint32_t box[2] = {1, kBlock};
+    if (!make_index_map(&mq, fp8, q_idx, 3, dims, strides, box)) return MSA_ERR_CUDA;
   }
   {
     const uint64_t dims[2] = {kDim, static_cast<uint64_t>(L)};
-    const uint64_t strides[1] = {kDim * 2};
-    const uint32_t box[2] = {64, msa::kIndexKeyTile};
-    if (!make_map(&mk, k_idx, 2, dims, strides, box)) return MSA_ERR_CUDA;
+    const uint64_t strides[1] = {kDim};
+    const uint32_t box[1] = {msa::kIndexKeyTile};
+    if (!make_index_map(&mk, fp8, k_idx, 2, dims, strides, box)) return MSA_ERR_CUDA;
   }
-  cudaError_t e = msa::launch_index_select_prefill(mq, mk, L, G, cfg->topk, sel, sel_score,
+  cudaError_t e = msa::launch_index_select_prefill(mq, mk, L, G, cfg->topk, fp8, sel, sel_score,
                                                    status_word(ws), wait_ns(cfg), stream);
   return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
 }

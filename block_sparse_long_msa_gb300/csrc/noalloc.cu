@@ -58,7 +58,8 @@ extern "C" msa_status_t msa_attn_prefill_noalloc(const msa_config_t* cfg, const 
                                                  const int32_t* sel, void* o, float* lse,
                                                  int32_t* device_status, cudaStream_t stream) {
   if (!cfg || cfg->num_groups < 1 || cfg->heads_per_group < 1 || cfg->topk < 1 ||
-      cfg->reserved != 0 || cfg->wait_limit_ns < 0 || !(cfg->softmax_scale == cfg->softmax_scale))
+      (cfg->index_dtype != MSA_INDEX_BF16 && cfg->index_dtype != MSA_INDEX_E4M3) ||
+      cfg->wait_limit_ns < 0 || !(cfg->softmax_scale == cfg->softmax_scale))
     return MSA_ERR_INVALID_ARG;
   if (cfg->head_dim != msa::kDim || cfg->index_dim != msa::kDim ||
       cfg->block_size != msa::kBlock || cfg->topk > msa::kTopMax || cfg->heads_per_group != 16)

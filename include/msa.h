@@ -54,6 +54,14 @@ typedef enum {
   MSA_ERR_DEVICE_BOUNDS = 6   /* device status: a page id or block id was out of range */
 } msa_status_t;
 
+/* Element type of the index vectors (q_idx, k_idx, the paged k_idx_pool).  E4M3 is the OCP
+ * 8-bit float (1 sign, 4 exponent bits with bias 7, 3 mantissa bits, no infinities): the
+ * indexer's QK product in FP8, as the pages' Blackwell kernel computes it ("MiniMax M3.1 Flash
+ * 开放权重与部署要点", section 权重能下载之后，为什么还要先看 vLLM, where FP8 is the compute type
+ * NVFP4-stored keys are dequantised to).  Scores accumulate in fp32 either way; e4m3 halves the
+ * index bytes and doubles the tensor-core rate. */
+typedef enum { MSA_INDEX_BF16 = 0, MSA_INDEX_E4M3 = 1 } msa_index_dtype_t;
+
 typedef struct {
   int32_t num_groups;      /* G: KV heads = GQA groups = index-query heads */
   int32_t heads_per_group; /* query heads per group; Hq = G * heads_per_group */
@@ -62,14 +70,14 @@ typedef struct {
   int32_t block_size;      /* B (128) */
   int32_t topk;            /* k, the local block included (1..16) */
   float softmax_scale;     /* multiplies q.k in the main branch (1/sqrt(d) in the tests) */
-  int32_t reserved;        /* must be 0 */
+  int32_t index_dtype;     /* msa_index_dtype_t of q_idx, k_idx and k_idx_pool (0: bf16) */
   int64_t wait_limit_ns;   /* bound on every device-side wait; 0 selects 2 seconds */
 } msa_config_t;
 
 /* A paged KV cache of B-token pages shared by `batch` sequences.  Logical block b of sequence s
  * lives in physical page page_table[s*max_pages + b]. */
 typedef struct {
-  const void* k_idx_pool;    /* bf16 [num_pages][B][d_i]: index keys */
+  const void* k_idx_pool;    /* index_dtype [num_pages][B][d_i]: index keys */
   const void* k_pool;        /* bf16 [num_pages][G][B][d]: keys, head-major inside a page */
   const void* v_pool;        /* bf16 [num_pages][G][B][d]: values, same layout */
   const int32_t* page_table; /* int32 [batch][max_pages], device */
@@ -88,10 +96,11 @@ size_t msa_index_select_workspace(const msa_config_t* cfg, int64_t num_queries, 
 
 /*
  * Index branch: block scores, max-pooling, per-group top-k with the forced local block.
- *   Prefill (paged == NULL): q_idx bf16 [L][G][d_i] (query i is the token at position i),
- *     k_idx bf16 [L][d_i].  Output rows: T = L.
- *   Decode (paged != NULL, k_idx and L ignored): q_idx bf16 [batch][G][d_i], one query per
+ *   Prefill (paged == NULL): q_idx [L][G][d_i] (query i is the token at position i),
+ *     k_idx [L][d_i].  Output rows: T = L.
+ *   Decode (paged != NULL, k_idx and L ignored): q_idx [batch][G][d_i], one query per
  *     sequence at position seq_lens[s]-1; index keys read from paged->k_idx_pool.  T = batch.
+ *   Index vectors are bf16 or e4m3 as cfg->index_dtype says.
  *   sel (out) int32 [G][T][k]: selected block ids, ascending, padded with -1 when fewer than k
  *     blocks exist.  Ranking is by raw score (higher first), ties to the lower block id.
  *   sel_score (out, optional, may be NULL) fp32 [G][T][k]: the pooled score of each selected

@@ -5,7 +5,8 @@ Attention ("MiniMax M3 算力省 20 倍", section 二 Index Branch / Main Branch
 block).  Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py`` use
 it.  It shares no code with the CUDA path and never imports it.
 
-Inputs are bf16 torch tensors on the CPU (or uint16 numpy arrays of bf16 bits); outputs are numpy.
+Inputs are bf16 torch tensors on the CPU (or uint16 numpy arrays of bf16 bits; index vectors may
+also be E4M3 tensors, decoded here from the format's definition); outputs are numpy.
 """
 from __future__ import annotations
 
@@ -50,12 +51,43 @@ def _load():
     return _lib
 
 
+def e4m3_values() -> np.ndarray:
+    """Value of every 8-bit E4M3 code (the OCP 8-bit float: sign, 4 exponent bits with bias 7,
+    3 mantissa bits; exponent field 0 is subnormal, m * 2^-9; code S.1111.111 is NaN; no
+    infinities), float64 [256], decoded from that definition."""
+    v = np.empty(256, np.float64)
+    for c in range(256):
+        s, e, m = c >> 7, (c >> 3) & 15, c & 7
+        if e == 15 and m == 7:
+            v[c] = np.nan
+            continue
+        mag = m * 2.0 ** -9 if e == 0 else (1.0 + m / 8.0) * 2.0 ** (e - 7)
+        v[c] = -mag if s else mag
+    return v
+
+
+def _e4m3_to_bf16_bits(codes: np.ndarray) -> np.ndarray:
+    """Every E4M3 value has at most 4 significant bits and an exponent within bf16's range, so
+    it is exactly a bf16 value: the top half of its fp32 pattern."""
+    f32 = e4m3_values()[codes].astype(np.float32)
+    u = f32.view(np.uint32)
+    finite = np.isfinite(f32)
+    assert not (u[finite] & 0xFFFF).any()
+    out = (u >> 16).astype(np.uint16)
+    out[~finite] = 0x7FC0
+    return out
+
+
 def _bits(x) -> np.ndarray:
-    """bf16 tensor/array -> contiguous uint16 numpy array of its bits."""
+    """bf16 (or E4M3, widened exactly to bf16) tensor/array -> contiguous uint16 numpy array of
+    bf16 bits."""
     if isinstance(x, np.ndarray):
         assert x.dtype == np.uint16
         return np.ascontiguousarray(x)
     import torch
+    if x.dtype == torch.float8_e4m3fn:
+        codes = x.detach().cpu().contiguous().view(torch.uint8).numpy()
+        return np.ascontiguousarray(_e4m3_to_bf16_bits(codes))
     assert x.dtype == torch.bfloat16, x.dtype
     return np.ascontiguousarray(x.detach().cpu().contiguous().view(torch.int16).numpy()
                                 .view(np.uint16))

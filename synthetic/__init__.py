@@ -210,9 +210,15 @@ def _planted_index(w: Workload, q_int: torch.Tensor, k_int: torch.Tensor, device
             q_int[rows, g, :] = torch.clamp(q_int[rows, g, :] + 4 * s, -8, 8)
 
 
+def as_index_dtype(t: torch.Tensor, index_dtype: str) -> torch.Tensor:
+    """Index vectors in the requested storage type: "bf16", or "e4m3" (torch.float8_e4m3fn).
+    The integer/8 values in [-1, 1] are exact in both, so this is a change of encoding only."""
+    return t if index_dtype == "bf16" else t.to(torch.float8_e4m3fn)
+
+
 def prefill_inputs(w: Workload, device="cpu", L: int | None = None,
-                   index_only: bool = False) -> dict:
-    """q [L][Hq][d], k/v [L][G][d], q_idx [L][G][di], k_idx [L][di]; all bf16."""
+                   index_only: bool = False, index_dtype: str = "bf16") -> dict:
+    """q [L][Hq][d], k/v [L][G][d] bf16; q_idx [L][G][di], k_idx [L][di] in index_dtype."""
     assert w.kind == "prefill"
     if L is not None:
         w = Workload(**{**w.__dict__, "L": L})
@@ -231,18 +237,21 @@ def prefill_inputs(w: Workload, device="cpu", L: int | None = None,
         _planted_index(w, q_int, k_int, device)
         out["q_idx"] = (q_int.to(torch.float32) / 8.0).to(torch.bfloat16)
         out["k_idx"] = (k_int.to(torch.float32) / 8.0).to(torch.bfloat16)
+    out["q_idx"] = as_index_dtype(out["q_idx"], index_dtype)
+    out["k_idx"] = as_index_dtype(out["k_idx"], index_dtype)
     out["workload"] = w
     return out
 
 
 def decode_inputs(w: Workload, device="cpu", batch: int | None = None,
-                  n_lo: int | None = None, n_hi: int | None = None, spare_pages: int = 3) -> dict:
+                  n_lo: int | None = None, n_hi: int | None = None, spare_pages: int = 3,
+                  index_dtype: str = "bf16") -> dict:
     """Paged decode inputs.
 
     seq_lens int32 [batch] (context length n, the new token's K/V/index key already written at
     position n-1); page_table int32 [batch][max_pages], a random permutation of a shared pool;
     pools: k_idx_pool [P][B][di], k_pool / v_pool [P][G][B][d] (head-major inside a page);
-    q [batch][Hq][d], q_idx [batch][G][di].
+    q [batch][Hq][d], q_idx [batch][G][di] (index vectors in index_dtype).
     """
     assert w.kind == "decode"
     batch = w.batch if batch is None else batch
@@ -265,8 +274,10 @@ def decode_inputs(w: Workload, device="cpu", batch: int | None = None,
         "num_pages": P,
         "max_pages": max_pages,
         "q": normal_bf16(w.seed, STREAM_Q, (batch, w.Hq, w.d), device),
-        "q_idx": int8th(w.seed, STREAM_QI, (batch, w.G, w.di), device),
-        "k_idx_pool": int8th(w.seed, STREAM_KI, (P, w.B, w.di), device),
+        "q_idx": as_index_dtype(int8th(w.seed, STREAM_QI, (batch, w.G, w.di), device),
+                                index_dtype),
+        "k_idx_pool": as_index_dtype(int8th(w.seed, STREAM_KI, (P, w.B, w.di), device),
+                                     index_dtype),
         "k_pool": normal_bf16(w.seed, STREAM_K, (P, w.G, w.B, w.d), device),
         "v_pool": normal_bf16(w.seed, STREAM_V, (P, w.G, w.B, w.d), device),
         "workload": Workload(**{**w.__dict__, "batch": batch, "n_lo": n_lo, "n_hi": n_hi}),

@@ -23,7 +23,8 @@ def msa():
 def gpu_decode(msa, w, inp):
     dev = torch.device("cuda")
     d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
-    cfg = msa.config(w.G, w.hpg, w.k, w.scale)
+    dt = "e4m3" if d["q_idx"].dtype == torch.float8_e4m3fn else "bf16"
+    cfg = msa.config(w.G, w.hpg, w.k, w.scale, index_dtype=dt)
     paged = msa.paged_kv(d["k_idx_pool"], d["k_pool"], d["v_pool"], d["page_table"],
                          d["seq_lens"])
     ws = torch.zeros(max(msa.msa_index_select_workspace(cfg, w.batch, 0, paged),
@@ -152,3 +153,34 @@ def test_decode_equals_last_prefill_row(msa):
     err = (o_d[0].float() - o_p[n - 1].float()).abs()
     assert err.max().item() <= MAX_ABS
     assert (lse_d[:, 0] - lse_p[:, n - 1]).abs().max().item() <= 1e-4
+
+
+# ---------------------------------- E4M3 index vectors ----------------------------------
+def _e4m3(inp):
+    return {**inp, "q_idx": synthetic.as_index_dtype(inp["q_idx"], "e4m3"),
+            "k_idx_pool": synthetic.as_index_dtype(inp["k_idx_pool"], "e4m3")}
+
+
+def test_e4m3_ragged_lengths(msa):
+    w, inp = _custom([1, 127, 128, 129, 1000, 3000, 2049], seed=13)
+    inp = _e4m3(inp)
+    check(w, inp, gpu_decode(msa, w, inp))
+
+
+@pytest.mark.parametrize("G,k", [(1, 4), (2, 16)])
+def test_e4m3_group_and_k_variants(msa, G, k):
+    w, inp = _custom([300, 5000, 129, 2560], seed=30 + G + k, G=G, k=k)
+    inp = _e4m3(inp)
+    check(w, inp, gpu_decode(msa, w, inp))
+
+
+def test_e4m3_full_size_decode_workload_equals_bf16(msa):
+    """The 64-sequence workload with an E4M3 index-key pool: parity with the oracle, and the
+    same selection as the bf16 pool holding the same values."""
+    w0 = synthetic.WORKLOADS["decode_b64_16K_256K"]
+    inp = synthetic.decode_inputs(w0, device="cuda", index_dtype="e4m3")
+    w = inp["workload"]
+    got = gpu_decode(msa, w, inp)
+    check(w, inp, got)
+    ref = synthetic.decode_inputs(w0, device="cuda")
+    assert np.array_equal(gpu_decode(msa, w, ref)[0], got[0])

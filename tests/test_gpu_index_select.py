@@ -1,4 +1,5 @@
-"""GPU parity of the index branch (msa_index_select, prefill) against the CPU oracle.
+"""GPU parity of the index branch (msa_index_select, prefill) against the CPU oracle, with bf16
+and with E4M3 index vectors (the FP8 indexer, tcgen05 kind::f8f6f4).
 
 Selections must match bit-exactly, and so must the pooled scores: index inputs sit on the
 integer/8 grid, so every fp32 tensor-core dot product is exact (see test_oracle_pins).
@@ -21,7 +22,8 @@ def msa():
 
 
 def _check(msa, w, q_idx, k_idx, rows=None):
-    cfg = msa.config(w.G, w.hpg, w.k, w.scale)
+    dt = "e4m3" if q_idx.dtype == torch.float8_e4m3fn else "bf16"
+    cfg = msa.config(w.G, w.hpg, w.k, w.scale, index_dtype=dt)
     sel, score = msa.msa_index_select(cfg, q_idx.cuda(), k_idx.cuda(), want_score=True)
     torch.cuda.synchronize()
     ref_sel, ref_score = oracle.select_prefill(q_idx, k_idx, w.B, w.k, rows=rows, want_score=True)
@@ -92,3 +94,55 @@ def test_full_size_128k_clustered_sampled_rows(msa):
     inp = synthetic.prefill_inputs(w, index_only=True)
     sel = _check(msa, w, inp["q_idx"], inp["k_idx"], rows=_stratified_rows(w.L, 160, 2))
     assert sel.shape[-1] == 16
+
+
+# ---------------------------------- E4M3 index vectors ----------------------------------
+def test_e4m3_tiny_workload_all_rows(msa):
+    w = synthetic.WORKLOADS["tiny_L2048"]
+    inp = synthetic.prefill_inputs(w, index_only=True, index_dtype="e4m3")
+    _check(msa, w, inp["q_idx"], inp["k_idx"])
+
+
+@pytest.mark.parametrize("L", [1, 129, 1000, 2048 + 77])
+def test_e4m3_ragged_lengths_all_rows(msa, L):
+    w = synthetic.WORKLOADS["prefill_L32K"]
+    inp = synthetic.prefill_inputs(w, index_only=True, L=L, index_dtype="e4m3")
+    _check(msa, synthetic.Workload(**{**w.__dict__, "L": L}), inp["q_idx"], inp["k_idx"])
+
+
+@pytest.mark.parametrize("G,k,L", [(2, 8, 3000), (1, 1, 700), (1, 16, 1900)])
+def test_e4m3_group_and_k_variants(msa, G, k, L):
+    w = synthetic.Workload("v8", "prefill", L=L, Hq=16 * G, G=G, k=k, seed=52 + G + k)
+    inp = synthetic.prefill_inputs(w, index_only=True, index_dtype="e4m3")
+    _check(msa, w, inp["q_idx"], inp["k_idx"])
+
+
+def test_e4m3_ties_duplicate_blocks(msa):
+    w = synthetic.Workload("ties8", "prefill", L=2560, Hq=64, G=4, k=6, seed=5)
+    inp = synthetic.prefill_inputs(w, index_only=True, index_dtype="e4m3")
+    k_idx = inp["k_idx"].view(torch.uint8).clone()
+    for b in (1, 3, 7, 11):
+        k_idx[b * 128:(b + 1) * 128] = k_idx[5 * 128:6 * 128]
+    _check(msa, w, inp["q_idx"], k_idx.view(torch.float8_e4m3fn))
+
+
+def test_e4m3_full_size_32k_sampled_rows_and_equal_to_bf16(msa):
+    """Sampled rows against the oracle; every row against the bf16 path on the same values."""
+    w = synthetic.WORKLOADS["prefill_L32K"]
+    inp = synthetic.prefill_inputs(w, index_only=True, index_dtype="e4m3")
+    got = _check(msa, w, inp["q_idx"], inp["k_idx"], rows=_stratified_rows(w.L, 256, 3))
+    ref = synthetic.prefill_inputs(w, index_only=True)
+    cfg = msa.config(w.G, w.hpg, w.k, w.scale)
+    cfg8 = msa.config(w.G, w.hpg, w.k, w.scale, index_dtype="e4m3")
+    s16 = msa.msa_index_select(cfg, ref["q_idx"].cuda(), ref["k_idx"].cuda())
+    s8 = msa.msa_index_select(cfg8, inp["q_idx"].cuda(), inp["k_idx"].cuda())
+    assert torch.equal(s16, s8)
+    assert got.shape[-1] == 16
+
+
+def test_e4m3_dtype_mismatch_is_rejected(msa):
+    w = synthetic.WORKLOADS["tiny_L2048"]
+    inp = synthetic.prefill_inputs(w, index_only=True)
+    cfg8 = msa.config(w.G, w.hpg, w.k, w.scale, index_dtype="e4m3")
+    with pytest.raises(msa.MsaError):
+        msa.msa_index_select(cfg8, inp["q_idx"].cuda(), inp["k_idx"].cuda())

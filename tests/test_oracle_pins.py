@@ -352,3 +352,38 @@ def test_compact_query_rows_match_full():
                                  q_compact=True)
     np.testing.assert_array_equal(o1, o2)
     np.testing.assert_array_equal(l1, l2)
+
+
+# ------------------------------------------------------------------------------------------
+# E4M3 index vectors (the FP8 indexer): the oracle decodes the codes itself
+# ------------------------------------------------------------------------------------------
+def test_e4m3_decoder_matches_library_and_definition():
+    """Every code against torch's float8_e4m3fn conversion (a library routine), plus values the
+    format definition fixes: 1.0, -1.0, the largest normal 448, the smallest normal 2^-6, the
+    smallest subnormal 2^-9, and the NaN code."""
+    v = oracle.e4m3_values()
+    lib = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).float().numpy()
+    nan = np.isnan(v)
+    assert np.array_equal(nan, np.isnan(lib))
+    assert np.array_equal(v[~nan], lib[~nan].astype(np.float64))
+    assert (v[0x38], v[0xB8], v[0x7E], v[0x08], v[0x01]) == (1.0, -1.0, 448.0, 2.0 ** -6, 2.0 ** -9)
+    assert nan.sum() == 2 and nan[0x7F] and nan[0xFF]
+
+
+def test_integer_eighths_are_exact_in_e4m3():
+    """The index inputs (integers in [-8, 8] over 8) lose nothing in E4M3: the FP8 indexer
+    scores them exactly as the bf16 one does."""
+    x = torch.arange(-8, 9, dtype=torch.float32) / 8
+    codes = x.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(oracle.e4m3_values()[codes], x.numpy().astype(np.float64))
+
+
+@pytest.mark.parametrize("L,G,k,seed", [(700, 2, 4, 3), (1300, 4, 16, 4)])
+def test_e4m3_selection_equals_bf16_selection(L, G, k, seed):
+    w = synthetic.Workload("e4", "prefill", L=L, Hq=16 * G, G=G, k=k, seed=seed)
+    a = synthetic.prefill_inputs(w, index_only=True)
+    b = synthetic.prefill_inputs(w, index_only=True, index_dtype="e4m3")
+    assert b["q_idx"].dtype == torch.float8_e4m3fn
+    sa, ca = oracle.select_prefill(a["q_idx"], a["k_idx"], w.B, k, want_score=True)
+    sb, cb = oracle.select_prefill(b["q_idx"], b["k_idx"], w.B, k, want_score=True)
+    assert np.array_equal(sa, sb) and np.array_equal(ca, cb)

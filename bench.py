@@ -152,18 +152,30 @@ class ClockSampler:
 # kernel's sources still hash to the value recorded with it; otherwise the traffic is null.
 CSRC = os.path.join(ROOT, "block_sparse_long_msa_gb300", "csrc")
 KERNEL_SOURCES = {
-    "main_branch": ["attn_prefill.cu", "common.cuh", "ptx.cuh"],
+    "attention": ["attn_prefill.cu", "common.cuh", "ptx.cuh"],
+    "combine": ["attn_prefill.cu", "common.cuh", "ptx.cuh"],
     "index": ["index_prefill.cu", "common.cuh", "ptx.cuh"],
+    "index_e4m3": ["index_prefill.cu", "common.cuh", "ptx.cuh"],
     "decode_scan": ["decode.cu", "common.cuh", "ptx.cuh"],
+    "decode_scan_e4m3": ["decode.cu", "common.cuh", "ptx.cuh"],
 }
 NCU_TRAFFIC = {
     # prefill L=32768, 64/4 heads, k=16 (profiles/dram_prefill_L32K_decode_b64.md)
-    "index": {"bytes_per_launch": 41909760, "workload": "prefill_L32K@32768",
-              "sources_sha256": "0f33ac3c78196a8d50dcacf237c9649b8fb27e4d91625b1c5efcc819bd23e39c"},
+    "attention": {"bytes_per_launch": 11717122048, "workload": "prefill_L32K@32768",
+                  "sources_sha256": "d02224ceafb9e7e7abf3ae27cd194069e4ac6028b352308685f9c49c58b659f9"},
+    "combine": {"bytes_per_launch": 9171763712, "workload": "prefill_L32K@32768",
+                "sources_sha256": "d02224ceafb9e7e7abf3ae27cd194069e4ac6028b352308685f9c49c58b659f9"},
+    "index": {"bytes_per_launch": 41901568, "workload": "prefill_L32K@32768",
+              "sources_sha256": "19aa52e0668db0df0eda7ab0cd5d476f4df84f64e3f989a29fda0ee2c2da868a"},
+    "index_e4m3": {"bytes_per_launch": 20994304, "workload": "prefill_L32K@32768",
+                   "sources_sha256": "19aa52e0668db0df0eda7ab0cd5d476f4df84f64e3f989a29fda0ee2c2da868a"},
     # decode, 64 sequences of 16K-256K tokens
-    "decode_scan": {"bytes_per_launch": 2088155136,
+    "decode_scan": {"bytes_per_launch": 2084859904,
                     "workload": "decode_b64_16K_256K@64x262144",
-                    "sources_sha256": "d32ca51ba84e840ef970e6e870773d2ce0b263594862f789179ffe9eab504635"},
+                    "sources_sha256": "c21202469676741a41e33b2d5f003257595663f91daf94f27fe0b3d27f7feadf"},
+    "decode_scan_e4m3": {"bytes_per_launch": 1044212736,
+                         "workload": "decode_b64_16K_256K@64x262144",
+                         "sources_sha256": "c21202469676741a41e33b2d5f003257595663f91daf94f27fe0b3d27f7feadf"},
 }
 
 
@@ -312,35 +324,34 @@ def run_msa(args, world, rank):
     total_ms = t0.elapsed_time(t1)
     total_ms = max_over_ranks(total_ms, world)
 
-    # attention_waves: the wave launches (attention of every work item, and the merge of the rows
-    # of all but the last wave on a few SMs); merge_last_wave: the merge of the last wave's rows
-    phase = {"index": 0.0, "schedule": 0.0, "attention_waves": 0.0, "merge_last_wave": 0.0}
+    phase = {"index": 0.0, "schedule": 0.0, "attention": 0.0, "combine": 0.0}
     for s in range(args.steps):
         m = marks[s]
         phase["index"] += starts[s].elapsed_time(m[0])
         for c in range(nchunks):
             phase["schedule"] += m[3 * c].elapsed_time(m[3 * c + 1])
-            phase["attention_waves"] += m[3 * c + 1].elapsed_time(m[3 * c + 2])
-            phase["merge_last_wave"] += m[3 * c + 2].elapsed_time(m[3 * c + 3])
+            phase["attention"] += m[3 * c + 1].elapsed_time(m[3 * c + 2])
+            phase["combine"] += m[3 * c + 2].elapsed_time(m[3 * c + 3])
     dec_sel_ms = sum(d[0].elapsed_time(d[1]) for d in dmarks) / args.steps
     dec_attn_ms = sum(d[1].elapsed_time(d[2]) for d in dmarks) / args.steps
     prefill_ms = sum(starts[s].elapsed_time(marks[s][-1]) for s in range(args.steps)) / args.steps
     dec_ms = dec_sel_ms + dec_attn_ms
-    main_ms = (phase["attention_waves"] + phase["merge_last_wave"]) / args.steps
-    per_launch_ms = {"index": phase["index"] / args.steps, "main_branch": main_ms}
+    per_launch_ms = {"index": phase["index"] / args.steps,
+                     "attention": phase["attention"] / (args.steps * nchunks),
+                     "combine": phase["combine"] / (args.steps * nchunks)}
 
     work = prefill_work(w)
     peaks = load_peaks()
     tensor_peak = peaks["bf16_tflops"]
-    # the main branch (attention waves + the last merge) as one unit: its attention and merge
-    # kernels share the launches, so their bytes are counted together
     roof = {
         "index": ("tensor", work["index_flops"] / (per_launch_ms["index"] * 1e-3) / 1e12,
                   tensor_peak, "TFLOP/s"),
-        "main_branch": ("hbm", (work["attn_bytes"] + work["combine_bytes"]) / (main_ms * 1e-3)
-                        / 1e9, peaks["hbm_gbs"], "GB/s"),
+        "attention": ("hbm", work["attn_bytes"] / nchunks / (per_launch_ms["attention"] * 1e-3)
+                      / 1e9, peaks["hbm_gbs"], "GB/s"),
+        "combine": ("hbm", work["combine_bytes"] / nchunks / (per_launch_ms["combine"] * 1e-3)
+                    / 1e9, peaks["hbm_gbs"], "GB/s"),
     }
-    dominant = max(("index", "main_branch"), key=lambda n: per_launch_ms[n])
+    dominant = max(("index", "attention", "combine"), key=lambda n: phase[n])
     bound, achieved, peak, unit = roof[dominant]
     traffic = measured_traffic(dominant, f"{w.name}@{L}")
 
@@ -474,6 +485,9 @@ def run_msa(args, world, rank):
             "prefill_tokens_per_s": world * L / (pre8_ms * 1e-3),
             "decode_index_ms": didx8_ms, "decode_index_ms_bf16": dec_sel_ms,
             "decode_scan_gbs": scan8_bytes / (didx8_ms * 1e-3) / 1e9,
+            "traffic": {"prefill_index": measured_traffic("index_e4m3", f"{w.name}@{L}"),
+                        "decode_scan": measured_traffic("decode_scan_e4m3",
+                                                        f"{dw.name}@{dw.batch}x{dw.n_hi}")},
             "decode_tokens_per_s": world * dw.batch / (dec8_ms * 1e-3),
             "gpu_launches": 3 * n8,
         }
@@ -541,10 +555,9 @@ def run_msa(args, world, rank):
                      "unit": unit, "frac": achieved / peak, "traffic": traffic,
                      "peak_source": peaks["source"]},
         "kernel_rooflines": {n: {"bound": r[0], "achieved": r[1], "peak": r[2], "unit": r[3],
-                                 "frac": r[1] / r[2], "ms_per_step": per_launch_ms[n]}
+                                 "frac": r[1] / r[2], "ms_per_launch": per_launch_ms[n]}
                              for n, r in roof.items()},
-        "tensor_frac_main_branch": work["attn_flops"] / ((phase["attention_waves"]
-                                                          + phase["merge_last_wave"]
+        "tensor_frac_main_branch": work["attn_flops"] / ((phase["attention"] + phase["combine"]
                                                           + phase["schedule"]) / args.steps
                                                          * 1e-3) / 1e12 / tensor_peak,
         "e2e": None if e2e_ms is None else {

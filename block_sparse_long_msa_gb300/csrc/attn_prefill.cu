@@ -16,12 +16,8 @@
 //                   repeated gathers of each query for its k blocks.
 //   5. sched_fill   per (group, query block): every (token, slot) lands at its place, lists stay
 //                   in ascending token order (deterministic, no global atomics)
-//   6. attn_kv_outer persistent tcgen05 kernel over work items (see below), launched in waves of
-//                   whole query ranges: in launch w most CTAs run the items of wave w while the
-//                   rest merge the rows of wave w-1 (complete since launch w-1 ended), so the
-//                   merge's partial reads stream while the MMA-latency-bound attention leaves
-//                   DRAM bandwidth unused; no CTA waits on another
-//   7. combine      per (token, group) of the last wave: fixed slot order, LSE-weighted merge
+//   6. attn_kv_outer persistent tcgen05 kernel over work items (see below)
+//   7. combine      per (token, group): fixed slot order, LSE-weighted merge
 #include <algorithm>
 
 #include "common.cuh"
@@ -38,9 +34,6 @@ constexpr int kItemTiles = 16;                            // tiles sharing one K
 constexpr int kItemTokens = kItemTiles * kTileTokens;     // 128
 constexpr uint32_t kPanel = 16384;
 constexpr int kMaxRanges = 16;
-constexpr int kMlStride = 2 * kHeadsPerGroup;  // floats per list position in the m / lse record
-constexpr int kWaves = 4;        // launches the work items are split into (by query range)
-constexpr int kMergeCtas = 32;   // CTAs of a launch that merge the previous wave's rows
 
 // ------------------------------------------------------------------------------------------
 // Scheduling
@@ -251,22 +244,14 @@ __global__ void sched_fill_kernel(SchedArgs a) {
 struct AttnArgs {
   const int4* items;
   const int32_t* n_items;
-  const int32_t* item_base;  // [nr][G][nbk]: first work item of each (range, group, block)
   const int32_t* list;
-  int32_t G, k, q0, nbk, nr;
+  int32_t G, k, q0;
   float scale_log2;       // softmax scale * log2(e)
   __half* po;             // [list position][16][128] unnormalised partial O (fp16)
-  float* pm;              // [list position][32]: 16 row maxima (natural-log units), then
-  float* plse;            // the 16 log-sum-exps (plse = pm + 16)
+  float* pm;              // [list position][16] row max (natural-log units)
+  float* plse;            // same, log-sum-exp
   int32_t* status;
   uint64_t wait_ns;
-  // one wave: CTAs [0, n_attn) run the work items of query ranges [r_lo, r_hi); the others merge
-  // the rows of chunk tokens [c_lo, c_hi), whose partials an earlier launch completed
-  int32_t n_attn, r_lo, r_hi, c_lo, c_hi;
-  const int32_t* pos;     // [(il*G + g)*k + s]: list position of each slot, -1 if none
-  int64_t L;
-  __nv_bfloat16* o;       // [L][G*16][128]
-  float* lse;             // [G*16][L]
 };
 
 struct ItemMeta {
@@ -321,209 +306,6 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
   return d;
 }
 
-// ------------------------------------------------------------------------------------------
-// Merge role of the wave kernel: per (token, group) row, the LSE-weighted merge of its k
-// partials (the arithmetic of combine_kernel, with M and den reduced over slots by a shuffle
-// tree).  A row's partials lie at k list positions (4 KB of O and a 128-byte m / lse record
-// each), fetched with bulk copies into a ring of half-row stages (first half: slots 0-7 and the
-// m / lse records of all 16 slots; second half: slots 8-15), so that a few SMs stream the
-// partials at a high rate while the others run attention.
-//   producers: warps 0-3, lanes 0-3, slot 4*warp + lane, reading list positions 8 rows ahead;
-//   consumers: three teams of four warps (4-7, 8-11, 12-15); team tm merges rows tm, tm+3, ...
-//   from half stages 2tm and 2tm+1.
-// ------------------------------------------------------------------------------------------
-constexpr int kCStages = 6;                                      // half rows
-constexpr uint32_t kCSlotO = kHeadsPerGroup * kDim * 2;          // 4 KB
-constexpr uint32_t kCStage = 8 * kCSlotO + 16 * kMlStride * 4;   // 32 KB O + 16 m / lse records
-constexpr uint32_t kCWeights = kCStages * kCStage;  // per consumer warp: [4 heads][16 slots]
-constexpr uint32_t kCBar = kCWeights + 12 * 256;
-// full[6] +0, empty[6] +48, masks[3][4] +96, abort +144
-constexpr uint32_t kCombSmem = kCBar + 192 + 1024;
-constexpr uint32_t kWaveSmem = kCombSmem > kAttnSmem ? kCombSmem : kAttnSmem;
-static_assert(kWaveSmem <= 232448, "wave kernel shared memory");
-
-__device__ __forceinline__ void merge_role(const AttnArgs& a, uint8_t* smem, int cta, int nct) {
-  const uint32_t base = smem_u32(smem);
-  const uint32_t bars = base + kCBar;
-  auto full = [&](int st) { return bars + 8 * st; };
-  auto empty = [&](int st) { return bars + 48 + 8 * st; };
-  volatile uint32_t* masks = reinterpret_cast<volatile uint32_t*>(smem + kCBar + 96);
-  volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + kCBar + 144);
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  if (tid == 0) {
-    for (int st = 0; st < kCStages; ++st) {
-      // first halves: all four producer warps (m / lse records); second halves: warps 2-3
-      mbar_init(full(st), (st & 1) ? 2 : 4);
-      mbar_init(empty(st), 4);  // one arrive per warp of the consuming team
-    }
-    *abort_flag = 0;
-    fence_mbar_init();
-  }
-  __syncthreads();
-  const int G = a.G, k = a.k;
-  const int nrows = (a.c_hi - a.c_lo) * G;
-  const int mine = nrows > cta ? (nrows - 1 - cta) / nct + 1 : 0;
-  const int row0 = a.c_lo * G + cta;  // my n-th row is the chunk's (token, group) row row0 + n*nct
-  if (warp < 4) {
-    // -------------------------------- producers --------------------------------
-    const int slot = 4 * warp + lane, half_o = warp >> 1;
-    auto slot_pos = [&](int n) -> int32_t {  // list position of my slot in my n-th row
-      if (lane >= 4 || n >= mine || slot >= k) return -1;
-      return a.pos[(static_cast<size_t>(row0) + static_cast<size_t>(n) * nct) * k + slot];
-    };
-    int32_t pa[8], pb[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) pa[u] = slot_pos(u);
-    int issued = 0;
-    bool ok = true;
-    for (int nb = 0; ok && nb < mine; nb += 8) {
-#pragma unroll
-      for (int u = 0; u < 8; ++u) pb[u] = slot_pos(nb + 8 + u);  // land during the next 8 rows
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int n = nb + u;
-        if (n >= mine) break;
-        const int sa = 2 * (n % 3), sb = sa + 1, ph = (n / 3) & 1;
-        const bool okw = !*abort_flag && mbar_wait(empty(sa), ph ^ 1, a.wait_ns) &&
-                         (half_o == 0 || mbar_wait(empty(sb), ph ^ 1, a.wait_ns));
-        if (!__all_sync(0xffffffffu, okw)) {
-          ok = false;
-          break;
-        }
-        const int32_t p = pa[u];
-        const uint32_t vm = __ballot_sync(0xffffffffu, p >= 0) & 0xfu;
-        if (lane == 0) {
-          masks[(n % 3) * 4 + warp] = vm << (4 * warp);
-          if (half_o == 0) {
-            mbar_arrive_expect_tx(full(sa), __popc(vm) * (kCSlotO + kMlStride * 4));
-          } else {
-            mbar_arrive_expect_tx(full(sa), __popc(vm) * kMlStride * 4);
-            mbar_arrive_expect_tx(full(sb), __popc(vm) * kCSlotO);
-          }
-        }
-        __syncwarp();
-        if (p >= 0) {
-          const int so = half_o ? sb : sa;
-          bulk_load(base + so * kCStage + (slot & 7) * kCSlotO,
-                    a.po + static_cast<size_t>(p) * kHeadsPerGroup * kDim, kCSlotO, full(so));
-          bulk_load(base + sa * kCStage + 8 * kCSlotO + slot * kMlStride * 4,
-                    a.pm + static_cast<size_t>(p) * kMlStride, kMlStride * 4, full(sa));
-        }
-        ++issued;
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) pa[u] = pb[u];
-    }
-    if (!ok) {
-      if (lane == 0) report_status(a.status, kStatusTimeout);
-      *abort_flag = 1;
-    }
-    // no copy may be in flight when the CTA exits: wait for the last rows issued
-    if (lane == 0)
-      for (int x = issued > 3 ? issued - 3 : 0; x < issued; ++x) {
-        mbar_wait(full(2 * (x % 3)), (x / 3) & 1, kDefaultWaitNs);
-        if (half_o) mbar_wait(full(2 * (x % 3) + 1), (x / 3) & 1, kDefaultWaitNs);
-      }
-  } else {
-    // -------------------------------- consumers --------------------------------
-    // Thread t of team tm: head t/8; weights of slots 2(t%8), 2(t%8)+1 (exchanged through a
-    // warp-private shared-memory row); dims (t%8)*8 .. +8 and 64 + (t%8)*8 .. +8.
-    const int tm = (warp - 4) >> 2, t = tid - 128 * (tm + 1);
-    const int hh = t >> 3, j8 = t & 7, d0 = j8 * 8;
-    float* wsm = reinterpret_cast<float*>(smem + kCWeights + (warp - 4) * 256) + (lane >> 3) * 16;
-    const float ninf = -__int_as_float(0x7f800000);
-    bool ok = true;
-    for (int n = tm; ok && n < mine; n += 3) {
-      const int ph = (n / 3) & 1;
-      float2 acc[8];
-#pragma unroll
-      for (int q = 0; q < 8; ++q) acc[q] = make_float2(0.f, 0.f);
-      float wv[16], M = 0.f, den = 0.f;
-      uint32_t valid = 0;
-#pragma unroll
-      for (int qt = 0; qt < 4; ++qt) {
-        const int st = 2 * tm + (qt >> 1);
-        if ((qt & 1) == 0 &&
-            !__all_sync(0xffffffffu, !*abort_flag && mbar_wait(full(st), ph, a.wait_ns))) {
-          ok = false;
-          break;
-        }
-        const uint8_t* stg = smem + st * kCStage;
-        if (qt == 0) {
-          valid = masks[tm * 4] | masks[tm * 4 + 1] | masks[tm * 4 + 2] | masks[tm * 4 + 3];
-          // M = max_s lse_s, den = sum_s exp(lse_s - M), w_s = exp(m_s - M)
-          const float* ml = reinterpret_cast<const float*>(stg + 8 * kCSlotO);
-          const int s0 = 2 * j8, s1 = s0 + 1;
-          const bool v0 = (valid >> s0) & 1, v1 = (valid >> s1) & 1;
-          const float l0 = v0 ? ml[s0 * kMlStride + 16 + hh] : ninf;
-          const float l1 = v1 ? ml[s1 * kMlStride + 16 + hh] : ninf;
-          M = fmaxf(l0, l1);
-#pragma unroll
-          for (int o = 4; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-          den = (v0 ? __expf(l0 - M) : 0.f) + (v1 ? __expf(l1 - M) : 0.f);
-#pragma unroll
-          for (int o = 4; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-          wsm[s0] = v0 ? __expf(ml[s0 * kMlStride + hh] - M) : 0.f;
-          wsm[s1] = v1 ? __expf(ml[s1 * kMlStride + hh] - M) : 0.f;
-          __syncwarp();
-#pragma unroll
-          for (int q = 0; q < 16; ++q) wv[q] = wsm[q];
-          __syncwarp();
-        }
-        // four slots' loads first (slots without a partial read as zero), then the FMAs
-        const uint8_t* src = stg + (hh * kDim + d0) * 2;
-        uint4 x[4][2];
-#pragma unroll
-        for (int s4 = 0; s4 < 4; ++s4) {
-          const int sl = qt * 4 + s4;
-          const bool v = (valid >> sl) & 1;
-          x[s4][0] = v ? *reinterpret_cast<const uint4*>(src + (sl & 7) * kCSlotO)
-                       : make_uint4(0, 0, 0, 0);
-          x[s4][1] = v ? *reinterpret_cast<const uint4*>(src + (sl & 7) * kCSlotO + 128)
-                       : make_uint4(0, 0, 0, 0);
-        }
-        if (qt & 1) {  // this half of the row is in registers: release its stage
-          __syncwarp();
-          if (lane == 0) mbar_arrive(empty(st));
-        }
-#pragma unroll
-        for (int s4 = 0; s4 < 4; ++s4) {
-          const float w = wv[qt * 4 + s4];
-          const float2 w2 = make_float2(w, w);
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            const uint32_t wd[4] = {x[s4][c].x, x[s4][c].y, x[s4][c].z, x[s4][c].w};
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-              acc[c * 4 + q] = ffma2(__half22float2(*reinterpret_cast<const __half2*>(&wd[q])), w2,
-                                     acc[c * 4 + q]);
-          }
-        }
-      }
-      if (!ok) break;
-      const int jr = cta + n * nct;
-      const int64_t i = static_cast<int64_t>(a.q0) + a.c_lo + jr / G;
-      const int h = (jr % G) * kHeadsPerGroup + hh;
-      const float inv = 1.f / den;
-      __nv_bfloat16* dst = a.o + (static_cast<size_t>(i) * G * kHeadsPerGroup + h) * kDim + d0;
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint4 o4;
-        o4.x = pack_bf16x2(acc[c * 4].x * inv, acc[c * 4].y * inv);
-        o4.y = pack_bf16x2(acc[c * 4 + 1].x * inv, acc[c * 4 + 1].y * inv);
-        o4.z = pack_bf16x2(acc[c * 4 + 2].x * inv, acc[c * 4 + 2].y * inv);
-        o4.w = pack_bf16x2(acc[c * 4 + 3].x * inv, acc[c * 4 + 3].y * inv);
-        *reinterpret_cast<uint4*>(dst + c * 64) = o4;
-      }
-      if (j8 == 0) a.lse[static_cast<size_t>(h) * a.L + i] = M + __logf(den);
-    }
-    if (!ok) {
-      if (lane == 0) report_status(a.status, kStatusTimeout);
-      *abort_flag = 1;
-    }
-  }
-}
-
 __global__ void __launch_bounds__(512, 1)
     attn_kv_outer_kernel(const __grid_constant__ CUtensorMap map_q,
                          const __grid_constant__ CUtensorMap map_k,
@@ -550,17 +332,8 @@ __global__ void __launch_bounds__(512, 1)
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + kSmemBar + kAbort);
   ItemMeta* meta = reinterpret_cast<ItemMeta*>(smem + kSmemMeta);
 
-  if (static_cast<int>(blockIdx.x) >= a.n_attn) {
-    merge_role(a, smem, static_cast<int>(blockIdx.x) - a.n_attn,
-               static_cast<int>(gridDim.x) - a.n_attn);
-    return;
-  }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // this wave's work items: those of query ranges [r_lo, r_hi), every n_attn-th from blockIdx.x
-  const int n_all = *a.n_items;
-  const int it0 = a.r_lo < a.nr ? a.item_base[a.r_lo * a.G * a.nbk] : n_all;
-  const int it1 = a.r_hi < a.nr ? a.item_base[a.r_hi * a.G * a.nbk] : n_all;
-  const int it_first = it0 + static_cast<int>(blockIdx.x), it_step = a.n_attn;
+  const int n_items = *a.n_items;
 
   if (threadIdx.x == 0) {
     for (int r = 0; r < kMetaRing; ++r) {
@@ -601,7 +374,7 @@ __global__ void __launch_bounds__(512, 1)
     int T = 0, q_issued = 0;
     bool ok = true;
     if (lane == 0) tma_prefetch_map(&map_q);
-    for (int it = it_first, n = 0; ok && it < it1; it += it_step, ++n) {
+    for (int it = blockIdx.x, n = 0; ok && it < n_items; it += gridDim.x, ++n) {
       const int r = n % kMetaRing;
       if (!__all_sync(0xffffffffu, !*abort_flag && mbar_wait(meta_empty(r),
                                                              ((n / kMetaRing) & 1) ^ 1,
@@ -656,7 +429,7 @@ __global__ void __launch_bounds__(512, 1)
     if (lane == 0) {
       bool ok = true;
       int T = 0;
-      for (int it = it_first, n = 0; ok && it < it1; it += it_step, ++n) {
+      for (int it = blockIdx.x, n = 0; ok && it < n_items; it += gridDim.x, ++n) {
         const int r = n % kMetaRing;
         if (*abort_flag || !mbar_wait(meta_full(r), (n / kMetaRing) & 1, a.wait_ns) ||
             !mbar_wait(k_full, n & 1, a.wait_ns)) {
@@ -698,7 +471,9 @@ __global__ void __launch_bounds__(512, 1)
     // --------------------- K loader + O = P V issuer (polling) ---------------------
     if (lane == 0) {
       tma_prefetch_map(&map_k);
-      const int n_mine = it1 > it_first ? (it1 - 1 - it_first) / it_step + 1 : 0;
+      const int n_mine = n_items > static_cast<int>(blockIdx.x)
+                             ? (n_items - 1 - static_cast<int>(blockIdx.x)) / gridDim.x + 1
+                             : 0;
       int nk = 0;                        // items whose K has been requested
       int b_n = 0, b_cnt = -1, b_t0 = 0, b_T = 0;  // P.V cursor
       bool ok = true, idle = false;
@@ -769,7 +544,7 @@ __global__ void __launch_bounds__(512, 1)
     if (lane == 0) tma_prefetch_map(&map_v);
     int issued = 0;
     bool ok = true;
-    for (int it = it_first, n = 0; it < it1; it += it_step, ++n) {
+    for (int it = blockIdx.x, n = 0; it < n_items; it += gridDim.x, ++n) {
       const int r = n % kMetaRing;
       const bool okw = !*abort_flag && mbar_wait(meta_full(r), (n / kMetaRing) & 1, a.wait_ns) &&
                        mbar_wait(v_empty, (n & 1) ^ 1, a.wait_ns);
@@ -814,7 +589,7 @@ __global__ void __launch_bounds__(512, 1)
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     int T = 0;
     bool ok = true;
-    for (int it = it_first, n = 0; ok && it < it1; it += it_step, ++n) {
+    for (int it = blockIdx.x, n = 0; ok && it < n_items; it += gridDim.x, ++n) {
       const int r = n % kMetaRing;
       if (!__all_sync(0xffffffffu, mbar_wait(meta_full(r), (n / kMetaRing) & 1, a.wait_ns))) {
         ok = false;
@@ -844,8 +619,8 @@ __global__ void __launch_bounds__(512, 1)
           tmem_ld32(sa + c * 32, v0);
           tmem_ld32(sa + c * 32 + 32, v1);
           tmem_ld_wait();
-          if (unmasked) {  // four independent three-input max chains
-            float m4[4] = {mraw, mraw, mraw, mraw};
+          if (unmasked) {
+            float m4[4] = {mraw, mraw, mraw, mraw};  // four independent three-input chains
 #pragma unroll
             for (int q = 0; q < 32; ++q)
               m4[q & 3] = fmax3(m4[q & 3], __uint_as_float(v0[q]), __uint_as_float(v1[q]));
@@ -892,8 +667,8 @@ __global__ void __launch_bounds__(512, 1)
         if (valid) {
           const size_t p = static_cast<size_t>(m.start) + t0 + tk;  // list position
           const float ln2 = 0.6931471805599453f;
-          a.pm[p * kMlStride + hh] = m2 * ln2;
-          a.plse[p * kMlStride + hh] = (m2 + __log2f(l)) * ln2;
+          a.pm[p * kHeadsPerGroup + hh] = m2 * ln2;
+          a.plse[p * kHeadsPerGroup + hh] = (m2 + __log2f(l)) * ln2;
         }
       }
     }
@@ -916,7 +691,7 @@ __global__ void __launch_bounds__(512, 1)
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t stg = base + kSmemO;
     int T = 0;
-    for (int it = it_first, n = 0; it < it1; it += it_step, ++n) {
+    for (int it = blockIdx.x, n = 0; it < n_items; it += gridDim.x, ++n) {
       const int r = n % kMetaRing;
       const bool okm = !*abort_flag && mbar_wait(meta_full(r), (n / kMetaRing) & 1, a.wait_ns);
       if (!__all_sync(0xffffffffu, okm)) {
@@ -989,23 +764,23 @@ __global__ void __launch_bounds__(512, 1)
 // ------------------------------------------------------------------------------------------
 struct CombineArgs {
   const int32_t* pos;          // [(il*G + g)*k + s]: list position of each slot, -1 if none
-  const __half* po;            // [list position][16][128]
-  const float* pm;             // [list position][32]: 16 m, then 16 lse (plse = pm + 16)
+  const __half* po;
+  const float* pm;
   const float* plse;
   int64_t L;                   // rows of sel / o / lse
-  int32_t G, k, q0, il0;       // rows q0+il0 .. q0+il0+gridDim.x-1
+  int32_t G, k, q0, nrows;     // rows q0 .. q0+nrows-1
   __nv_bfloat16* o;            // [L][G*16][128]
   float* lse;                  // [G*16][L]
 };
 
 __global__ void __launch_bounds__(128) combine_kernel(CombineArgs a) {
-  const int il = a.il0 + static_cast<int>(blockIdx.x), g = blockIdx.y;
+  const int il = blockIdx.x, g = blockIdx.y;
   const int64_t i = static_cast<int64_t>(a.q0) + il;
   const int t = threadIdx.x, hh = t >> 3, d0 = (t & 7) * 16;
   const int32_t* prow = a.pos + (static_cast<size_t>(il) * a.G + g) * a.k;
   float M = -__int_as_float(0x7f800000);
   for (int s = 0; s < a.k; ++s)
-    if (prow[s] >= 0) M = fmaxf(M, a.plse[static_cast<size_t>(prow[s]) * kMlStride + hh]);
+    if (prow[s] >= 0) M = fmaxf(M, a.plse[static_cast<size_t>(prow[s]) * kHeadsPerGroup + hh]);
   float acc[16];
 #pragma unroll
   for (int q = 0; q < 16; ++q) acc[q] = 0.f;
@@ -1013,9 +788,8 @@ __global__ void __launch_bounds__(128) combine_kernel(CombineArgs a) {
   for (int s = 0; s < a.k; ++s) {
     if (prow[s] < 0) continue;  // padding (and out-of-range ids, which were flagged)
     const size_t r = static_cast<size_t>(prow[s]) * kHeadsPerGroup + hh;
-    const size_t rm = static_cast<size_t>(prow[s]) * kMlStride + hh;
-    den += __expf(a.plse[rm] - M);
-    const float w = __expf(a.pm[rm] - M);
+    den += __expf(a.plse[r] - M);
+    const float w = __expf(a.pm[r] - M);
     const uint4* src = reinterpret_cast<const uint4*>(a.po + r * kDim + d0);
 #pragma unroll
     for (int h2 = 0; h2 < 2; ++h2) {
@@ -1047,8 +821,7 @@ __global__ void __launch_bounds__(128) combine_kernel(CombineArgs a) {
 }  // namespace
 
 // Query ranges of a chunk: as many as keep the expected (group, block) list of a range at one
-// full work item or more (ranges that cut lists shorter would pad tiles and reload K/V per
-// item); the work items are launched in waves of whole ranges.
+// full work item or more (ranges that cut lists shorter would pad tiles and reload K/V per item).
 RangePlan plan_ranges(int64_t q0, int64_t q1, int k) {
   RangePlan p{};
   const int64_t nbq = (q1 - q0 + kBlock - 1) / kBlock, nbk = (q1 + kBlock - 1) / kBlock;
@@ -1057,17 +830,11 @@ RangePlan plan_ranges(int64_t q0, int64_t q1, int k) {
       std::min<int64_t>(kMaxRanges, std::max<int64_t>(1, per_list / kItemTokens)));
   p.rq = static_cast<int>((nbq + nr_want - 1) / nr_want);
   p.nr = static_cast<int>((nbq + p.rq - 1) / p.rq);
-  p.waves = std::min(p.nr, kWaves);
   return p;
 }
 
-int prefill_chunk_launches(int64_t q0, int64_t q1, int k, int num_sms) {
-  const RangePlan p = plan_ranges(q0, q1, k);
-  const bool merge = num_sms > kMergeCtas + 1;
-  // five scheduling kernels, one wave kernel per wave (plus a combine per later wave when the
-  // GPU is too small to split), the combine of the last wave
-  return 5 + p.waves + (merge ? 0 : p.waves - 1) + 1;
-}
+// five scheduling kernels, the attention kernel, the combine
+int prefill_chunk_launches() { return 7; }
 
 PrefillWorkspace prefill_workspace_layout(int64_t L, int G, int k, int64_t chunk) {
   PrefillWorkspace w{};
@@ -1087,9 +854,8 @@ PrefillWorkspace prefill_workspace_layout(int64_t L, int G, int k, int64_t chunk
   w.items = off;     off += up(sizeof(int4) * max_items);
   w.list = off;      off += up(sizeof(int32_t) * units);
   w.pos = off;       off += up(sizeof(int32_t) * units);
-  w.pm = off;        // m and lse interleaved per list position: one 128-byte record each
-  w.plse = off + sizeof(float) * kHeadsPerGroup;
-  off += up(sizeof(float) * units * kMlStride);
+  w.pm = off;        off += up(sizeof(float) * units * kHeadsPerGroup);
+  w.plse = off;      off += up(sizeof(float) * units * kHeadsPerGroup);
   w.po = off;        off += up(sizeof(__half) * units * kHeadsPerGroup * kDim);
   w.total = off;
   w.chunk = chunk;
@@ -1148,25 +914,18 @@ cudaError_t launch_attn_prefill_chunk(const CUtensorMap& map_q, const CUtensorMa
   AttnArgs a{};
   a.items = s.items;
   a.n_items = s.n_items;
-  a.item_base = s.item_base;
   a.list = s.list;
   a.G = G;
   a.k = k;
   a.q0 = s.q0;
-  a.nbk = s.nbk;
-  a.nr = s.nr;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.po = reinterpret_cast<__half*>(ws + w.po);
   a.pm = reinterpret_cast<float*>(ws + w.pm);
   a.plse = reinterpret_cast<float*>(ws + w.plse);
   a.status = s.status;
   a.wait_ns = wait_ns;
-  a.pos = s.pos;
-  a.L = L;
-  a.o = reinterpret_cast<__nv_bfloat16*>(o);
-  a.lse = lse;
   if ((e = cudaFuncSetAttribute(attn_kv_outer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                kWaveSmem)) != cudaSuccess)
+                                kAttnSmem)) != cudaSuccess)
     return e;
   // partial O as a 2-D fp16 tensor [positions * 16 rows][128]: the epilogue's TMA stores, a
   // full tile (128 rows) or one token (16 rows) at a time
@@ -1182,38 +941,11 @@ cudaError_t launch_attn_prefill_chunk(const CUtensorMap& map_q, const CUtensorMa
                      box_tok))
       return cudaErrorInvalidValue;
   }
-  // Waves of query ranges.  Launch w runs the work items of wave w on most SMs while the rest
-  // merge the rows of wave w-1 (complete since the previous launch ended); the last wave's rows
-  // are merged by combine_kernel on the whole GPU.  The merge traffic (about as many bytes as
-  // the attention kernel writes) thus streams while the attention kernel, bound by MMA latency,
-  // leaves DRAM bandwidth unused.
-  const int n_chunk = static_cast<int>(q1 - q0);
-  const int waves = plan.waves;
-  auto range_lo = [&](int wv) { return wv * s.nr / waves; };
-  auto tok_of_range = [&](int r) { return std::min(n_chunk, r * s.rq * kBlock); };
-  const int grid_all = static_cast<int>(std::min<int64_t>(w.max_items, num_sms));
+  const int grid = static_cast<int>(std::min<int64_t>(w.max_items, num_sms));
   if (marks && marks[1]) cudaEventRecord(marks[1], stream);
-  for (int wv = 0; wv < waves; ++wv) {
-    AttnArgs aw = a;
-    aw.r_lo = range_lo(wv);
-    aw.r_hi = range_lo(wv + 1);
-    const bool merge = wv > 0 && num_sms > kMergeCtas + 1;
-    aw.c_lo = merge ? tok_of_range(range_lo(wv - 1)) : 0;
-    aw.c_hi = merge ? tok_of_range(range_lo(wv)) : 0;
-    const int grid = merge ? num_sms : grid_all;
-    aw.n_attn = merge ? num_sms - kMergeCtas : grid;
-    if (wv > 0 && !merge) {  // too few SMs to split: merge the previous wave on its own
-      CombineArgs c{};
-      c.pos = s.pos; c.po = a.po; c.pm = a.pm; c.plse = a.plse; c.L = L; c.G = G; c.k = k;
-      c.q0 = s.q0; c.o = a.o; c.lse = lse;
-      c.il0 = tok_of_range(range_lo(wv - 1));
-      const int rows = tok_of_range(range_lo(wv)) - c.il0;
-      if (rows > 0) combine_kernel<<<dim3(rows, G), 128, 0, stream>>>(c);
-    }
-    attn_kv_outer_kernel<<<grid, 512, kWaveSmem, stream>>>(map_q, map_k, map_v, map_po,
-                                                            map_po_tok, aw);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  }
+  attn_kv_outer_kernel<<<grid, 512, kAttnSmem, stream>>>(map_q, map_k, map_v, map_po,
+                                                          map_po_tok, a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   CombineArgs c{};
   c.pos = s.pos;
@@ -1224,12 +956,11 @@ cudaError_t launch_attn_prefill_chunk(const CUtensorMap& map_q, const CUtensorMa
   c.G = G;
   c.k = k;
   c.q0 = s.q0;
-  c.il0 = tok_of_range(range_lo(waves - 1));
-  c.o = a.o;
+  c.nrows = static_cast<int32_t>(q1 - q0);
+  c.o = reinterpret_cast<__nv_bfloat16*>(o);
   c.lse = lse;
   if (marks && marks[2]) cudaEventRecord(marks[2], stream);
-  const int rows = n_chunk - c.il0;
-  if (rows > 0) combine_kernel<<<dim3(rows, G), 128, 0, stream>>>(c);
+  combine_kernel<<<dim3(c.nrows, G), 128, 0, stream>>>(c);
   return cudaGetLastError();
 }
 

@@ -25,11 +25,11 @@ struct PrefillWorkspace {
 };
 PrefillWorkspace prefill_workspace_layout(int64_t L, int G, int k, int64_t chunk);
 struct RangePlan {
-  int rq, nr, waves;  // query blocks per range, ranges, launches the work items are split into
+  int rq, nr;  // query blocks per query range, number of ranges
 };
 RangePlan plan_ranges(int64_t q0, int64_t q1, int k);
 // Kernel launches one call of launch_attn_prefill_chunk makes.
-int prefill_chunk_launches(int64_t q0, int64_t q1, int k, int num_sms);
+int prefill_chunk_launches();
 cudaError_t launch_attn_prefill_chunk(const CUtensorMap& map_q, const CUtensorMap& map_k,
                                       const CUtensorMap& map_v, const int32_t* sel, int64_t L,
                                       int G, int k, float scale, int64_t q0, int64_t q1,

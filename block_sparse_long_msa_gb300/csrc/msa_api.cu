@@ -215,15 +215,8 @@ int64_t msa_prefill_chunk_tokens(const msa_config_t* cfg, int64_t L) {
 
 int32_t msa_attn_prefill_launches(const msa_config_t* cfg, int64_t L) {
   if (check_config(cfg) != MSA_OK || L <= 0 || L > kMaxPrefillTokens) return 0;
-  int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    return 0;
   const int64_t chunk = prefill_chunk(L);
-  int32_t n = 0;
-  for (int64_t q0 = 0; q0 < L; q0 += chunk)
-    n += msa::prefill_chunk_launches(q0, q0 + chunk < L ? q0 + chunk : L, cfg->topk, sms);
-  return n;
+  return static_cast<int32_t>((L + chunk - 1) / chunk) * msa::prefill_chunk_launches();
 }
 
 msa_status_t msa_attn_prefill(const msa_config_t* cfg, const void* q, const void* k,

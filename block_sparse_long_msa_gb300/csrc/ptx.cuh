@@ -81,31 +81,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
   }
 }
 
-// Non-blocking test of the phase with the given parity.
-__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// As mbar_wait, but polling (the thread never suspends): for short waits on a critical chain
-// where the SM has few other warps to run.
-__device__ __forceinline__ bool mbar_wait_poll(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
-  if (mbar_test_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  while (true) {
-#pragma unroll 1
-    for (int i = 0; i < 64; ++i)
-      if (mbar_test_wait(bar, parity)) return true;
-    if (globaltimer_ns() - t0 > limit_ns) return false;
-  }
-}
-
 // max(a, b, c) in one instruction (three-input max.f32, sm_100 family); a NaN operand is
 // ignored as in fmaxf.
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
@@ -143,16 +118,6 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t sr
   asm volatile(
       "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(map),
       "r"(src), "r"(c0), "r"(c1)
-      : "memory");
-}
-// Global -> shared contiguous copy (no tensor map), completing on an mbarrier; both addresses
-// 16-byte aligned, bytes a multiple of 16.
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
-                                          uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-          "r"(dst),
-      "l"(src), "r"(bytes), "r"(bar)
       : "memory");
 }
 __device__ __forceinline__ void bulk_commit() {

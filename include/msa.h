@@ -130,9 +130,8 @@ msa_status_t msa_attn_prefill(const msa_config_t* cfg, const void* q, const void
  * Instrumented form of msa_attn_prefill, for timing its phases; results are identical.
  * marks (may be NULL) are caller-created CUDA events (timing enabled).  On `stream` the call
  * records, for query chunk c: marks[3c] before the scheduling kernels, marks[3c+1] before the
- * first attention wave (the waves also merge the rows of all but the last wave), marks[3c+2]
- * before the merge of the last wave's rows, and marks[3*chunks] after it.  Recording stops
- * after n_marks events.  Chunks are msa_prefill_chunk_tokens() long.
+ * attention kernel, marks[3c+2] before the combine kernel, and marks[3*chunks] after the last
+ * combine.  Recording stops after n_marks events.  Chunks are msa_prefill_chunk_tokens() long.
  */
 msa_status_t msa_attn_prefill_marked(const msa_config_t* cfg, const void* q, const void* k,
                                      const void* v, int64_t L, const int32_t* sel, void* o,
@@ -142,8 +141,8 @@ msa_status_t msa_attn_prefill_marked(const msa_config_t* cfg, const void* q, con
 /* Query tokens per main-branch pass of msa_attn_prefill (its workspace covers one pass). */
 int64_t msa_prefill_chunk_tokens(const msa_config_t* cfg, int64_t L);
 
-/* Kernel launches one msa_attn_prefill call of length L enqueues on the current device (for
- * launch accounting; 0 for invalid arguments).  No GPU work. */
+/* Kernel launches one msa_attn_prefill call of length L enqueues (for launch accounting; 0 for
+ * invalid arguments).  No GPU work. */
 int32_t msa_attn_prefill_launches(const msa_config_t* cfg, int64_t L);
 
 /*

@@ -264,11 +264,13 @@ constexpr int kMetaRing = 4;  // > items that can be in flight between the gathe
 constexpr uint32_t kSmemK = 0;                             // K of the current item (32 KB)
 constexpr uint32_t kSmemV = 32768;                         // V of the current item (32 KB)
 constexpr uint32_t kSmemQ = 65536;                         // 3 x 32 KB
-constexpr uint32_t kSmemO = kSmemQ + kQStages * 32768;     // O staging tile for TMA stores
-constexpr uint32_t kSmemMeta = kSmemO + 32768;             // 4 x ItemMeta
+constexpr uint32_t kSmemO = kSmemQ + kQStages * 32768;     // 2 x O staging tile (TMA stores)
+constexpr uint32_t kSmemMeta = kSmemO + 2 * 32768;         // 4 x ItemMeta
 constexpr uint32_t kSmemBar = kSmemMeta + kMetaRing * sizeof(ItemMeta);
 constexpr uint32_t kAttnBarBytes = 512;
-constexpr uint32_t kAttnSmem = kSmemBar + kAttnBarBytes + 1024;
+// the dynamic shared memory must start on a 1024-byte boundary (checked at kernel entry): the
+// layout uses all but a few hundred bytes of the 227 KB a CTA may have
+constexpr uint32_t kAttnSmem = kSmemBar + kAttnBarBytes;
 static_assert(kAttnSmem <= 232448, "attention kernel shared memory");
 constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, false, false);
 constexpr uint32_t kIdescPV = idesc_f16_f32(128, 128, false, true);  // P, V in fp16
@@ -312,10 +314,13 @@ __global__ void __launch_bounds__(512, 1)
                          const __grid_constant__ CUtensorMap map_v,
                          const __grid_constant__ CUtensorMap map_po,
                          const __grid_constant__ CUtensorMap map_po_tok, AttnArgs a) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw;
   const uint32_t base = smem_u32(smem);
+  if (base & 1023u) {  // the swizzled tiles need 1024-byte alignment; never seen, but checked
+    if (threadIdx.x == 0) report_status(a.status, kStatusBounds);
+    return;
+  }
   const uint32_t bars = base + kSmemBar;
   auto meta_full = [&](int r) { return bars + kBMetaFull + 8 * r; };
   auto meta_empty = [&](int r) { return bars + kBMetaEmpty + 8 * r; };
@@ -689,7 +694,6 @@ __global__ void __launch_bounds__(512, 1)
       tma_prefetch_map(&map_po_tok);
     }
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t stg = base + kSmemO;
     int T = 0;
     for (int it = blockIdx.x, n = 0; it < n_items; it += gridDim.x, ++n) {
       const int r = n % kMetaRing;
@@ -725,7 +729,10 @@ __global__ void __launch_bounds__(512, 1)
         }
         tc_fence_before();
         mbar_arrive(o_empty);
-        if (et < 16) bulk_wait_read0();  // the previous tile's stores have read the staging tile
+        // two staging tiles: this tile's was last used two tiles ago, whose stores have read it
+        // once at most one (the previous tile's) bulk group is still reading
+        const uint32_t stg = base + kSmemO + (T & 1) * 32768u;
+        if (et < 16) bulk_wait_read1();
         named_barrier(1, 128);
 #pragma unroll
         for (int c8 = 0; c8 < 16; ++c8)  // 16-byte chunk c8 = columns [8 c8, 8 c8 + 8)

@@ -485,8 +485,8 @@ __global__ void __launch_bounds__(512, 1)
       uint64_t idle_since = 0;
       while (ok && (nk < n_mine || b_n < n_mine)) {
         bool progressed = false;
-        if (nk < n_mine && mbar_try_wait(meta_full(nk % kMetaRing), (nk / kMetaRing) & 1) &&
-            mbar_try_wait(k_empty, (nk & 1) ^ 1)) {
+        if (nk < n_mine && mbar_test_wait(meta_full(nk % kMetaRing), (nk / kMetaRing) & 1) &&
+            mbar_test_wait(k_empty, (nk & 1) ^ 1)) {
           const int r = nk % kMetaRing;
           const int g = meta[r].g, b = meta[r].b;
           mbar_arrive_expect_tx(k_full, 32768);
@@ -496,13 +496,13 @@ __global__ void __launch_bounds__(512, 1)
           progressed = true;
         }
         if (b_n < n_mine) {
-          if (b_cnt < 0 && mbar_try_wait(v_ready, b_n & 1)) {  // V of item b_n converted
+          if (b_cnt < 0 && mbar_test_wait(v_ready, b_n & 1)) {  // V of item b_n converted
             b_cnt = meta[b_n % kMetaRing].count;
             b_t0 = 0;
           }
           const int s3 = b_T % 3;
-          if (b_cnt >= 0 && mbar_try_wait(p_full(s3 * 2 + (b_T & 1)), (b_T / 6) & 1) &&
-              mbar_try_wait(o_empty, (b_T & 1) ^ 1)) {
+          if (b_cnt >= 0 && mbar_test_wait(p_full(s3 * 2 + (b_T & 1)), (b_T / 6) & 1) &&
+              mbar_test_wait(o_empty, (b_T & 1) ^ 1)) {
             tc_fence_after();
             const uint32_t pa = tmem + s3 * 128, vb = base + kSmemV;
 #pragma unroll
@@ -531,7 +531,6 @@ __global__ void __launch_bounds__(512, 1)
           } else if (now - idle_since > a.wait_ns || *abort_flag) {
             ok = false;
           }
-          __nanosleep(32);
         }
       }
       if (!ok) {
@@ -720,6 +719,10 @@ __global__ void __launch_bounds__(512, 1)
           tmem_ld32(tmem + lane_base + 384 + h * 64, v0);
           tmem_ld32(tmem + lane_base + 384 + h * 64 + 32, v1);
           tmem_ld_wait();
+          if (h == 1) {  // the accumulator is in registers: the next P.V may start
+            tc_fence_before();
+            mbar_arrive(o_empty);
+          }
 #pragma unroll
           for (int q = 0; q < 16; ++q) {
             ph[h * 32 + q] = pack_f16x2(__uint_as_float(v0[2 * q]), __uint_as_float(v0[2 * q + 1]));
@@ -727,8 +730,6 @@ __global__ void __launch_bounds__(512, 1)
                 pack_f16x2(__uint_as_float(v1[2 * q]), __uint_as_float(v1[2 * q + 1]));
           }
         }
-        tc_fence_before();
-        mbar_arrive(o_empty);
         // two staging tiles: this tile's was last used two tiles ago, whose stores have read it
         // once at most one (the previous tile's) bulk group is still reading
         const uint32_t stg = base + kSmemO + (T & 1) * 32768u;

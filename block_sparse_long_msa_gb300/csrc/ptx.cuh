@@ -81,6 +81,20 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
   }
 }
 
+// Non-blocking test of the phase with the given parity (try_wait may suspend the thread for a
+// while; a polling loop that watches several barriers must not).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // max(a, b, c) in one instruction (three-input max.f32, sm_100 family); a NaN operand is
 // ignored as in fmaxf.
 __device__ __forceinline__ float fmax3(float a, float b, float c) {

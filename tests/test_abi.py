@@ -69,3 +69,21 @@ def test_host_argument_checks(lib):
     # workspace queries are pure host arithmetic
     assert msa.msa_index_select_workspace(cfg, 32768, 32768) >= msa.WS_HEADER_BYTES
     assert lib.msa_index_select_workspace(ctypes.byref(bad), 1, 1, None) == 0
+
+
+def test_launch_count_and_index_dtype_config(lib):
+    """The prefill launch count is host arithmetic (seven kernels per 65,536-token chunk); an
+    index_dtype other than bf16 (0) or e4m3 (1) is an invalid config."""
+    import block_sparse_long_msa_gb300 as msa
+    cfg = msa.config(4, 16, 16)
+    assert msa.msa_prefill_chunk_tokens(cfg, 32768) == 32768
+    assert msa.msa_attn_prefill_launches(cfg, 32768) == 7
+    assert msa.msa_attn_prefill_launches(cfg, 131072) == 14
+    assert msa.msa_attn_prefill_launches(cfg, 1 << 20) == 7 * 16
+    assert msa.msa_attn_prefill_launches(cfg, 0) == 0
+    assert msa.msa_attn_prefill_launches(msa.config(4, 16, 16, index_dtype="e4m3"), 2048) == 7
+    bad = msa.config(4, 16, 16)
+    bad.index_dtype = 2
+    assert msa.msa_attn_prefill_launches(bad, 2048) == 0
+    assert lib.msa_index_select(ctypes.byref(bad), None, None, 0, None, None, None, None, 0,
+                                None) == msa.MSA_ERR_INVALID_ARG

@@ -239,7 +239,9 @@ __global__ void sched_fill_kernel(SchedArgs a) {
 // MMAs, so each chain signals its consumer when it is done while the tensor pipe interleaves
 // them.  K and V are single-buffered (K paced by the S issuer, V by the P.V issuer), which frees
 // shared memory for a three-deep query ring that covers the gather latency.  Partial outputs
-// are kept in work-list order, so a full tile leaves with two TMA stores.
+// are kept in work-list order, so a full tile leaves with two TMA stores, from one of two
+// staging tiles.  The kernel's DRAM traffic is mostly these partial writes (4 KiB per (token,
+// group, block) unit), which bound it: the MMA chains and the softmax have slack.
 // ------------------------------------------------------------------------------------------
 struct AttnArgs {
   const int4* items;
@@ -682,10 +684,12 @@ __global__ void __launch_bounds__(512, 1)
     }
   } else {
     // ------------------------------- epilogue -------------------------------
-    // O (fp32, TMEM) -> fp16 rows in a 128-byte-swizzled staging tile -> one TMA store per
-    // (token, 64-column half): each token's 16 heads are 4 KB contiguous in the partial buffer.
-    // Every epilogue thread runs the same loop, so the named barriers always pair up; after an
-    // abort the waits are skipped and nothing more is stored.
+    // O (fp32, TMEM) -> fp16 rows in a 128-byte-swizzled staging tile (two, used alternately)
+    // -> TMA stores: each token's 16 heads are 4 KB contiguous in the partial buffer, and the
+    // tokens of a tile are consecutive list positions, so a full tile is two stores (one per
+    // 64-column half) and a short last tile one store per (token, half).  Every epilogue thread
+    // runs the same loop, so the named barriers always pair up; after an abort the waits are
+    // skipped and nothing more is stored.
     const int et = threadIdx.x - 384;
     const int row = (warp & 3) * 32 + lane;
     if (et == 0) {

@@ -10,8 +10,9 @@
 //   log-sum-exp combine.
 //
 // The scan is the dominant stream of this step (every index key of every sequence, 32 KiB per
-// page); it is fed by TMA into a deep shared-memory ring and scored by tcgen05 with the page as
-// the 128-row A operand, so the SM's issue slots stay free for the max-pool.
+// page in bf16, 16 KiB in e4m3); it is fed by TMA into a deep shared-memory ring and scored by
+// tcgen05 with the page as the 128-row A operand, so the SM's issue slots stay free for the
+// max-pool.
 #include <algorithm>
 
 #include "common.cuh"

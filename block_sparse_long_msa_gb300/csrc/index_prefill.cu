@@ -7,8 +7,8 @@
 //
 // One CTA owns one query block qb (128 queries) for gpc groups (two when G is even, else one).
 // The gpc index-query tiles stay in shared memory; the keys of blocks 0..qb-1 stream through a
-// TMA ring in tiles of 256 keys (two blocks), so every MMA is M=128 x N=256 x K=16: the tensor
-// core runs an N=256 step in about the time of an N=128 one.  Score tiles go to two 256-column
+// TMA ring in tiles of 256 keys (two blocks), so every MMA is M=128 x N=256 (x K=16 in bf16,
+// K=32 in e4m3): the tensor core runs an N=256 step in about the time of an N=128 one.  Score tiles go to two 256-column
 // TMEM accumulators; work unit u = (key tile u / gpc, group u % gpc) takes slot u & 1, so with
 // two groups each slot belongs to one group and each group's MMAs overlap the other group's
 // epilogue.  Roles:

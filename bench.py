@@ -161,21 +161,21 @@ KERNEL_SOURCES = {
 }
 NCU_TRAFFIC = {
     # prefill L=32768, 64/4 heads, k=16 (profiles/dram_prefill_L32K_decode_b64.md)
-    "attention": {"bytes_per_launch": 11717122048, "workload": "prefill_L32K@32768",
-                  "sources_sha256": "d02224ceafb9e7e7abf3ae27cd194069e4ac6028b352308685f9c49c58b659f9"},
-    "combine": {"bytes_per_launch": 9171763712, "workload": "prefill_L32K@32768",
-                "sources_sha256": "d02224ceafb9e7e7abf3ae27cd194069e4ac6028b352308685f9c49c58b659f9"},
-    "index": {"bytes_per_launch": 41901568, "workload": "prefill_L32K@32768",
-              "sources_sha256": "19aa52e0668db0df0eda7ab0cd5d476f4df84f64e3f989a29fda0ee2c2da868a"},
-    "index_e4m3": {"bytes_per_launch": 20994304, "workload": "prefill_L32K@32768",
-                   "sources_sha256": "19aa52e0668db0df0eda7ab0cd5d476f4df84f64e3f989a29fda0ee2c2da868a"},
+    "attention": {"bytes_per_launch": 11531566848, "workload": "prefill_L32K@32768",
+                  "sources_sha256": "ce1f4aa5d529e711a4530fcf6826850ea7383d0e37e169c6cd7e3a74cb1bd331"},
+    "combine": {"bytes_per_launch": 9171465728, "workload": "prefill_L32K@32768",
+                "sources_sha256": "ce1f4aa5d529e711a4530fcf6826850ea7383d0e37e169c6cd7e3a74cb1bd331"},
+    "index": {"bytes_per_launch": 41901824, "workload": "prefill_L32K@32768",
+              "sources_sha256": "309806ea3e1382b034cfa7653a37b3419fd33cb090802446c196888ded88de12"},
+    "index_e4m3": {"bytes_per_launch": 20994560, "workload": "prefill_L32K@32768",
+                   "sources_sha256": "309806ea3e1382b034cfa7653a37b3419fd33cb090802446c196888ded88de12"},
     # decode, 64 sequences of 16K-256K tokens
-    "decode_scan": {"bytes_per_launch": 2084859904,
+    "decode_scan": {"bytes_per_launch": 2084641280,
                     "workload": "decode_b64_16K_256K@64x262144",
-                    "sources_sha256": "c21202469676741a41e33b2d5f003257595663f91daf94f27fe0b3d27f7feadf"},
-    "decode_scan_e4m3": {"bytes_per_launch": 1044212736,
+                    "sources_sha256": "b49a6969bae2ab9901e0ccafa2bdd59ad4a9456914edfc3ecc69e200c93f8d5f"},
+    "decode_scan_e4m3": {"bytes_per_launch": 1044227840,
                          "workload": "decode_b64_16K_256K@64x262144",
-                         "sources_sha256": "c21202469676741a41e33b2d5f003257595663f91daf94f27fe0b3d27f7feadf"},
+                         "sources_sha256": "b49a6969bae2ab9901e0ccafa2bdd59ad4a9456914edfc3ecc69e200c93f8d5f"},
 }
 
 

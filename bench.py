@@ -5,7 +5,14 @@
 
 A step is one full pass of the hot path over one batch of synthetic input resident in HBM:
 index selection (score + max-pool + top-k) followed by the main branch (scheduling, KV-outer
-attention, combine) on the 64/4-head, L = 32768 prefill workload.  Prints ONE JSON line (rank 0).
+attention, combine) on the 64/4-head, L = 32768 prefill workload, then one paged decode step of
+the 64-sequence workload (reported under "decode").  Prints ONE JSON line (rank 0) with:
+  value / roofline / kernel_rooflines  prefill tokens/s and each kernel against the measured peaks
+  attention_write_bound  the attention's partial-output writes against a write-only rate
+                         measured in the same run (a fill of a buffer larger than L2)
+  e2e                    the same step through the public API from pinned host buffers
+  e4m3_index             the index kernels timed again with e4m3 index vectors (same selections)
+  cpu_baseline           the CPU oracle on a bounded sample, on this host's cores
 
 The path has no exchange step, so N > 1 runs N independent replicas (one per GPU, weak scaling)
 with a barrier and the max over ranks around the timed region.

@@ -147,7 +147,8 @@ int32_t msa_attn_prefill_launches(const msa_config_t* cfg, int64_t L);
 
 /*
  * msa_attn_prefill_noalloc — msa_attn_prefill for callers that cannot allocate device memory.
- * (The paper has no counterpart: this is a deployment convenience of this library.)
+ * (The method's description has no counterpart: this is a deployment convenience of this
+ * library.)
  *
  * Some callers are handed only their input and output tensors and are not allowed to allocate:
  * a plugin or callback inside another framework's memory pool, code on a latency-critical path

@@ -146,3 +146,29 @@ def test_full_size_1m_hot_sampled_rows(msa):
     assert err.max() <= MAX_ABS and err.mean() <= MEAN_ABS, msg
     assert lerr.max() <= MAX_ABS and lerr.mean() <= MEAN_ABS, msg
     print(f"[parity {w.name} L={w.L}] {msg}")
+
+
+def _random_shapes(n, seed):
+    """n seeded (L, G, k) draws: L in [130, 2600] (ragged tails), G in {1, 2, 4}, k in [1, 16]."""
+    Ls = synthetic.uniform_int(seed, 81, n, 130, 2600).tolist()
+    Gs = synthetic.uniform_int(seed, 82, n, 0, 2).tolist()
+    ks = synthetic.uniform_int(seed, 83, n, 1, 16).tolist()
+    return [(L, (1, 2, 4)[g], k) for L, g, k in zip(Ls, Gs, ks)]
+
+
+@pytest.mark.parametrize("L,G,k", _random_shapes(6, 2024))
+@pytest.mark.parametrize("index_dtype", ["bf16", "e4m3"])
+def test_random_shapes_all_rows(msa, L, G, k, index_dtype):
+    """Seeded random shapes, every row: selection bit-exact and O / LSE within tolerance, with
+    bf16 and with e4m3 index vectors (the same integer/8 values)."""
+    w = synthetic.Workload("rand", "prefill", L=L, Hq=16 * G, G=G, k=k, seed=L * 7 + G * 3 + k)
+    inp = synthetic.prefill_inputs(w, index_dtype=index_dtype)
+    cfg = msa.config(w.G, w.hpg, w.k, w.scale, index_dtype=index_dtype)
+    dev = torch.device("cuda")
+    d = {k_: v.to(dev) for k_, v in inp.items() if isinstance(v, torch.Tensor)}
+    sel = msa.msa_index_select(cfg, d["q_idx"], d["k_idx"])
+    ws = torch.zeros(msa.msa_attn_prefill_workspace(cfg, w.L), dtype=torch.uint8, device=dev)
+    o, lse = msa.msa_attn_prefill(cfg, d["q"], d["k"], d["v"], sel, ws=ws)
+    torch.cuda.synchronize()
+    assert msa.msa_get_device_status(ws) == 0
+    compare(w, inp, sel.cpu().numpy(), o.float().cpu().numpy(), lse.cpu().numpy())

@@ -719,6 +719,7 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(DecCombineArgs a) {
 #pragma unroll
   for (int q = 0; q < 16; ++q) acc[q] = 0.f;
   float den = 0.f;
+#pragma unroll 4
   for (int j = 0; j < a.k; ++j) {
     const float l = a.plse[(u0 + j) * kHeads + hh];
     if (l == -__int_as_float(0x7f800000)) continue;

@@ -87,3 +87,20 @@ def test_launch_count_and_index_dtype_config(lib):
     assert msa.msa_attn_prefill_launches(bad, 2048) == 0
     assert lib.msa_index_select(ctypes.byref(bad), None, None, 0, None, None, None, None, 0,
                                 None) == msa.MSA_ERR_INVALID_ARG
+
+
+def test_empty_inputs_return_before_any_gpu_work(lib):
+    """L = 0 (prefill) and batch = 0 (decode) are valid calls that enqueue nothing."""
+    import block_sparse_long_msa_gb300 as msa
+    cfg = msa.config(4, 16, 16)
+    p = ctypes.c_void_p(0x10000)  # 16-byte aligned, never dereferenced
+    ws = msa.msa_attn_prefill_workspace(cfg, 0)
+    assert lib.msa_attn_prefill(ctypes.byref(cfg), p, p, p, 0, p, p, p, p, ws, None) == msa.MSA_OK
+    assert lib.msa_index_select(ctypes.byref(cfg), p, p, 0, None, p, None, p,
+                                msa.msa_index_select_workspace(cfg, 0, 0), None) == msa.MSA_OK
+    paged = msa.MsaPagedKV(0x10000, 0x10000, 0x10000, 0x10000, 0x10000, 0, 1, 1, 0)
+    wsd = msa.msa_attn_decode_workspace(cfg, paged)
+    assert lib.msa_attn_decode(ctypes.byref(cfg), p, ctypes.byref(paged), p, p, p, p, wsd,
+                               None) == msa.MSA_OK
+    assert lib.msa_index_select(ctypes.byref(cfg), p, None, 0, ctypes.byref(paged), p, None, p,
+                                msa.msa_index_select_workspace(cfg, 0, 0, paged), None) == msa.MSA_OK

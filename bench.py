@@ -8,8 +8,6 @@ index selection (score + max-pool + top-k) followed by the main branch (scheduli
 attention, combine) on the 64/4-head, L = 32768 prefill workload, then one paged decode step of
 the 64-sequence workload (reported under "decode").  Prints ONE JSON line (rank 0) with:
   value / roofline / kernel_rooflines  prefill tokens/s and each kernel against the measured peaks
-  attention_write_bound  the attention's partial-output writes against a write-only rate
-                         measured in the same run (a fill of a buffer larger than L2)
   e2e                    the same step through the public API from pinned host buffers
   e4m3_index             the index kernels timed again with e4m3 index vectors (same selections)
   cpu_baseline           the CPU oracle on a bounded sample, on this host's cores
@@ -204,23 +202,6 @@ def measured_traffic(kernel: str, workload: str):
     return t["bytes_per_launch"]
 
 
-def measure_write_gbs(dev, nbytes=4 << 30, reps=5):
-    """DRAM write rate of a plain fill of a buffer larger than L2 (write-only traffic), measured
-    on this GPU: the ceiling for a kernel whose DRAM traffic is mostly writes."""
-    buf = torch.empty(nbytes, dtype=torch.uint8, device=dev)
-    buf.fill_(1)
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    a.record()
-    for i in range(reps):
-        buf.fill_(i)
-    b.record()
-    torch.cuda.synchronize()
-    gbs = nbytes * reps / (a.elapsed_time(b) * 1e-3) / 1e9
-    del buf
-    return gbs
-
-
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -366,7 +347,6 @@ def run_msa(args, world, rank):
 
     work = prefill_work(w)
     peaks = load_peaks()
-    write_gbs = measure_write_gbs(dev)
     tensor_peak = peaks["bf16_tflops"]
     roof = {
         "index": ("tensor", work["index_flops"] / (per_launch_ms["index"] * 1e-3) / 1e12,
@@ -582,16 +562,6 @@ def run_msa(args, world, rank):
         "kernel_rooflines": {n: {"bound": r[0], "achieved": r[1], "peak": r[2], "unit": r[3],
                                  "frac": r[1] / r[2], "ms_per_launch": per_launch_ms[n]}
                              for n, r in roof.items()},
-        # the attention kernel's DRAM traffic is mostly the fp16 partial outputs it writes:
-        # against the measured write-only rate of this GPU (a fill) it is write-bound
-        "attention_write_bound": {
-            "bytes_written": work["units"] * w.hpg * (w.d * 2 + 8),
-            "achieved_gbs": work["units"] * w.hpg * (w.d * 2 + 8) / nchunks
-                            / (per_launch_ms["attention"] * 1e-3) / 1e9,
-            "write_peak_gbs": write_gbs,
-            "frac": work["units"] * w.hpg * (w.d * 2 + 8) / nchunks
-                    / (per_launch_ms["attention"] * 1e-3) / 1e9 / write_gbs,
-            "peak_source": "measured in this run: fill of a 4 GiB buffer"},
         "tensor_frac_main_branch": work["attn_flops"] / ((phase["attention"] + phase["combine"]
                                                           + phase["schedule"]) / args.steps
                                                          * 1e-3) / 1e12 / tensor_peak,

@@ -241,7 +241,7 @@ __global__ void sched_fill_kernel(SchedArgs a) {
 // shared memory for a three-deep query ring that covers the gather latency.  Partial outputs
 // are kept in work-list order, so a full tile leaves with two TMA stores, from one of two
 // staging tiles.  The kernel's DRAM traffic is mostly these partial writes (4 KiB per (token,
-// group, block) unit), which bound it: the MMA chains and the softmax have slack.
+// group, block) unit).
 // ------------------------------------------------------------------------------------------
 struct AttnArgs {
   const int4* items;

@@ -166,21 +166,21 @@ KERNEL_SOURCES = {
 }
 NCU_TRAFFIC = {
     # prefill L=32768, 64/4 heads, k=16 (profiles/dram_prefill_L32K_decode_b64.md)
-    "attention": {"bytes_per_launch": 11531566848, "workload": "prefill_L32K@32768",
-                  "sources_sha256": "ce1f4aa5d529e711a4530fcf6826850ea7383d0e37e169c6cd7e3a74cb1bd331"},
-    "combine": {"bytes_per_launch": 9171465728, "workload": "prefill_L32K@32768",
-                "sources_sha256": "ce1f4aa5d529e711a4530fcf6826850ea7383d0e37e169c6cd7e3a74cb1bd331"},
-    "index": {"bytes_per_launch": 41901824, "workload": "prefill_L32K@32768",
+    "attention": {"bytes_per_launch": 11535790592, "workload": "prefill_L32K@32768",
+                  "sources_sha256": "e5197b3f399b103129f1599695e311f5265ba10c8e86aa1b2afe56ddb1456a55"},
+    "combine": {"bytes_per_launch": 9195154176, "workload": "prefill_L32K@32768",
+                "sources_sha256": "e5197b3f399b103129f1599695e311f5265ba10c8e86aa1b2afe56ddb1456a55"},
+    "index": {"bytes_per_launch": 41901568, "workload": "prefill_L32K@32768",
               "sources_sha256": "309806ea3e1382b034cfa7653a37b3419fd33cb090802446c196888ded88de12"},
-    "index_e4m3": {"bytes_per_launch": 20994560, "workload": "prefill_L32K@32768",
+    "index_e4m3": {"bytes_per_launch": 20994304, "workload": "prefill_L32K@32768",
                    "sources_sha256": "309806ea3e1382b034cfa7653a37b3419fd33cb090802446c196888ded88de12"},
     # decode, 64 sequences of 16K-256K tokens
-    "decode_scan": {"bytes_per_launch": 2084641280,
+    "decode_scan": {"bytes_per_launch": 2084630016,
                     "workload": "decode_b64_16K_256K@64x262144",
-                    "sources_sha256": "b49a6969bae2ab9901e0ccafa2bdd59ad4a9456914edfc3ecc69e200c93f8d5f"},
-    "decode_scan_e4m3": {"bytes_per_launch": 1044227840,
+                    "sources_sha256": "fe02b7dd37fa4eb7898e1bb8b2c816e4e8afe589294aa997d720326240227ab1"},
+    "decode_scan_e4m3": {"bytes_per_launch": 1044207872,
                          "workload": "decode_b64_16K_256K@64x262144",
-                         "sources_sha256": "b49a6969bae2ab9901e0ccafa2bdd59ad4a9456914edfc3ecc69e200c93f8d5f"},
+                         "sources_sha256": "fe02b7dd37fa4eb7898e1bb8b2c816e4e8afe589294aa997d720326240227ab1"},
 }
 
 

@@ -10,6 +10,7 @@ the 64-sequence workload (reported under "decode").  Prints ONE JSON line (rank 
   value / roofline / kernel_rooflines  prefill tokens/s and each kernel against the measured peaks
   e2e                    the same step through the public API from pinned host buffers
   e4m3_index             the index kernels timed again with e4m3 index vectors (same selections)
+  index_scores           the index kernels timed again exporting every block's pooled score
   cpu_baseline           the CPU oracle on a bounded sample, on this host's cores
 
 The path has no exchange step, so N > 1 runs N independent replicas (one per GPU, weak scaling)
@@ -52,6 +53,8 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e4m3-index", action="store_true",
                    help="skip timing the e4m3 (FP8) index kernels beside the bf16 step")
+    p.add_argument("--no-index-scores", action="store_true",
+                   help="skip timing the index kernels with the block-score export")
     p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--L", type=int, default=0, help="override the workload length (profiling)")
     return p.parse_args()
@@ -497,6 +500,53 @@ def run_msa(args, world, rank):
             "gpu_launches": 3 * n8,
         }
 
+    # ---- block-score export (the indexer's KL alignment input): the same index kernels also
+    # write every block's pooled score, [G][L][nb] for prefill, [G][batch][max_pages] for decode;
+    # timed alone, against the selection-only launch of the same kernels ----
+    scores = None
+    if not args.no_index_scores:
+        def timed_alone(fn, n):
+            for _ in range(max(3, args.warmup)):
+                fn()
+            a0, a1 = ev(), ev()
+            torch.cuda.synchronize()
+            a0.record(stream)
+            for _ in range(n):
+                fn()
+            a1.record(stream)
+            torch.cuda.synchronize()
+            return a0.elapsed_time(a1) / n
+
+        nsc = max(3, args.steps)
+        nb = (L + w.B - 1) // w.B
+        bs = torch.empty((w.G, L, nb), dtype=torch.float32, device=dev)
+        dbs = torch.empty((dw.G, dw.batch, dinp["max_pages"]), dtype=torch.float32, device=dev)
+        sel_s, dsel_s = torch.empty_like(sel), torch.empty_like(dsel)
+        sc_ms = timed_alone(lambda: msa.msa_index_select_scores(
+            cfg, inp["q_idx"], inp["k_idx"], sel=sel_s, block_scores=bs, ws=ws, stream=stream),
+            nsc)
+        plain_ms = timed_alone(lambda: msa.msa_index_select(
+            cfg, inp["q_idx"], inp["k_idx"], sel=sel, ws=ws, stream=stream), nsc)
+        dsc_ms = timed_alone(lambda: msa.msa_index_select_scores(
+            dcfg, dinp["q_idx"], paged=paged, sel=dsel_s, block_scores=dbs, ws=dws,
+            stream=stream), nsc)
+        dplain_ms = timed_alone(lambda: msa.msa_index_select(
+            dcfg, dinp["q_idx"], paged=paged, sel=dsel, ws=dws, stream=stream), nsc)
+        assert torch.equal(sel_s, sel) and torch.equal(dsel_s, dsel), "score export selection"
+        out_b, dout_b = bs.numel() * 4, dbs.numel() * 4
+        scores = {
+            "note": "msa_index_select_scores: the index kernels also write every block's pooled "
+                    "score (+inf own block, -inf later blocks); each timed alone, back to back, "
+                    "beside the selection-only launch of the same kernels",
+            "prefill_ms": sc_ms, "prefill_ms_select_only": plain_ms,
+            "prefill_output_bytes": out_b,
+            "prefill_extra_gbs": out_b / max(sc_ms - plain_ms, 1e-6) / 1e6,
+            "decode_ms": dsc_ms, "decode_ms_select_only": dplain_ms,
+            "decode_output_bytes": dout_b,
+            "gpu_launches": 2 * nsc + 4 * nsc,
+        }
+        del bs, dbs
+
     cpu_base = None
     dec_cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -579,6 +629,7 @@ def run_msa(args, world, rank):
     }
     line["decode"]["cpu_baseline"] = dec_cpu
     line["e4m3_index"] = e4m3
+    line["index_scores"] = scores
     if rank == 0:
         print(json.dumps(line), flush=True)
 

@@ -17,7 +17,8 @@ MSA_OK, MSA_ERR_INVALID_ARG, MSA_ERR_UNSUPPORTED, MSA_ERR_WORKSPACE = 0, 1, 2, 3
 MSA_ERR_CUDA, MSA_ERR_DEVICE_TIMEOUT, MSA_ERR_DEVICE_BOUNDS = 4, 5, 6
 WS_HEADER_BYTES = 256
 
-EXPORTS = ("msa_index_select_workspace", "msa_index_select", "msa_attn_prefill_workspace",
+EXPORTS = ("msa_index_select_workspace", "msa_index_select", "msa_index_select_scores",
+           "msa_attn_prefill_workspace",
            "msa_attn_prefill", "msa_attn_prefill_marked", "msa_prefill_chunk_tokens",
            "msa_attn_prefill_launches",
            "msa_attn_decode_workspace", "msa_attn_decode",
@@ -62,6 +63,7 @@ def lib() -> ctypes.CDLL:
         L.msa_index_select_workspace.argtypes = [cfgp, i64, i64, pagedp]
         L.msa_index_select_workspace.restype = sz
         L.msa_index_select.argtypes = [cfgp, P, P, i64, pagedp, P, P, P, sz, P]
+        L.msa_index_select_scores.argtypes = [cfgp, P, P, i64, pagedp, P, P, P, P, sz, P]
         L.msa_attn_prefill_workspace.argtypes = [cfgp, i64]
         L.msa_attn_prefill_workspace.restype = sz
         L.msa_attn_prefill.argtypes = [cfgp, P, P, P, i64, P, P, P, P, sz, P]
@@ -78,7 +80,8 @@ def lib() -> ctypes.CDLL:
         L.msa_reset_device_status.argtypes = [P, P]
         L.msa_status_string.argtypes = [ctypes.c_int]
         L.msa_status_string.restype = ctypes.c_char_p
-        for name in ("msa_index_select", "msa_attn_prefill", "msa_attn_prefill_marked",
+        for name in ("msa_index_select", "msa_index_select_scores", "msa_attn_prefill",
+                     "msa_attn_prefill_marked",
                      "msa_attn_decode",
                      "msa_get_device_status", "msa_reset_device_status"):
             getattr(L, name).restype = ctypes.c_int
@@ -170,6 +173,33 @@ def msa_index_select(cfg: MsaConfig, q_idx, k_idx=None, paged: MsaPagedKV | None
                                 _ptr(sel_score), _ptr(ws), ws.numel(), _stream(stream))
     _check(st, "msa_index_select")
     return (sel, sel_score) if want_score else sel
+
+
+def msa_index_select_scores(cfg: MsaConfig, q_idx, k_idx=None, paged: MsaPagedKV | None = None,
+                            sel=None, block_scores=None, ws=None, stream=None):
+    """Index branch plus every block's pooled score.  Returns (sel int32 [G][T][k],
+    block_scores fp32 [G][T][nb]); nb = ceil(L/128) for prefill, max_pages for decode.
+    Entries: the pooled score for blocks before the query's own, +inf for its own, -inf after."""
+    import torch
+    _index_dtype_ok(cfg, q_idx, k_idx)
+    T = q_idx.shape[0]
+    L = 0 if paged is not None else k_idx.shape[0]
+    G, k = cfg.num_groups, cfg.topk
+    nb = paged.max_pages if paged is not None else (L + cfg.block_size - 1) // cfg.block_size
+    if sel is None:
+        sel = torch.empty((G, T, k), dtype=torch.int32, device=q_idx.device)
+    if block_scores is None:
+        block_scores = torch.empty((G, T, nb), dtype=torch.float32, device=q_idx.device)
+    elif (block_scores.dtype != torch.float32 or tuple(block_scores.shape) != (G, T, nb)
+          or not block_scores.is_contiguous()):
+        raise MsaError(MSA_ERR_INVALID_ARG, f"block_scores must be contiguous fp32 {(G, T, nb)}")
+    ws = _workspace(msa_index_select_workspace(cfg, T, L, paged), q_idx.device, ws)
+    st = lib().msa_index_select_scores(ctypes.byref(cfg), _ptr(q_idx), _ptr(k_idx), L,
+                                       ctypes.byref(paged) if paged is not None else None,
+                                       _ptr(sel), None, _ptr(block_scores), _ptr(ws), ws.numel(),
+                                       _stream(stream))
+    _check(st, "msa_index_select_scores")
+    return sel, block_scores
 
 
 def msa_attn_prefill_workspace(cfg: MsaConfig, L: int) -> int:

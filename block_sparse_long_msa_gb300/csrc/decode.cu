@@ -342,6 +342,8 @@ struct TopkArgs {
   int32_t batch, max_pages, G, k;
   int32_t* sel;       // [G][batch][k]
   float* sel_score;   // optional, same shape
+  float* block_scores;  // optional [G][batch][max_pages]: pooled score of every block (+inf
+                        // the local one, -inf later ones)
   int32_t* status;
 };
 
@@ -358,11 +360,21 @@ __global__ void __launch_bounds__(128) decode_topk_kernel(TopkArgs a) {
       out[r] = -1;
       if (out_s) out_s[r] = -__int_as_float(0x7f800000);
     }
+    if (a.block_scores)
+      for (int b = lane; b < a.max_pages; b += 32)
+        a.block_scores[(static_cast<size_t>(g) * a.batch + s) * a.max_pages + b] =
+            -__int_as_float(0x7f800000);
     return;
   }
   const int bi = (n - 1) / kBlock;
   TopList list;
   list.clear();
+  float* bsrow = a.block_scores
+                     ? a.block_scores + (static_cast<size_t>(g) * a.batch + s) * a.max_pages
+                     : nullptr;
+  if (bsrow)  // the local block is never scored; later blocks are not causal
+    for (int b = bi + lane; b < a.max_pages; b += 32)
+      bsrow[b] = b == bi ? __int_as_float(0x7f800000) : -__int_as_float(0x7f800000);
   const float4* row = a.scores + (static_cast<size_t>(s) * a.G + g) * a.max_pages;
   // eight loads in flight per lane, then eight inserts (blocks stay ascending per lane)
   for (int b0 = 0; b0 < bi; b0 += 8 * 32) {
@@ -378,7 +390,10 @@ __global__ void __launch_bounds__(128) decode_topk_kernel(TopkArgs a) {
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
       const int b = b0 + q * 32 + lane;
-      if (b < bi) list.insert(sc[q], b);
+      if (b < bi) {
+        list.insert(sc[q], b);
+        if (bsrow) bsrow[b] = sc[q];
+      }
     }
   }
   const int take = min(a.k - 1, bi);
@@ -756,8 +771,9 @@ size_t decode_select_workspace_bytes(int batch, int G, int max_pages) {
 cudaError_t launch_decode_select(const CUtensorMap& map_k, const CUtensorMap& map_q,
                                  const int32_t* page_table, const int32_t* seq_lens, int batch,
                                  int max_pages, int num_pages, int G, int k, bool fp8,
-                                 float* scores, int32_t* sel, float* sel_score, int32_t* status,
-                                 uint64_t wait_ns, int num_sms, cudaStream_t stream) {
+                                 float* scores, int32_t* sel, float* sel_score,
+                                 float* block_scores, int32_t* status, uint64_t wait_ns,
+                                 int num_sms, cudaStream_t stream) {
   ScanArgs a{};
   a.page_table = page_table;
   a.seq_lens = seq_lens;
@@ -794,6 +810,7 @@ cudaError_t launch_decode_select(const CUtensorMap& map_k, const CUtensorMap& ma
   t.k = k;
   t.sel = sel;
   t.sel_score = sel_score;
+  t.block_scores = block_scores;
   t.status = status;
   decode_topk_kernel<<<(batch * G * 32 + 127) / 128, 128, 0, stream>>>(t);
   return cudaGetLastError();

@@ -61,6 +61,7 @@ struct IndexPrefillArgs {
   int32_t G, gpc, k, nb, ns;
   int32_t* sel;
   float* sel_score;
+  float* block_scores;  // optional [G][L][nb]: every block's pooled score (+inf local, -inf later)
   int32_t* status;
   uint64_t wait_ns;
 };
@@ -244,6 +245,13 @@ __global__ void __launch_bounds__(384, 1)
       }
       list.insert(mx[0], 2 * t);
       if (2 * t + 1 < nkey) list.insert(mx[1], 2 * t + 1);
+      const int64_t ib = static_cast<int64_t>(qb) * kBlock + row;
+      if (a.block_scores && ib < a.L) {
+        float* bs = a.block_scores +
+                    (static_cast<size_t>(g0 + (gpc == 2 ? e : 0)) * a.L + ib) * a.nb + 2 * t;
+        bs[0] = mx[0];
+        if (2 * t + 1 < nkey) bs[1] = mx[1];
+      }
     }
     if (!ok) {
       report_status(a.status, kStatusTimeout);
@@ -276,6 +284,17 @@ __global__ void __launch_bounds__(384, 1)
       const size_t off = (static_cast<size_t>(g) * a.L + i) * a.k;
       write_sel_row(list, n, qb, a.k, a.sel + off, a.sel_score ? a.sel_score + off : nullptr);
     }
+    if (a.block_scores && (gpc == 2 || e == 0) && ok && !*abort_flag) {
+      // Row tails: +inf at the local block (never scored), -inf after it (not causal).  The
+      // warp walks its 32 rows with the lanes along the columns, so each store is contiguous.
+      const int g = g0 + (gpc == 2 ? e : 0);
+      const int64_t r0 = static_cast<int64_t>(qb) * kBlock + (warp & 3) * 32;
+      for (int r = 0; r < 32 && r0 + r < a.L; ++r) {
+        float* bs = a.block_scores + (static_cast<size_t>(g) * a.L + r0 + r) * a.nb;
+        for (int b = qb + lane; b < a.nb; b += 32)
+          bs[b] = b == qb ? __int_as_float(0x7f800000) : -__int_as_float(0x7f800000);
+      }
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -293,8 +312,8 @@ size_t smem_bytes(int gpc, int ns) {
 
 template <bool kF8>
 cudaError_t launch(const CUtensorMap& map_q, const CUtensorMap& map_k, int64_t L, int G, int k,
-                   int32_t* sel, float* sel_score, int32_t* status, uint64_t wait_ns,
-                   cudaStream_t stream) {
+                   int32_t* sel, float* sel_score, float* block_scores, int32_t* status,
+                   uint64_t wait_ns, cudaStream_t stream) {
   const int nb = static_cast<int>((L + kBlock - 1) / kBlock);
   const int gpc = (G % 2 == 0) ? 2 : 1;  // groups per CTA
   int ns = IdxTiles<kF8>::kMaxStages;    // key stages
@@ -304,7 +323,7 @@ cudaError_t launch(const CUtensorMap& map_q, const CUtensorMap& map_k, int64_t L
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  IndexPrefillArgs a{L, G, gpc, k, nb, ns, sel, sel_score, status, wait_ns};
+  IndexPrefillArgs a{L, G, gpc, k, nb, ns, sel, sel_score, block_scores, status, wait_ns};
   index_select_prefill_kernel<kF8><<<nb * (G / gpc), 384, smem, stream>>>(map_q, map_k, a);
   return cudaGetLastError();
 }
@@ -313,10 +332,12 @@ cudaError_t launch(const CUtensorMap& map_q, const CUtensorMap& map_k, int64_t L
 
 cudaError_t launch_index_select_prefill(const CUtensorMap& map_q, const CUtensorMap& map_k,
                                         int64_t L, int G, int k, bool fp8, int32_t* sel,
-                                        float* sel_score, int32_t* status, uint64_t wait_ns,
-                                        cudaStream_t stream) {
-  return fp8 ? launch<true>(map_q, map_k, L, G, k, sel, sel_score, status, wait_ns, stream)
-             : launch<false>(map_q, map_k, L, G, k, sel, sel_score, status, wait_ns, stream);
+                                        float* sel_score, float* block_scores, int32_t* status,
+                                        uint64_t wait_ns, cudaStream_t stream) {
+  return fp8 ? launch<true>(map_q, map_k, L, G, k, sel, sel_score, block_scores, status, wait_ns,
+                            stream)
+             : launch<false>(map_q, map_k, L, G, k, sel, sel_score, block_scores, status,
+                             wait_ns, stream);
 }
 
 }  // namespace msa

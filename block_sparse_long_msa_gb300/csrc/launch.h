@@ -12,10 +12,11 @@ namespace msa {
 // Keys per tile of the prefill index kernel (two blocks): the box height of its key tensor map.
 constexpr int kIndexKeyTile = 256;
 // fp8: index vectors are e4m3 (else bf16); the tensor maps' element type must match.
+// block_scores (optional): [G][L][nb] pooled score of every block (+inf local, -inf later).
 cudaError_t launch_index_select_prefill(const CUtensorMap& map_q, const CUtensorMap& map_k,
                                         int64_t L, int G, int k, bool fp8, int32_t* sel,
-                                        float* sel_score, int32_t* status, uint64_t wait_ns,
-                                        cudaStream_t stream);
+                                        float* sel_score, float* block_scores, int32_t* status,
+                                        uint64_t wait_ns, cudaStream_t stream);
 
 // Byte offsets of the prefill main-branch workspace (after the 256-byte status header).
 struct PrefillWorkspace {
@@ -41,8 +42,9 @@ size_t decode_select_workspace_bytes(int batch, int G, int max_pages);
 cudaError_t launch_decode_select(const CUtensorMap& map_k, const CUtensorMap& map_q,
                                  const int32_t* page_table, const int32_t* seq_lens, int batch,
                                  int max_pages, int num_pages, int G, int k, bool fp8,
-                                 float* scores, int32_t* sel, float* sel_score, int32_t* status,
-                                 uint64_t wait_ns, int num_sms, cudaStream_t stream);
+                                 float* scores, int32_t* sel, float* sel_score,
+                                 float* block_scores, int32_t* status, uint64_t wait_ns,
+                                 int num_sms, cudaStream_t stream);
 size_t decode_attn_workspace_bytes(int batch, int G, int k);
 cudaError_t launch_decode_attn(const CUtensorMap& map_kp, const CUtensorMap& map_vp,
                                const void* q, const int32_t* sel, const int32_t* page_table,

@@ -91,7 +91,8 @@ bool sm_count(int* sms) {
 
 msa_status_t index_select_paged(const msa_config_t* cfg, const void* q_idx,
                                 const msa_paged_kv_t* paged, int32_t* sel, float* sel_score,
-                                void* ws, size_t ws_bytes, cudaStream_t stream) {
+                                float* block_scores, void* ws, size_t ws_bytes,
+                                cudaStream_t stream) {
   msa_status_t st = check_paged(paged, false);
   if (st != MSA_OK) return st;
   const int G = cfg->num_groups;
@@ -117,8 +118,8 @@ msa_status_t index_select_paged(const msa_config_t* cfg, const void* q_idx,
   float* scores = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + MSA_WS_HEADER_BYTES);
   cudaError_t e = msa::launch_decode_select(mk, mq, paged->page_table, paged->seq_lens,
                                             paged->batch, paged->max_pages, paged->num_pages, G,
-                                            cfg->topk, fp8, scores, sel, sel_score, status_word(ws),
-                                            wait_ns(cfg), sms, stream);
+                                            cfg->topk, fp8, scores, sel, sel_score, block_scores,
+                                            status_word(ws), wait_ns(cfg), sms, stream);
   return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
 }
 
@@ -170,14 +171,21 @@ size_t msa_index_select_workspace(const msa_config_t* cfg, int64_t num_queries, 
   return bytes;
 }
 
-msa_status_t msa_index_select(const msa_config_t* cfg, const void* q_idx, const void* k_idx,
-                              int64_t L, const msa_paged_kv_t* paged, int32_t* sel,
-                              float* sel_score, void* ws, size_t ws_bytes, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Both index-branch entries: block_scores (optional) also receives every block's pooled score.
+msa_status_t index_select(const msa_config_t* cfg, const void* q_idx, const void* k_idx,
+                          int64_t L, const msa_paged_kv_t* paged, int32_t* sel, float* sel_score,
+                          float* block_scores, void* ws, size_t ws_bytes, cudaStream_t stream) {
   msa_status_t st = check_config(cfg);
   if (st != MSA_OK) return st;
   if (!q_idx || !sel || !ws || !aligned16(q_idx)) return MSA_ERR_INVALID_ARG;
   const int G = cfg->num_groups;
-  if (paged) return index_select_paged(cfg, q_idx, paged, sel, sel_score, ws, ws_bytes, stream);
+  if (paged)
+    return index_select_paged(cfg, q_idx, paged, sel, sel_score, block_scores, ws, ws_bytes,
+                              stream);
   if (!k_idx || !aligned16(k_idx) || L < 0) return MSA_ERR_INVALID_ARG;
   if (G != 1 && G != 2 && G != 4) return MSA_ERR_UNSUPPORTED;
   if (L > (static_cast<int64_t>(1) << 31) - kBlock) return MSA_ERR_UNSUPPORTED;
@@ -198,8 +206,28 @@ msa_status_t msa_index_select(const msa_config_t* cfg, const void* q_idx, const 
     if (!make_index_map(&mk, fp8, k_idx, 2, dims, strides, box)) return MSA_ERR_CUDA;
   }
   cudaError_t e = msa::launch_index_select_prefill(mq, mk, L, G, cfg->topk, fp8, sel, sel_score,
-                                                   status_word(ws), wait_ns(cfg), stream);
+                                                   block_scores, status_word(ws), wait_ns(cfg),
+                                                   stream);
   return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+msa_status_t msa_index_select(const msa_config_t* cfg, const void* q_idx, const void* k_idx,
+                              int64_t L, const msa_paged_kv_t* paged, int32_t* sel,
+                              float* sel_score, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  return index_select(cfg, q_idx, k_idx, L, paged, sel, sel_score, nullptr, ws, ws_bytes, stream);
+}
+
+msa_status_t msa_index_select_scores(const msa_config_t* cfg, const void* q_idx,
+                                     const void* k_idx, int64_t L, const msa_paged_kv_t* paged,
+                                     int32_t* sel, float* sel_score, float* block_scores,
+                                     void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (!block_scores) return MSA_ERR_INVALID_ARG;
+  return index_select(cfg, q_idx, k_idx, L, paged, sel, sel_score, block_scores, ws, ws_bytes,
+                      stream);
 }
 
 size_t msa_attn_prefill_workspace(const msa_config_t* cfg, int64_t L) {

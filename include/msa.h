@@ -110,6 +110,24 @@ msa_status_t msa_index_select(const msa_config_t* cfg, const void* q_idx, const 
                               int64_t L, const msa_paged_kv_t* paged, int32_t* sel,
                               float* sel_score, void* ws, size_t ws_bytes, cudaStream_t stream);
 
+/*
+ * Index branch with every block's pooled score exported, for the KL alignment of the indexer
+ * ("MiniMax M3 算力省 20 倍", section 三 item 1: the indexer's block distribution is fitted to the
+ * main branch's group-mean attention; that loss and its gradient live outside this library).
+ * Same arguments, workspace and outputs as msa_index_select, plus
+ *   block_scores (out, required) fp32, prefill [G][L][nb] with nb = ceil(L / B), decode
+ *     [G][batch][max_pages]: for query i in block b(i) and every block c < b(i) the max-pooled
+ *     raw score max over j in c of q_idx[i,g] . k_idx[j]; +inf at c = b(i) (the forced local
+ *     block, never scored); -inf for c > b(i) (not causal).  A decode row whose seq_lens entry
+ *     is out of range (MSA_ERR_DEVICE_BOUNDS) is all -inf.  The scores are bit-identical to the
+ *     ones that msa_index_select ranks.
+ * Returns MSA_ERR_INVALID_ARG if block_scores is NULL.
+ */
+msa_status_t msa_index_select_scores(const msa_config_t* cfg, const void* q_idx,
+                                     const void* k_idx, int64_t L, const msa_paged_kv_t* paged,
+                                     int32_t* sel, float* sel_score, float* block_scores,
+                                     void* ws, size_t ws_bytes, cudaStream_t stream);
+
 /* Workspace bytes for msa_attn_prefill over L tokens. */
 size_t msa_attn_prefill_workspace(const msa_config_t* cfg, int64_t L);
 

@@ -2,7 +2,7 @@
 
 Python face of ``msa_oracle.c``: a plain CPU, fp64-accumulation restatement of MiniMax Sparse
 Attention ("MiniMax M3 算力省 20 倍", section 二 Index Branch / Main Branch, section 三 item 4 local
-block).  Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py`` use
+block, section 三 item 1 for the block scores exported to the indexer's KL alignment).  Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py`` use
 it.  It shares no code with the CUDA path and never imports it.
 
 Inputs are bf16 torch tensors on the CPU (or uint16 numpy arrays of bf16 bits; index vectors may
@@ -46,6 +46,8 @@ def _load():
         lib.oracle_select_decode.argtypes = [P, P, P, i64, P, i64, i32, i32, i32, i32, P, P]
         lib.oracle_attn_decode.argtypes = [P, P, P, P, i64, P, i64, i32, i32, i32, i32, i32, f64,
                                            P, P, P]
+        lib.oracle_block_scores_prefill.argtypes = [P, P, i64, i32, i32, i32, P, i64, P]
+        lib.oracle_block_scores_decode.argtypes = [P, P, P, i64, P, i64, i32, i32, i32, P]
         lib.oracle_num_threads.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -122,6 +124,30 @@ def select_prefill(q_idx, k_idx, B: int, k: int, rows=None, want_score: bool = F
     _load().oracle_select_prefill(_ptr(qi), _ptr(ki), L, G, di, B, k, _ptr(rows), len(rows),
                                   _ptr(sel), _ptr(score) if want_score else None)
     return (sel, score) if want_score else sel
+
+
+def block_scores_prefill(q_idx, k_idx, B: int, rows=None):
+    """Every block's pooled index score, float64 [G][nrows][ceil(L/B)]: the block max of the raw
+    dot products for blocks before the query's own, +inf for its own, -inf after it."""
+    qi, ki = _bits(q_idx), _bits(k_idx)
+    L, G, di = qi.shape
+    assert ki.shape == (L, di)
+    rows = np.arange(L, dtype=np.int64) if rows is None else np.ascontiguousarray(rows, np.int64)
+    out = np.empty((G, len(rows), (L + B - 1) // B), np.float64)
+    _load().oracle_block_scores_prefill(_ptr(qi), _ptr(ki), L, G, di, B, _ptr(rows), len(rows),
+                                        _ptr(out))
+    return out
+
+
+def block_scores_decode(q_idx, k_idx_pool, page_table, seq_lens, B: int):
+    """Paged decode: float64 [G][batch][max_pages], same entries as block_scores_prefill."""
+    qi, kp = _bits(q_idx), _bits(k_idx_pool)
+    pt, sl = _i32(page_table), _i32(seq_lens)
+    batch, G, di = qi.shape
+    out = np.empty((G, batch, pt.shape[1]), np.float64)
+    _load().oracle_block_scores_decode(_ptr(qi), _ptr(kp), _ptr(pt), pt.shape[1], _ptr(sl), batch,
+                                       G, di, B, _ptr(out))
+    return out
 
 
 def attn_prefill(q, kk, vv, sel, B: int, k: int, scale: float, rows=None, q_compact=False):

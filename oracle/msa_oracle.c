@@ -23,6 +23,8 @@
  *    o      = sum_j exp(z_j - m) v[j,g,:] / l,   lse = m + ln(l)
  *  Decode: the same rules for one query per sequence at position n-1 (n = context length, the
  *  new token already in the cache), keys/values read through the page table.
+ *  Exported block scores (section 三 item 1, the indexer's KL alignment needs them): S[b] for
+ *  every b < b_i, +inf at b_i, -inf after it.
  *
  * Readings where the pages are silent: ties rank the lower block id first; the local block is
  * never scored (every other candidate block lies wholly in the causal past); the score is the raw
@@ -129,6 +131,58 @@ void oracle_select_prefill(const uint16_t* q_idx, const uint16_t* k_idx, int64_t
                        score ? score + ((size_t)g * nrows + r) * k : NULL);
         }
         free(cand);
+    }
+}
+
+/*
+ * Every block's pooled index score for one (query, group), as exported for the indexer's KL
+ * alignment ("MiniMax M3 算力省 20 倍", section 三 item 1, which fits the indexer's block scores to
+ * the main branch's attention): out[c] = max over the B tokens j of block c of the raw dot
+ * product q . k_idx[j] for c < b_i; +inf at c = b_i (the forced local block, never scored);
+ * -inf for b_i < c < nb (not causal).
+ */
+static void block_scores_one(const uint16_t* q, const uint16_t* kbase, const int32_t* page_row,
+                             int di, int B, int64_t i, int64_t nb, double* out) {
+    const int64_t bi = i / B;
+    for (int64_t c = 0; c < nb; ++c) {
+        if (c == bi) { out[c] = INFINITY; continue; }
+        if (c > bi) { out[c] = -INFINITY; continue; }
+        double best = -INFINITY;
+        for (int t = 0; t < B; ++t) {
+            const uint16_t* kr = idx_key_row(kbase, page_row, B, di, c * B + t);
+            double s = 0.0;
+            for (int d = 0; d < di; ++d) s += bf(q[d]) * bf(kr[d]);
+            if (s > best) best = s;
+        }
+        out[c] = best;
+    }
+}
+
+/* Prefill: out [G][nrows][nb] for the query positions rows[r], nb = ceil(L / B). */
+void oracle_block_scores_prefill(const uint16_t* q_idx, const uint16_t* k_idx, int64_t L, int G,
+                                 int di, int B, const int64_t* rows, int64_t nrows, double* out) {
+    const int64_t nb = (L + B - 1) / B;
+    #pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t rg = 0; rg < nrows * G; ++rg) {
+        int64_t r = rg / G;
+        int g = (int)(rg % G);
+        block_scores_one(q_idx + ((size_t)rows[r] * G + g) * di, k_idx, NULL, di, B, rows[r], nb,
+                         out + ((size_t)g * nrows + r) * nb);
+    }
+}
+
+/* Decode: out [G][batch][max_pages], keys through the page table; query at seq_lens[s]-1. */
+void oracle_block_scores_decode(const uint16_t* q_idx, const uint16_t* k_idx_pool,
+                                const int32_t* page_table, int64_t max_pages,
+                                const int32_t* seq_lens, int64_t batch, int G, int di, int B,
+                                double* out) {
+    #pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t sg = 0; sg < batch * G; ++sg) {
+        int64_t s = sg / G;
+        int g = (int)(sg % G);
+        block_scores_one(q_idx + ((size_t)s * G + g) * di, k_idx_pool,
+                         page_table + (size_t)s * max_pages, di, B, (int64_t)seq_lens[s] - 1,
+                         max_pages, out + ((size_t)g * batch + s) * max_pages);
     }
 }
 

@@ -98,6 +98,12 @@ def test_empty_inputs_return_before_any_gpu_work(lib):
     assert lib.msa_attn_prefill(ctypes.byref(cfg), p, p, p, 0, p, p, p, p, ws, None) == msa.MSA_OK
     assert lib.msa_index_select(ctypes.byref(cfg), p, p, 0, None, p, None, p,
                                 msa.msa_index_select_workspace(cfg, 0, 0), None) == msa.MSA_OK
+    wsi = msa.msa_index_select_workspace(cfg, 0, 0)
+    assert lib.msa_index_select_scores(ctypes.byref(cfg), p, p, 0, None, p, None, p, p, wsi,
+                                       None) == msa.MSA_OK
+    # the score export requires its output
+    assert lib.msa_index_select_scores(ctypes.byref(cfg), p, p, 0, None, p, None, None, p, wsi,
+                                       None) == msa.MSA_ERR_INVALID_ARG
     paged = msa.MsaPagedKV(0x10000, 0x10000, 0x10000, 0x10000, 0x10000, 0, 1, 1, 0)
     wsd = msa.msa_attn_decode_workspace(cfg, paged)
     assert lib.msa_attn_decode(ctypes.byref(cfg), p, ctypes.byref(paged), p, p, p, p, wsd,

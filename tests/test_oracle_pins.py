@@ -7,7 +7,9 @@
   attention (torch SDPA in fp64, a library routine);
 * k = 1 reduces to block-local causal attention (SDPA with a block-diagonal causal mask);
 * equal block scores rank the lower block id first; permuting tokens inside a selected
-  non-local block changes nothing; a decode at position n-1 equals the last prefill row.
+  non-local block changes nothing; a decode at position n-1 equals the last prefill row;
+* the exported block scores (section 三 item 1) equal a dense numpy max-pool under the causal
+  mask, and ranking them reproduces the selection.
 """
 import math
 import os
@@ -89,6 +91,8 @@ def test_golden_uniform_case():
     sel = oracle.select_prefill(q_idx, k_idx, B, k)
     assert sel.tolist()[0] == [[int(x) for x in r] for r in c["sel_group0"]]
     assert sel.tolist()[1] == [[int(x) for x in r] for r in c["sel_group1"]]
+    bs = oracle.block_scores_prefill(q_idx, k_idx, B)
+    assert bs.tolist()[0] == c["bs_group0"] and bs.tolist()[1] == c["bs_group1"]
     q = torch.zeros(L, Hq, d, dtype=torch.bfloat16)
     kk = torch.zeros(L, G, d, dtype=torch.bfloat16)
     vv = torch.zeros(L, G, d, dtype=torch.bfloat16)
@@ -173,6 +177,48 @@ def test_selection_matches_bruteforce(L, B, G, k, seed):
                     assert score[g, i, r] == np.inf
                 else:
                     assert score[g, i, r] == s[g, i, b * B:(b + 1) * B].max()
+
+
+@pytest.mark.parametrize("L,B,G,seed", [(1, 4, 1, 0), (17, 4, 2, 1), (64, 8, 3, 2), (50, 4, 1, 3),
+                                       (96, 4, 4, 5)])
+def test_block_scores_match_dense_pooling(L, B, G, seed):
+    """Exported block scores against a dense numpy formulation: the L x L score matrix padded to
+    whole blocks with -inf, reshaped and reduced by max, then the causal mask (+inf on the
+    diagonal block, -inf above it)."""
+    di = 8
+    qi = synthetic.int8th(seed, 4, (L, G, di))
+    ki = synthetic.int8th(seed, 5, (L, di))
+    bs = oracle.block_scores_prefill(qi, ki, B)
+    nb = (L + B - 1) // B
+    s = np.full((G, L, nb * B), -np.inf)
+    s[:, :, :L] = np.einsum("igd,jd->gij", qi.double().numpy(), ki.double().numpy())
+    pooled = s.reshape(G, L, nb, B).max(axis=3)
+    own = (np.arange(L) // B)[:, None]
+    blk = np.arange(nb)[None, :]
+    ref = np.where(blk < own, pooled, np.where(blk == own, np.inf, -np.inf))
+    np.testing.assert_array_equal(bs, np.broadcast_to(ref, bs.shape))
+    rows = np.array([0, L - 1, L // 2], np.int64)
+    np.testing.assert_array_equal(oracle.block_scores_prefill(qi, ki, B, rows=rows), bs[:, rows])
+
+
+@pytest.mark.parametrize("L,B,G,k,seed", [(17, 4, 2, 3, 1), (64, 8, 3, 2, 2), (96, 4, 4, 4, 5)])
+def test_block_scores_rank_to_the_selection(L, B, G, k, seed):
+    """The selection is the local block plus the k-1 best exported scores below it (ties to the
+    lower id, a stable sort on the negated score), and the selection's scores are gathered from
+    the exported row."""
+    di = 8
+    qi = synthetic.int8th(seed, 4, (L, G, di))
+    ki = synthetic.int8th(seed, 5, (L, di))
+    sel, score = oracle.select_prefill(qi, ki, B, k, want_score=True)
+    bs = oracle.block_scores_prefill(qi, ki, B)
+    for g in range(G):
+        for i in range(L):
+            bi = i // B
+            order = np.argsort(-bs[g, i, :bi], kind="stable")[:k - 1]
+            want = sorted(order.tolist() + [bi])
+            assert sel[g, i].tolist() == want + [-1] * (k - len(want))
+            for r in range(len(want)):
+                assert score[g, i, r] == bs[g, i, sel[g, i, r]]
 
 
 @pytest.mark.parametrize("L,B,Hq,G,k,seed", [(33, 4, 4, 2, 3, 0), (64, 8, 6, 3, 2, 1),
@@ -302,6 +348,7 @@ def test_decode_equals_last_prefill_row():
     qi_dec = synthetic.int8th(4, 4, (len(lens), G, di))
     seq = torch.tensor(lens, dtype=torch.int32)
     sel_d, sc_d = oracle.select_decode(qi_dec, pools["k_idx_pool"], pt, seq, B, k, want_score=True)
+    bs_d = oracle.block_scores_decode(qi_dec, pools["k_idx_pool"], pt, seq, B)
     o_d, lse_d = oracle.attn_decode(q_dec, pools["k_pool"], pools["v_pool"], pt, seq, sel_d, B, k,
                                     0.25)
     for s, n in enumerate(lens):
@@ -317,6 +364,10 @@ def test_decode_equals_last_prefill_row():
         sel_p, sc_p = oracle.select_prefill(qi, ki, B, k, rows=rows, want_score=True)
         np.testing.assert_array_equal(sel_p[:, 0], sel_d[:, s])
         np.testing.assert_array_equal(sc_p[:, 0], sc_d[:, s])
+        bs_p = oracle.block_scores_prefill(qi, ki, B, rows=rows)
+        npg = (n + B - 1) // B
+        np.testing.assert_array_equal(bs_p[:, 0], bs_d[:, s, :npg])
+        assert (bs_d[:, s, npg:] == -np.inf).all()
         o_p, lse_p = oracle.attn_prefill(q, kk, vv, sel_p, B, k, 0.25, rows=rows)
         np.testing.assert_allclose(o_p[0], o_d[s], rtol=0, atol=1e-13)
         np.testing.assert_allclose(lse_p[:, 0], lse_d[:, s], rtol=0, atol=1e-13)

@@ -169,21 +169,21 @@ KERNEL_SOURCES = {
 }
 NCU_TRAFFIC = {
     # prefill L=32768, 64/4 heads, k=16 (profiles/dram_prefill_L32K_decode_b64.md)
-    "attention": {"bytes_per_launch": 11535790592, "workload": "prefill_L32K@32768",
+    "attention": {"bytes_per_launch": 11520171776, "workload": "prefill_L32K@32768",
                   "sources_sha256": "e5197b3f399b103129f1599695e311f5265ba10c8e86aa1b2afe56ddb1456a55"},
-    "combine": {"bytes_per_launch": 9195154176, "workload": "prefill_L32K@32768",
+    "combine": {"bytes_per_launch": 9194800896, "workload": "prefill_L32K@32768",
                 "sources_sha256": "e5197b3f399b103129f1599695e311f5265ba10c8e86aa1b2afe56ddb1456a55"},
-    "index": {"bytes_per_launch": 41901568, "workload": "prefill_L32K@32768",
-              "sources_sha256": "309806ea3e1382b034cfa7653a37b3419fd33cb090802446c196888ded88de12"},
-    "index_e4m3": {"bytes_per_launch": 20994304, "workload": "prefill_L32K@32768",
-                   "sources_sha256": "309806ea3e1382b034cfa7653a37b3419fd33cb090802446c196888ded88de12"},
+    "index": {"bytes_per_launch": 41903616, "workload": "prefill_L32K@32768",
+              "sources_sha256": "549e86cc1e19b86d0fd21c929853b80722a68fa8fe9701ae39a3cc23b5248ac2"},
+    "index_e4m3": {"bytes_per_launch": 21018283, "workload": "prefill_L32K@32768",
+                   "sources_sha256": "549e86cc1e19b86d0fd21c929853b80722a68fa8fe9701ae39a3cc23b5248ac2"},
     # decode, 64 sequences of 16K-256K tokens
-    "decode_scan": {"bytes_per_launch": 2084630016,
+    "decode_scan": {"bytes_per_launch": 2084858880,
                     "workload": "decode_b64_16K_256K@64x262144",
-                    "sources_sha256": "fe02b7dd37fa4eb7898e1bb8b2c816e4e8afe589294aa997d720326240227ab1"},
-    "decode_scan_e4m3": {"bytes_per_launch": 1044207872,
+                    "sources_sha256": "dac618d1eddf570b7d04faeac74cab4a1eaa454df93f12722ccc6bcf103222ad"},
+    "decode_scan_e4m3": {"bytes_per_launch": 1044214869,
                          "workload": "decode_b64_16K_256K@64x262144",
-                         "sources_sha256": "fe02b7dd37fa4eb7898e1bb8b2c816e4e8afe589294aa997d720326240227ab1"},
+                         "sources_sha256": "dac618d1eddf570b7d04faeac74cab4a1eaa454df93f12722ccc6bcf103222ad"},
 }
 
 

@@ -110,3 +110,16 @@ def test_empty_inputs_return_before_any_gpu_work(lib):
                                None) == msa.MSA_OK
     assert lib.msa_index_select(ctypes.byref(cfg), p, None, 0, ctypes.byref(paged), p, None, p,
                                 msa.msa_index_select_workspace(cfg, 0, 0, paged), None) == msa.MSA_OK
+
+
+def test_block_scores_output_is_checked_before_any_call():
+    """The binding rejects a block_scores buffer of the wrong shape or type before it reaches the
+    library (no device work is enqueued)."""
+    import torch
+    import block_sparse_long_msa_gb300 as msa
+    cfg = msa.config(4, 16, 16)
+    q_idx = torch.zeros(300, 4, 128, dtype=torch.bfloat16)
+    k_idx = torch.zeros(300, 128, dtype=torch.bfloat16)
+    for bad in (torch.zeros(4, 300, 2), torch.zeros(4, 300, 3, dtype=torch.float64)):
+        with pytest.raises(msa.MsaError):
+            msa.msa_index_select_scores(cfg, q_idx, k_idx, block_scores=bad)

@@ -11,6 +11,7 @@ the 64-sequence workload (reported under "decode").  Prints ONE JSON line (rank 
   e2e                    the same step through the public API from pinned host buffers
   e4m3_index             the index kernels timed again with e4m3 index vectors (same selections)
   index_scores           the index kernels timed again exporting every block's pooled score
+  cuda_graph             the small prefill pass eager against a CUDA-graph replay of the same calls
   cpu_baseline           the CPU oracle on a bounded sample, on this host's cores
 
 The path has no exchange step, so N > 1 runs N independent replicas (one per GPU, weak scaling)
@@ -55,6 +56,8 @@ def parse():
                    help="skip timing the e4m3 (FP8) index kernels beside the bf16 step")
     p.add_argument("--no-index-scores", action="store_true",
                    help="skip timing the index kernels with the block-score export")
+    p.add_argument("--no-graph", action="store_true",
+                   help="skip timing the small prefill pass as a CUDA-graph replay")
     p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--L", type=int, default=0, help="override the workload length (profiling)")
     return p.parse_args()
@@ -547,6 +550,64 @@ def run_msa(args, world, rank):
         }
         del bs, dbs
 
+    # ---- the L = 2,048 prefill pass (launch-bound: eight short kernels) eager and as a replay of
+    # a CUDA graph captured from the same calls (the library enqueues only, so it captures) ----
+    graph = None
+    if not args.no_graph:
+        tw = synthetic.WORKLOADS["tiny_L2048"]
+        tinp = synthetic.prefill_inputs(tw, device=dev)
+        tcfg = msa.config(tw.G, tw.hpg, tw.k, tw.scale)
+        tws_i = torch.zeros(msa.msa_index_select_workspace(tcfg, tw.L, tw.L), dtype=torch.uint8,
+                            device=dev)
+        tws_a = torch.zeros(msa.msa_attn_prefill_workspace(tcfg, tw.L), dtype=torch.uint8,
+                            device=dev)
+        tsel = torch.empty((tw.G, tw.L, tw.k), dtype=torch.int32, device=dev)
+        to = torch.empty_like(tinp["q"])
+        tlse = torch.empty((tw.Hq, tw.L), dtype=torch.float32, device=dev)
+
+        def tiny_pass():
+            msa.msa_index_select(tcfg, tinp["q_idx"], tinp["k_idx"], sel=tsel, ws=tws_i)
+            msa.msa_attn_prefill(tcfg, tinp["q"], tinp["k"], tinp["v"], tsel, o=to, lse=tlse,
+                                 ws=tws_a)
+
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for _ in range(3):
+                tiny_pass()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        cg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(cg):
+            tiny_pass()
+        ntiny = 50
+
+        def timed_cur(fn):
+            for _ in range(3):
+                fn()
+            a0, a1 = ev(), ev()
+            torch.cuda.synchronize()
+            a0.record()
+            for _ in range(ntiny):
+                fn()
+            a1.record()
+            torch.cuda.synchronize()
+            return a0.elapsed_time(a1) / ntiny
+
+        eager_ms = timed_cur(tiny_pass)
+        graph_ms = timed_cur(cg.replay)
+        graph = {
+            "workload": tw.name, "L": tw.L,
+            "note": "index select + main branch of the small workload, back to back (inputs of "
+                    "8 MiB stay in L2); eager calls against a replay of a CUDA graph captured "
+                    "from the same calls",
+            "eager_ms": eager_ms, "graph_ms": graph_ms,
+            "tokens_per_s_eager": tw.L / (eager_ms * 1e-3),
+            "tokens_per_s_graph": tw.L / (graph_ms * 1e-3),
+            "launches_per_pass": 1 + msa.msa_attn_prefill_launches(tcfg, tw.L),
+        }
+        del cg
+
     cpu_base = None
     dec_cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -630,6 +691,7 @@ def run_msa(args, world, rank):
     line["decode"]["cpu_baseline"] = dec_cpu
     line["e4m3_index"] = e4m3
     line["index_scores"] = scores
+    line["cuda_graph"] = graph
     if rank == 0:
         print(json.dumps(line), flush=True)
 

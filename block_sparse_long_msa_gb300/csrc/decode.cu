@@ -333,8 +333,10 @@ __global__ void __launch_bounds__(256, 1)
 }
 
 // ------------------------------------------------------------------------------------------
-// Top-k: one warp per (sequence, group).  Lane l streams blocks l, l+32, ... (ascending, so the
-// strict rank test keeps the tie rule), then k-1 rounds of a warp arg-max pop the winners.
+// Top-k: one CTA of four warps per (sequence, group).  Lane l of warp w streams blocks
+// 32w + l, 32w + l + 128, ... into its own rank-ordered list; k-1 rounds of a warp arg-max pop
+// each warp's best into shared memory, and warp 0 merges the four lists the same way.  Ranking
+// compares (score, block id), so the order in which candidates arrive does not matter.
 // ------------------------------------------------------------------------------------------
 struct TopkArgs {
   const float4* scores;
@@ -348,40 +350,40 @@ struct TopkArgs {
 };
 
 __global__ void __launch_bounds__(128) decode_topk_kernel(TopkArgs a) {
-  const int wg = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-  if (wg >= a.batch * a.G) return;
-  const int s = wg / a.G, g = wg % a.G;
+  __shared__ float cand_s[4][kListMax];
+  __shared__ int32_t cand_b[4][kListMax];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int s = blockIdx.x / a.G, g = blockIdx.x % a.G;  // grid = batch * G
   const int n = a.seq_lens[s];
   int32_t* out = a.sel + (static_cast<size_t>(g) * a.batch + s) * a.k;
   float* out_s = a.sel_score ? a.sel_score + (static_cast<size_t>(g) * a.batch + s) * a.k : nullptr;
-  if (n <= 0 || (n - 1) / kBlock >= a.max_pages) {
-    if (lane == 0) report_status(a.status, kStatusBounds);
-    for (int r = lane; r < a.k; r += 32) {
-      out[r] = -1;
-      if (out_s) out_s[r] = -__int_as_float(0x7f800000);
-    }
-    if (a.block_scores)
-      for (int b = lane; b < a.max_pages; b += 32)
-        a.block_scores[(static_cast<size_t>(g) * a.batch + s) * a.max_pages + b] =
-            -__int_as_float(0x7f800000);
-    return;
-  }
-  const int bi = (n - 1) / kBlock;
-  TopList list;
-  list.clear();
   float* bsrow = a.block_scores
                      ? a.block_scores + (static_cast<size_t>(g) * a.batch + s) * a.max_pages
                      : nullptr;
+  const float ninf = -__int_as_float(0x7f800000), pinf = __int_as_float(0x7f800000);
+  if (n <= 0 || (n - 1) / kBlock >= a.max_pages) {  // the same outcome for the whole CTA
+    if (threadIdx.x == 0) report_status(a.status, kStatusBounds);
+    if (warp == 0)
+      for (int r = lane; r < a.k; r += 32) {
+        out[r] = -1;
+        if (out_s) out_s[r] = ninf;
+      }
+    if (bsrow)
+      for (int b = threadIdx.x; b < a.max_pages; b += 128) bsrow[b] = ninf;
+    return;
+  }
+  const int bi = (n - 1) / kBlock;
   if (bsrow)  // the local block is never scored; later blocks are not causal
-    for (int b = bi + lane; b < a.max_pages; b += 32)
-      bsrow[b] = b == bi ? __int_as_float(0x7f800000) : -__int_as_float(0x7f800000);
+    for (int b = bi + threadIdx.x; b < a.max_pages; b += 128) bsrow[b] = b == bi ? pinf : ninf;
   const float4* row = a.scores + (static_cast<size_t>(s) * a.G + g) * a.max_pages;
-  // eight loads in flight per lane, then eight inserts (blocks stay ascending per lane)
-  for (int b0 = 0; b0 < bi; b0 += 8 * 32) {
+  TopList list;
+  list.clear();
+  // eight loads in flight per lane, then eight inserts
+  for (int b0 = warp * 32; b0 < bi; b0 += 8 * 128) {
     float sc[8];
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
-      const int b = b0 + q * 32 + lane;
+      const int b = b0 + q * 128 + lane;
       if (b < bi) {
         const float4 v = row[b];
         sc[q] = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
@@ -389,7 +391,7 @@ __global__ void __launch_bounds__(128) decode_topk_kernel(TopkArgs a) {
     }
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
-      const int b = b0 + q * 32 + lane;
+      const int b = b0 + q * 128 + lane;
       if (b < bi) {
         list.insert(sc[q], b);
         if (bsrow) bsrow[b] = sc[q];
@@ -397,11 +399,11 @@ __global__ void __launch_bounds__(128) decode_topk_kernel(TopkArgs a) {
     }
   }
   const int take = min(a.k - 1, bi);
-  int my_id = 0x7fffffff;
-  float my_sc = 0.f;
-  for (int r = 0; r < take; ++r) {
-    float bs = list.s[0];
-    int bb = list.b[0];
+  // r-th round: the warp's r-th best (score, block) reaches every lane; its owner pops it.
+  // Empty entries (-inf, INT_MAX) rank last, so a warp with fewer blocks pads with them.
+  auto pop_best = [&](float& bs, int& bb) {
+    bs = list.s[0];
+    bb = list.b[0];
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       const float os = __shfl_xor_sync(0xffffffffu, bs, o);
@@ -411,15 +413,36 @@ __global__ void __launch_bounds__(128) decode_topk_kernel(TopkArgs a) {
         bb = ob;
       }
     }
-    if (list.b[0] == bb) {  // the winner pops its head (block ids are unique)
+    if (list.b[0] == bb) {
 #pragma unroll
       for (int q = 0; q + 1 < kListMax; ++q) {
         list.s[q] = list.s[q + 1];
         list.b[q] = list.b[q + 1];
       }
-      list.s[kListMax - 1] = -__int_as_float(0x7f800000);
+      list.s[kListMax - 1] = ninf;
       list.b[kListMax - 1] = 0x7fffffff;
     }
+  };
+  for (int r = 0; r < take; ++r) {
+    float bs;
+    int bb;
+    pop_best(bs, bb);
+    if (lane == 0) {
+      cand_s[warp][r] = bs;
+      cand_b[warp][r] = bb;
+    }
+  }
+  __syncthreads();
+  if (warp != 0) return;
+  list.clear();
+  for (int c = lane; c < 4 * take; c += 32)
+    list.insert(cand_s[c / take][c % take], cand_b[c / take][c % take]);
+  int my_id = 0x7fffffff;
+  float my_sc = 0.f;
+  for (int r = 0; r < take; ++r) {
+    float bs;
+    int bb;
+    pop_best(bs, bb);
     if (lane == r) {
       my_id = bb;
       my_sc = bs;
@@ -437,7 +460,7 @@ __global__ void __launch_bounds__(128) decode_topk_kernel(TopkArgs a) {
   }
   for (int r = take + lane; r < a.k; r += 32) {
     out[r] = r == take ? bi : -1;
-    if (out_s) out_s[r] = r == take ? __int_as_float(0x7f800000) : -__int_as_float(0x7f800000);
+    if (out_s) out_s[r] = r == take ? pinf : ninf;
   }
 }
 
@@ -812,7 +835,7 @@ cudaError_t launch_decode_select(const CUtensorMap& map_k, const CUtensorMap& ma
   t.sel_score = sel_score;
   t.block_scores = block_scores;
   t.status = status;
-  decode_topk_kernel<<<(batch * G * 32 + 127) / 128, 128, 0, stream>>>(t);
+  decode_topk_kernel<<<batch * G, 128, 0, stream>>>(t);
   return cudaGetLastError();
 }
 

@@ -16,7 +16,7 @@
 //                   repeated gathers of each query for its k blocks.
 //   5. sched_fill   per (group, query block): every (token, slot) lands at its place, lists stay
 //                   in ascending token order (deterministic, no global atomics)
-//   6. attn_kv_outer persistent tcgen05 kernel over work items (see below)
+//   6. attn_kv_outer persistent tcgen05 kernel over work items, taken from a counter (below)
 //   7. combine      per (token, group): fixed slot order, LSE-weighted merge
 #include <algorithm>
 
@@ -184,7 +184,10 @@ __global__ void __launch_bounds__(1024) sched_bases_kernel(SchedArgs a) {
   const int total = block_exclusive_scan(
       a.nr * a.G * a.nbk, [rcnt](int i) { return items_of(rcnt[i]); }, a.item_base, warp_sums,
       &carry);
-  if (threadIdx.x == 0) *a.n_items = total;
+  if (threadIdx.x == 0) {
+    *a.n_items = total;
+    a.n_items[1] = 0;  // the attention kernel's work counter
+  }
 }
 
 __global__ void sched_items_kernel(SchedArgs a) {
@@ -225,7 +228,9 @@ __global__ void sched_fill_kernel(SchedArgs a) {
 }
 
 // ------------------------------------------------------------------------------------------
-// KV-outer attention.  One persistent CTA per SM walks its work items; per item it stages K_b
+// KV-outer attention.  One persistent CTA per SM takes work items from a global counter as it
+// has room for the next one (items of uneven size then even out across SMs; taken in order,
+// they keep the query-range order that L2 relies on); per item it stages K_b
 // and V_b of group g (TMA; V converted to fp16 in place) and the item's token list, then for
 // every tile of 8 tokens gathers their 16 query heads (TMA, 16 rows per token) and runs
 //   S = Q K^T (tcgen05, fp32 in TMEM) -> softmax rows (causal limit only in the local block)
@@ -246,6 +251,7 @@ __global__ void sched_fill_kernel(SchedArgs a) {
 struct AttnArgs {
   const int4* items;
   const int32_t* n_items;
+  int32_t* next_item;     // work counter: each CTA takes the next item when it has room
   const int32_t* list;
   int32_t G, k, q0;
   float scale_log2;       // softmax scale * log2(e)
@@ -381,7 +387,7 @@ __global__ void __launch_bounds__(512, 1)
     int T = 0, q_issued = 0;
     bool ok = true;
     if (lane == 0) tma_prefetch_map(&map_q);
-    for (int it = blockIdx.x, n = 0; ok && it < n_items; it += gridDim.x, ++n) {
+    for (int n = 0; ok; ++n) {
       const int r = n % kMetaRing;
       if (!__all_sync(0xffffffffu, !*abort_flag && mbar_wait(meta_empty(r),
                                                              ((n / kMetaRing) & 1) ^ 1,
@@ -389,8 +395,18 @@ __global__ void __launch_bounds__(512, 1)
         ok = false;
         break;
       }
-      const int4 item = a.items[it];
+      int it = 0;
+      if (lane == 0) it = atomicAdd(a.next_item, 1);
+      it = __shfl_sync(0xffffffffu, it, 0);
       ItemMeta& m = meta[r];
+      if (it >= n_items) {  // no work left: an end marker for the other roles
+        if (lane == 0) {
+          m.count = -1;
+          mbar_arrive(meta_full(r));
+        }
+        break;
+      }
+      const int4 item = a.items[it];
       for (int j = lane; j < item.w; j += 32) m.tok[j] = a.list[item.z + j];
       if (lane == 0) {
         m.g = item.x;
@@ -436,14 +452,18 @@ __global__ void __launch_bounds__(512, 1)
     if (lane == 0) {
       bool ok = true;
       int T = 0;
-      for (int it = blockIdx.x, n = 0; ok && it < n_items; it += gridDim.x, ++n) {
+      for (int n = 0; ok; ++n) {
         const int r = n % kMetaRing;
-        if (*abort_flag || !mbar_wait(meta_full(r), (n / kMetaRing) & 1, a.wait_ns) ||
-            !mbar_wait(k_full, n & 1, a.wait_ns)) {
+        if (*abort_flag || !mbar_wait(meta_full(r), (n / kMetaRing) & 1, a.wait_ns)) {
           ok = false;
           break;
         }
         const int cnt = meta[r].count;
+        if (cnt < 0) break;
+        if (!mbar_wait(k_full, n & 1, a.wait_ns)) {
+          ok = false;
+          break;
+        }
         for (int t0 = 0; t0 < cnt; t0 += kTileTokens, ++T) {
           const int qs = T % kQStages, s3 = T % 3;
           // S(T) reuses the S/P slot of tile T-3: in-order issue keeps the parities unambiguous
@@ -478,24 +498,27 @@ __global__ void __launch_bounds__(512, 1)
     // --------------------- K loader + O = P V issuer (polling) ---------------------
     if (lane == 0) {
       tma_prefetch_map(&map_k);
-      const int n_mine = n_items > static_cast<int>(blockIdx.x)
-                             ? (n_items - 1 - static_cast<int>(blockIdx.x)) / gridDim.x + 1
-                             : 0;
+      int n_mine = 0x7fffffff;  // items of this CTA, known at the end marker
       int nk = 0;                        // items whose K has been requested
       int b_n = 0, b_cnt = -1, b_t0 = 0, b_T = 0;  // P.V cursor
       bool ok = true, idle = false;
       uint64_t idle_since = 0;
       while (ok && (nk < n_mine || b_n < n_mine)) {
         bool progressed = false;
-        if (nk < n_mine && mbar_test_wait(meta_full(nk % kMetaRing), (nk / kMetaRing) & 1) &&
-            mbar_test_wait(k_empty, (nk & 1) ^ 1)) {
+        // one test of the item's barrier decides both cases: the end marker, or a K to load
+        if (nk < n_mine && mbar_test_wait(meta_full(nk % kMetaRing), (nk / kMetaRing) & 1)) {
           const int r = nk % kMetaRing;
-          const int g = meta[r].g, b = meta[r].b;
-          mbar_arrive_expect_tx(k_full, 32768);
-          tma_load_3d(base + kSmemK, &map_k, k_full, 0, g, b * kBlock);
-          tma_load_3d(base + kSmemK + kPanel, &map_k, k_full, 64, g, b * kBlock);
-          ++nk;
-          progressed = true;
+          if (meta[r].count < 0) {
+            n_mine = nk;
+            progressed = true;
+          } else if (mbar_test_wait(k_empty, (nk & 1) ^ 1)) {
+            const int g = meta[r].g, b = meta[r].b;
+            mbar_arrive_expect_tx(k_full, 32768);
+            tma_load_3d(base + kSmemK, &map_k, k_full, 0, g, b * kBlock);
+            tma_load_3d(base + kSmemK + kPanel, &map_k, k_full, 64, g, b * kBlock);
+            ++nk;
+            progressed = true;
+          }
         }
         if (b_n < n_mine) {
           if (b_cnt < 0 && mbar_test_wait(v_ready, b_n & 1)) {  // V of item b_n converted
@@ -550,11 +573,15 @@ __global__ void __launch_bounds__(512, 1)
     if (lane == 0) tma_prefetch_map(&map_v);
     int issued = 0;
     bool ok = true;
-    for (int it = blockIdx.x, n = 0; it < n_items; it += gridDim.x, ++n) {
+    for (int n = 0;; ++n) {
       const int r = n % kMetaRing;
-      const bool okw = !*abort_flag && mbar_wait(meta_full(r), (n / kMetaRing) & 1, a.wait_ns) &&
-                       mbar_wait(v_empty, (n & 1) ^ 1, a.wait_ns);
-      if (!__all_sync(0xffffffffu, okw)) {
+      if (!__all_sync(0xffffffffu, !*abort_flag && mbar_wait(meta_full(r), (n / kMetaRing) & 1,
+                                                             a.wait_ns))) {
+        ok = false;
+        break;
+      }
+      if (meta[r].count < 0) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(v_empty, (n & 1) ^ 1, a.wait_ns))) {
         ok = false;
         break;
       }
@@ -595,13 +622,14 @@ __global__ void __launch_bounds__(512, 1)
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     int T = 0;
     bool ok = true;
-    for (int it = blockIdx.x, n = 0; ok && it < n_items; it += gridDim.x, ++n) {
+    for (int n = 0; ok; ++n) {
       const int r = n % kMetaRing;
       if (!__all_sync(0xffffffffu, mbar_wait(meta_full(r), (n / kMetaRing) & 1, a.wait_ns))) {
         ok = false;
         break;
       }
       const ItemMeta& m = meta[r];
+      if (m.count < 0) break;
       const int count = m.count, b = m.b;
       for (int t0 = 0; t0 < count; t0 += kTileTokens, ++T) {
         if ((T & 1) != wg) continue;
@@ -698,14 +726,16 @@ __global__ void __launch_bounds__(512, 1)
     }
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     int T = 0;
-    for (int it = blockIdx.x, n = 0; it < n_items; it += gridDim.x, ++n) {
+    for (int n = 0;; ++n) {
       const int r = n % kMetaRing;
       const bool okm = !*abort_flag && mbar_wait(meta_full(r), (n / kMetaRing) & 1, a.wait_ns);
       if (!__all_sync(0xffffffffu, okm)) {
         report_status(a.status, kStatusTimeout);
         *abort_flag = 1;
+        break;
       }
       const ItemMeta& m = meta[r];
+      if (m.count < 0) break;
       const int count = min(max(m.count, 0), kItemTokens);
       for (int t0 = 0; t0 < count; t0 += kTileTokens, ++T) {
         const bool oko = !*abort_flag && mbar_wait(o_full, T & 1, a.wait_ns);
@@ -929,6 +959,7 @@ cudaError_t launch_attn_prefill_chunk(const CUtensorMap& map_q, const CUtensorMa
   AttnArgs a{};
   a.items = s.items;
   a.n_items = s.n_items;
+  a.next_item = s.n_items + 1;
   a.list = s.list;
   a.G = G;
   a.k = k;

@@ -172,21 +172,21 @@ KERNEL_SOURCES = {
 }
 NCU_TRAFFIC = {
     # prefill L=32768, 64/4 heads, k=16 (profiles/dram_prefill_L32K_decode_b64.md)
-    "attention": {"bytes_per_launch": 11520171776, "workload": "prefill_L32K@32768",
-                  "sources_sha256": "e5197b3f399b103129f1599695e311f5265ba10c8e86aa1b2afe56ddb1456a55"},
-    "combine": {"bytes_per_launch": 9194800896, "workload": "prefill_L32K@32768",
-                "sources_sha256": "e5197b3f399b103129f1599695e311f5265ba10c8e86aa1b2afe56ddb1456a55"},
+    "attention": {"bytes_per_launch": 9829865472, "workload": "prefill_L32K@32768",
+                  "sources_sha256": "ba3257374b6348a8e0954b69f2bd5aed57c2d637c3b05ef0ce2023073755132f"},
+    "combine": {"bytes_per_launch": 9195437824, "workload": "prefill_L32K@32768",
+                "sources_sha256": "ba3257374b6348a8e0954b69f2bd5aed57c2d637c3b05ef0ce2023073755132f"},
     "index": {"bytes_per_launch": 41903616, "workload": "prefill_L32K@32768",
               "sources_sha256": "549e86cc1e19b86d0fd21c929853b80722a68fa8fe9701ae39a3cc23b5248ac2"},
-    "index_e4m3": {"bytes_per_launch": 21018283, "workload": "prefill_L32K@32768",
+    "index_e4m3": {"bytes_per_launch": 21011413, "workload": "prefill_L32K@32768",
                    "sources_sha256": "549e86cc1e19b86d0fd21c929853b80722a68fa8fe9701ae39a3cc23b5248ac2"},
     # decode, 64 sequences of 16K-256K tokens
-    "decode_scan": {"bytes_per_launch": 2084858880,
+    "decode_scan": {"bytes_per_launch": 2084700160,
                     "workload": "decode_b64_16K_256K@64x262144",
-                    "sources_sha256": "dac618d1eddf570b7d04faeac74cab4a1eaa454df93f12722ccc6bcf103222ad"},
-    "decode_scan_e4m3": {"bytes_per_launch": 1044214869,
+                    "sources_sha256": "994ce2153b759ea1038980cc54121fca1a7ce5a247759beee4807547bab49afc"},
+    "decode_scan_e4m3": {"bytes_per_launch": 1044300331,
                          "workload": "decode_b64_16K_256K@64x262144",
-                         "sources_sha256": "dac618d1eddf570b7d04faeac74cab4a1eaa454df93f12722ccc6bcf103222ad"},
+                         "sources_sha256": "994ce2153b759ea1038980cc54121fca1a7ce5a247759beee4807547bab49afc"},
 }
 
 

@@ -438,3 +438,6 @@ def test_e4m3_selection_equals_bf16_selection(L, G, k, seed):
     sa, ca = oracle.select_prefill(a["q_idx"], a["k_idx"], w.B, k, want_score=True)
     sb, cb = oracle.select_prefill(b["q_idx"], b["k_idx"], w.B, k, want_score=True)
     assert np.array_equal(sa, sb) and np.array_equal(ca, cb)
+    rows = np.array([0, w.B - 1, w.B, L // 2, L - 1], np.int64)
+    assert np.array_equal(oracle.block_scores_prefill(a["q_idx"], a["k_idx"], w.B, rows=rows),
+                          oracle.block_scores_prefill(b["q_idx"], b["k_idx"], w.B, rows=rows))

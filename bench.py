@@ -172,10 +172,10 @@ KERNEL_SOURCES = {
 }
 NCU_TRAFFIC = {
     # prefill L=32768, 64/4 heads, k=16 (profiles/dram_prefill_L32K_decode_b64.md)
-    "attention": {"bytes_per_launch": 9829865472, "workload": "prefill_L32K@32768",
-                  "sources_sha256": "ba3257374b6348a8e0954b69f2bd5aed57c2d637c3b05ef0ce2023073755132f"},
-    "combine": {"bytes_per_launch": 9195437824, "workload": "prefill_L32K@32768",
-                "sources_sha256": "ba3257374b6348a8e0954b69f2bd5aed57c2d637c3b05ef0ce2023073755132f"},
+    "attention": {"bytes_per_launch": 9828836096, "workload": "prefill_L32K@32768",
+                  "sources_sha256": "7d4d5adc609b717953302cb6c3fc4d49f754da7eae7cf3f27036282b37e8205c"},
+    "combine": {"bytes_per_launch": 9194790912, "workload": "prefill_L32K@32768",
+                "sources_sha256": "7d4d5adc609b717953302cb6c3fc4d49f754da7eae7cf3f27036282b37e8205c"},
     "index": {"bytes_per_launch": 41903616, "workload": "prefill_L32K@32768",
               "sources_sha256": "549e86cc1e19b86d0fd21c929853b80722a68fa8fe9701ae39a3cc23b5248ac2"},
     "index_e4m3": {"bytes_per_launch": 21011413, "workload": "prefill_L32K@32768",

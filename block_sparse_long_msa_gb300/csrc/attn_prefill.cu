@@ -630,7 +630,9 @@ __global__ void __launch_bounds__(512, 1)
       }
       const ItemMeta& m = meta[r];
       if (m.count < 0) break;
-      const int count = m.count, b = m.b;
+      // read before this warpgroup's last arrival on the item: once every P of the item is
+      // consumed the epilogue can finish it and the ring slot be refilled
+      const int count = m.count, b = m.b, start = m.start;
       for (int t0 = 0; t0 < count; t0 += kTileTokens, ++T) {
         if ((T & 1) != wg) continue;
         const int s3 = T % 3;
@@ -699,7 +701,7 @@ __global__ void __launch_bounds__(512, 1)
         tc_fence_before();
         mbar_arrive(p_full(s3 * 2 + wg));
         if (valid) {
-          const size_t p = static_cast<size_t>(m.start) + t0 + tk;  // list position
+          const size_t p = static_cast<size_t>(start) + t0 + tk;  // list position
           const float ln2 = 0.6931471805599453f;
           a.pm[p * kHeadsPerGroup + hh] = m2 * ln2;
           a.plse[p * kHeadsPerGroup + hh] = (m2 + __log2f(l)) * ln2;

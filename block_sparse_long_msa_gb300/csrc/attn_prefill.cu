@@ -351,7 +351,10 @@ __global__ void __launch_bounds__(512, 1)
   if (threadIdx.x == 0) {
     for (int r = 0; r < kMetaRing; ++r) {
       mbar_init(meta_full(r), 1);
-      mbar_init(meta_empty(r), 128);
+      // the epilogue's 128 threads when the item is finished, and one arrival from each of the
+      // eight softmax warps once it has copied the item's fields (a warpgroup may own no tile of
+      // an item, and nothing else would keep the slot from being refilled under its reads)
+      mbar_init(meta_empty(r), 128 + 8);
     }
     mbar_init(k_full, 1);
     mbar_init(k_empty, 1);
@@ -630,9 +633,12 @@ __global__ void __launch_bounds__(512, 1)
       }
       const ItemMeta& m = meta[r];
       if (m.count < 0) break;
-      // read before this warpgroup's last arrival on the item: once every P of the item is
-      // consumed the epilogue can finish it and the ring slot be refilled
+      // the slot is refilled only after every softmax warp has copied these fields (its arrival
+      // below) and the epilogue has finished the item; the token ids of a tile are read before
+      // the tile's P is released, so the item cannot be finished under those reads
       const int count = m.count, b = m.b, start = m.start;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(meta_empty(r));
       for (int t0 = 0; t0 < count; t0 += kTileTokens, ++T) {
         if ((T & 1) != wg) continue;
         const int s3 = T % 3;

@@ -23,21 +23,27 @@ static __device__ __align__(256) uint8_t g_noalloc_scratch[kScratchBytes];
 namespace {
 
 struct DeviceScratch {
-  std::once_flag once;
-  void* ptr = nullptr;
-  cudaError_t err = cudaSuccess;
+  std::mutex mu;
+  void* ptr = nullptr;  // set once the lookup has succeeded on this device
 };
 DeviceScratch g_scratch[kMaxDevices];
 
 // Set-up, once per device, with that device current: the device address of the scratch array.
+// Only a successful lookup is kept; a failed one (for example made while the stream was being
+// captured) clears the runtime's last error and is tried again by the next call.
 void* scratch_on_current_device() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
   DeviceScratch& s = g_scratch[dev];
-  std::call_once(s.once, [&s] {
-    s.err = cudaGetSymbolAddress(&s.ptr, g_noalloc_scratch);
-    if (s.err != cudaSuccess) s.ptr = nullptr;
-  });
+  std::lock_guard<std::mutex> lock(s.mu);
+  if (!s.ptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) == cudaSuccess) {
+      s.ptr = p;
+    } else {
+      (void)cudaGetLastError();
+    }
+  }
   return s.ptr;
 }
 

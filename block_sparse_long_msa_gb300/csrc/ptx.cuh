@@ -69,18 +69,6 @@ __device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t par
       : "memory");
   return ok != 0;
 }
-// Wait for the phase with the given parity to complete; gives up after limit_ns of wall time.
-// Waiting threads are suspended rather than spinning, so they leave the issue slots of their
-// SM sub-partition to the warps doing work.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  while (true) {
-    if (mbar_try_wait_suspend(bar, parity, 100000u)) return true;
-    if (globaltimer_ns() - t0 > limit_ns) return false;
-  }
-}
-
 // Non-blocking test of the phase with the given parity (try_wait may suspend the thread for a
 // while; a polling loop that watches several barriers must not).
 __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
@@ -94,6 +82,27 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+
+// Wait for the phase with the given parity to complete; gives up after limit_ns of wall time.
+// Waiting threads are suspended rather than spinning, so they leave the issue slots of their
+// SM sub-partition to the warps doing work.  A limit under 100 us is kept to closely instead:
+// try_wait may suspend the thread for a time of the hardware's choosing, so such a wait polls
+// with test_wait.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  if (limit_ns < 100000u) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_test_wait(bar, parity))
+      if (globaltimer_ns() - t0 > limit_ns) return false;
+    return true;
+  }
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait_suspend(bar, parity, 100000u)) return true;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
+}
+
 
 // max(a, b, c) in one instruction (three-input max.f32, sm_100 family); a NaN operand is
 // ignored as in fmaxf.
@@ -352,6 +361,45 @@ __device__ __forceinline__ void mma_m16n8k16_bf16(float (&d)[4], const uint32_t 
       "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// The same with fp16 inputs.
+__device__ __forceinline__ void mma_m16n8k16_f16(float (&d)[4], const uint32_t (&a)[4],
+                                                 uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_shared_v2(uint32_t addr, uint32_t a, uint32_t b) {
+  asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
+}
+// Four e4m3 values (bytes of w, lowest first) -> two fp16 pairs, exactly (every e4m3 value is
+// an fp16 value).
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 a, b;\n\t"
+      "mov.b32 {a, b}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, a;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+// Two fp16 -> two bf16, exact for values of at most 8 significant bits inside bf16's range
+// (such as the e4m3 values).
+__device__ __forceinline__ uint32_t f16x2_to_bf16x2(uint32_t h) {
+  float lo, hi;
+  asm("{\n\t.reg .b16 l, h;\n\t"
+      "mov.b32 {l, h}, %2;\n\t"
+      "cvt.f32.f16 %0, l;\n\t"
+      "cvt.f32.f16 %1, h;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(h));
+  return pack_bf16x2(lo, hi);
 }
 __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t (&r)[4]) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"

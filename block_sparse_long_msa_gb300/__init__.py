@@ -18,6 +18,7 @@ MSA_ERR_CUDA, MSA_ERR_DEVICE_TIMEOUT, MSA_ERR_DEVICE_BOUNDS = 4, 5, 6
 WS_HEADER_BYTES = 256
 
 EXPORTS = ("msa_index_select_workspace", "msa_index_select", "msa_index_select_scores",
+           "msa_index_candidates", "msa_index_merge",
            "msa_attn_prefill_workspace",
            "msa_attn_prefill", "msa_attn_prefill_marked", "msa_prefill_chunk_tokens",
            "msa_attn_prefill_launches",
@@ -38,7 +39,7 @@ class MsaPagedKV(ctypes.Structure):
                 ("v_pool", ctypes.c_void_p), ("page_table", ctypes.c_void_p),
                 ("seq_lens", ctypes.c_void_p), ("batch", ctypes.c_int32),
                 ("max_pages", ctypes.c_int32), ("num_pages", ctypes.c_int32),
-                ("reserved", ctypes.c_int32)]
+                ("kv_dtype", ctypes.c_int32)]
 
 
 class MsaError(RuntimeError):
@@ -64,6 +65,9 @@ def lib() -> ctypes.CDLL:
         L.msa_index_select_workspace.restype = sz
         L.msa_index_select.argtypes = [cfgp, P, P, i64, pagedp, P, P, P, sz, P]
         L.msa_index_select_scores.argtypes = [cfgp, P, P, i64, pagedp, P, P, P, P, sz, P]
+        L.msa_index_candidates.argtypes = [cfgp, P, P, i64, pagedp, ctypes.c_int32,
+                                           ctypes.c_int32, P, P, P, sz, P]
+        L.msa_index_merge.argtypes = [cfgp, ctypes.c_int32, P, P, i64, P, P, P, P, sz, P]
         L.msa_attn_prefill_workspace.argtypes = [cfgp, i64]
         L.msa_attn_prefill_workspace.restype = sz
         L.msa_attn_prefill.argtypes = [cfgp, P, P, P, i64, P, P, P, P, sz, P]
@@ -80,7 +84,8 @@ def lib() -> ctypes.CDLL:
         L.msa_reset_device_status.argtypes = [P, P]
         L.msa_status_string.argtypes = [ctypes.c_int]
         L.msa_status_string.restype = ctypes.c_char_p
-        for name in ("msa_index_select", "msa_index_select_scores", "msa_attn_prefill",
+        for name in ("msa_index_select", "msa_index_select_scores", "msa_index_candidates",
+                     "msa_index_merge", "msa_attn_prefill",
                      "msa_attn_prefill_marked",
                      "msa_attn_decode",
                      "msa_get_device_status", "msa_reset_device_status"):
@@ -142,11 +147,24 @@ def _workspace(nbytes: int, device, ws):
     return ws
 
 
+KV_DTYPES = {"bf16": 0, "e4m3": 1}  # msa_kv_dtype_t
+
+
 def paged_kv(k_idx_pool, k_pool, v_pool, page_table, seq_lens) -> MsaPagedKV:
+    """The paged cache; K/V pools of torch.bfloat16 or torch.float8_e4m3fn (both the same)."""
+    import torch
     batch, max_pages = page_table.shape
+    kv = 0
+    if k_pool is not None:
+        if v_pool is not None and v_pool.dtype != k_pool.dtype:
+            raise MsaError(MSA_ERR_INVALID_ARG, "k_pool and v_pool must have the same dtype")
+        if k_pool.dtype == torch.float8_e4m3fn:
+            kv = KV_DTYPES["e4m3"]
+        elif k_pool.dtype != torch.bfloat16:
+            raise MsaError(MSA_ERR_INVALID_ARG, f"K/V pools must be bf16 or e4m3, got {k_pool.dtype}")
     return MsaPagedKV(k_idx_pool.data_ptr(), k_pool.data_ptr() if k_pool is not None else None,
                       v_pool.data_ptr() if v_pool is not None else None, page_table.data_ptr(),
-                      seq_lens.data_ptr(), batch, max_pages, k_idx_pool.shape[0], 0)
+                      seq_lens.data_ptr(), batch, max_pages, k_idx_pool.shape[0], kv)
 
 
 def msa_index_select_workspace(cfg: MsaConfig, num_queries: int, num_keys: int,
@@ -200,6 +218,53 @@ def msa_index_select_scores(cfg: MsaConfig, q_idx, k_idx=None, paged: MsaPagedKV
                                        _stream(stream))
     _check(st, "msa_index_select_scores")
     return sel, block_scores
+
+
+def msa_index_candidates(cfg: MsaConfig, q_idx, k_idx=None, L: int | None = None,
+                         paged: MsaPagedKV | None = None, block_begin: int = 0,
+                         block_end: int = 1 << 30, cand_score=None, cand_block=None, ws=None,
+                         stream=None):
+    """One shard of the context-parallel index branch: the top-(k-1) (score, block) candidates
+    of key blocks [block_begin, block_end), in rank order, fp32 / int32 [G][T][k-1].
+
+    Prefill: q_idx [L][G][di] holds every query, k_idx only the shard's keys (positions
+    block_begin*128 .. ), L the whole length (default q_idx.shape[0]).  Decode: pass `paged`."""
+    import torch
+    _index_dtype_ok(cfg, q_idx, k_idx)
+    T = q_idx.shape[0]
+    if paged is None and L is None:
+        L = T
+    Lc = 0 if paged is not None else L
+    G, w = cfg.num_groups, max(cfg.topk - 1, 0)
+    if cand_score is None:
+        cand_score = torch.empty((G, T, w), dtype=torch.float32, device=q_idx.device)
+    if cand_block is None:
+        cand_block = torch.empty((G, T, w), dtype=torch.int32, device=q_idx.device)
+    ws = _workspace(msa_index_select_workspace(cfg, T, Lc, paged), q_idx.device, ws)
+    st = lib().msa_index_candidates(ctypes.byref(cfg), _ptr(q_idx), _ptr(k_idx), Lc,
+                                    ctypes.byref(paged) if paged is not None else None,
+                                    block_begin, block_end, _ptr(cand_score), _ptr(cand_block),
+                                    _ptr(ws), ws.numel(), _stream(stream))
+    _check(st, "msa_index_candidates")
+    return cand_score, cand_block
+
+
+def msa_index_merge(cfg: MsaConfig, cand_score, cand_block, seq_lens=None, sel=None,
+                    sel_score=None, want_score: bool = False, ws=None, stream=None):
+    """Selection [G][T][k] from the stacked candidates [R][G][T][k-1] of R disjoint shards.
+    seq_lens: decode context lengths [T] (None for prefill: query t at position t)."""
+    import torch
+    R, G, T, _ = cand_block.shape
+    if sel is None:
+        sel = torch.empty((G, T, cfg.topk), dtype=torch.int32, device=cand_block.device)
+    if want_score and sel_score is None:
+        sel_score = torch.empty((G, T, cfg.topk), dtype=torch.float32, device=cand_block.device)
+    ws = _workspace(WS_HEADER_BYTES, cand_block.device, ws)
+    st = lib().msa_index_merge(ctypes.byref(cfg), R, _ptr(cand_score), _ptr(cand_block), T,
+                               _ptr(seq_lens), _ptr(sel), _ptr(sel_score), _ptr(ws), ws.numel(),
+                               _stream(stream))
+    _check(st, "msa_index_merge")
+    return (sel, sel_score) if want_score else sel
 
 
 def msa_attn_prefill_workspace(cfg: MsaConfig, L: int) -> int:

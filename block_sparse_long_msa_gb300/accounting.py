@@ -47,14 +47,16 @@ def decode_index_bytes(seq_lens, B: int, di: int, G: int) -> int:
     return sum(((n - 1) // B) * B * di * 2 for n in seq_lens) + len(seq_lens) * G * di * 2
 
 
-def decode_attn_bytes(seq_lens, B: int, d: int, G: int, Hq: int, k: int) -> int:
-    """K and V of the selected blocks (whole pages, the local one up to n), plus q and o."""
+def decode_attn_bytes(seq_lens, B: int, d: int, G: int, Hq: int, k: int,
+                      kv_bytes: int = 2) -> int:
+    """K and V of the selected blocks (whole pages, the local one up to n; kv_bytes per element),
+    plus q and o (bf16)."""
     total = 0
     for n in seq_lens:
         bi = (n - 1) // B
         blocks = min(k - 1, bi)
         toks = blocks * B + (n - bi * B)
-        total += toks * G * d * 2 * 2
+        total += toks * G * d * kv_bytes * 2
     return total + len(seq_lens) * Hq * d * 2 * 2
 
 

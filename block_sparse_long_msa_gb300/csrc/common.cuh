@@ -102,4 +102,17 @@ __device__ __forceinline__ void write_sel_row(const TopList& list, int n, int32_
   }
 }
 
+// Write one candidate row of a key-block shard (context-parallel index branch): the first n
+// entries of the rank-ordered list (score desc, block asc), then (-inf, -1) up to width = k - 1.
+__device__ __forceinline__ void write_cand_row(const TopList& list, int n, int width,
+                                               float* score_row, int32_t* block_row) {
+#pragma unroll
+  for (int r = 0; r < kListMax; ++r) {
+    if (r >= width) break;
+    const bool real = r < n;
+    score_row[r] = real ? list.s[r] : -__int_as_float(0x7f800000);
+    block_row[r] = real ? list.b[r] : -1;
+  }
+}
+
 }  // namespace msa

@@ -66,15 +66,17 @@ struct ScanArgs {
   const int32_t* page_table;
   const int32_t* seq_lens;
   int32_t batch, max_pages, num_pages, G;
+  int32_t kb0, kb1;  // logical blocks scanned: [kb0, kb1) (0, max_pages: all of them)
   float4* scores;    // [batch][G][max_pages]: per-warp maxima of the 4 epilogue warps
   int32_t* status;
   uint64_t wait_ns;
 };
 
-// Index pages scored for sequence s: those strictly before the query's page.
+// Index pages scored for sequence s: those of [kb0, kb1) strictly before the query's page.
 __device__ __forceinline__ int scan_pages(const ScanArgs& a, int s) {
   const int n = a.seq_lens[s];
-  return n > 0 ? min((n - 1) / kBlock, a.max_pages) : 0;
+  const int before = n > 0 ? min((n - 1) / kBlock, a.max_pages) : 0;
+  return max(0, min(before, a.kb1) - a.kb0);
 }
 
 // The pages of all sequences, concatenated in (sequence, block) order, are split into equal
@@ -120,7 +122,7 @@ __device__ void scan_range(const ScanArgs& a, int lane, int* out /* s0, b0, coun
 }
 
 struct PageWalk {
-  int s, b, left, ns;
+  int s, b, left, ns;  // b counts the scanned pages of sequence s, from 0
   __device__ __forceinline__ void init(const ScanArgs& a, const volatile int* r) {
     s = r[0];
     b = r[1] - 1;
@@ -137,7 +139,7 @@ struct PageWalk {
       b = 0;
       ns = scan_pages(a, s);
     }
-    return b;
+    return a.kb0 + b;
   }
 };
 
@@ -250,9 +252,11 @@ __global__ void __launch_bounds__(256, 1)
         }
         more = more && sa[0] >= 0;
       }
+      // Drain (bounded by the default limit, not the caller's): after an abort the newest load
+      // of every stage may still be in flight; the CTA stays until it has landed.
       if (*abort_flag) {
         for (int x = (p > kScanStages ? p - kScanStages : 0); x < p; ++x)
-          mbar_wait(full(x % kScanStages), (x / kScanStages) & 1, a.wait_ns);
+          mbar_wait(full(x % kScanStages), (x / kScanStages) & 1, kDefaultWaitNs);
       }
     }
   } else if (warp == 1) {
@@ -287,8 +291,10 @@ __global__ void __launch_bounds__(256, 1)
         report_status(a.status, kStatusTimeout);
         *abort_flag = 1;
       }
+      // every MMA this thread issued has finished before the TMEM is released (the default
+      // limit, so that a short caller limit cannot cut the drain short)
       mma_commit(drain_bar);
-      mbar_wait(drain_bar, 0, a.wait_ns);
+      mbar_wait(drain_bar, 0, kDefaultWaitNs);
     }
   } else if (warp >= 4) {
     // epilogue: thread = key of the page; the warp's max over its 32 keys per group
@@ -342,10 +348,13 @@ struct TopkArgs {
   const float4* scores;
   const int32_t* seq_lens;
   int32_t batch, max_pages, G, k;
+  int32_t kb0, kb1;   // logical blocks ranked: [kb0, kb1)
   int32_t* sel;       // [G][batch][k]
   float* sel_score;   // optional, same shape
   float* block_scores;  // optional [G][batch][max_pages]: pooled score of every block (+inf
                         // the local one, -inf later ones)
+  float* cand_score;    // candidate mode (cand_block set): [G][batch][k-1] in rank order
+  int32_t* cand_block;
   int32_t* status;
 };
 
@@ -355,8 +364,12 @@ __global__ void __launch_bounds__(128) decode_topk_kernel(TopkArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int s = blockIdx.x / a.G, g = blockIdx.x % a.G;  // grid = batch * G
   const int n = a.seq_lens[s];
-  int32_t* out = a.sel + (static_cast<size_t>(g) * a.batch + s) * a.k;
-  float* out_s = a.sel_score ? a.sel_score + (static_cast<size_t>(g) * a.batch + s) * a.k : nullptr;
+  const bool cand = a.cand_block != nullptr;
+  const int width = cand ? a.k - 1 : a.k;  // entries per output row
+  int32_t* out = (cand ? a.cand_block : a.sel) + (static_cast<size_t>(g) * a.batch + s) * width;
+  float* out_s = cand ? a.cand_score + (static_cast<size_t>(g) * a.batch + s) * width
+                 : a.sel_score ? a.sel_score + (static_cast<size_t>(g) * a.batch + s) * a.k
+                               : nullptr;
   float* bsrow = a.block_scores
                      ? a.block_scores + (static_cast<size_t>(g) * a.batch + s) * a.max_pages
                      : nullptr;
@@ -364,7 +377,7 @@ __global__ void __launch_bounds__(128) decode_topk_kernel(TopkArgs a) {
   if (n <= 0 || (n - 1) / kBlock >= a.max_pages) {  // the same outcome for the whole CTA
     if (threadIdx.x == 0) report_status(a.status, kStatusBounds);
     if (warp == 0)
-      for (int r = lane; r < a.k; r += 32) {
+      for (int r = lane; r < width; r += 32) {
         out[r] = -1;
         if (out_s) out_s[r] = ninf;
       }
@@ -376,15 +389,17 @@ __global__ void __launch_bounds__(128) decode_topk_kernel(TopkArgs a) {
   if (bsrow)  // the local block is never scored; later blocks are not causal
     for (int b = bi + threadIdx.x; b < a.max_pages; b += 128) bsrow[b] = b == bi ? pinf : ninf;
   const float4* row = a.scores + (static_cast<size_t>(s) * a.G + g) * a.max_pages;
+  // the ranked blocks: [lo, hi), strictly before the local block
+  const int lo = a.kb0, hi = min(a.kb1, bi);
   TopList list;
   list.clear();
   // eight loads in flight per lane, then eight inserts
-  for (int b0 = warp * 32; b0 < bi; b0 += 8 * 128) {
+  for (int b0 = lo + warp * 32; b0 < hi; b0 += 8 * 128) {
     float sc[8];
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
       const int b = b0 + q * 128 + lane;
-      if (b < bi) {
+      if (b < hi) {
         const float4 v = row[b];
         sc[q] = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
       }
@@ -392,13 +407,13 @@ __global__ void __launch_bounds__(128) decode_topk_kernel(TopkArgs a) {
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
       const int b = b0 + q * 128 + lane;
-      if (b < bi) {
+      if (b < hi) {
         list.insert(sc[q], b);
         if (bsrow) bsrow[b] = sc[q];
       }
     }
   }
-  const int take = min(a.k - 1, bi);
+  const int take = min(a.k - 1, max(0, hi - lo));
   // r-th round: the warp's r-th best (score, block) reaches every lane; its owner pops it.
   // Empty entries (-inf, INT_MAX) rank last, so a warp with fewer blocks pads with them.
   auto pop_best = [&](float& bs, int& bb) {
@@ -448,6 +463,13 @@ __global__ void __launch_bounds__(128) decode_topk_kernel(TopkArgs a) {
       my_sc = bs;
     }
   }
+  if (cand) {  // lane r holds the r-th ranked block
+    for (int r = lane; r < width; r += 32) {
+      out[r] = r < take ? my_id : -1;
+      out_s[r] = r < take ? my_sc : ninf;
+    }
+    return;
+  }
   // lanes 0..take-1 hold the winners; place each at its rank by block id
   int rank = 0;
   for (int q = 0; q < take; ++q) {
@@ -470,6 +492,10 @@ __global__ void __launch_bounds__(128) decode_topk_kernel(TopkArgs a) {
 // 1-4 each score 32 keys (S = q K^T with m16n8k16 MMAs, M = the group's 16 heads), exchange row
 // maxima, sums and their slice of P through shared memory, and then each computes O = P V for 32
 // of the 128 output dimensions over all the page's keys, written straight to the partial.
+// With an e4m3 K/V cache (kKV8) the pages arrive as 16 KiB e4m3 tiles; each compute warp widens
+// just the part it reads (K of its 32 keys to bf16, V of its 32 dimensions to fp16) into a
+// private swizzled buffer and releases the stage at once.  S stays a bf16 product (q exact); P
+// and V go into an fp16 product (every e4m3 value is exact in both types).
 // ------------------------------------------------------------------------------------------
 struct DecAttnArgs {
   const __nv_bfloat16* q;  // [batch][G*16][128]
@@ -485,21 +511,34 @@ struct DecAttnArgs {
   uint64_t wait_ns;
 };
 
-constexpr int kDecStages = 3;
-constexpr uint32_t kDecStage = 65536;
-// Per unit the four warps exchange their row maxima and row sums and the bf16 P tile (16 rows x
-// 128 keys, 128-byte swizzled panels); two copies, by unit parity, so a warp may start the next
-// unit while another still reads this one's.
-constexpr uint32_t kDecP = kDecStages * kDecStage;  // 2 x 4 KB
-constexpr uint32_t kDecPBytes = kHeads * kBlock * 2;
-constexpr uint32_t kDecML = kDecP + 2 * kDecPBytes;  // 2 x (max, sum) x 4 warps x 16 rows fp32
-constexpr uint32_t kDecBar = kDecML + 2 * 2 * 4 * kHeads * 4;
+// Shared-memory layout of the decode attention kernel, by K/V storage type.
+template <bool kKV8>
+struct DecLayout {
+  static constexpr int kStages = kKV8 ? 4 : 3;
+  static constexpr uint32_t kTile = kKV8 ? 16384 : 32768;  // one K or V page tile
+  static constexpr uint32_t kStage = 2 * kTile;
+  // e4m3: per compute warp, K of its 32 keys in bf16 (32 rows x 256 B) and V of its 32
+  // dimensions in fp16 (128 rows x 64 B)
+  static constexpr uint32_t kPriv = kStages * kStage;
+  static constexpr uint32_t kPrivWarp = 8192 + 8192;
+  static constexpr uint32_t kP = kPriv + (kKV8 ? 4 * kPrivWarp : 0);
+  // Per unit the four warps exchange their row maxima and row sums and the P tile (16 rows x
+  // 128 keys, 128-byte swizzled panels); two copies, by unit parity, so a warp may start the
+  // next unit while another still reads this one's.
+  static constexpr uint32_t kPBytes = kHeads * kBlock * 2;
+  static constexpr uint32_t kML = kP + 2 * kPBytes;  // 2 x (max, sum) x 4 warps x 16 rows fp32
+  static constexpr uint32_t kBar = kML + 2 * 2 * 4 * kHeads * 4;
+  static constexpr uint32_t kSmem = kBar + 128 + 1024;
+};
+constexpr int kDecMaxStages = 4;
 constexpr uint32_t kDecBarFull = 0, kDecBarEmpty = 32, kDecAbort = 64;
-constexpr uint32_t kDecSmem = kDecBar + 128 + 1024;
-static_assert(kDecBarFull + 8 * kDecStages <= kDecBarEmpty, "decode attention barriers");
-static_assert(kDecBarEmpty + 8 * kDecStages <= kDecAbort, "decode attention barriers");
+static_assert(kDecBarFull + 8 * kDecMaxStages <= kDecBarEmpty, "decode attention barriers");
+static_assert(kDecBarEmpty + 8 * kDecMaxStages <= kDecAbort, "decode attention barriers");
 static_assert(kDecAbort + 4 <= 128, "decode attention barriers");
-static_assert(kDecSmem <= 232448, "decode attention shared memory");
+static_assert(DecLayout<false>::kStages <= kDecMaxStages && DecLayout<true>::kStages <= kDecMaxStages,
+              "decode attention stages");
+static_assert(DecLayout<false>::kSmem <= 232448, "decode attention shared memory");
+static_assert(DecLayout<true>::kSmem <= 232448, "decode attention shared memory (e4m3)");
 
 struct UnitInfo {
   int s, g, b, page, lim;
@@ -529,24 +568,38 @@ __device__ __forceinline__ uint32_t swz(uint32_t tile, int row, int chunk) {
   return tile + (chunk >> 3) * kPanel + row * 128 + (((chunk & 7) ^ (row & 7)) << 4);
 }
 
-// The 16 x 128 bf16 P tile: two 64-key panels of 16 rows x 128 bytes, 16-byte chunks XOR-swizzled
-// by row, so the stores of a warp and the ldmatrix reads both spread over all banks.
+// The 16 x 128 P tile: two 64-key panels of 16 rows x 128 bytes, 16-byte chunks XOR-swizzled by
+// row, so the stores of a warp and the ldmatrix reads both spread over all banks.
 __device__ __forceinline__ uint32_t dec_p_addr(uint32_t tile, int row, int chunk) {
   return tile + (chunk >> 3) * (kHeads * 128) + row * 128 + (((chunk & 7) ^ (row & 7)) << 4);
 }
 
+// Private bf16 K buffer of a warp (its 32 keys x 256 B): 16-byte chunk c of key row r; the low
+// three chunk bits are XOR-ed with the row, so the 8 rows an ldmatrix reads hit distinct banks.
+__device__ __forceinline__ uint32_t kpriv_addr(uint32_t buf, int r, int c) {
+  return buf + r * 256 + (((c & 8) | ((c & 7) ^ (r & 7))) << 4);
+}
+// Private fp16 V buffer of a warp (128 keys x its 32 dimensions = 64 B): chunk c (0..3) of key
+// row r, XOR-ed with bits 1..2 of the row (8 consecutive rows then cover all 32 banks).
+__device__ __forceinline__ uint32_t vpriv_addr(uint32_t buf, int r, int c) {
+  return buf + r * 64 + ((c ^ ((r >> 1) & 3)) << 4);
+}
+
+template <bool kKV8>
 __global__ void __launch_bounds__(160, 1)
     decode_attn_kernel(const __grid_constant__ CUtensorMap map_kp,
                        const __grid_constant__ CUtensorMap map_vp, DecAttnArgs a) {
+  using Lay = DecLayout<kKV8>;
+  constexpr int kDecStages = Lay::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t base = smem_u32(smem);
-  const uint32_t bars = base + kDecBar;
+  const uint32_t bars = base + Lay::kBar;
   auto full = [&](int s) { return bars + kDecBarFull + 8 * s; };
   auto empty = [&](int s) { return bars + kDecBarEmpty + 8 * s; };
-  volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + kDecBar + kDecAbort);
-  float* mlx = reinterpret_cast<float*>(smem + kDecML);
+  volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + Lay::kBar + kDecAbort);
+  float* mlx = reinterpret_cast<float*>(smem + Lay::kML);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int u0 = blockIdx.x * a.per_cta, u1 = min(a.units, u0 + a.per_cta);
 
@@ -574,18 +627,23 @@ __global__ void __launch_bounds__(160, 1)
           *abort_flag = 1;
           break;
         }
-        const uint32_t sb = base + st * kDecStage;
+        const uint32_t sb = base + st * Lay::kStage;
         const int row0 = (x.page * a.G + x.g) * kBlock;
-        mbar_arrive_expect_tx(full(st), kDecStage);
-        tma_load_2d(sb, &map_kp, full(st), 0, row0);
-        tma_load_2d(sb + kPanel, &map_kp, full(st), 64, row0);
-        tma_load_2d(sb + 32768, &map_vp, full(st), 0, row0);
-        tma_load_2d(sb + 32768 + kPanel, &map_vp, full(st), 64, row0);
+        mbar_arrive_expect_tx(full(st), Lay::kStage);
+        if (kKV8) {  // one 128 x 128-byte box per tile
+          tma_load_2d(sb, &map_kp, full(st), 0, row0);
+          tma_load_2d(sb + Lay::kTile, &map_vp, full(st), 0, row0);
+        } else {     // two 64-element panels per tile
+          tma_load_2d(sb, &map_kp, full(st), 0, row0);
+          tma_load_2d(sb + kPanel, &map_kp, full(st), 64, row0);
+          tma_load_2d(sb + Lay::kTile, &map_vp, full(st), 0, row0);
+          tma_load_2d(sb + Lay::kTile + kPanel, &map_vp, full(st), 64, row0);
+        }
         ++p;
       }
-      if (*abort_flag) {
+      if (*abort_flag) {  // in-flight loads land before the producer exits (default limit)
         for (int x = (p > kDecStages ? p - kDecStages : 0); x < p; ++x)
-          mbar_wait(full(x % kDecStages), (x / kDecStages) & 1, a.wait_ns);
+          mbar_wait(full(x % kDecStages), (x / kDecStages) & 1, kDefaultWaitNs);
       }
     }
     return;  // the producer takes no part in the compute warps' named barriers
@@ -594,6 +652,7 @@ __global__ void __launch_bounds__(160, 1)
   // ------------------------------ compute warps 1..4 ------------------------------
   const int w = warp - 1;
   const int gid = lane >> 2, tq = lane & 3;
+  const uint32_t kp = base + Lay::kPriv + w * Lay::kPrivWarp, vp = kp + 8192;  // e4m3 only
   uint32_t qa[8][4];
   int cur_sg = -1;
   int p = 0;
@@ -625,9 +684,33 @@ __global__ void __launch_bounds__(160, 1)
       *abort_flag = 1;  // keep going with whatever is in the buffer: every warp still meets
                         // the same barriers, and the status word marks the output invalid
     }
-    const uint32_t kt = base + st * kDecStage, vt = kt + 32768;
+    const uint32_t kt = base + st * Lay::kStage, vt = kt + Lay::kTile;
+    if (kKV8) {
+      // K rows [32w, 32w+32): lane takes bytes [4 lane, 4 lane + 4) of each row
+#pragma unroll 4
+      for (int it = 0; it < 32; ++it) {
+        const int r = 32 * w + it;
+        const uint32_t src = kt + r * 128 + (((lane >> 2) ^ (r & 7)) << 4) + (lane & 3) * 4;
+        uint32_t h0, h1;
+        e4m3x4_to_f16x4(ld_shared_u32(src), h0, h1);
+        st_shared_v2(kpriv_addr(kp, it, lane >> 1) + (lane & 1) * 8, f16x2_to_bf16x2(h0),
+                     f16x2_to_bf16x2(h1));
+      }
+      // V columns [32w, 32w+32) of all 128 keys: 4 keys per step, 8 lanes per key
+#pragma unroll 4
+      for (int it = 0; it < 32; ++it) {
+        const int r = it * 4 + (lane >> 3);
+        const int c = 2 * w + ((lane & 7) >> 2);
+        const uint32_t src = vt + r * 128 + ((c ^ (r & 7)) << 4) + (lane & 3) * 4;
+        uint32_t h0, h1;
+        e4m3x4_to_f16x4(ld_shared_u32(src), h0, h1);
+        st_shared_v2(vpriv_addr(vp, r, (lane & 7) >> 1) + (lane & 1) * 8, h0, h1);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty(st));  // the stage is no longer read
+    }
     const int par = p & 1;
-    const uint32_t pt = base + kDecP + par * kDecPBytes;  // this unit's P tile
+    const uint32_t pt = base + Lay::kP + par * Lay::kPBytes;  // this unit's P tile
     float* mx = mlx + par * (2 * 4 * kHeads);              // [4 warps][16] maxima
     float* ls = mx + 4 * kHeads;                           // [4 warps][16] sums
     // S = q K^T over this warp's 32 keys: 4 n-tiles of 8 keys
@@ -640,7 +723,9 @@ __global__ void __launch_bounds__(160, 1)
 #pragma unroll
       for (int kk = 0; kk < 8; kk += 2) {
         uint32_t r[4];
-        ldmatrix_x4(swz(kt, key, 2 * kk + (lane >> 3)), r);
+        ldmatrix_x4(kKV8 ? kpriv_addr(kp, j * 8 + (lane & 7), 2 * kk + (lane >> 3))
+                         : swz(kt, key, 2 * kk + (lane >> 3)),
+                    r);
         mma_m16n8k16_bf16(sacc[j], qa[kk], r[0], r[1]);
         mma_m16n8k16_bf16(sacc[j], qa[kk + 1], r[2], r[3]);
       }
@@ -674,7 +759,8 @@ __global__ void __launch_bounds__(160, 1)
       M0 = fmaxf(M0, mx[q * kHeads + gid]);
       M1 = fmaxf(M1, mx[q * kHeads + gid + 8]);
     }
-    // P = exp2(z - M) for this warp's keys -> bf16 into the shared P tile; partial row sums
+    // P = exp2(z - M) for this warp's keys -> bf16 (fp16 with an e4m3 cache) into the shared P
+    // tile; partial row sums
     float l0 = 0.f, l1 = 0.f;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -683,8 +769,10 @@ __global__ void __launch_bounds__(160, 1)
       l0 += p0 + p1;
       l1 += p2 + p3;
       const int chunk = w * 4 + j;  // keys [8 chunk, 8 chunk + 8)
-      st_shared_u32(dec_p_addr(pt, gid, chunk) + tq * 4, pack_bf16x2(p0, p1));
-      st_shared_u32(dec_p_addr(pt, gid + 8, chunk) + tq * 4, pack_bf16x2(p2, p3));
+      st_shared_u32(dec_p_addr(pt, gid, chunk) + tq * 4,
+                    kKV8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1));
+      st_shared_u32(dec_p_addr(pt, gid + 8, chunk) + tq * 4,
+                    kKV8 ? pack_f16x2(p2, p3) : pack_bf16x2(p2, p3));
     }
     l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
     l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
@@ -713,13 +801,19 @@ __global__ void __launch_bounds__(160, 1)
 #pragma unroll
       for (int nt = 0; nt < 4; nt += 2) {
         uint32_t r[4];
-        ldmatrix_x4_trans(swz(vt, key, w * 4 + nt + (mtx >> 1)), r);
-        mma_m16n8k16_bf16(oacc[nt], pa, r[0], r[1]);
-        mma_m16n8k16_bf16(oacc[nt + 1], pa, r[2], r[3]);
+        if (kKV8) {
+          ldmatrix_x4_trans(vpriv_addr(vp, key, nt + (mtx >> 1)), r);
+          mma_m16n8k16_f16(oacc[nt], pa, r[0], r[1]);
+          mma_m16n8k16_f16(oacc[nt + 1], pa, r[2], r[3]);
+        } else {
+          ldmatrix_x4_trans(swz(vt, key, w * 4 + nt + (mtx >> 1)), r);
+          mma_m16n8k16_bf16(oacc[nt], pa, r[0], r[1]);
+          mma_m16n8k16_bf16(oacc[nt + 1], pa, r[2], r[3]);
+        }
       }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(empty(st));
+    if (!kKV8 && lane == 0) mbar_arrive(empty(st));
     ++p;
     const float i0 = 1.f / L0, i1 = 1.f / L1;
     float* dst = a.po + static_cast<size_t>(u) * kHeads * kDim;
@@ -796,7 +890,8 @@ cudaError_t launch_decode_select(const CUtensorMap& map_k, const CUtensorMap& ma
                                  int max_pages, int num_pages, int G, int k, bool fp8,
                                  float* scores, int32_t* sel, float* sel_score,
                                  float* block_scores, int32_t* status, uint64_t wait_ns,
-                                 int num_sms, cudaStream_t stream) {
+                                 int num_sms, cudaStream_t stream, int kb0, int kb1,
+                                 float* cand_score, int32_t* cand_block) {
   ScanArgs a{};
   a.page_table = page_table;
   a.seq_lens = seq_lens;
@@ -804,6 +899,8 @@ cudaError_t launch_decode_select(const CUtensorMap& map_k, const CUtensorMap& ma
   a.max_pages = max_pages;
   a.num_pages = num_pages;
   a.G = G;
+  a.kb0 = kb0;
+  a.kb1 = kb1;
   a.scores = reinterpret_cast<float4*>(scores);
   a.status = status;
   a.wait_ns = wait_ns;
@@ -831,9 +928,13 @@ cudaError_t launch_decode_select(const CUtensorMap& map_k, const CUtensorMap& ma
   t.max_pages = max_pages;
   t.G = G;
   t.k = k;
+  t.kb0 = kb0;
+  t.kb1 = kb1;
   t.sel = sel;
   t.sel_score = sel_score;
   t.block_scores = block_scores;
+  t.cand_score = cand_score;
+  t.cand_block = cand_block;
   t.status = status;
   decode_topk_kernel<<<batch * G, 128, 0, stream>>>(t);
   return cudaGetLastError();
@@ -849,7 +950,7 @@ cudaError_t launch_decode_attn(const CUtensorMap& map_kp, const CUtensorMap& map
                                const int32_t* seq_lens, int batch, int max_pages, int num_pages,
                                int G, int k, float scale, uint8_t* scratch, void* o, float* lse,
                                int32_t* status, uint64_t wait_ns, int num_sms,
-                               cudaStream_t stream) {
+                               cudaStream_t stream, bool kv_fp8) {
   DecAttnArgs a{};
   a.q = static_cast<const __nv_bfloat16*>(q);
   a.sel = sel;
@@ -868,10 +969,22 @@ cudaError_t launch_decode_attn(const CUtensorMap& map_kp, const CUtensorMap& map
   a.plse = reinterpret_cast<float*>(scratch + static_cast<size_t>(a.units) * kHeads * kDim * 4);
   a.status = status;
   a.wait_ns = wait_ns;
-  cudaError_t e = cudaFuncSetAttribute(decode_attn_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kDecSmem);
-  if (e != cudaSuccess) return e;
-  decode_attn_kernel<<<grid, 160, kDecSmem, stream>>>(map_kp, map_vp, a);
+  cudaError_t e;
+  if (kv_fp8) {
+    constexpr uint32_t smem = DecLayout<true>::kSmem;
+    if ((e = cudaFuncSetAttribute(decode_attn_kernel<true>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) !=
+        cudaSuccess)
+      return e;
+    decode_attn_kernel<true><<<grid, 160, smem, stream>>>(map_kp, map_vp, a);
+  } else {
+    constexpr uint32_t smem = DecLayout<false>::kSmem;
+    if ((e = cudaFuncSetAttribute(decode_attn_kernel<false>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) !=
+        cudaSuccess)
+      return e;
+    decode_attn_kernel<false><<<grid, 160, smem, stream>>>(map_kp, map_vp, a);
+  }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   DecCombineArgs c{a.po, a.plse, batch, G, k, static_cast<__nv_bfloat16*>(o), lse};
   decode_combine_kernel<<<dim3(batch, G), 128, 0, stream>>>(c);

@@ -64,6 +64,13 @@ struct IndexPrefillArgs {
   float* block_scores;  // optional [G][L][nb]: every block's pooled score (+inf local, -inf later)
   int32_t* status;
   uint64_t wait_ns;
+  // Key blocks scored: [kb0, kb1) (the whole causal range: 0, nb).  The key tensor map starts at
+  // block kb0.  With cand_block set, each row's top-(k-1) of those blocks is written in rank
+  // order to cand_score / cand_block [G][L][k-1] (a shard of the context-parallel index branch)
+  // instead of the selection.
+  int32_t kb0, kb1;
+  float* cand_score;
+  int32_t* cand_block;
 };
 
 // Shared memory: gpc index-query tiles, ns key stages, then the barrier block.
@@ -95,7 +102,8 @@ __global__ void __launch_bounds__(384, 1)
   const int cpq = a.G / gpc;                                    // CTAs per query block
   const int qb = a.nb - 1 - static_cast<int>(blockIdx.x) / cpq;  // heaviest query blocks first
   const int g0 = (static_cast<int>(blockIdx.x) % cpq) * gpc;
-  const int nkey = qb;                                          // key blocks 0..qb-1
+  // key blocks kb0 .. kb0+nkey-1: those of the range strictly before the query block
+  const int nkey = max(0, min(a.kb1, qb) - a.kb0);
   const int ntiles = (nkey + 1) / 2;
   const int nunits = ntiles * gpc;
 
@@ -243,12 +251,13 @@ __global__ void __launch_bounds__(384, 1)
         }
         mx[h] = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
       }
-      list.insert(mx[0], 2 * t);
-      if (2 * t + 1 < nkey) list.insert(mx[1], 2 * t + 1);
+      list.insert(mx[0], a.kb0 + 2 * t);
+      if (2 * t + 1 < nkey) list.insert(mx[1], a.kb0 + 2 * t + 1);
       const int64_t ib = static_cast<int64_t>(qb) * kBlock + row;
       if (a.block_scores && ib < a.L) {
         float* bs = a.block_scores +
-                    (static_cast<size_t>(g0 + (gpc == 2 ? e : 0)) * a.L + ib) * a.nb + 2 * t;
+                    (static_cast<size_t>(g0 + (gpc == 2 ? e : 0)) * a.L + ib) * a.nb + a.kb0 +
+                    2 * t;
         bs[0] = mx[0];
         if (2 * t + 1 < nkey) bs[1] = mx[1];
       }
@@ -280,9 +289,14 @@ __global__ void __launch_bounds__(384, 1)
     if ((gpc == 2 || e == 0) && ok && !*abort_flag && i < a.L) {
       const int n = min(a.k - 1, nkey);
       const int g = g0 + (gpc == 2 ? e : 0);
-      list.truncate_and_sort_by_block(n);
-      const size_t off = (static_cast<size_t>(g) * a.L + i) * a.k;
-      write_sel_row(list, n, qb, a.k, a.sel + off, a.sel_score ? a.sel_score + off : nullptr);
+      if (a.cand_block) {  // the list is in rank order
+        const size_t off = (static_cast<size_t>(g) * a.L + i) * (a.k - 1);
+        write_cand_row(list, n, a.k - 1, a.cand_score + off, a.cand_block + off);
+      } else {
+        list.truncate_and_sort_by_block(n);
+        const size_t off = (static_cast<size_t>(g) * a.L + i) * a.k;
+        write_sel_row(list, n, qb, a.k, a.sel + off, a.sel_score ? a.sel_score + off : nullptr);
+      }
     }
     if (a.block_scores && (gpc == 2 || e == 0) && ok && !*abort_flag) {
       // Row tails: +inf at the local block (never scored), -inf after it (not causal).  The
@@ -313,7 +327,8 @@ size_t smem_bytes(int gpc, int ns) {
 template <bool kF8>
 cudaError_t launch(const CUtensorMap& map_q, const CUtensorMap& map_k, int64_t L, int G, int k,
                    int32_t* sel, float* sel_score, float* block_scores, int32_t* status,
-                   uint64_t wait_ns, cudaStream_t stream) {
+                   uint64_t wait_ns, int kb0, int kb1, float* cand_score, int32_t* cand_block,
+                   cudaStream_t stream) {
   const int nb = static_cast<int>((L + kBlock - 1) / kBlock);
   const int gpc = (G % 2 == 0) ? 2 : 1;  // groups per CTA
   int ns = IdxTiles<kF8>::kMaxStages;    // key stages
@@ -323,7 +338,9 @@ cudaError_t launch(const CUtensorMap& map_q, const CUtensorMap& map_k, int64_t L
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  IndexPrefillArgs a{L, G, gpc, k, nb, ns, sel, sel_score, block_scores, status, wait_ns};
+  IndexPrefillArgs a{L,       G,       gpc,  k,   nb,         ns,         sel,
+                     sel_score, block_scores, status, wait_ns, kb0, kb1, cand_score,
+                     cand_block};
   index_select_prefill_kernel<kF8><<<nb * (G / gpc), 384, smem, stream>>>(map_q, map_k, a);
   return cudaGetLastError();
 }
@@ -333,11 +350,12 @@ cudaError_t launch(const CUtensorMap& map_q, const CUtensorMap& map_k, int64_t L
 cudaError_t launch_index_select_prefill(const CUtensorMap& map_q, const CUtensorMap& map_k,
                                         int64_t L, int G, int k, bool fp8, int32_t* sel,
                                         float* sel_score, float* block_scores, int32_t* status,
-                                        uint64_t wait_ns, cudaStream_t stream) {
+                                        uint64_t wait_ns, cudaStream_t stream, int kb0, int kb1,
+                                        float* cand_score, int32_t* cand_block) {
   return fp8 ? launch<true>(map_q, map_k, L, G, k, sel, sel_score, block_scores, status, wait_ns,
-                            stream)
+                            kb0, kb1, cand_score, cand_block, stream)
              : launch<false>(map_q, map_k, L, G, k, sel, sel_score, block_scores, status,
-                             wait_ns, stream);
+                             wait_ns, kb0, kb1, cand_score, cand_block, stream);
 }
 
 }  // namespace msa

@@ -13,10 +13,15 @@ namespace msa {
 constexpr int kIndexKeyTile = 256;
 // fp8: index vectors are e4m3 (else bf16); the tensor maps' element type must match.
 // block_scores (optional): [G][L][nb] pooled score of every block (+inf local, -inf later).
+// kb0, kb1: the key blocks scored (0, nb for the selection); map_k starts at block kb0.  With
+// cand_block set, each row's top-(k-1) of those blocks goes to cand_score / cand_block
+// [G][L][k-1] in rank order instead of the selection (a context-parallel shard).
 cudaError_t launch_index_select_prefill(const CUtensorMap& map_q, const CUtensorMap& map_k,
                                         int64_t L, int G, int k, bool fp8, int32_t* sel,
                                         float* sel_score, float* block_scores, int32_t* status,
-                                        uint64_t wait_ns, cudaStream_t stream);
+                                        uint64_t wait_ns, cudaStream_t stream, int kb0 = 0,
+                                        int kb1 = 0x7fffffff, float* cand_score = nullptr,
+                                        int32_t* cand_block = nullptr);
 
 // Byte offsets of the prefill main-branch workspace (after the 256-byte status header).
 struct PrefillWorkspace {
@@ -39,18 +44,31 @@ cudaError_t launch_attn_prefill_chunk(const CUtensorMap& map_q, const CUtensorMa
                                       cudaEvent_t* marks);
 
 size_t decode_select_workspace_bytes(int batch, int G, int max_pages);
+// kb0, kb1: the logical blocks scanned (0, max_pages for the selection).  With cand_block set,
+// each (sequence, group) row's top-(k-1) of those blocks goes to cand_score / cand_block
+// [G][batch][k-1] in rank order instead of the selection (a context-parallel shard).
 cudaError_t launch_decode_select(const CUtensorMap& map_k, const CUtensorMap& map_q,
                                  const int32_t* page_table, const int32_t* seq_lens, int batch,
                                  int max_pages, int num_pages, int G, int k, bool fp8,
                                  float* scores, int32_t* sel, float* sel_score,
                                  float* block_scores, int32_t* status, uint64_t wait_ns,
-                                 int num_sms, cudaStream_t stream);
+                                 int num_sms, cudaStream_t stream, int kb0 = 0,
+                                 int kb1 = 0x7fffffff, float* cand_score = nullptr,
+                                 int32_t* cand_block = nullptr);
+// Merge of the candidates of num_shards disjoint key-block shards ([R][G][T][k-1] each) into the
+// selection sel [G][T][k] (sel_score optional): rank by (score desc, block asc), keep
+// min(k-1, blocks before the query's own), add the local block, ascending, -1 padded.
+// seq_lens: decode (query t at seq_lens[t]-1); nullptr: prefill (query t at position t).
+cudaError_t launch_index_merge(const float* cand_score, const int32_t* cand_block,
+                               int num_shards, int64_t T, int G, int k,
+                               const int32_t* seq_lens, int32_t* sel, float* sel_score,
+                               int32_t* status, cudaStream_t stream);
 size_t decode_attn_workspace_bytes(int batch, int G, int k);
 cudaError_t launch_decode_attn(const CUtensorMap& map_kp, const CUtensorMap& map_vp,
                                const void* q, const int32_t* sel, const int32_t* page_table,
                                const int32_t* seq_lens, int batch, int max_pages, int num_pages,
                                int G, int k, float scale, uint8_t* scratch, void* o, float* lse,
                                int32_t* status, uint64_t wait_ns, int num_sms,
-                               cudaStream_t stream);
+                               cudaStream_t stream, bool kv_fp8 = false);
 
 }  // namespace msa

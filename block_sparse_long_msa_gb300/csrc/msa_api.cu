@@ -73,7 +73,8 @@ int64_t prefill_chunk(int64_t L) {
 
 msa_status_t check_paged(const msa_paged_kv_t* p, bool need_kv) {
   if (!p || !p->k_idx_pool || !p->page_table || !p->seq_lens || p->batch < 0 ||
-      p->max_pages < 1 || p->num_pages < 1 || p->reserved != 0 || !aligned16(p->k_idx_pool))
+      p->max_pages < 1 || p->num_pages < 1 || !aligned16(p->k_idx_pool) ||
+      (p->kv_dtype != MSA_KV_BF16 && p->kv_dtype != MSA_KV_E4M3))
     return MSA_ERR_INVALID_ARG;
   if (need_kv && (!p->k_pool || !p->v_pool || !aligned16(p->k_pool) || !aligned16(p->v_pool)))
     return MSA_ERR_INVALID_ARG;
@@ -187,7 +188,7 @@ msa_status_t index_select(const msa_config_t* cfg, const void* q_idx, const void
     return index_select_paged(cfg, q_idx, paged, sel, sel_score, block_scores, ws, ws_bytes,
                               stream);
   if (!k_idx || !aligned16(k_idx) || L < 0) return MSA_ERR_INVALID_ARG;
-  if (G != 1 && G != 2 && G != 4) return MSA_ERR_UNSUPPORTED;
+  if (G > 4) return MSA_ERR_UNSUPPORTED;  // odd G: one group per CTA
   if (L > (static_cast<int64_t>(1) << 31) - kBlock) return MSA_ERR_UNSUPPORTED;
   if (ws_bytes < msa_index_select_workspace(cfg, L, L, nullptr)) return MSA_ERR_WORKSPACE;
   if (L == 0) return MSA_OK;
@@ -228,6 +229,94 @@ msa_status_t msa_index_select_scores(const msa_config_t* cfg, const void* q_idx,
   if (!block_scores) return MSA_ERR_INVALID_ARG;
   return index_select(cfg, q_idx, k_idx, L, paged, sel, sel_score, block_scores, ws, ws_bytes,
                       stream);
+}
+
+msa_status_t msa_index_candidates(const msa_config_t* cfg, const void* q_idx, const void* k_idx,
+                                  int64_t L, const msa_paged_kv_t* paged, int32_t block_begin,
+                                  int32_t block_end, float* cand_score, int32_t* cand_block,
+                                  void* ws, size_t ws_bytes, cudaStream_t stream) {
+  msa_status_t st = check_config(cfg);
+  if (st != MSA_OK) return st;
+  if (!q_idx || !ws || !aligned16(q_idx) || block_begin < 0 || block_end < block_begin)
+    return MSA_ERR_INVALID_ARG;
+  const int G = cfg->num_groups;
+  if (G > 4) return MSA_ERR_UNSUPPORTED;
+  if (cfg->topk == 1) return MSA_OK;  // no candidate slots: the local block is the selection
+  if (!cand_score || !cand_block) return MSA_ERR_INVALID_ARG;
+  const bool fp8 = index_fp8(cfg);
+  int sms = 0;
+  if (paged) {
+    if ((st = check_paged(paged, false)) != MSA_OK) return st;
+    if (ws_bytes < msa_index_select_workspace(cfg, paged->batch, 0, paged))
+      return MSA_ERR_WORKSPACE;
+    if (paged->batch == 0) return MSA_OK;
+    CUtensorMap mk, mq;
+    {
+      const uint64_t dims[2] = {kDim, static_cast<uint64_t>(paged->num_pages) * kBlock};
+      const uint64_t strides[1] = {kDim};
+      const uint32_t box[1] = {kBlock};
+      if (!make_index_map(&mk, fp8, paged->k_idx_pool, 2, dims, strides, box))
+        return MSA_ERR_CUDA;
+    }
+    {
+      const uint64_t dims[2] = {kDim, static_cast<uint64_t>(paged->batch) * G};
+      const uint64_t strides[1] = {kDim};
+      const uint32_t box[1] = {static_cast<uint32_t>(G)};
+      if (!make_index_map(&mq, fp8, q_idx, 2, dims, strides, box)) return MSA_ERR_CUDA;
+    }
+    if (!sm_count(&sms)) return MSA_ERR_CUDA;
+    const int kb1 = block_end < paged->max_pages ? block_end : paged->max_pages;
+    float* scores = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + MSA_WS_HEADER_BYTES);
+    cudaError_t e = msa::launch_decode_select(
+        mk, mq, paged->page_table, paged->seq_lens, paged->batch, paged->max_pages,
+        paged->num_pages, G, cfg->topk, fp8, scores, nullptr, nullptr, nullptr, status_word(ws),
+        wait_ns(cfg), sms, stream, block_begin < kb1 ? block_begin : kb1, kb1, cand_score,
+        cand_block);
+    return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+  }
+  if (!k_idx || !aligned16(k_idx) || L < 0) return MSA_ERR_INVALID_ARG;
+  if (L > (static_cast<int64_t>(1) << 31) - kBlock) return MSA_ERR_UNSUPPORTED;
+  if (ws_bytes < msa_index_select_workspace(cfg, L, L, nullptr)) return MSA_ERR_WORKSPACE;
+  if (L == 0) return MSA_OK;
+  const int64_t nb = (L + kBlock - 1) / kBlock;
+  const int64_t kb1 = block_end < nb ? block_end : nb;
+  const int64_t kb0 = block_begin < kb1 ? block_begin : kb1;
+  // k_idx holds the keys of the shard only: positions [kb0 * B, min(kb1 * B, L))
+  const int64_t rows = (kb1 * kBlock < L ? kb1 * kBlock : L) - kb0 * kBlock;
+  CUtensorMap mq, mk;
+  {
+    const uint64_t dims[3] = {kDim, static_cast<uint64_t>(G), static_cast<uint64_t>(L)};
+    const uint64_t strides[2] = {kDim, static_cast<uint64_t>(G) * kDim};
+    const uint32_t box[2] = {1, kBlock};
+    if (!make_index_map(&mq, fp8, q_idx, 3, dims, strides, box)) return MSA_ERR_CUDA;
+  }
+  {
+    const uint64_t dims[2] = {kDim, static_cast<uint64_t>(rows > 0 ? rows : 1)};
+    const uint64_t strides[1] = {kDim};
+    const uint32_t box[1] = {msa::kIndexKeyTile};
+    if (!make_index_map(&mk, fp8, k_idx, 2, dims, strides, box)) return MSA_ERR_CUDA;
+  }
+  cudaError_t e = msa::launch_index_select_prefill(
+      mq, mk, L, G, cfg->topk, fp8, nullptr, nullptr, nullptr, status_word(ws), wait_ns(cfg),
+      stream, static_cast<int>(kb0), static_cast<int>(kb1), cand_score, cand_block);
+  return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+}
+
+msa_status_t msa_index_merge(const msa_config_t* cfg, int32_t num_shards,
+                             const float* cand_score, const int32_t* cand_block, int64_t T,
+                             const int32_t* seq_lens, int32_t* sel, float* sel_score, void* ws,
+                             size_t ws_bytes, cudaStream_t stream) {
+  msa_status_t st = check_config(cfg);
+  if (st != MSA_OK) return st;
+  if (num_shards < 1 || T < 0 || !sel || !ws) return MSA_ERR_INVALID_ARG;
+  if (cfg->topk > 1 && (!cand_score || !cand_block)) return MSA_ERR_INVALID_ARG;
+  if (ws_bytes < MSA_WS_HEADER_BYTES) return MSA_ERR_WORKSPACE;
+  if (!seq_lens && T > (static_cast<int64_t>(1) << 31) - kBlock) return MSA_ERR_UNSUPPORTED;
+  if (T == 0) return MSA_OK;
+  cudaError_t e = msa::launch_index_merge(cand_score, cand_block, num_shards, T,
+                                          cfg->num_groups, cfg->topk, seq_lens, sel, sel_score,
+                                          status_word(ws), stream);
+  return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
 }
 
 size_t msa_attn_prefill_workspace(const msa_config_t* cfg, int64_t L) {
@@ -323,13 +412,18 @@ msa_status_t msa_attn_decode(const msa_config_t* cfg, const void* q, const msa_p
   if (ws_bytes < msa_attn_decode_workspace(cfg, paged)) return MSA_ERR_WORKSPACE;
   if (paged->batch == 0) return MSA_OK;
   const int G = cfg->num_groups;
+  const bool kv8 = paged->kv_dtype == MSA_KV_E4M3;
   CUtensorMap mk, mv;
   {
+    // rows of 128 elements: two 64-element bf16 panels, or one 128-byte e4m3 box
     const uint64_t dims[2] = {kDim, static_cast<uint64_t>(paged->num_pages) * G * kBlock};
-    const uint64_t strides[1] = {kDim * 2};
-    const uint32_t box[2] = {64, kBlock};
-    if (!make_map(&mk, paged->k_pool, 2, dims, strides, box)) return MSA_ERR_CUDA;
-    if (!make_map(&mv, paged->v_pool, 2, dims, strides, box)) return MSA_ERR_CUDA;
+    const uint64_t strides[1] = {kDim * (kv8 ? 1u : 2u)};
+    const uint32_t box[2] = {kv8 ? 128u : 64u, kBlock};
+    const CUtensorMapDataType t =
+        kv8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    if (!msa::encode_tmap(&mk, t, paged->k_pool, 2, dims, strides, box) ||
+        !msa::encode_tmap(&mv, t, paged->v_pool, 2, dims, strides, box))
+      return MSA_ERR_CUDA;
   }
   int sms = 0;
   if (!sm_count(&sms)) return MSA_ERR_CUDA;
@@ -337,7 +431,7 @@ msa_status_t msa_attn_decode(const msa_config_t* cfg, const void* q, const msa_p
       mk, mv, q, sel, paged->page_table, paged->seq_lens, paged->batch, paged->max_pages,
       paged->num_pages, G, cfg->topk, cfg->softmax_scale,
       static_cast<uint8_t*>(ws) + MSA_WS_HEADER_BYTES, o, lse, status_word(ws), wait_ns(cfg), sms,
-      stream);
+      stream, kv8);
   return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
 }
 

@@ -62,6 +62,12 @@ typedef enum {
  * index bytes and doubles the tensor-core rate. */
 typedef enum { MSA_INDEX_BF16 = 0, MSA_INDEX_E4M3 = 1 } msa_index_dtype_t;
 
+/* Element type of the paged K and V pools.  E4M3 is the same OCP 8-bit float: an FP8 KV cache
+ * ("MiniMax M3.1 Flash 开放权重与部署要点", section 稀疏注意力为什么还会撞上显存墙, where the
+ * FP8 cache halves the bytes per token), read by the decode attention and widened exactly in
+ * the kernel (to bf16 for q.K, to fp16 for P.V).  The values are used as stored: no scale. */
+typedef enum { MSA_KV_BF16 = 0, MSA_KV_E4M3 = 1 } msa_kv_dtype_t;
+
 typedef struct {
   int32_t num_groups;      /* G: KV heads = GQA groups = index-query heads */
   int32_t heads_per_group; /* query heads per group; Hq = G * heads_per_group */
@@ -78,15 +84,15 @@ typedef struct {
  * lives in physical page page_table[s*max_pages + b]. */
 typedef struct {
   const void* k_idx_pool;    /* index_dtype [num_pages][B][d_i]: index keys */
-  const void* k_pool;        /* bf16 [num_pages][G][B][d]: keys, head-major inside a page */
-  const void* v_pool;        /* bf16 [num_pages][G][B][d]: values, same layout */
+  const void* k_pool;        /* kv_dtype [num_pages][G][B][d]: keys, head-major inside a page */
+  const void* v_pool;        /* kv_dtype [num_pages][G][B][d]: values, same layout */
   const int32_t* page_table; /* int32 [batch][max_pages], device */
   const int32_t* seq_lens;   /* int32 [batch], device: context length n >= 1 per sequence; the
                                 query is the token at n-1, already written to the cache */
   int32_t batch;
   int32_t max_pages;         /* row length of page_table; n <= max_pages * B is required */
   int32_t num_pages;         /* pool size; page ids must lie in [0, num_pages) */
-  int32_t reserved;          /* must be 0 */
+  int32_t kv_dtype;          /* msa_kv_dtype_t of k_pool and v_pool (0: bf16) */
 } msa_paged_kv_t;
 
 /* Workspace bytes for msa_index_select: num_queries = L for prefill (paged == NULL), the batch
@@ -127,6 +133,49 @@ msa_status_t msa_index_select_scores(const msa_config_t* cfg, const void* q_idx,
                                      const void* k_idx, int64_t L, const msa_paged_kv_t* paged,
                                      int32_t* sel, float* sel_score, float* block_scores,
                                      void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Context-parallel index branch, step 1 of 2: the candidates of one shard of the key blocks.
+ * The pages describe the indexer's decode running context-parallel over several GPUs
+ * ("MiniMax M3.1 Flash 开放权重与部署要点", section 权重能下载之后，为什么还要先看 vLLM: 4 GB300 at
+ * 512K context).  Each GPU holds the index keys of a range of blocks, ranks its own blocks and
+ * keeps its top-(k-1); the candidates of all shards are exchanged (an all-gather of
+ * (k-1) x (4 + 4) bytes per (query, group)) and msa_index_merge ranks them into the selection.
+ * Every block of the global top-(k-1) is within its own shard's top-(k-1), so the merged
+ * selection equals msa_index_select's bit for bit when the shards cover [0, nb) without overlap.
+ *   Shard: logical key blocks [block_begin, block_end) (clamped to the sequence); only blocks
+ *     strictly before a query's own block are ranked for it (the local block is added by the
+ *     merge).
+ *   Prefill (paged == NULL): q_idx [L][G][d_i] (all queries); k_idx holds the index keys of the
+ *     shard only, positions [block_begin*B, min(block_end*B, L)) as [rows][d_i]; L is the whole
+ *     sequence length.  T = L.
+ *   Decode (paged != NULL, k_idx and L ignored): q_idx [batch][G][d_i]; only the page-table
+ *     entries of blocks in the shard are read.  T = batch.
+ *   cand_score (out) fp32 [G][T][k-1], cand_block (out) int32 [G][T][k-1]: the shard's
+ *     top-(k-1) in rank order (score desc, block asc), padded with (-inf, -1).  With k = 1 there
+ *     is nothing to write and both may be NULL.
+ *   ws / ws_bytes: as for msa_index_select with the same arguments.
+ */
+msa_status_t msa_index_candidates(const msa_config_t* cfg, const void* q_idx, const void* k_idx,
+                                  int64_t L, const msa_paged_kv_t* paged, int32_t block_begin,
+                                  int32_t block_end, float* cand_score, int32_t* cand_block,
+                                  void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Context-parallel index branch, step 2 of 2: the selection from the candidates of num_shards
+ * disjoint shards, stacked as cand_score / cand_block [num_shards][G][T][k-1] (the all-gather's
+ * output).  Ranks the union by (score desc, block asc), keeps min(k-1, blocks before the
+ * query's own) of them, adds the local block and writes sel [G][T][k] ascending, -1 padded
+ * (sel_score optional, as msa_index_select writes it).
+ *   seq_lens (device, int32 [T]): decode, query t is the token at seq_lens[t]-1; NULL: prefill,
+ *     query t is the token at position t.
+ *   ws: at least MSA_WS_HEADER_BYTES; a candidate at or after its query's own block, or a
+ *     context length <= 0, is skipped and flagged as MSA_ERR_DEVICE_BOUNDS.
+ */
+msa_status_t msa_index_merge(const msa_config_t* cfg, int32_t num_shards,
+                             const float* cand_score, const int32_t* cand_block, int64_t T,
+                             const int32_t* seq_lens, int32_t* sel, float* sel_score, void* ws,
+                             size_t ws_bytes, cudaStream_t stream);
 
 /* Workspace bytes for msa_attn_prefill over L tokens. */
 size_t msa_attn_prefill_workspace(const msa_config_t* cfg, int64_t L);

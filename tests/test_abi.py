@@ -66,6 +66,17 @@ def test_host_argument_checks(lib):
     assert lib.msa_index_select(ctypes.byref(cfg), ctypes.c_void_p(0x1002),
                                 ctypes.c_void_p(0x2000), 16, None, ctypes.c_void_p(0x3000), None,
                                 ctypes.c_void_p(0x4000), 1 << 20, None) == msa.MSA_ERR_INVALID_ARG
+    # more than four groups: refused on the host (pointers never dereferenced)
+    g5 = msa.config(5, 16, 16)
+    assert lib.msa_index_select(ctypes.byref(g5), ctypes.c_void_p(0x1000),
+                                ctypes.c_void_p(0x2000), 16, None, ctypes.c_void_p(0x3000), None,
+                                ctypes.c_void_p(0x4000), 1 << 20, None) == msa.MSA_ERR_UNSUPPORTED
+    # a paged cache with an unknown K/V storage type is refused before any work
+    pk = msa.MsaPagedKV(0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 1, 1, 1, 7)
+    assert lib.msa_attn_decode(ctypes.byref(cfg), ctypes.c_void_p(0x6000), ctypes.byref(pk),
+                               ctypes.c_void_p(0x7000), ctypes.c_void_p(0x8000),
+                               ctypes.c_void_p(0x9000), ctypes.c_void_p(0xa000), 1 << 20,
+                               None) == msa.MSA_ERR_INVALID_ARG
     # workspace queries are pure host arithmetic
     assert msa.msa_index_select_workspace(cfg, 32768, 32768) >= msa.WS_HEADER_BYTES
     assert lib.msa_index_select_workspace(ctypes.byref(bad), 1, 1, None) == 0

@@ -73,7 +73,7 @@ def test_ragged_lengths_all_rows(msa, L):
     compare(w, inp, *run_gpu(msa, w, inp))
 
 
-@pytest.mark.parametrize("G,k,L", [(2, 8, 3000), (1, 1, 700), (4, 2, 1500)])
+@pytest.mark.parametrize("G,k,L", [(2, 8, 3000), (1, 1, 700), (4, 2, 1500), (3, 7, 1400)])
 def test_group_and_k_variants(msa, G, k, L):
     w = synthetic.Workload("v", "prefill", L=L, Hq=16 * G, G=G, k=k, seed=77 + G * k)
     inp = synthetic.prefill_inputs(w)

@@ -103,7 +103,7 @@ def test_ragged_lengths(msa):
     check(w, inp, gpu_decode(msa, w, inp))
 
 
-@pytest.mark.parametrize("G,k", [(1, 4), (2, 8), (4, 1)])
+@pytest.mark.parametrize("G,k", [(1, 4), (2, 8), (4, 1), (3, 16)])
 def test_group_and_k_variants(msa, G, k):
     w, inp = _custom([300, 5000, 129, 2560], seed=20 + G + k, G=G, k=k)
     check(w, inp, gpu_decode(msa, w, inp))
@@ -184,3 +184,44 @@ def test_e4m3_full_size_decode_workload_equals_bf16(msa):
     check(w, inp, got)
     ref = synthetic.decode_inputs(w0, device="cuda")
     assert np.array_equal(gpu_decode(msa, w, ref)[0], got[0])
+
+
+# ------------------------------------ E4M3 K/V cache ------------------------------------
+def _e4m3_kv(inp):
+    """The same pools stored as e4m3 (each value rounded to the nearest e4m3 value by torch's
+    cast: an encoding of the input, no arithmetic of the method).  The oracle decodes the
+    codes exactly, so the parity bar is the one of the bf16 cache."""
+    return {**inp, "k_pool": inp["k_pool"].to(torch.float8_e4m3fn),
+            "v_pool": inp["v_pool"].to(torch.float8_e4m3fn)}
+
+
+def test_e4m3_kv_ragged_lengths(msa):
+    w, inp = _custom([1, 127, 128, 129, 1000, 3000, 2049], seed=14)
+    inp = _e4m3_kv(inp)
+    check(w, inp, gpu_decode(msa, w, inp))
+
+
+@pytest.mark.parametrize("G,k", [(1, 4), (2, 8), (3, 16), (4, 1)])
+def test_e4m3_kv_group_and_k_variants(msa, G, k):
+    w, inp = _custom([300, 5000, 129, 2560], seed=40 + G + k, G=G, k=k)
+    inp = _e4m3_kv(inp)
+    check(w, inp, gpu_decode(msa, w, inp))
+
+
+def test_e4m3_kv_and_index_full_size_decode_workload(msa):
+    """The 64-sequence workload with every pool in e4m3 (index keys, K, V): selection equal to
+    the bf16-index one, O and LSE within the tolerance of the oracle on the e4m3 values."""
+    w0 = synthetic.WORKLOADS["decode_b64_16K_256K"]
+    inp = synthetic.decode_inputs(w0, device="cuda", index_dtype="e4m3")
+    inp = _e4m3_kv(inp)
+    w = inp["workload"]
+    got = gpu_decode(msa, w, inp)
+    check(w, inp, got)
+
+
+def test_e4m3_kv_pools_must_share_a_dtype(msa):
+    w, inp = _custom([300, 700], seed=15)
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    with pytest.raises(msa.MsaError):
+        msa.paged_kv(d["k_idx_pool"], d["k_pool"].to(torch.float8_e4m3fn), d["v_pool"],
+                     d["page_table"], d["seq_lens"])

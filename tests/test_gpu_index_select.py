@@ -59,7 +59,8 @@ def test_ragged_lengths_all_rows(msa, L):
     assert (sel[..., :].max(-1) == np.arange(L) // 128).all()  # local block is the largest id
 
 
-@pytest.mark.parametrize("G,k,L", [(2, 8, 3000), (1, 1, 700), (4, 2, 1500), (2, 16, 640)])
+@pytest.mark.parametrize("G,k,L", [(2, 8, 3000), (1, 1, 700), (4, 2, 1500), (2, 16, 640),
+                                   (3, 6, 1700)])
 def test_group_and_k_variants(msa, G, k, L):
     w = synthetic.Workload("v", "prefill", L=L, Hq=16 * G, G=G, k=k, seed=42 + G + k)
     inp = synthetic.prefill_inputs(w, index_only=True)
@@ -110,7 +111,7 @@ def test_e4m3_ragged_lengths_all_rows(msa, L):
     _check(msa, synthetic.Workload(**{**w.__dict__, "L": L}), inp["q_idx"], inp["k_idx"])
 
 
-@pytest.mark.parametrize("G,k,L", [(2, 8, 3000), (1, 1, 700), (1, 16, 1900)])
+@pytest.mark.parametrize("G,k,L", [(2, 8, 3000), (1, 1, 700), (1, 16, 1900), (3, 12, 1300)])
 def test_e4m3_group_and_k_variants(msa, G, k, L):
     w = synthetic.Workload("v8", "prefill", L=L, Hq=16 * G, G=G, k=k, seed=52 + G + k)
     inp = synthetic.prefill_inputs(w, index_only=True, index_dtype="e4m3")

@@ -5,14 +5,18 @@
 
 A step is one full pass of the hot path over one batch of synthetic input resident in HBM:
 index selection (score + max-pool + top-k) followed by the main branch (scheduling, KV-outer
-attention, combine) on the 64/4-head, L = 32768 prefill workload, then one paged decode step of
-the 64-sequence workload (reported under "decode").  Prints ONE JSON line (rank 0) with:
-  value / roofline / kernel_rooflines  prefill tokens/s and each kernel against the measured peaks
-  e2e                    the same step through the public API from pinned host buffers
-  e4m3_index             the index kernels timed again with e4m3 index vectors (same selections)
-  index_scores           the index kernels timed again exporting every block's pooled score
-  cuda_graph             the small prefill pass eager against a CUDA-graph replay of the same calls
-  cpu_baseline           the CPU oracle on a bounded sample, on this host's cores
+attention, combine) on the 64/4-head, L = 1,048,576 prefill workload with hot key blocks, then
+one paged decode step of the 64-sequence workload (reported under "decode").  Prints ONE JSON line
+(rank 0) with:
+  value / roofline / kernel_rooflines / main_branch  prefill tokens/s and each kernel against the
+                                                     measured peaks
+  e2e                  the same step through the public API from pinned host buffers
+  prefill_workloads    the L = 32,768 and L = 131,072 (clustered) prefills, each timed the same way
+                       with its own rooflines and CPU baseline (and, for 32K, the block-score
+                       export timed beside the selection-only kernels)
+  e4m3_index           the same step timed with e4m3 index vectors (same selections, asserted)
+  cuda_graph           the small prefill pass eager against a CUDA-graph replay of the same calls
+  cpu_baseline         the CPU oracle on a bounded sample, on this host's cores
 
 The path has no exchange step, so N > 1 runs N independent replicas (one per GPU, weak scaling)
 with a barrier and the max over ranks around the timed region.
@@ -44,21 +48,28 @@ METRIC = "MSA prefill tokens/s and decode tokens/s at 1 GB300; % tensor/HBM roof
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=60)
+    p.add_argument("--steps", type=int, default=20)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="msa", choices=["msa", "reference"])
-    p.add_argument("--workload", default="prefill_L32K")
+    p.add_argument("--workload", default="prefill_L1M_hot")
+    p.add_argument("--sub-workloads", default="prefill_L32K,prefill_L128K_clustered",
+                   help="other prefill workloads timed after the headline one (comma list)")
+    p.add_argument("--scores-workload", default="prefill_L32K",
+                   help="the sub-workload on which the block-score export is timed")
     p.add_argument("--decode-workload", default="decode_b64_16K_256K")
     p.add_argument("--decode-batch", type=int, default=0, help="override (profiling)")
     p.add_argument("--decode-nmax", type=int, default=0, help="override (profiling)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e4m3-index", action="store_true",
-                   help="skip timing the e4m3 (FP8) index kernels beside the bf16 step")
+                   help="skip the step with e4m3 (FP8) index vectors")
+    p.add_argument("--e4m3-steps", type=int, default=8)
     p.add_argument("--no-index-scores", action="store_true",
                    help="skip timing the index kernels with the block-score export")
     p.add_argument("--no-graph", action="store_true",
                    help="skip timing the small prefill pass as a CUDA-graph replay")
-    p.add_argument("--e2e-steps", type=int, default=20)
+    p.add_argument("--e2e-steps", type=int, default=10)
+    p.add_argument("--cp-shards", type=int, default=4,
+                   help="shards of the context-parallel decode index branch (0: skip)")
     p.add_argument("--L", type=int, default=0, help="override the workload length (profiling)")
     return p.parse_args()
 
@@ -159,7 +170,7 @@ class ClockSampler:
 
 
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu capture
-# of the named kernel (profiles/ has the capture summaries).  A figure is reported only while the
+# of the named kernel on the named workload.  A figure is reported only while the
 # kernel's sources still hash to the value recorded with it; otherwise the traffic is null.
 CSRC = os.path.join(ROOT, "block_sparse_long_msa_gb300", "csrc")
 KERNEL_SOURCES = {
@@ -171,22 +182,22 @@ KERNEL_SOURCES = {
     "decode_scan_e4m3": ["decode.cu", "common.cuh", "ptx.cuh"],
 }
 NCU_TRAFFIC = {
-    # prefill L=32768, 64/4 heads, k=16 (profiles/dram_prefill_L32K_decode_b64.md)
-    "attention": {"bytes_per_launch": 9828836096, "workload": "prefill_L32K@32768",
-                  "sources_sha256": "7d4d5adc609b717953302cb6c3fc4d49f754da7eae7cf3f27036282b37e8205c"},
-    "combine": {"bytes_per_launch": 9194790912, "workload": "prefill_L32K@32768",
-                "sources_sha256": "7d4d5adc609b717953302cb6c3fc4d49f754da7eae7cf3f27036282b37e8205c"},
-    "index": {"bytes_per_launch": 41903616, "workload": "prefill_L32K@32768",
-              "sources_sha256": "549e86cc1e19b86d0fd21c929853b80722a68fa8fe9701ae39a3cc23b5248ac2"},
-    "index_e4m3": {"bytes_per_launch": 21011413, "workload": "prefill_L32K@32768",
-                   "sources_sha256": "549e86cc1e19b86d0fd21c929853b80722a68fa8fe9701ae39a3cc23b5248ac2"},
+    # prefill L=32768, 64/4 heads, k=16
+    "attention": [{"bytes_per_launch": 9828836096, "workload": "prefill_L32K@32768",
+                   "sources_sha256": "7d4d5adc609b717953302cb6c3fc4d49f754da7eae7cf3f27036282b37e8205c"}],
+    "combine": [{"bytes_per_launch": 9194790912, "workload": "prefill_L32K@32768",
+                 "sources_sha256": "7d4d5adc609b717953302cb6c3fc4d49f754da7eae7cf3f27036282b37e8205c"}],
+    "index": [{"bytes_per_launch": 41903616, "workload": "prefill_L32K@32768",
+               "sources_sha256": "549e86cc1e19b86d0fd21c929853b80722a68fa8fe9701ae39a3cc23b5248ac2"}],
+    "index_e4m3": [{"bytes_per_launch": 21011413, "workload": "prefill_L32K@32768",
+                    "sources_sha256": "549e86cc1e19b86d0fd21c929853b80722a68fa8fe9701ae39a3cc23b5248ac2"}],
     # decode, 64 sequences of 16K-256K tokens
-    "decode_scan": {"bytes_per_launch": 2084700160,
-                    "workload": "decode_b64_16K_256K@64x262144",
-                    "sources_sha256": "994ce2153b759ea1038980cc54121fca1a7ce5a247759beee4807547bab49afc"},
-    "decode_scan_e4m3": {"bytes_per_launch": 1044300331,
-                         "workload": "decode_b64_16K_256K@64x262144",
-                         "sources_sha256": "994ce2153b759ea1038980cc54121fca1a7ce5a247759beee4807547bab49afc"},
+    "decode_scan": [{"bytes_per_launch": 2084700160,
+                     "workload": "decode_b64_16K_256K@64x262144",
+                     "sources_sha256": "994ce2153b759ea1038980cc54121fca1a7ce5a247759beee4807547bab49afc"}],
+    "decode_scan_e4m3": [{"bytes_per_launch": 1044300331,
+                          "workload": "decode_b64_16K_256K@64x262144",
+                          "sources_sha256": "994ce2153b759ea1038980cc54121fca1a7ce5a247759beee4807547bab49afc"}],
 }
 
 
@@ -202,10 +213,10 @@ def sources_sha256(kernel: str) -> str:
 def measured_traffic(kernel: str, workload: str):
     """ncu DRAM bytes per launch, or None unless they were taken on this workload with the
     current kernel sources."""
-    t = NCU_TRAFFIC.get(kernel)
-    if not t or t["workload"] != workload or t["sources_sha256"] != sources_sha256(kernel):
-        return None
-    return t["bytes_per_launch"]
+    for t in NCU_TRAFFIC.get(kernel, []):
+        if t["workload"] == workload and t["sources_sha256"] == sources_sha256(kernel):
+            return t["bytes_per_launch"]
+    return None
 
 
 def load_peaks():
@@ -240,183 +251,337 @@ def prefill_work(w, sel_counts=None):
     }
 
 
-def decode_work(w, seq_lens, index_bytes=2):
+def decode_work(w, seq_lens, index_bytes=2, kv_bytes=2):
     """Algorithmic bytes of one decode step: the scan reads every index key strictly before each
     query's page (plus the index queries); the attention reads K and V of the selected pages
-    (the local page up to n) plus q and o.  index_bytes: bytes per index element (2 bf16, 1
-    e4m3)."""
+    (the local page up to n) plus q and o.  index_bytes / kv_bytes: bytes per element of the
+    index keys and of the K/V pools (2 bf16, 1 e4m3)."""
     lens = [int(n) for n in seq_lens]
     scan = acc.decode_index_bytes(lens, w.B, w.di, w.G) * index_bytes // 2
-    attn = acc.decode_attn_bytes(lens, w.B, w.d, w.G, w.Hq, w.k)
+    attn = acc.decode_attn_bytes(lens, w.B, w.d, w.G, w.Hq, w.k, kv_bytes=kv_bytes)
     return {"scan_bytes": scan, "attn_bytes": attn}
 
 
 # ------------------------------------------------------------------------------------------
 # MSA arm
 # ------------------------------------------------------------------------------------------
-def run_msa(args, world, rank):
-    import block_sparse_long_msa_gb300 as msa
-    msa.lib()
-    w = workload(args)
-    assert w.kind == "prefill", "the bench step is the prefill pass"
-    dev = torch.device("cuda", torch.cuda.current_device())
-    inp = synthetic.prefill_inputs(w, device=dev)
-    cfg = msa.config(w.G, w.hpg, w.k, w.scale)
-    L = w.L
-    sel = torch.empty((w.G, L, w.k), dtype=torch.int32, device=dev)
-    o = torch.empty((L, w.Hq, w.d), dtype=torch.bfloat16, device=dev)
-    lse = torch.empty((w.Hq, L), dtype=torch.float32, device=dev)
-    ws_bytes = max(msa.msa_attn_prefill_workspace(cfg, L),
-                   msa.msa_index_select_workspace(cfg, L, L))
-    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
-    nchunks = -(-L // msa.msa_prefill_chunk_tokens(cfg, L))
-    launches_per_step = 1 + msa.msa_attn_prefill_launches(cfg, L)
-    stream = torch.cuda.current_stream()
+def _event(stream):
+    e = torch.cuda.Event(enable_timing=True)
+    e.record(stream)  # materialise the handle
+    return e
 
-    def ev():
-        e = torch.cuda.Event(enable_timing=True)
-        e.record(stream)  # materialise the handle
-        return e
 
-    nmarks = 3 * nchunks + 1
+class PrefillCase:
+    """Device inputs, outputs and workspace of one prefill workload, and the calls of a pass."""
 
-    # ---- decode: one new token for each of the 64 sequences of the paged workload ----
-    dw0 = synthetic.WORKLOADS[args.decode_workload]
-    dinp = synthetic.decode_inputs(dw0, device=dev, batch=args.decode_batch or None,
-                                   n_hi=args.decode_nmax or None)
-    dw = dinp["workload"]
-    dcfg = msa.config(dw.G, dw.hpg, dw.k, dw.scale)
-    paged = msa.paged_kv(dinp["k_idx_pool"], dinp["k_pool"], dinp["v_pool"], dinp["page_table"],
-                         dinp["seq_lens"])
-    dsel = torch.empty((dw.G, dw.batch, dw.k), dtype=torch.int32, device=dev)
-    do = torch.empty((dw.batch, dw.Hq, dw.d), dtype=torch.bfloat16, device=dev)
-    dlse = torch.empty((dw.Hq, dw.batch), dtype=torch.float32, device=dev)
-    dws = torch.zeros(max(msa.msa_index_select_workspace(dcfg, dw.batch, 0, paged),
-                          msa.msa_attn_decode_workspace(dcfg, paged)), dtype=torch.uint8,
-                      device=dev)
-    dec_launches = 4
+    def __init__(self, msa, w, dev, index_dtype="bf16"):
+        self.msa, self.w = msa, w
+        self.inp = synthetic.prefill_inputs(w, device=dev, index_dtype=index_dtype)
+        self.cfg = msa.config(w.G, w.hpg, w.k, w.scale, index_dtype=index_dtype)
+        L = w.L
+        self.sel = torch.empty((w.G, L, w.k), dtype=torch.int32, device=dev)
+        self.o = torch.empty((L, w.Hq, w.d), dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty((w.Hq, L), dtype=torch.float32, device=dev)
+        self.ws = torch.zeros(max(msa.msa_attn_prefill_workspace(self.cfg, L),
+                                  msa.msa_index_select_workspace(self.cfg, L, L)),
+                              dtype=torch.uint8, device=dev)
+        self.nchunks = -(-L // msa.msa_prefill_chunk_tokens(self.cfg, L))
+        self.launches = 1 + msa.msa_attn_prefill_launches(self.cfg, L)
 
-    def step(marks=None, start=None, dmarks=None):
+    def nmarks(self):
+        return 3 * self.nchunks + 1
+
+    def run(self, marks=None, start=None, stream=None, cfg_index=None, q_idx=None, k_idx=None):
+        """Index selection, then the main branch.  cfg_index/q_idx/k_idx: another encoding of
+        the same index vectors (the e4m3 indexer)."""
         if start is not None:
             start.record(stream)
-        msa.msa_index_select(cfg, inp["q_idx"], inp["k_idx"], sel=sel, ws=ws)
-        msa.msa_attn_prefill(cfg, inp["q"], inp["k"], inp["v"], sel, o=o, lse=lse, ws=ws,
-                             marks=marks)
-        if dmarks is not None:
-            dmarks[0].record(stream)
-        msa.msa_index_select(dcfg, dinp["q_idx"], paged=paged, sel=dsel, ws=dws)
-        if dmarks is not None:
-            dmarks[1].record(stream)
-        msa.msa_attn_decode(dcfg, dinp["q"], paged, dsel, o=do, lse=dlse, ws=dws)
-        if dmarks is not None:
-            dmarks[2].record(stream)
+        self.msa.msa_index_select(cfg_index or self.cfg,
+                                  self.inp["q_idx"] if q_idx is None else q_idx,
+                                  self.inp["k_idx"] if k_idx is None else k_idx, sel=self.sel,
+                                  ws=self.ws, stream=stream)
+        self.msa.msa_attn_prefill(self.cfg, self.inp["q"], self.inp["k"], self.inp["v"],
+                                  self.sel, o=self.o, lse=self.lse, ws=self.ws, stream=stream,
+                                  marks=marks)
 
-    for _ in range(args.warmup):
+    def phases(self, starts, marks):
+        """Per-step milliseconds of each phase, from the events of run(marks, start)."""
+        n = len(starts)
+        ph = {"index": 0.0, "schedule": 0.0, "attention": 0.0, "combine": 0.0, "prefill": 0.0}
+        for s in range(n):
+            m = marks[s]
+            ph["index"] += starts[s].elapsed_time(m[0])
+            for c in range(self.nchunks):
+                ph["schedule"] += m[3 * c].elapsed_time(m[3 * c + 1])
+                ph["attention"] += m[3 * c + 1].elapsed_time(m[3 * c + 2])
+                ph["combine"] += m[3 * c + 2].elapsed_time(m[3 * c + 3])
+            ph["prefill"] += starts[s].elapsed_time(m[-1])
+        return {k: v / n for k, v in ph.items()}
+
+
+class DecodeCase:
+    """The paged decode workload: one new token for each sequence."""
+
+    def __init__(self, msa, dw0, dev, batch=None, n_hi=None, index_dtype="bf16"):
+        self.msa = msa
+        self.inp = synthetic.decode_inputs(dw0, device=dev, batch=batch, n_hi=n_hi,
+                                           index_dtype=index_dtype)
+        dw = self.w = self.inp["workload"]
+        self.cfg = msa.config(dw.G, dw.hpg, dw.k, dw.scale, index_dtype=index_dtype)
+        self.paged = msa.paged_kv(self.inp["k_idx_pool"], self.inp["k_pool"], self.inp["v_pool"],
+                                  self.inp["page_table"], self.inp["seq_lens"])
+        self.sel = torch.empty((dw.G, dw.batch, dw.k), dtype=torch.int32, device=dev)
+        self.o = torch.empty((dw.batch, dw.Hq, dw.d), dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty((dw.Hq, dw.batch), dtype=torch.float32, device=dev)
+        self.ws = torch.zeros(max(msa.msa_index_select_workspace(self.cfg, dw.batch, 0,
+                                                                 self.paged),
+                                  msa.msa_attn_decode_workspace(self.cfg, self.paged)),
+                              dtype=torch.uint8, device=dev)
+        self.launches = 4
+
+    def with_encoding(self, cfg, k_idx_pool, k_pool, v_pool):
+        self.cfg = cfg
+        self.paged = self.msa.paged_kv(k_idx_pool, k_pool, v_pool, self.inp["page_table"],
+                                       self.inp["seq_lens"])
+        return self
+
+    def run(self, marks=None, stream=None, q_idx=None):
+        if marks is not None:
+            marks[0].record(stream)
+        self.msa.msa_index_select(self.cfg, self.inp["q_idx"] if q_idx is None else q_idx,
+                                  paged=self.paged, sel=self.sel, ws=self.ws, stream=stream)
+        if marks is not None:
+            marks[1].record(stream)
+        self.msa.msa_attn_decode(self.cfg, self.inp["q"], self.paged, self.sel, o=self.o,
+                                 lse=self.lse, ws=self.ws, stream=stream)
+        if marks is not None:
+            marks[2].record(stream)
+
+
+def check_status(msa, *wss):
+    for ws in wss:
+        st = msa.msa_get_device_status(ws)
+        if st != 0:
+            raise RuntimeError(f"device status {st}")
+
+
+def prefill_report(w, ph, nchunks, peaks):
+    """Rooflines of one prefill pass from its per-step phase times (ms).
+
+    The index kernel and the attention kernel are contractions: their achieved rate is their
+    algorithmic FLOPs over their time, against the bf16 tensor peak (burst for passes of a few
+    milliseconds, sustained for passes that run for tenths of a second and more, as the long
+    step keeps the part at its power limit).  The attention's HBM rate of its algorithmic bytes
+    is given beside it; the combine is a stream over the partials (HBM)."""
+    work = prefill_work(w)
+    long_pass = ph["prefill"] >= 50.0
+    t_peak = peaks["bf16_tflops_sustained"] if long_pass else peaks["bf16_tflops"]
+    t_kind = "sustained" if long_pass else "burst"
+    main_ms = ph["schedule"] + ph["attention"] + ph["combine"]
+    idx_tf = work["index_flops"] / (ph["index"] * 1e-3) / 1e12
+    att_tf = work["attn_flops"] / (ph["attention"] * 1e-3) / 1e12
+    att_gbs = work["attn_bytes"] / (ph["attention"] * 1e-3) / 1e9
+    com_gbs = work["combine_bytes"] / (ph["combine"] * 1e-3) / 1e9
+    main_tf = work["attn_flops"] / (main_ms * 1e-3) / 1e12
+
+    def tensor(a):
+        return {"bound": "tensor", "achieved": a, "peak": t_peak, "unit": "TFLOP/s",
+                "frac": a / t_peak, "peak_kind": t_kind,
+                "frac_of_burst": a / peaks["bf16_tflops"],
+                "frac_of_sustained": a / peaks["bf16_tflops_sustained"]}
+
+    kernels = {
+        "index": {**tensor(idx_tf), "ms_per_launch": ph["index"],
+                  "algorithmic_flops": work["index_flops"]},
+        "attention": {**tensor(att_tf), "ms_per_launch": ph["attention"] / nchunks,
+                      "algorithmic_flops": work["attn_flops"],
+                      "hbm_gbs_of_algorithmic_bytes": att_gbs,
+                      "hbm_frac": att_gbs / peaks["hbm_gbs"],
+                      "algorithmic_bytes": work["attn_bytes"]},
+        "combine": {"bound": "hbm", "achieved": com_gbs, "peak": peaks["hbm_gbs"],
+                    "unit": "GB/s", "frac": com_gbs / peaks["hbm_gbs"],
+                    "ms_per_launch": ph["combine"] / nchunks,
+                    "algorithmic_bytes": work["combine_bytes"]},
+    }
+    main = {**tensor(main_tf), "ms": main_ms,
+            "note": "attention FLOPs over schedule + attention + combine time"}
+    dominant = max(("index", "attention", "combine"), key=lambda n: ph[n])
+    return work, kernels, main, dominant
+
+
+def prefill_object(case, ph, peaks, world, steps):
+    w = case.w
+    work, kernels, main, dominant = prefill_report(w, ph, case.nchunks, peaks)
+    dk = kernels[dominant]
+    traffic = measured_traffic(dominant, f"{w.name}@{w.L}")
+    roof = {"bound": dk["bound"], "kernel": dominant, "achieved": dk["achieved"],
+            "peak": dk["peak"], "unit": dk["unit"], "frac": dk["frac"],
+            "traffic": traffic,
+            "peak_source": peaks["source"]}
+    return {
+        "workload": w.name, "L": w.L,
+        "value": world * w.L / (ph["prefill"] * 1e-3), "unit": "tokens/s",
+        "ms_per_pass": ph["prefill"],
+        "phases_ms_per_pass": {k: ph[k] for k in ("index", "schedule", "attention", "combine")},
+        "query_chunks": case.nchunks,
+        "roofline": roof,
+        "kernel_rooflines": kernels,
+        "main_branch": main,
+        "gpu_launches": case.launches * steps,
+    }
+
+
+def decode_object(dc, ph, peaks, world, steps, index_bytes=2, kv_bytes=2):
+    dw = dc.w
+    dwork = decode_work(dw, dc.inp["seq_lens"].tolist(), index_bytes=index_bytes,
+                        kv_bytes=kv_bytes)
+    sel_ms, att_ms = ph["index_select"], ph["attention"]
+    step_ms = sel_ms + att_ms
+    scan_gbs = dwork["scan_bytes"] / (sel_ms * 1e-3) / 1e9
+    att_gbs = dwork["attn_bytes"] / (att_ms * 1e-3) / 1e9
+    step_gbs = (dwork["scan_bytes"] + dwork["attn_bytes"]) / (step_ms * 1e-3) / 1e9
+    scan_kernel = "decode_scan" if index_bytes == 2 else "decode_scan_e4m3"
+    return {
+        "metric": "MSA paged decode tokens/s (one new token per sequence per step)",
+        "value": world * dw.batch / (step_ms * 1e-3), "unit": "tokens/s",
+        "ms_per_step": step_ms,
+        "config": {"workload": dw.name, "batch": dw.batch, "n_min": dw.n_lo, "n_max": dw.n_hi,
+                   "context_tokens": int(dc.inp["seq_lens"].sum().item()), "Hq": dw.Hq,
+                   "G": dw.G, "k": dw.k, "pages": dc.inp["num_pages"],
+                   "index_dtype": "bf16" if index_bytes == 2 else "e4m3",
+                   "kv_dtype": "bf16" if kv_bytes == 2 else "e4m3"},
+        "phases_ms_per_step": {"index_select": sel_ms, "attention": att_ms},
+        "roofline": {"bound": "hbm", "kernel": "index page scan (+ top-k merge)",
+                     "achieved": scan_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": scan_gbs / peaks["hbm_gbs"],
+                     "frac_vs_8TBs": scan_gbs / 8000.0,
+                     "traffic": measured_traffic(scan_kernel,
+                                                 f"{dw.name}@{dw.batch}x{dw.n_hi}"),
+                     "peak_source": peaks["source"]},
+        "attention_roofline": {"bound": "hbm", "achieved": att_gbs, "peak": peaks["hbm_gbs"],
+                               "unit": "GB/s", "frac": att_gbs / peaks["hbm_gbs"],
+                               "frac_vs_8TBs": att_gbs / 8000.0},
+        "step_hbm_frac": step_gbs / peaks["hbm_gbs"],
+        "step_hbm_frac_vs_8TBs": step_gbs / 8000.0,
+        "hbm_frac_headline": "frac: against the measured copy bandwidth of this GPU; "
+                             "frac_vs_8TBs: against a nominal 8 TB/s",
+        "algorithmic_bytes": dwork,
+        "gpu_launches": dc.launches * steps,
+        "cpu_baseline": None,
+    }
+
+
+def time_prefill_decode(case, dc, steps, warmup, world, stream, clocks=False, **kw):
+    """Warm-up, then `steps` timed steps of prefill (+ decode when dc is given).  Returns the
+    total milliseconds (max over ranks), the prefill phases, the decode phases and the clock
+    summary (when asked)."""
+    def step(marks=None, start=None, dmarks=None):
+        case.run(marks=marks, start=start, stream=stream, **kw)
+        if dc is not None:
+            dc.run(marks=dmarks, stream=stream)
+
+    for _ in range(warmup):
         step()
     torch.cuda.synchronize()
-    status = msa.msa_get_device_status(ws) or msa.msa_get_device_status(dws)
-    if status != 0:
-        raise RuntimeError(f"device status {status} after warm-up")
-
-    starts = [ev() for _ in range(args.steps)]
-    marks = [[ev() for _ in range(nmarks)] for _ in range(args.steps)]
-    dmarks = [[ev() for _ in range(3)] for _ in range(args.steps)]
-    t0, t1 = ev(), ev()
+    check_status(case.msa, case.ws, *([dc.ws] if dc is not None else []))
+    starts = [_event(stream) for _ in range(steps)]
+    marks = [[_event(stream) for _ in range(case.nmarks())] for _ in range(steps)]
+    dmarks = [[_event(stream) for _ in range(3)] for _ in range(steps)]
+    t0, t1 = _event(stream), _event(stream)
     torch.cuda.synchronize()
-    with ClockSampler(torch.cuda.current_device()) as clocks:
-        barrier(world)
-        torch.cuda.synchronize()
-        t0.record(stream)
-        for s in range(args.steps):
-            step(marks[s], starts[s], dmarks[s])
-        t1.record(stream)
-        torch.cuda.synchronize()
-        barrier(world)
-    total_ms = t0.elapsed_time(t1)
-    total_ms = max_over_ranks(total_ms, world)
+    sampler = ClockSampler(torch.cuda.current_device()) if clocks else None
+    if sampler:
+        sampler.__enter__()
+    barrier(world)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for s in range(steps):
+        step(marks[s], starts[s], dmarks[s] if dc is not None else None)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    if sampler:
+        sampler.__exit__(None, None, None)
+    check_status(case.msa, case.ws, *([dc.ws] if dc is not None else []))
+    total_ms = max_over_ranks(t0.elapsed_time(t1), world)
+    ph = case.phases(starts, marks)
+    ph = {k: max_over_ranks(v, world) for k, v in ph.items()}
+    dph = None
+    if dc is not None:
+        dph = {"index_select": sum(d[0].elapsed_time(d[1]) for d in dmarks) / steps,
+               "attention": sum(d[1].elapsed_time(d[2]) for d in dmarks) / steps}
+        dph = {k: max_over_ranks(v, world) for k, v in dph.items()}
+    return total_ms, ph, dph, (sampler.summary() if sampler else None)
 
-    phase = {"index": 0.0, "schedule": 0.0, "attention": 0.0, "combine": 0.0}
-    for s in range(args.steps):
-        m = marks[s]
-        phase["index"] += starts[s].elapsed_time(m[0])
-        for c in range(nchunks):
-            phase["schedule"] += m[3 * c].elapsed_time(m[3 * c + 1])
-            phase["attention"] += m[3 * c + 1].elapsed_time(m[3 * c + 2])
-            phase["combine"] += m[3 * c + 2].elapsed_time(m[3 * c + 3])
-    dec_sel_ms = sum(d[0].elapsed_time(d[1]) for d in dmarks) / args.steps
-    dec_attn_ms = sum(d[1].elapsed_time(d[2]) for d in dmarks) / args.steps
-    prefill_ms = sum(starts[s].elapsed_time(marks[s][-1]) for s in range(args.steps)) / args.steps
-    dec_ms = dec_sel_ms + dec_attn_ms
-    per_launch_ms = {"index": phase["index"] / args.steps,
-                     "attention": phase["attention"] / (args.steps * nchunks),
-                     "combine": phase["combine"] / (args.steps * nchunks)}
 
-    work = prefill_work(w)
-    peaks = load_peaks()
-    tensor_peak = peaks["bf16_tflops"]
-    roof = {
-        "index": ("tensor", work["index_flops"] / (per_launch_ms["index"] * 1e-3) / 1e12,
-                  tensor_peak, "TFLOP/s"),
-        "attention": ("hbm", work["attn_bytes"] / nchunks / (per_launch_ms["attention"] * 1e-3)
-                      / 1e9, peaks["hbm_gbs"], "GB/s"),
-        "combine": ("hbm", work["combine_bytes"] / nchunks / (per_launch_ms["combine"] * 1e-3)
-                    / 1e9, peaks["hbm_gbs"], "GB/s"),
-    }
-    dominant = max(("index", "attention", "combine"), key=lambda n: phase[n])
-    bound, achieved, peak, unit = roof[dominant]
-    traffic = measured_traffic(dominant, f"{w.name}@{L}")
+def host_memory_available():
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return 0
 
-    # ---------------- end-to-end through the public API from pinned host buffers ------------
-    # Each step copies its inputs in from pinned host memory and its results out, through the
-    # same public calls.  The prefill tensors are double-buffered on the device and the copies
-    # run on their own streams, so step s+1's inputs arrive and step s-1's results leave while
-    # step s computes; the decode step's small inputs and outputs travel on the compute stream.
-    e2e_on = args.e2e_steps > 0
-    pin = (lambda t: t.cpu().pin_memory()) if e2e_on else (lambda t: t[:0].cpu())
+
+def e2e_leg(msa, case, dc, steps, world, stream):
+    """The same step through the public API with every step's inputs copied in from pinned host
+    memory and its results copied back (inside the timed region).  The prefill tensors are
+    double-buffered on the device and the copies run on copy streams of their own, so step s+1's
+    inputs arrive and step s-1's results leave while step s computes; the decode step's small
+    inputs and outputs travel on the compute stream.  Returns (ms, h2d bytes, d2h bytes)."""
     names_in = ("q", "k", "v", "q_idx", "k_idx")
-    host_in = {k: pin(inp[k]) for k in names_in}
-    host_out = [pin(t) for t in (o, lse, sel)]
-    nbuf = 2 if e2e_on else 1
-    dev_in = [{k: torch.empty_like(inp[k]) if e2e_on else inp[k] for k in names_in}
-              for _ in range(nbuf)]
-    dev_out = [[torch.empty_like(t) if e2e_on else t for t in (o, lse, sel)] for _ in range(nbuf)]
+    inp = case.inp
+    outs = (case.o, case.lse, case.sel)
     h2d = sum(inp[k].numel() * inp[k].element_size() for k in names_in)
-    d2h = sum(t.numel() * t.element_size() for t in (o, lse, sel))
+    d2h = sum(t.numel() * t.element_size() for t in outs)
+    dnames = ("q", "q_idx", "seq_lens", "page_table")
+    h2d += sum(dc.inp[k].numel() * dc.inp[k].element_size() for k in dnames)
+    d2h += sum(t.numel() * t.element_size() for t in (dc.o, dc.lse, dc.sel))
 
-    dhost_in = {k: pin(dinp[k]) for k in ("q", "q_idx", "seq_lens", "page_table")}
-    ddev_in = {k: dinp[k] for k in dhost_in}
-    dhost_out = [pin(t) for t in (do, dlse, dsel)]
-    h2d += sum(dinp[k].numel() * dinp[k].element_size() for k in dhost_in)
-    d2h += sum(t.numel() * t.element_size() for t in (do, dlse, dsel))
+    def pinned_copy(t):
+        h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+        h.copy_(t)
+        return h
 
+    host_in = {k: pinned_copy(inp[k]) for k in names_in}
+    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+    dev_in = [{k: inp[k] for k in names_in}, {k: torch.empty_like(inp[k]) for k in names_in}]
+    dev_out = [list(outs), [torch.empty_like(t) for t in outs]]
+    dhost_in = {k: pinned_copy(dc.inp[k]) for k in dnames}
+    ddev_in = {k: dc.inp[k] for k in dnames}
+    dhost_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                 for t in (dc.o, dc.lse, dc.sel)]
     s_h2d, s_d2h = torch.cuda.Stream(), torch.cuda.Stream()
-    ev_in = [torch.cuda.Event() for _ in range(nbuf)]      # inputs of buffer b landed
-    ev_used = [torch.cuda.Event() for _ in range(nbuf)]    # compute done with buffer b
-    ev_out = [torch.cuda.Event() for _ in range(nbuf)]     # results of buffer b copied out
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_used = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+    cfg = case.cfg
 
     def e2e_step(i):
-        b = i % nbuf
+        b = i % 2
         with torch.cuda.stream(s_h2d):
-            if i >= nbuf:
+            if i >= 2:
                 s_h2d.wait_event(ev_used[b])
             for k_, t in host_in.items():
                 dev_in[b][k_].copy_(t, non_blocking=True)
             ev_in[b].record(s_h2d)
         stream.wait_event(ev_in[b])
-        if i >= nbuf:
+        if i >= 2:
             stream.wait_event(ev_out[b])
         ob, lb, sb = dev_out[b]
         di = dev_in[b]
-        msa.msa_index_select(cfg, di["q_idx"], di["k_idx"], sel=sb, ws=ws, stream=stream)
-        msa.msa_attn_prefill(cfg, di["q"], di["k"], di["v"], sb, o=ob, lse=lb, ws=ws,
+        msa.msa_index_select(cfg, di["q_idx"], di["k_idx"], sel=sb, ws=case.ws, stream=stream)
+        msa.msa_attn_prefill(cfg, di["q"], di["k"], di["v"], sb, o=ob, lse=lb, ws=case.ws,
                              stream=stream)
         for k_, t in dhost_in.items():
             ddev_in[k_].copy_(t, non_blocking=True)
-        msa.msa_index_select(dcfg, ddev_in["q_idx"], paged=paged, sel=dsel, ws=dws,
+        msa.msa_index_select(dc.cfg, ddev_in["q_idx"], paged=dc.paged, sel=dc.sel, ws=dc.ws,
                              stream=stream)
-        msa.msa_attn_decode(dcfg, ddev_in["q"], paged, dsel, o=do, lse=dlse, ws=dws,
-                            stream=stream)
-        for hd, t in zip(dhost_out, (do, dlse, dsel)):
+        msa.msa_attn_decode(dc.cfg, ddev_in["q"], dc.paged, dc.sel, o=dc.o, lse=dc.lse,
+                            ws=dc.ws, stream=stream)
+        for hd, t in zip(dhost_out, (dc.o, dc.lse, dc.sel)):
             hd.copy_(t, non_blocking=True)
         ev_used[b].record(stream)
         with torch.cuda.stream(s_d2h):
@@ -425,285 +590,348 @@ def run_msa(args, world, rank):
                 hd.copy_(t, non_blocking=True)
             ev_out[b].record(s_d2h)
 
-    e2e_ms = None
-    if args.e2e_steps > 0:
-        for i in range(2 * nbuf):
-            e2e_step(i)
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        barrier(world)
-        torch.cuda.synchronize()
-        e0.record(s_h2d)  # the first operation of the timed region
-        for i in range(args.e2e_steps):
-            e2e_step(i)
-        s_d2h.wait_stream(stream)
-        e1.record(s_d2h)  # after the last copy out, which follows everything else
-        torch.cuda.synchronize()
-        e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
-        # the pipelined step computed the same selection as the resident-input step
-        assert torch.equal(host_out[2], sel.cpu()), "end-to-end selection differs"
-    status = msa.msa_get_device_status(ws)
-    if status != 0:
-        raise RuntimeError(f"device status {status} after timed region")
+    ref_sel = case.sel.clone()  # the resident-input step's selection
+    for i in range(4):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0.record(s_h2d)  # the first operation of the timed region
+    for i in range(steps):
+        e2e_step(i)
+    s_d2h.wait_stream(stream)
+    e1.record(s_d2h)  # after the last copy out, which follows everything else
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1), world)
+    check_status(msa, case.ws, dc.ws)
+    # the pipelined steps computed the same selection as the resident-input step
+    assert torch.equal(host_out[2], ref_sel.cpu()), "end-to-end selection differs"
+    del host_in, host_out, dev_in, dev_out, dhost_in, dhost_out
+    return ms, h2d, d2h
 
-    # ---- e4m3 index vectors (the FP8 indexer, tcgen05 kind::f8f6f4): the integer/8 index
-    # inputs are exact in e4m3, so the selections must equal the bf16 ones; the two index
-    # kernels are timed alone and the step throughputs recomputed with their times ----
+
+def timed_alone(fn, n, warmup, stream):
+    for _ in range(max(3, warmup)):
+        fn()
+    a0, a1 = _event(stream), _event(stream)
+    torch.cuda.synchronize()
+    a0.record(stream)
+    for _ in range(n):
+        fn()
+    a1.record(stream)
+    torch.cuda.synchronize()
+    return a0.elapsed_time(a1) / n
+
+
+def run_msa(args, world, rank):
+    import block_sparse_long_msa_gb300 as msa
+    msa.lib()
+    peaks = load_peaks()
+    w = workload(args)
+    assert w.kind == "prefill", "the bench step is a prefill pass plus a decode step"
+    dev = torch.device("cuda", torch.cuda.current_device())
+    stream = torch.cuda.current_stream()
+    K, W = args.steps, args.warmup
+
+    # ---------------- headline: prefill of the main workload + one decode step ----------------
+    case = PrefillCase(msa, w, dev)
+    dc = DecodeCase(msa, synthetic.WORKLOADS[args.decode_workload], dev,
+                    batch=args.decode_batch or None, n_hi=args.decode_nmax or None)
+    total_ms, ph, dph, clocks = time_prefill_decode(case, dc, K, W, world, stream, clocks=True)
+    head = prefill_object(case, ph, peaks, world, K)
+    decode = decode_object(dc, dph, peaks, world, K)
+
+    # ---------------- end to end through the public API from pinned host buffers -------------
+    e2e = None
+    if args.e2e_steps > 0:
+        need = 1.6 * sum(t.numel() * t.element_size()
+                         for t in list(case.inp[k] for k in ("q", "k", "v", "q_idx", "k_idx"))
+                         + [case.o, case.lse, case.sel])
+        avail = host_memory_available()
+        if avail and avail < need:
+            e2e = {"value": None, "unit": "tokens/s",
+                   "skipped": f"host memory available {avail / 2**30:.0f} GiB < "
+                              f"{need / 2**30:.0f} GiB"}
+        else:
+            ms, h2d, d2h = e2e_leg(msa, case, dc, args.e2e_steps, world, stream)
+            e2e = {"value": world * w.L * args.e2e_steps / (ms * 1e-3), "unit": "tokens/s",
+                   "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                   "steps": args.e2e_steps, "ms_per_step": ms / args.e2e_steps,
+                   "note": "prefill tokens over the whole step (prefill + decode) with every "
+                           "step's inputs copied from pinned host memory and its outputs copied "
+                           "back, on copy streams of their own (device buffers doubled, so the "
+                           "copies of neighbouring steps overlap the compute); the decode KV "
+                           "cache is resident state"}
+
+    # ---- e4m3 index vectors (the FP8 indexer, tcgen05 kind::f8f6f4): a real e4m3 step, timed
+    # like the headline one; the integer/8 inputs are exact in e4m3, so the selections must be
+    # the bf16 ones ----
     e4m3 = None
     if not args.no_e4m3_index:
         f8 = torch.float8_e4m3fn
-        q8, k8 = inp["q_idx"].to(f8), inp["k_idx"].to(f8)
-        dq8, dk8 = dinp["q_idx"].to(f8), dinp["k_idx_pool"].to(f8)
+        ref_sel, ref_dsel = case.sel.clone(), dc.sel.clone()
+        q8, k8 = case.inp["q_idx"].to(f8), case.inp["k_idx"].to(f8)
         cfg8 = msa.config(w.G, w.hpg, w.k, w.scale, index_dtype="e4m3")
-        dcfg8 = msa.config(dw.G, dw.hpg, dw.k, dw.scale, index_dtype="e4m3")
-        paged8 = msa.paged_kv(dk8, dinp["k_pool"], dinp["v_pool"], dinp["page_table"],
-                              dinp["seq_lens"])
-        sel8, dsel8 = torch.empty_like(sel), torch.empty_like(dsel)
-
-        def timed(fn, n):
-            for _ in range(max(3, args.warmup)):
-                fn()
-            a0, a1 = ev(), ev()
-            torch.cuda.synchronize()
-            a0.record(stream)
-            for _ in range(n):
-                fn()
-            a1.record(stream)
-            torch.cuda.synchronize()
-            return a0.elapsed_time(a1) / n
-
-        n8 = max(3, args.steps)
-        idx8_ms = timed(lambda: msa.msa_index_select(cfg8, q8, k8, sel=sel8, ws=ws), n8)
-        didx8_ms = timed(lambda: msa.msa_index_select(dcfg8, dq8, paged=paged8, sel=dsel8,
-                                                      ws=dws), n8)
-        msa.msa_index_select(cfg, inp["q_idx"], inp["k_idx"], sel=sel, ws=ws)
-        msa.msa_index_select(dcfg, dinp["q_idx"], paged=paged, sel=dsel, ws=dws)
+        dw = dc.w
+        dcfg_bf16, dpaged_bf16 = dc.cfg, dc.paged
+        dk8 = dc.inp["k_idx_pool"].to(f8)
+        dq8 = dc.inp["q_idx"].to(f8)
+        kp8, vp8 = dc.inp["k_pool"].to(f8), dc.inp["v_pool"].to(f8)  # the FP8 K/V cache
+        dc.with_encoding(msa.config(dw.G, dw.hpg, dw.k, dw.scale, index_dtype="e4m3"), dk8,
+                         kp8, vp8)
+        dq_bf16 = dc.inp["q_idx"]
+        dc.inp["q_idx"] = dq8
+        K8 = max(3, min(K, args.e4m3_steps))
+        _, ph8, dph8, _ = time_prefill_decode(case, dc, K8, min(W, 3), world, stream,
+                                              cfg_index=cfg8, q_idx=q8, k_idx=k8)
         torch.cuda.synchronize()
-        assert torch.equal(sel8, sel) and torch.equal(dsel8, dsel), "e4m3 selection differs"
-        idx16_ms = phase["index"] / args.steps
-        pre8_ms = prefill_ms - idx16_ms + idx8_ms
-        dec8_ms = dec_attn_ms + didx8_ms
-        scan8_bytes = decode_work(dw, dinp["seq_lens"].tolist(), index_bytes=1)["scan_bytes"]
+        assert torch.equal(case.sel, ref_sel) and torch.equal(dc.sel, ref_dsel), \
+            "e4m3 selection differs"
+        pre8 = prefill_object(case, ph8, peaks, world, K8)
+        fp8_peak = 2 * (peaks["bf16_tflops_sustained"] if ph8["prefill"] >= 50.0
+                        else peaks["bf16_tflops"])
+        idx_tf = pre8["kernel_rooflines"]["index"]["achieved"]
         e4m3 = {
             "note": "index vectors in e4m3 (exact for the integer/8 inputs: same selections, "
-                    "asserted); the main branch is unchanged, so the step times below are the "
-                    "measured bf16 steps with the e4m3 index kernels' measured times in place "
-                    "of the bf16 ones",
-            "prefill_index_ms": idx8_ms, "prefill_index_ms_bf16": idx16_ms,
-            "prefill_index_tflops": work["index_flops"] / (idx8_ms * 1e-3) / 1e12,
-            "prefill_index_frac_of_fp8_peak": work["index_flops"] / (idx8_ms * 1e-3) / 1e12
-                                              / (2 * tensor_peak),
-            "prefill_tokens_per_s": world * L / (pre8_ms * 1e-3),
-            "decode_index_ms": didx8_ms, "decode_index_ms_bf16": dec_sel_ms,
-            "decode_scan_gbs": scan8_bytes / (didx8_ms * 1e-3) / 1e9,
-            "traffic": {"prefill_index": measured_traffic("index_e4m3", f"{w.name}@{L}"),
-                        "decode_scan": measured_traffic("decode_scan_e4m3",
-                                                        f"{dw.name}@{dw.batch}x{dw.n_hi}")},
-            "decode_tokens_per_s": world * dw.batch / (dec8_ms * 1e-3),
-            "gpu_launches": 3 * n8,
+                    "asserted); steps timed as the headline step (index select + main branch, "
+                    "then the decode step with every pool in e4m3: index keys, K and V)",
+            "prefill_tokens_per_s": pre8["value"], "prefill_ms_per_pass": pre8["ms_per_pass"],
+            "phases_ms_per_pass": pre8["phases_ms_per_pass"],
+            "prefill_index_tflops": idx_tf,
+            "prefill_index_frac_of_fp8_peak": idx_tf / fp8_peak,
+            "fp8_peak_tflops": fp8_peak,
+            "fp8_peak_note": "the measured bf16 peak x 2 (the nominal fp8:bf16 ratio)",
+            "decode": decode_object(dc, dph8, peaks, world, K8, index_bytes=1, kv_bytes=1),
+            "steps": K8,
+            "gpu_launches": (case.launches + dc.launches) * K8,
         }
+        e4m3["decode"].pop("cpu_baseline", None)
+        dc.cfg, dc.paged = dcfg_bf16, dpaged_bf16
+        dc.inp["q_idx"] = dq_bf16
+        del q8, k8, dk8, dq8, kp8, vp8
 
-    # ---- block-score export (the indexer's KL alignment input): the same index kernels also
-    # write every block's pooled score, [G][L][nb] for prefill, [G][batch][max_pages] for decode;
-    # timed alone, against the selection-only launch of the same kernels ----
-    scores = None
-    if not args.no_index_scores:
-        def timed_alone(fn, n):
-            for _ in range(max(3, args.warmup)):
-                fn()
-            a0, a1 = ev(), ev()
-            torch.cuda.synchronize()
-            a0.record(stream)
-            for _ in range(n):
-                fn()
-            a1.record(stream)
-            torch.cuda.synchronize()
-            return a0.elapsed_time(a1) / n
+    # ---- context-parallel index branch of the decode step, its R shards run one after another
+    # on this GPU: per-shard candidate kernels and the merge (the all-gather between GPUs is
+    # not measured here) ----
+    cpi = None if args.cp_shards < 2 else cp_indexer_object(msa, dc, args.cp_shards, K, W,
+                                                            stream)
 
-        nsc = max(3, args.steps)
-        nb = (L + w.B - 1) // w.B
-        bs = torch.empty((w.G, L, nb), dtype=torch.float32, device=dev)
-        dbs = torch.empty((dw.G, dw.batch, dinp["max_pages"]), dtype=torch.float32, device=dev)
-        sel_s, dsel_s = torch.empty_like(sel), torch.empty_like(dsel)
-        sc_ms = timed_alone(lambda: msa.msa_index_select_scores(
-            cfg, inp["q_idx"], inp["k_idx"], sel=sel_s, block_scores=bs, ws=ws, stream=stream),
-            nsc)
-        plain_ms = timed_alone(lambda: msa.msa_index_select(
-            cfg, inp["q_idx"], inp["k_idx"], sel=sel, ws=ws, stream=stream), nsc)
-        dsc_ms = timed_alone(lambda: msa.msa_index_select_scores(
-            dcfg, dinp["q_idx"], paged=paged, sel=dsel_s, block_scores=dbs, ws=dws,
-            stream=stream), nsc)
-        dplain_ms = timed_alone(lambda: msa.msa_index_select(
-            dcfg, dinp["q_idx"], paged=paged, sel=dsel, ws=dws, stream=stream), nsc)
-        assert torch.equal(sel_s, sel) and torch.equal(dsel_s, dsel), "score export selection"
-        out_b, dout_b = bs.numel() * 4, dbs.numel() * 4
-        scores = {
-            "note": "msa_index_select_scores: the index kernels also write every block's pooled "
-                    "score (+inf own block, -inf later blocks); each timed alone, back to back, "
-                    "beside the selection-only launch of the same kernels",
-            "prefill_ms": sc_ms, "prefill_ms_select_only": plain_ms,
-            "prefill_output_bytes": out_b,
-            "prefill_extra_gbs": out_b / max(sc_ms - plain_ms, 1e-6) / 1e6,
-            "decode_ms": dsc_ms, "decode_ms_select_only": dplain_ms,
-            "decode_output_bytes": dout_b,
-            "gpu_launches": 2 * nsc + 4 * nsc,
-        }
-        del bs, dbs
-
-    # ---- the L = 2,048 prefill pass (launch-bound: eight short kernels) eager and as a replay of
-    # a CUDA graph captured from the same calls (the library enqueues only, so it captures) ----
-    graph = None
-    if not args.no_graph:
-        tw = synthetic.WORKLOADS["tiny_L2048"]
-        tinp = synthetic.prefill_inputs(tw, device=dev)
-        tcfg = msa.config(tw.G, tw.hpg, tw.k, tw.scale)
-        tws_i = torch.zeros(msa.msa_index_select_workspace(tcfg, tw.L, tw.L), dtype=torch.uint8,
-                            device=dev)
-        tws_a = torch.zeros(msa.msa_attn_prefill_workspace(tcfg, tw.L), dtype=torch.uint8,
-                            device=dev)
-        tsel = torch.empty((tw.G, tw.L, tw.k), dtype=torch.int32, device=dev)
-        to = torch.empty_like(tinp["q"])
-        tlse = torch.empty((tw.Hq, tw.L), dtype=torch.float32, device=dev)
-
-        def tiny_pass():
-            msa.msa_index_select(tcfg, tinp["q_idx"], tinp["k_idx"], sel=tsel, ws=tws_i)
-            msa.msa_attn_prefill(tcfg, tinp["q"], tinp["k"], tinp["v"], tsel, o=to, lse=tlse,
-                                 ws=tws_a)
-
-        side = torch.cuda.Stream()
-        side.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(side):
-            for _ in range(3):
-                tiny_pass()
-        torch.cuda.current_stream().wait_stream(side)
-        torch.cuda.synchronize()
-        cg = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(cg):
-            tiny_pass()
-        ntiny = 50
-
-        def timed_cur(fn):
-            for _ in range(3):
-                fn()
-            a0, a1 = ev(), ev()
-            torch.cuda.synchronize()
-            a0.record()
-            for _ in range(ntiny):
-                fn()
-            a1.record()
-            torch.cuda.synchronize()
-            return a0.elapsed_time(a1) / ntiny
-
-        eager_ms = timed_cur(tiny_pass)
-        graph_ms = timed_cur(cg.replay)
-        graph = {
-            "workload": tw.name, "L": tw.L,
-            "note": "index select + main branch of the small workload, back to back (inputs of "
-                    "8 MiB stay in L2); eager calls against a replay of a CUDA graph captured "
-                    "from the same calls",
-            "eager_ms": eager_ms, "graph_ms": graph_ms,
-            "tokens_per_s_eager": tw.L / (eager_ms * 1e-3),
-            "tokens_per_s_graph": tw.L / (graph_ms * 1e-3),
-            "launches_per_pass": 1 + msa.msa_attn_prefill_launches(tcfg, tw.L),
-        }
-        del cg
-
-    cpu_base = None
-    dec_cpu = None
+    # ---------------- CPU oracle on a bounded sample of the headline workload ----------------
+    cpu_base, dec_cpu = None, None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu_base = cpu_baseline(w, {k: inp[k].cpu() for k in ("q", "k", "v", "q_idx", "k_idx")},
-                                target_s=15.0)
-        dec_cpu = decode_cpu_baseline(dw, dinp)
+        cpu_base = cpu_baseline(w, case.inp, target_s=15.0)
+        dec_cpu = decode_cpu_baseline(dc.w, dc.inp)
+    decode["cpu_baseline"] = dec_cpu
+    del case
+    torch.cuda.empty_cache()
 
-    ms_per_step = total_ms / args.steps
-    prefill_ms = max_over_ranks(prefill_ms, world)
-    dec_ms = max_over_ranks(dec_ms, world)
-    value = world * L / (prefill_ms * 1e-3)
-    dwork = decode_work(dw, dinp["seq_lens"].tolist())
-    dec_scan_gbs = dwork["scan_bytes"] / (dec_sel_ms * 1e-3) / 1e9
-    dec_attn_gbs = dwork["attn_bytes"] / (dec_attn_ms * 1e-3) / 1e9
-    dec_step_gbs = (dwork["scan_bytes"] + dwork["attn_bytes"]) / (dec_ms * 1e-3) / 1e9
-    decode = {
-        "metric": "MSA paged decode tokens/s (one new token per sequence per step)",
-        "value": world * dw.batch / (dec_ms * 1e-3), "unit": "tokens/s",
-        "ms_per_step": dec_ms,
-        "config": {"workload": dw.name, "batch": dw.batch, "n_min": dw.n_lo, "n_max": dw.n_hi,
-                   "context_tokens": int(dinp["seq_lens"].sum().item()), "Hq": dw.Hq,
-                   "G": dw.G, "k": dw.k, "pages": dinp["num_pages"]},
-        "phases_ms_per_step": {"index_select": dec_sel_ms, "attention": dec_attn_ms},
-        "roofline": {"bound": "hbm", "kernel": "index page scan (+ top-k merge)",
-                     "achieved": dec_scan_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": dec_scan_gbs / peaks["hbm_gbs"],
-                     "traffic": measured_traffic("decode_scan",
-                                                 f"{dw.name}@{dw.batch}x{dw.n_hi}"),
-                     "peak_source": peaks["source"]},
-        "attention_roofline": {"bound": "hbm", "achieved": dec_attn_gbs, "peak": peaks["hbm_gbs"],
-                               "unit": "GB/s", "frac": dec_attn_gbs / peaks["hbm_gbs"]},
-        "step_hbm_frac": dec_step_gbs / peaks["hbm_gbs"],
-        "algorithmic_bytes": dwork,
-        "gpu_launches": dec_launches * args.steps,
-        "cpu_baseline": None,
-    }
+    # ---------------- the other prefill workloads, each timed the same way ----------------
+    subs = []
+    for name in [s for s in args.sub_workloads.split(",") if s]:
+        sw = synthetic.WORKLOADS[name]
+        sc = PrefillCase(msa, sw, dev)
+        _, sph, _, _ = time_prefill_decode(sc, None, K, W, world, stream)
+        obj = prefill_object(sc, sph, peaks, world, K)
+        if rank == 0 and world == 1 and not args.no_cpu_baseline:
+            obj["cpu_baseline"] = cpu_baseline(sw, sc.inp, target_s=8.0)
+        if name == args.scores_workload and not args.no_index_scores:
+            obj["index_scores"] = index_scores_object(msa, sc, dc, K, W, stream)
+        subs.append(obj)
+        del sc
+        torch.cuda.empty_cache()
+
+    graph = None if args.no_graph else cuda_graph_object(msa, dev)
+
+    value = head["value"]
     line = {
         "metric": METRIC,
         "value": value,
         "unit": "tokens/s",
         "n_gpus": world,
-        "steps": args.steps,
-        "warmup": args.warmup,
-        "ms_per_step": ms_per_step,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": total_ms / K,
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded SplitMix64; N(0,1) q/k/v, integer/8 index q/k)",
-        "config": {"workload": w.name, "L": L, "Hq": w.Hq, "G": w.G, "d": w.d, "B": w.B,
+        "config": {"workload": w.name, "L": w.L, "Hq": w.Hq, "G": w.G, "d": w.d, "B": w.B,
                    "k": w.k, "parallelism": f"replicas x{world}",
-                   "step": "prefill (index select + main branch over all L queries) + one paged "
-                           "decode step of the 64-sequence workload; value = prefill tokens/s",
-                   "l2": f"inputs larger than L2 (q {L * w.Hq * w.d * 2 / 2**20:.0f} MiB) and "
-                         f"{work['units'] * w.hpg * (w.d * 2 + 8) / 2**30:.1f} GiB of partials "
-                         f"per step"},
-        "phases_ms_per_step": {k: v / args.steps for k, v in phase.items()},
-        "prefill_ms_per_step": prefill_ms,
-        "gpu_launches": (launches_per_step + dec_launches) * args.steps,
-        "roofline": {"bound": bound, "kernel": dominant, "achieved": achieved, "peak": peak,
-                     "unit": unit, "frac": achieved / peak, "traffic": traffic,
-                     "peak_source": peaks["source"]},
-        "kernel_rooflines": {n: {"bound": r[0], "achieved": r[1], "peak": r[2], "unit": r[3],
-                                 "frac": r[1] / r[2], "ms_per_launch": per_launch_ms[n]}
-                             for n, r in roof.items()},
-        "tensor_frac_main_branch": work["attn_flops"] / ((phase["attention"] + phase["combine"]
-                                                          + phase["schedule"]) / args.steps
-                                                         * 1e-3) / 1e12 / tensor_peak,
-        "e2e": None if e2e_ms is None else {
-                "value": world * L * args.e2e_steps / (e2e_ms * 1e-3), "unit": "tokens/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "note": "prefill tokens over the whole step (prefill + decode) with every step's "
-                        "inputs copied from pinned host memory and its outputs copied back, on "
-                        "copy streams of their own (device buffers doubled, so the copies of "
-                        "neighbouring steps overlap the compute); the decode KV cache is "
-                        "resident state"},
-        "clocks": clocks.summary(),
+                   "step": f"prefill of the {w.name} workload (index select + main branch over "
+                           f"all L queries) + one paged decode step of the "
+                           f"{dc.w.batch}-sequence workload; value = prefill tokens/s",
+                   "l2": f"inputs larger than L2 (q {w.L * w.Hq * w.d * 2 / 2**20:.0f} MiB)"},
+        "prefill_ms_per_step": head["ms_per_pass"],
+        "phases_ms_per_step": head["phases_ms_per_pass"],
+        "gpu_launches": (case_launches(msa, w) + dc.launches) * K,
+        "roofline": head["roofline"],
+        "kernel_rooflines": head["kernel_rooflines"],
+        "main_branch": head["main_branch"],
+        "tensor_frac_main_branch": head["main_branch"]["frac"],
+        "e2e": e2e,
+        "clocks": clocks,
         "cpu_baseline": cpu_base,
         "decode": decode,
+        "prefill_workloads": subs,
+        "e4m3_index": e4m3,
+        "cp_indexer": cpi,
+        "cuda_graph": graph,
     }
-    line["decode"]["cpu_baseline"] = dec_cpu
-    line["e4m3_index"] = e4m3
-    line["index_scores"] = scores
-    line["cuda_graph"] = graph
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def case_launches(msa, w):
+    cfg = msa.config(w.G, w.hpg, w.k, w.scale)
+    return 1 + msa.msa_attn_prefill_launches(cfg, w.L)
+
+
+def cp_indexer_object(msa, dc, R, K, W, stream):
+    from block_sparse_long_msa_gb300 import cp
+    dw = dc.w
+    bounds = cp.split_by_work(cp.decode_work(dc.inp["seq_lens"].tolist(), dc.inp["max_pages"]),
+                              R)
+    wdt = dw.k - 1
+    dev = dc.sel.device
+    cs = torch.empty((R, dw.G, dw.batch, wdt), dtype=torch.float32, device=dev)
+    cb = torch.empty((R, dw.G, dw.batch, wdt), dtype=torch.int32, device=dev)
+    sel = torch.empty_like(dc.sel)
+    n = max(3, K)
+    shard_ms = []
+    for r, (b0, b1) in enumerate(bounds):
+        shard_ms.append(timed_alone(lambda: msa.msa_index_candidates(
+            dc.cfg, dc.inp["q_idx"], paged=dc.paged, block_begin=b0, block_end=b1,
+            cand_score=cs[r], cand_block=cb[r], ws=dc.ws, stream=stream), n, W, stream))
+    merge_ms = timed_alone(lambda: msa.msa_index_merge(dc.cfg, cs, cb, seq_lens=dc.inp["seq_lens"],
+                                                       sel=sel, ws=dc.ws, stream=stream), n, W,
+                           stream)
+    single_ms = timed_alone(lambda: msa.msa_index_select(
+        dc.cfg, dc.inp["q_idx"], paged=dc.paged, sel=dc.sel, ws=dc.ws, stream=stream), n, W,
+        stream)
+    check_status(msa, dc.ws)
+    assert torch.equal(sel, dc.sel), "context-parallel selection differs"
+    pages = [sum(max(0, min(b1, (int(x) - 1) // dw.B) - b0) for x in dc.inp["seq_lens"].tolist())
+             for b0, b1 in bounds]
+    return {
+        "note": f"the decode step's index branch split into {R} shards of logical blocks with "
+                "about equal pages (one per GPU in a context-parallel run), run one after "
+                "another on this GPU, then merged; selection asserted equal to the single "
+                "call.  The all-gather between GPUs is not measured (one GPU per box).",
+        "shards": bounds, "pages_per_shard": pages,
+        "shard_ms": shard_ms, "merge_ms": merge_ms, "single_call_ms": single_ms,
+        "exchange_bytes_per_rank": dw.G * dw.batch * wdt * 8,
+        "gpu_launches": (2 * R + 1 + 2) * n,
+    }
+
+
+def index_scores_object(msa, sc, dc, K, W, stream):
+    """Block-score export (the indexer's KL alignment input): the same index kernels also write
+    every block's pooled score, [G][L][nb] for prefill, [G][batch][max_pages] for decode; each
+    timed alone, against the selection-only launch of the same kernels."""
+    w, dw = sc.w, dc.w
+    n = max(3, K)
+    nb = (w.L + w.B - 1) // w.B
+    dev = sc.sel.device
+    bs = torch.empty((w.G, w.L, nb), dtype=torch.float32, device=dev)
+    dbs = torch.empty((dw.G, dw.batch, dc.inp["max_pages"]), dtype=torch.float32, device=dev)
+    sel_s, dsel_s = torch.empty_like(sc.sel), torch.empty_like(dc.sel)
+    q, k = sc.inp["q_idx"], sc.inp["k_idx"]
+    sc_ms = timed_alone(lambda: msa.msa_index_select_scores(
+        sc.cfg, q, k, sel=sel_s, block_scores=bs, ws=sc.ws, stream=stream), n, W, stream)
+    plain_ms = timed_alone(lambda: msa.msa_index_select(
+        sc.cfg, q, k, sel=sc.sel, ws=sc.ws, stream=stream), n, W, stream)
+    dsc_ms = timed_alone(lambda: msa.msa_index_select_scores(
+        dc.cfg, dc.inp["q_idx"], paged=dc.paged, sel=dsel_s, block_scores=dbs, ws=dc.ws,
+        stream=stream), n, W, stream)
+    dplain_ms = timed_alone(lambda: msa.msa_index_select(
+        dc.cfg, dc.inp["q_idx"], paged=dc.paged, sel=dc.sel, ws=dc.ws, stream=stream), n, W,
+        stream)
+    assert torch.equal(sel_s, sc.sel) and torch.equal(dsel_s, dc.sel), "score export selection"
+    out_b, dout_b = bs.numel() * 4, dbs.numel() * 4
+    return {
+        "note": "msa_index_select_scores: the index kernels also write every block's pooled "
+                "score (+inf own block, -inf later blocks); each timed alone, back to back, "
+                "beside the selection-only launch of the same kernels",
+        "prefill_ms": sc_ms, "prefill_ms_select_only": plain_ms,
+        "prefill_output_bytes": out_b,
+        "prefill_extra_gbs": out_b / max(sc_ms - plain_ms, 1e-6) / 1e6,
+        "decode_ms": dsc_ms, "decode_ms_select_only": dplain_ms,
+        "decode_output_bytes": dout_b,
+        "gpu_launches": 2 * n + 4 * n,
+    }
+
+
+def cuda_graph_object(msa, dev):
+    """The L = 2,048 prefill pass (launch-bound: eight short kernels) eager and as a replay of a
+    CUDA graph captured from the same calls (the library enqueues only, so it captures)."""
+    tw = synthetic.WORKLOADS["tiny_L2048"]
+    tinp = synthetic.prefill_inputs(tw, device=dev)
+    tcfg = msa.config(tw.G, tw.hpg, tw.k, tw.scale)
+    tws_i = torch.zeros(msa.msa_index_select_workspace(tcfg, tw.L, tw.L), dtype=torch.uint8,
+                        device=dev)
+    tws_a = torch.zeros(msa.msa_attn_prefill_workspace(tcfg, tw.L), dtype=torch.uint8,
+                        device=dev)
+    tsel = torch.empty((tw.G, tw.L, tw.k), dtype=torch.int32, device=dev)
+    to = torch.empty_like(tinp["q"])
+    tlse = torch.empty((tw.Hq, tw.L), dtype=torch.float32, device=dev)
+
+    def tiny_pass():
+        msa.msa_index_select(tcfg, tinp["q_idx"], tinp["k_idx"], sel=tsel, ws=tws_i)
+        msa.msa_attn_prefill(tcfg, tinp["q"], tinp["k"], tinp["v"], tsel, o=to, lse=tlse,
+                             ws=tws_a)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            tiny_pass()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    cg = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(cg):
+        tiny_pass()
+    cur = torch.cuda.current_stream()
+    eager_ms = timed_alone(tiny_pass, 50, 3, cur)
+    graph_ms = timed_alone(cg.replay, 50, 3, cur)
+    del cg
+    return {
+        "workload": tw.name, "L": tw.L,
+        "note": "index select + main branch of the small workload, back to back (inputs of "
+                "8 MiB stay in L2); eager calls against a replay of a CUDA graph captured "
+                "from the same calls",
+        "eager_ms": eager_ms, "graph_ms": graph_ms,
+        "tokens_per_s_eager": tw.L / (eager_ms * 1e-3),
+        "tokens_per_s_graph": tw.L / (graph_ms * 1e-3),
+        "launches_per_pass": 1 + msa.msa_attn_prefill_launches(tcfg, tw.L),
+    }
 
 
 # ------------------------------------------------------------------------------------------
 # CPU oracle timing (the reference arm, and the cpu_baseline of the MSA arm)
 # ------------------------------------------------------------------------------------------
-def _oracle_rows(w, inp, rows):
+def _host_index_and_kv(inp):
+    """k, v, q_idx, k_idx of a prefill workload on the host (q stays where it is: the oracle is
+    given only the query rows it samples)."""
+    return {k: inp[k].cpu() for k in ("k", "v", "q_idx", "k_idx")}
+
+
+def _q_rows(w, inp, rows):
+    """The sampled rows of q on the host: gathered from the device tensor when there is one,
+    else generated directly (the generator is counter-based, so the rows are the same)."""
+    if "q" in inp:
+        idx = torch.from_numpy(rows).to(inp["q"].device)
+        return inp["q"].index_select(0, idx).cpu()
+    return synthetic.prefill_q_rows(w, rows)
+
+
+def _oracle_rows(w, host, q_rows, rows):
     import oracle
     t = time.perf_counter()
-    sel = oracle.select_prefill(inp["q_idx"], inp["k_idx"], w.B, w.k, rows=rows)
-    oracle.attn_prefill(inp["q"], inp["k"], inp["v"], sel, w.B, w.k, w.scale, rows=rows)
+    sel = oracle.select_prefill(host["q_idx"], host["k_idx"], w.B, w.k, rows=rows)
+    oracle.attn_prefill(q_rows, host["k"], host["v"], sel, w.B, w.k, w.scale, rows=rows,
+                        q_compact=True)
     return time.perf_counter() - t
 
 
@@ -714,13 +942,17 @@ def _strided_rows(L, n, phase=0):
 
 
 def cpu_baseline(w, inp, target_s=15.0):
+    """The oracle (index selection + attention, all groups and heads) on evenly strided query
+    rows of the workload, about target_s of CPU work; copies to the host are untimed."""
     import oracle
     oracle.build()
-    n = 64
-    dt = _oracle_rows(w, inp, _strided_rows(w.L, n))
+    host = _host_index_and_kv(inp)
+    n = 32
+    rows = _strided_rows(w.L, n)
+    dt = _oracle_rows(w, host, _q_rows(w, inp, rows), rows)
     n2 = int(min(w.L, max(n, n * target_s / max(dt, 1e-3))))
     rows = _strided_rows(w.L, n2, 1)
-    dt2 = _oracle_rows(w, inp, rows)
+    dt2 = _oracle_rows(w, host, _q_rows(w, inp, rows), rows)
     return {"value": len(rows) / dt2, "unit": "tokens/s", "cores": oracle.num_threads(),
             "kind": "oracle",
             "sample": f"{len(rows)} evenly strided query rows of the L={w.L} workload "
@@ -781,18 +1013,22 @@ def run_reference(args, world, rank):
     oracle.build()
     w = workload(args)
     dev = "cuda" if torch.cuda.is_available() else "cpu"
-    inp = {k: v.cpu() for k, v in synthetic.prefill_inputs(w, device=dev).items()
-           if isinstance(v, torch.Tensor)}
+    # the index vectors and K/V of the whole workload; q only for the rows each step samples
+    inp = synthetic.prefill_inputs(w, device=dev, without_q=True)
+    host = _host_index_and_kv(inp)
+    del inp
     budget_s = 150.0
-    cal = _oracle_rows(w, inp, _strided_rows(w.L, 16))
-    per_row = cal / 16
+    rows = _strided_rows(w.L, 8)
+    cal = _oracle_rows(w, host, synthetic.prefill_q_rows(w, rows), rows)
+    per_row = cal / 8
     rows_per_step = int(max(4, min(2048, budget_s / (args.steps + args.warmup) / per_row)))
     for s in range(args.warmup):
-        _oracle_rows(w, inp, _strided_rows(w.L, rows_per_step, s + 1))
+        rows = _strided_rows(w.L, rows_per_step, s + 1)
+        _oracle_rows(w, host, synthetic.prefill_q_rows(w, rows), rows)
     total, n = 0.0, 0
     for s in range(args.steps):
         rows = _strided_rows(w.L, rows_per_step, args.warmup + s + 1)
-        total += _oracle_rows(w, inp, rows)
+        total += _oracle_rows(w, host, synthetic.prefill_q_rows(w, rows), rows)
         n += len(rows)
     value = n / total
     cb = {"value": value, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",

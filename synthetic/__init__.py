@@ -68,6 +68,12 @@ def hashes(seed: int, stream: int, start: int, n: int, device="cpu") -> torch.Te
     return splitmix64(idx * _GAMMA + key)
 
 
+def hashes_at(seed: int, stream: int, idx: torch.Tensor) -> torch.Tensor:
+    """64-bit hashes of the listed element indices of one stream (int64 tensor, any shape)."""
+    key = _s64(stream_key(seed, stream))
+    return splitmix64(idx.to(torch.int64) * _GAMMA + key)
+
+
 def _fill(out_flat: torch.Tensor, seed: int, stream: int, fn) -> None:
     n = out_flat.numel()
     for s in range(0, n, _CHUNK):
@@ -217,15 +223,18 @@ def as_index_dtype(t: torch.Tensor, index_dtype: str) -> torch.Tensor:
 
 
 def prefill_inputs(w: Workload, device="cpu", L: int | None = None,
-                   index_only: bool = False, index_dtype: str = "bf16") -> dict:
-    """q [L][Hq][d], k/v [L][G][d] bf16; q_idx [L][G][di], k_idx [L][di] in index_dtype."""
+                   index_only: bool = False, index_dtype: str = "bf16",
+                   without_q: bool = False) -> dict:
+    """q [L][Hq][d], k/v [L][G][d] bf16; q_idx [L][G][di], k_idx [L][di] in index_dtype.
+    without_q leaves q out (prefill_q_rows gives any of its rows)."""
     assert w.kind == "prefill"
     if L is not None:
         w = Workload(**{**w.__dict__, "L": L})
     L = w.L
     out = {}
     if not index_only:
-        out["q"] = normal_bf16(w.seed, STREAM_Q, (L, w.Hq, w.d), device)
+        if not without_q:
+            out["q"] = normal_bf16(w.seed, STREAM_Q, (L, w.Hq, w.d), device)
         out["k"] = normal_bf16(w.seed, STREAM_K, (L, w.G, w.d), device)
         out["v"] = normal_bf16(w.seed, STREAM_V, (L, w.G, w.d), device)
     if w.planted == "none":
@@ -241,6 +250,16 @@ def prefill_inputs(w: Workload, device="cpu", L: int | None = None,
     out["k_idx"] = as_index_dtype(out["k_idx"], index_dtype)
     out["workload"] = w
     return out
+
+
+def prefill_q_rows(w: Workload, rows, device="cpu") -> torch.Tensor:
+    """Rows `rows` of the workload's q, [len(rows)][Hq][d] bf16, equal to
+    prefill_inputs(w)["q"][rows] without generating the rest (the generator is counter-based)."""
+    rows = torch.as_tensor(rows, dtype=torch.int64, device=device)
+    row = w.Hq * w.d
+    idx = rows[:, None] * row + torch.arange(row, dtype=torch.int64, device=device)[None, :]
+    return _box_muller(hashes_at(w.seed, STREAM_Q, idx)).to(torch.bfloat16).view(
+        len(rows), w.Hq, w.d)
 
 
 def decode_inputs(w: Workload, device="cpu", batch: int | None = None,

@@ -78,6 +78,16 @@ def test_generator_ranges_and_determinism():
     assert torch.equal(torch.sort(p).values, torch.arange(1000))
 
 
+def test_query_rows_generated_alone_equal_the_full_tensor():
+    w = synthetic.Workload(**{**synthetic.WORKLOADS["prefill_L32K"].__dict__, "L": 700})
+    full = synthetic.prefill_inputs(w)
+    rows = np.array([0, 1, 255, 256, 511, 699], np.int64)
+    assert torch.equal(synthetic.prefill_q_rows(w, rows), full["q"][torch.from_numpy(rows)])
+    rest = synthetic.prefill_inputs(w, without_q=True)
+    assert "q" not in rest and all(torch.equal(rest[k], full[k])
+                                   for k in ("k", "v", "q_idx", "k_idx"))
+
+
 # ----------------------------------------------------------------------------------------------
 # Hand-worked fixtures
 # ----------------------------------------------------------------------------------------------

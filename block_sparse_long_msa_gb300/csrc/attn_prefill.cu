@@ -33,7 +33,9 @@ constexpr int kHeadsPerGroup = 16;
 constexpr int kItemTiles = 16;                            // tiles sharing one K/V staging
 constexpr int kItemTokens = kItemTiles * kTileTokens;     // 128
 constexpr uint32_t kPanel = 16384;
-constexpr int kMaxRanges = 16;
+constexpr int kMaxRanges = 32;                            // <= 32: one warp lane per range
+constexpr int kRangeBlocks = 16;                          // query blocks per range (2,048 tokens)
+constexpr int64_t kScanEntries = 65536;                   // bound on nr * G * nbk
 
 // ------------------------------------------------------------------------------------------
 // Scheduling
@@ -125,10 +127,28 @@ __global__ void sched_scan_kernel(SchedArgs a) {
     start = q < first ? 0 : h[q];
   }
   const int next = __shfl_down_sync(0xffffffffu, start, 1);
+  const int cnt = lane < a.nr ? (lane + 1 < a.nr ? next : run) - start : 0;
+  // Consecutive ranges are merged into segments of at least one full work item (a sparse list
+  // would otherwise be cut into short items, each reloading K and V for a few tokens); a
+  // segment's tokens are listed under its last range, so its items run with that range's.
+  int seg_cnt = 0, seg_start = 0, acc = 0, open_at = 0;
+  for (int r = 0; r < a.nr; ++r) {
+    const int c = __shfl_sync(0xffffffffu, cnt, r);
+    const int st = __shfl_sync(0xffffffffu, start, r);
+    if (acc == 0) open_at = st;
+    acc += c;
+    if (acc >= kItemTokens || r == a.nr - 1) {
+      if (lane == r) {
+        seg_cnt = acc;
+        seg_start = open_at;
+      }
+      acc = 0;
+    }
+  }
   if (lane < a.nr) {
     const size_t idx = static_cast<size_t>(lane) * a.G * a.nbk + warp;
-    a.rstart[idx] = start;
-    a.rcnt[idx] = (lane + 1 < a.nr ? next : run) - start;
+    a.rstart[idx] = seg_start;
+    a.rcnt[idx] = seg_cnt;
   }
 }
 
@@ -873,14 +893,16 @@ __global__ void __launch_bounds__(128) combine_kernel(CombineArgs a) {
 
 }  // namespace
 
-// Query ranges of a chunk: as many as keep the expected (group, block) list of a range at one
-// full work item or more (ranges that cut lists shorter would pad tiles and reload K/V per item).
-RangePlan plan_ranges(int64_t q0, int64_t q1, int k) {
+// Query ranges of a chunk: 2,048 tokens each (16 query blocks; at most kMaxRanges, so longer
+// chunks get longer ranges).  Work items run range by range, so the query gathers of the CTAs
+// working at one time fall in one range (32 MiB of q at 64 heads), which L2 holds; each list is
+// cut at range boundaries only where it has a full item's worth of tokens (sched_scan).
+RangePlan plan_ranges(int64_t q0, int64_t q1, int G) {
   RangePlan p{};
   const int64_t nbq = (q1 - q0 + kBlock - 1) / kBlock, nbk = (q1 + kBlock - 1) / kBlock;
-  const int64_t per_list = (q1 - q0) * k / std::max<int64_t>(1, nbk);  // tokens per (g, b) list
-  const int nr_want = static_cast<int>(
-      std::min<int64_t>(kMaxRanges, std::max<int64_t>(1, per_list / kItemTokens)));
+  int64_t nr_want = std::min<int64_t>(kMaxRanges, (nbq + kRangeBlocks - 1) / kRangeBlocks);
+  // the one-CTA scan of sched_bases walks nr * G * nbk item counts: keep it to 64 rounds
+  nr_want = std::max<int64_t>(1, std::min<int64_t>(nr_want, kScanEntries / (G * nbk)));
   p.rq = static_cast<int>((nbq + nr_want - 1) / nr_want);
   p.nr = static_cast<int>((nbq + p.rq - 1) / p.rq);
   return p;
@@ -895,14 +917,16 @@ PrefillWorkspace prefill_workspace_layout(int64_t L, int G, int k, int64_t chunk
   const int64_t nbk = (L + kBlock - 1) / kBlock;
   const int64_t nbq = (chunk + kBlock - 1) / kBlock;
   const int64_t units = chunk * G * k;
-  const int64_t max_items = kMaxRanges * G * nbk + (units + kItemTokens - 1) / kItemTokens;
+  // ranges a chunk of nbq query blocks can have (at most; plan_ranges)
+  const int64_t nr = std::min<int64_t>(kMaxRanges, (nbq + kRangeBlocks - 1) / kRangeBlocks);
+  const int64_t max_items = nr * G * nbk + (units + kItemTokens - 1) / kItemTokens;
   size_t off = 256;  // status header
   w.hist = off;      off += up(sizeof(int32_t) * G * nbk * nbq);
   w.cnt = off;       off += up(sizeof(int32_t) * G * nbk);
   w.list_base = off; off += up(sizeof(int32_t) * G * nbk);
-  w.rstart = off;    off += up(sizeof(int32_t) * kMaxRanges * G * nbk);
-  w.rcnt = off;      off += up(sizeof(int32_t) * kMaxRanges * G * nbk);
-  w.item_base = off; off += up(sizeof(int32_t) * kMaxRanges * G * nbk);
+  w.rstart = off;    off += up(sizeof(int32_t) * nr * G * nbk);
+  w.rcnt = off;      off += up(sizeof(int32_t) * nr * G * nbk);
+  w.item_base = off; off += up(sizeof(int32_t) * nr * G * nbk);
   w.n_items = off;   off += 256;
   w.items = off;     off += up(sizeof(int4) * max_items);
   w.list = off;      off += up(sizeof(int32_t) * units);
@@ -936,7 +960,7 @@ cudaError_t launch_attn_prefill_chunk(const CUtensorMap& map_q, const CUtensorMa
   s.item_base = reinterpret_cast<int32_t*>(ws + w.item_base);
   s.rstart = reinterpret_cast<int32_t*>(ws + w.rstart);
   s.rcnt = reinterpret_cast<int32_t*>(ws + w.rcnt);
-  const RangePlan plan = plan_ranges(q0, q1, k);
+  const RangePlan plan = plan_ranges(q0, q1, G);
   s.rq = plan.rq;
   s.nr = plan.nr;
   s.n_items = reinterpret_cast<int32_t*>(ws + w.n_items);

@@ -12,10 +12,14 @@
 // TMEM accumulators; work unit u = (key tile u / gpc, group u % gpc) takes slot u & 1, so with
 // two groups each slot belongs to one group and each group's MMAs overlap the other group's
 // epilogue.  Roles:
-//   warp 0      TMA producer (index-query tiles once, then key tiles)
-//   warp 1      TMEM owner + single-thread tcgen05.mma issuer
-//   warps 4..11 two epilogue warpgroups; warpgroup e drains slot e: thread r owns query row r,
-//               pulls its 256 scores, max-pools them per block and keeps a register top-15.
+//   warps 0..7  two epilogue warpgroups; warpgroup e drains slot e: thread r owns query row r and
+//               takes the two block maxima of its 256 scores straight from the TMEM loads
+//               (tcgen05.ld.red), then keeps a register top-15
+//   warp 8      TMA producer (index-query tiles once, then key tiles)
+//   warp 9      TMEM owner + single-thread tcgen05.mma issuer
+// A slot is MMA'd, then drained, then MMA'd again, so the drain (four waves of two 32-column TMEM
+// loads, each wave bound by the load latency) is on the critical path once the MMA runs at the
+// fp8 rate.
 // With one group per CTA the two warpgroups see alternate key tiles and merge their lists at the
 // end; the full (score desc, block asc) comparison of the list keeps the tie rule.
 #include "common.cuh"
@@ -74,8 +78,11 @@ struct IndexPrefillArgs {
 };
 
 // Shared memory: gpc index-query tiles, ns key stages, then the barrier block.
+constexpr int kIndexThreads = 320;
+constexpr int kWarpProducer = 8, kWarpMma = 9;
+
 template <bool kF8>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(kIndexThreads, 1)
     index_select_prefill_kernel(const __grid_constant__ CUtensorMap map_q,
                                 const __grid_constant__ CUtensorMap map_k, IndexPrefillArgs a) {
   using T = IdxTiles<kF8>;
@@ -121,7 +128,7 @@ __global__ void __launch_bounds__(384, 1)
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 1) {
+  if (warp == kWarpMma) {
     tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), 512);
     tmem_relinquish();
   }
@@ -130,7 +137,7 @@ __global__ void __launch_bounds__(384, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
+  if (warp == kWarpProducer) {
     // ---------------- TMA producer ----------------
     if (lane == 0 && nkey > 0) {
       tma_prefetch_map(&map_q);
@@ -168,7 +175,7 @@ __global__ void __launch_bounds__(384, 1)
           mbar_wait(b_full(it % ns), (it / ns) & 1, kDefaultWaitNs);
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == kWarpMma) {
     // ---------------- MMA issuer ----------------
     if (lane == 0 && nkey > 0) {
       bool ok = mbar_wait(bar_q, 0, a.wait_ns);
@@ -211,9 +218,9 @@ __global__ void __launch_bounds__(384, 1)
       mma_commit(drain_bar);
       mbar_wait(drain_bar, 0, kDefaultWaitNs);
     }
-  } else if (warp >= 4) {
+  } else {
     // ------------- epilogue warpgroup e: slot e -> max-pool -> top-k -------------
-    const int e = (warp >> 2) - 1;
+    const int e = warp >> 2;
     const int row = (warp & 3) * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t acc = tmem + lane_base + e * kIndexKeyTile;
@@ -228,29 +235,26 @@ __global__ void __launch_bounds__(384, 1)
         break;
       }
       tc_fence_after();
-      // 64-column loads reduced with four independent max chains; the slot is released as soon
-      // as the last load has landed
-      float mx[2];
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const float ninf = -__int_as_float(0x7f800000);
-        float m4[4] = {ninf, ninf, ninf, ninf};
+      // The block maxima come out of the TMEM loads themselves (tcgen05.ld.red .max over each
+      // load's 32 columns); the loaded values are not needed.  Two loads in flight per wait (a
+      // third would not fit the registers a thread may hold); the slot is released as soon as
+      // the last load has landed.
+      float mx[2] = {-__int_as_float(0x7f800000), -__int_as_float(0x7f800000)};
 #pragma unroll 1
-        for (int c = 0; c < 2; ++c) {
-          uint32_t v0[32], v1[32];
-          tmem_ld32(acc + h * kBlock + c * 64, v0);
-          tmem_ld32(acc + h * kBlock + c * 64 + 32, v1);
-          tmem_ld_wait();
-          if (h == 1 && c == 1) {
-            tc_fence_before();
-            mbar_arrive(acc_empty(e));
-          }
-#pragma unroll
-          for (int q = 0; q < 32; ++q)
-            m4[q & 3] = fmax3(m4[q & 3], __uint_as_float(v0[q]), __uint_as_float(v1[q]));
-        }
-        mx[h] = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+      for (int c = 0; c < 4; ++c) {  // columns [64c, 64c + 64): block c / 2
+        uint32_t v0[32], v1[32];
+        float a0, a1;
+        tmem_ld32_max(acc + c * 64, v0, a0);
+        tmem_ld32_max(acc + c * 64 + 32, v1, a1);
+        tmem_ld_wait();
+        const float m = fmaxf(a0, a1);
+        if (c < 2)
+          mx[0] = fmaxf(mx[0], m);
+        else
+          mx[1] = fmaxf(mx[1], m);
       }
+      tc_fence_before();
+      mbar_arrive(acc_empty(e));
       list.insert(mx[0], a.kb0 + 2 * t);
       if (2 * t + 1 < nkey) list.insert(mx[1], a.kb0 + 2 * t + 1);
       const int64_t ib = static_cast<int64_t>(qb) * kBlock + row;
@@ -312,7 +316,7 @@ __global__ void __launch_bounds__(384, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == kWarpMma) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -341,7 +345,8 @@ cudaError_t launch(const CUtensorMap& map_q, const CUtensorMap& map_k, int64_t L
   IndexPrefillArgs a{L,       G,       gpc,  k,   nb,         ns,         sel,
                      sel_score, block_scores, status, wait_ns, kb0, kb1, cand_score,
                      cand_block};
-  index_select_prefill_kernel<kF8><<<nb * (G / gpc), 384, smem, stream>>>(map_q, map_k, a);
+  index_select_prefill_kernel<kF8><<<nb * (G / gpc), kIndexThreads, smem, stream>>>(map_q, map_k,
+                                                                                   a);
   return cudaGetLastError();
 }
 

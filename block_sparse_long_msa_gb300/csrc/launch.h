@@ -33,7 +33,7 @@ PrefillWorkspace prefill_workspace_layout(int64_t L, int G, int k, int64_t chunk
 struct RangePlan {
   int rq, nr;  // query blocks per query range, number of ranges
 };
-RangePlan plan_ranges(int64_t q0, int64_t q1, int k);
+RangePlan plan_ranges(int64_t q0, int64_t q1, int G);
 // Kernel launches one call of launch_attn_prefill_chunk makes.
 int prefill_chunk_launches();
 cudaError_t launch_attn_prefill_chunk(const CUtensorMap& map_q, const CUtensorMap& map_k,

@@ -527,18 +527,19 @@ def host_memory_available():
 
 def e2e_leg(msa, case, dc, steps, world, stream):
     """The same step through the public API with every step's inputs copied in from pinned host
-    memory and its results copied back (inside the timed region).  The prefill tensors are
-    double-buffered on the device and the copies run on copy streams of their own, so step s+1's
-    inputs arrive and step s-1's results leave while step s computes; the decode step's small
-    inputs and outputs travel on the compute stream.  Returns (ms, h2d bytes, d2h bytes)."""
+    memory and its results copied back (inside the timed region).  All tensors a step copies
+    (prefill and decode) are double-buffered on the device, and every copy runs on one of two
+    copy streams, so step s+1's inputs arrive and step s-1's results leave while step s
+    computes, and no copy waits in a copy engine's queue in front of the compute stream.
+    Returns (ms, h2d bytes, d2h bytes)."""
     names_in = ("q", "k", "v", "q_idx", "k_idx")
+    dnames = ("q", "q_idx", "seq_lens", "page_table")
     inp = case.inp
     outs = (case.o, case.lse, case.sel)
+    douts = (dc.o, dc.lse, dc.sel)
     h2d = sum(inp[k].numel() * inp[k].element_size() for k in names_in)
-    d2h = sum(t.numel() * t.element_size() for t in outs)
-    dnames = ("q", "q_idx", "seq_lens", "page_table")
     h2d += sum(dc.inp[k].numel() * dc.inp[k].element_size() for k in dnames)
-    d2h += sum(t.numel() * t.element_size() for t in (dc.o, dc.lse, dc.sel))
+    d2h = sum(t.numel() * t.element_size() for t in outs + douts)
 
     def pinned_copy(t):
         h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
@@ -546,13 +547,14 @@ def e2e_leg(msa, case, dc, steps, world, stream):
         return h
 
     host_in = {k: pinned_copy(inp[k]) for k in names_in}
-    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
-    dev_in = [{k: inp[k] for k in names_in}, {k: torch.empty_like(inp[k]) for k in names_in}]
-    dev_out = [list(outs), [torch.empty_like(t) for t in outs]]
     dhost_in = {k: pinned_copy(dc.inp[k]) for k in dnames}
-    ddev_in = {k: dc.inp[k] for k in dnames}
-    dhost_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-                 for t in (dc.o, dc.lse, dc.sel)]
+    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs + douts]
+    dev_in = [{**{k: inp[k] for k in names_in}, **{"d_" + k: dc.inp[k] for k in dnames}},
+              {**{k: torch.empty_like(inp[k]) for k in names_in},
+               **{"d_" + k: torch.empty_like(dc.inp[k]) for k in dnames}}]
+    dev_out = [list(outs + douts), [torch.empty_like(t) for t in outs + douts]]
+    pagedb = [msa.paged_kv(dc.inp["k_idx_pool"], dc.inp["k_pool"], dc.inp["v_pool"],
+                           dev_in[b]["d_page_table"], dev_in[b]["d_seq_lens"]) for b in range(2)]
     s_h2d, s_d2h = torch.cuda.Stream(), torch.cuda.Stream()
     ev_in = [torch.cuda.Event() for _ in range(2)]
     ev_used = [torch.cuda.Event() for _ in range(2)]
@@ -564,25 +566,23 @@ def e2e_leg(msa, case, dc, steps, world, stream):
         with torch.cuda.stream(s_h2d):
             if i >= 2:
                 s_h2d.wait_event(ev_used[b])
+            for k_, t in dhost_in.items():
+                dev_in[b]["d_" + k_].copy_(t, non_blocking=True)
             for k_, t in host_in.items():
                 dev_in[b][k_].copy_(t, non_blocking=True)
             ev_in[b].record(s_h2d)
         stream.wait_event(ev_in[b])
         if i >= 2:
             stream.wait_event(ev_out[b])
-        ob, lb, sb = dev_out[b]
+        ob, lb, sb, dob, dlb, dsb = dev_out[b]
         di = dev_in[b]
         msa.msa_index_select(cfg, di["q_idx"], di["k_idx"], sel=sb, ws=case.ws, stream=stream)
         msa.msa_attn_prefill(cfg, di["q"], di["k"], di["v"], sb, o=ob, lse=lb, ws=case.ws,
                              stream=stream)
-        for k_, t in dhost_in.items():
-            ddev_in[k_].copy_(t, non_blocking=True)
-        msa.msa_index_select(dc.cfg, ddev_in["q_idx"], paged=dc.paged, sel=dc.sel, ws=dc.ws,
+        msa.msa_index_select(dc.cfg, di["d_q_idx"], paged=pagedb[b], sel=dsb, ws=dc.ws,
                              stream=stream)
-        msa.msa_attn_decode(dc.cfg, ddev_in["q"], dc.paged, dc.sel, o=dc.o, lse=dc.lse,
-                            ws=dc.ws, stream=stream)
-        for hd, t in zip(dhost_out, (dc.o, dc.lse, dc.sel)):
-            hd.copy_(t, non_blocking=True)
+        msa.msa_attn_decode(dc.cfg, di["d_q"], pagedb[b], dsb, o=dob, lse=dlb, ws=dc.ws,
+                            stream=stream)
         ev_used[b].record(stream)
         with torch.cuda.stream(s_d2h):
             s_d2h.wait_event(ev_used[b])
@@ -590,7 +590,7 @@ def e2e_leg(msa, case, dc, steps, world, stream):
                 hd.copy_(t, non_blocking=True)
             ev_out[b].record(s_d2h)
 
-    ref_sel = case.sel.clone()  # the resident-input step's selection
+    ref_sel, ref_dsel = case.sel.clone(), dc.sel.clone()  # the resident-input step's selections
     for i in range(4):
         e2e_step(i)
     torch.cuda.synchronize()
@@ -605,9 +605,10 @@ def e2e_leg(msa, case, dc, steps, world, stream):
     torch.cuda.synchronize()
     ms = max_over_ranks(e0.elapsed_time(e1), world)
     check_status(msa, case.ws, dc.ws)
-    # the pipelined steps computed the same selection as the resident-input step
+    # the pipelined steps computed the same selections as the resident-input step
     assert torch.equal(host_out[2], ref_sel.cpu()), "end-to-end selection differs"
-    del host_in, host_out, dev_in, dev_out, dhost_in, dhost_out
+    assert torch.equal(host_out[5], ref_dsel.cpu()), "end-to-end decode selection differs"
+    del host_in, host_out, dev_in, dev_out, dhost_in
     return ms, h2d, d2h
 
 

@@ -182,22 +182,47 @@ KERNEL_SOURCES = {
     "decode_scan_e4m3": ["decode.cu", "common.cuh", "ptx.cuh"],
 }
 NCU_TRAFFIC = {
-    # prefill L=32768, 64/4 heads, k=16
-    "attention": [{"bytes_per_launch": 9828836096, "workload": "prefill_L32K@32768",
-                   "sources_sha256": "7d4d5adc609b717953302cb6c3fc4d49f754da7eae7cf3f27036282b37e8205c"}],
-    "combine": [{"bytes_per_launch": 9194790912, "workload": "prefill_L32K@32768",
-                 "sources_sha256": "7d4d5adc609b717953302cb6c3fc4d49f754da7eae7cf3f27036282b37e8205c"}],
-    "index": [{"bytes_per_launch": 41903616, "workload": "prefill_L32K@32768",
-               "sources_sha256": "549e86cc1e19b86d0fd21c929853b80722a68fa8fe9701ae39a3cc23b5248ac2"}],
-    "index_e4m3": [{"bytes_per_launch": 21011413, "workload": "prefill_L32K@32768",
-                    "sources_sha256": "549e86cc1e19b86d0fd21c929853b80722a68fa8fe9701ae39a3cc23b5248ac2"}],
+    # index kernel: L=1,048,576 hot blocks and L=32,768 (profile_case, second launch)
+    "index": [{"bytes_per_launch": 22924614912, "workload": "prefill_L1M_hot@1048576",
+               "sources_sha256": "5349d3312bd0bf376d0903be3af3814f85f37ca024e6f34f29091bdabf43b274"},
+              {"bytes_per_launch": 41905664, "workload": "prefill_L32K@32768",
+               "sources_sha256": "5349d3312bd0bf376d0903be3af3814f85f37ca024e6f34f29091bdabf43b274"}],
+    "index_e4m3": [{"bytes_per_launch": 7807967232, "workload": "prefill_L1M_hot@1048576",
+                    "sources_sha256": "5349d3312bd0bf376d0903be3af3814f85f37ca024e6f34f29091bdabf43b274"},
+                   {"bytes_per_launch": 20997632, "workload": "prefill_L32K@32768",
+                    "sources_sha256": "5349d3312bd0bf376d0903be3af3814f85f37ca024e6f34f29091bdabf43b274"}],
+    # attention and combine per launch (one query chunk): L=32,768 (its one chunk); L=131,072
+    # (second chunk); L=1,048,576 (8th of 16 chunks, a middle one)
+    "attention": [{"bytes_per_launch": 9906456320, "workload": "prefill_L32K@32768",
+                   "sources_sha256": "d98350c3d0d851f10cfb97ed7e8e492b5174a6df8014fa897331e73b48970534"},
+                  {"bytes_per_launch": 20751655168, "workload": "prefill_L128K_clustered@131072",
+                   "sources_sha256": "d98350c3d0d851f10cfb97ed7e8e492b5174a6df8014fa897331e73b48970534"},
+                  {"bytes_per_launch": 33448929280, "workload": "prefill_L1M_hot@1048576",
+                   "sources_sha256": "d98350c3d0d851f10cfb97ed7e8e492b5174a6df8014fa897331e73b48970534"}],
+    "combine": [{"bytes_per_launch": 9193131776, "workload": "prefill_L32K@32768",
+                 "sources_sha256": "d98350c3d0d851f10cfb97ed7e8e492b5174a6df8014fa897331e73b48970534"},
+                {"bytes_per_launch": 18668413440, "workload": "prefill_L128K_clustered@131072",
+                 "sources_sha256": "d98350c3d0d851f10cfb97ed7e8e492b5174a6df8014fa897331e73b48970534"},
+                {"bytes_per_launch": 18935632640, "workload": "prefill_L1M_hot@1048576",
+                 "sources_sha256": "d98350c3d0d851f10cfb97ed7e8e492b5174a6df8014fa897331e73b48970534"}],
     # decode, 64 sequences of 16K-256K tokens
-    "decode_scan": [{"bytes_per_launch": 2084700160,
+    "decode_scan": [{"bytes_per_launch": 2087746304,
                      "workload": "decode_b64_16K_256K@64x262144",
-                     "sources_sha256": "994ce2153b759ea1038980cc54121fca1a7ce5a247759beee4807547bab49afc"}],
-    "decode_scan_e4m3": [{"bytes_per_launch": 1044300331,
+                     "sources_sha256": "0575040a09534ddf37df1b7229e2c7493631706ebd9c3c5bb1c7b56f0c5279d9"}],
+    "decode_scan_e4m3": [{"bytes_per_launch": 1047515904,
                           "workload": "decode_b64_16K_256K@64x262144",
-                          "sources_sha256": "994ce2153b759ea1038980cc54121fca1a7ce5a247759beee4807547bab49afc"}],
+                          "sources_sha256": "0575040a09534ddf37df1b7229e2c7493631706ebd9c3c5bb1c7b56f0c5279d9"}],
+}
+# Tensor-pipe activity from the same captures (sm__pipe_tensor_cycles_active, % of elapsed
+# cycles: a fraction of the part's nominal tensor rate at the clock of the moment).
+NCU_TENSOR_PIPE = {
+    "index": [{"pct": 69.23, "workload": "prefill_L1M_hot@1048576", "sources_sha256": "5349d3312bd0bf376d0903be3af3814f85f37ca024e6f34f29091bdabf43b274"},
+              {"pct": 57.04, "workload": "prefill_L32K@32768", "sources_sha256": "5349d3312bd0bf376d0903be3af3814f85f37ca024e6f34f29091bdabf43b274"}],
+    "index_e4m3": [{"pct": 45.18, "workload": "prefill_L1M_hot@1048576",
+                    "sources_sha256": "5349d3312bd0bf376d0903be3af3814f85f37ca024e6f34f29091bdabf43b274"},
+                   {"pct": 32.15, "workload": "prefill_L32K@32768", "sources_sha256": "5349d3312bd0bf376d0903be3af3814f85f37ca024e6f34f29091bdabf43b274"}],
+    # attention: ncu --set full at L=8,192 (the 32K kernel at a capture-sized length)
+    "attention": [{"pct": 42.02, "workload": "prefill_L32K@8192", "sources_sha256": "d98350c3d0d851f10cfb97ed7e8e492b5174a6df8014fa897331e73b48970534"}],
 }
 
 
@@ -217,6 +242,17 @@ def measured_traffic(kernel: str, workload: str):
         if t["workload"] == workload and t["sources_sha256"] == sources_sha256(kernel):
             return t["bytes_per_launch"]
     return None
+
+
+def measured_tensor_pipe(kernel: str, workload: str = None):
+    """ncu tensor-pipe activity (% of elapsed cycles) with the workload it was taken on, for
+    the current kernel sources: the given workload's if there is one, else any."""
+    found = [t for t in NCU_TENSOR_PIPE.get(kernel, [])
+             if t["sources_sha256"] == sources_sha256(kernel)]
+    for t in found:
+        if t["workload"] == workload:
+            return {"pct_of_elapsed": t["pct"], "workload": t["workload"]}
+    return {"pct_of_elapsed": found[0]["pct"], "workload": found[0]["workload"]} if found else None
 
 
 def load_peaks():
@@ -365,7 +401,7 @@ def check_status(msa, *wss):
             raise RuntimeError(f"device status {st}")
 
 
-def prefill_report(w, ph, nchunks, peaks):
+def prefill_report(w, ph, nchunks, peaks, index_kernel="index"):
     """Rooflines of one prefill pass from its per-step phase times (ms).
 
     The index kernel and the attention kernel are contractions: their achieved rate is their
@@ -390,18 +426,23 @@ def prefill_report(w, ph, nchunks, peaks):
                 "frac_of_burst": a / peaks["bf16_tflops"],
                 "frac_of_sustained": a / peaks["bf16_tflops_sustained"]}
 
+    wl = f"{w.name}@{w.L}"
     kernels = {
         "index": {**tensor(idx_tf), "ms_per_launch": ph["index"],
-                  "algorithmic_flops": work["index_flops"]},
+                  "algorithmic_flops": work["index_flops"],
+                  "ncu_tensor_pipe": measured_tensor_pipe(index_kernel, wl)},
         "attention": {**tensor(att_tf), "ms_per_launch": ph["attention"] / nchunks,
                       "algorithmic_flops": work["attn_flops"],
+                      "ncu_tensor_pipe": measured_tensor_pipe("attention", wl),
+                      "ncu_traffic_per_launch": measured_traffic("attention", wl),
                       "hbm_gbs_of_algorithmic_bytes": att_gbs,
                       "hbm_frac": att_gbs / peaks["hbm_gbs"],
                       "algorithmic_bytes": work["attn_bytes"]},
         "combine": {"bound": "hbm", "achieved": com_gbs, "peak": peaks["hbm_gbs"],
                     "unit": "GB/s", "frac": com_gbs / peaks["hbm_gbs"],
                     "ms_per_launch": ph["combine"] / nchunks,
-                    "algorithmic_bytes": work["combine_bytes"]},
+                    "algorithmic_bytes": work["combine_bytes"],
+                    "ncu_traffic_per_launch": measured_traffic("combine", wl)},
     }
     main = {**tensor(main_tf), "ms": main_ms,
             "note": "attention FLOPs over schedule + attention + combine time"}
@@ -409,11 +450,12 @@ def prefill_report(w, ph, nchunks, peaks):
     return work, kernels, main, dominant
 
 
-def prefill_object(case, ph, peaks, world, steps):
+def prefill_object(case, ph, peaks, world, steps, index_kernel="index"):
     w = case.w
-    work, kernels, main, dominant = prefill_report(w, ph, case.nchunks, peaks)
+    work, kernels, main, dominant = prefill_report(w, ph, case.nchunks, peaks, index_kernel)
     dk = kernels[dominant]
-    traffic = measured_traffic(dominant, f"{w.name}@{w.L}")
+    traffic = measured_traffic(index_kernel if dominant == "index" else dominant,
+                               f"{w.name}@{w.L}")
     roof = {"bound": dk["bound"], "kernel": dominant, "achieved": dk["achieved"],
             "peak": dk["peak"], "unit": dk["unit"], "frac": dk["frac"],
             "traffic": traffic,
@@ -689,7 +731,7 @@ def run_msa(args, world, rank):
         torch.cuda.synchronize()
         assert torch.equal(case.sel, ref_sel) and torch.equal(dc.sel, ref_dsel), \
             "e4m3 selection differs"
-        pre8 = prefill_object(case, ph8, peaks, world, K8)
+        pre8 = prefill_object(case, ph8, peaks, world, K8, index_kernel="index_e4m3")
         fp8_peak = 2 * (peaks["bf16_tflops_sustained"] if ph8["prefill"] >= 50.0
                         else peaks["bf16_tflops"])
         idx_tf = pre8["kernel_rooflines"]["index"]["achieved"]

@@ -492,10 +492,13 @@ __global__ void __launch_bounds__(128) decode_topk_kernel(TopkArgs a) {
 // 1-4 each score 32 keys (S = q K^T with m16n8k16 MMAs, M = the group's 16 heads), exchange row
 // maxima, sums and their slice of P through shared memory, and then each computes O = P V for 32
 // of the 128 output dimensions over all the page's keys, written straight to the partial.
-// With an e4m3 K/V cache (kKV8) the pages arrive as 16 KiB e4m3 tiles; each compute warp widens
-// just the part it reads (K of its 32 keys to bf16, V of its 32 dimensions to fp16) into a
-// private swizzled buffer and releases the stage at once.  S stays a bf16 product (q exact); P
-// and V go into an fp16 product (every e4m3 value is exact in both types).
+// With an e4m3 K/V cache (kKV8) the pages arrive as 16 KiB e4m3 tiles and both products run in
+// fp16 (every e4m3 value is an fp16 value; q is rounded to fp16 once per (sequence, group),
+// which is exact for |q| >= 2^-17).  For S each thread loads its B fragments straight from the
+// staged e4m3 tile: inside every 16-wide k-step the head dimension is permuted, the same way for
+// q and K, so that a thread's four k elements are four adjacent bytes (one 32-bit load, two
+// conversions).  V, read transposed by P.V, is widened by each warp for its 32 dimensions into a
+// private swizzled fp16 buffer.
 // ------------------------------------------------------------------------------------------
 struct DecAttnArgs {
   const __nv_bfloat16* q;  // [batch][G*16][128]
@@ -517,10 +520,9 @@ struct DecLayout {
   static constexpr int kStages = kKV8 ? 4 : 3;
   static constexpr uint32_t kTile = kKV8 ? 16384 : 32768;  // one K or V page tile
   static constexpr uint32_t kStage = 2 * kTile;
-  // e4m3: per compute warp, K of its 32 keys in bf16 (32 rows x 256 B) and V of its 32
-  // dimensions in fp16 (128 rows x 64 B)
+  // e4m3: per compute warp, V of its 32 dimensions in fp16 (128 rows x 64 B)
   static constexpr uint32_t kPriv = kStages * kStage;
-  static constexpr uint32_t kPrivWarp = 8192 + 8192;
+  static constexpr uint32_t kPrivWarp = 8192;
   static constexpr uint32_t kP = kPriv + (kKV8 ? 4 * kPrivWarp : 0);
   // Per unit the four warps exchange their row maxima and row sums and the P tile (16 rows x
   // 128 keys, 128-byte swizzled panels); two copies, by unit parity, so a warp may start the
@@ -574,11 +576,6 @@ __device__ __forceinline__ uint32_t dec_p_addr(uint32_t tile, int row, int chunk
   return tile + (chunk >> 3) * (kHeads * 128) + row * 128 + (((chunk & 7) ^ (row & 7)) << 4);
 }
 
-// Private bf16 K buffer of a warp (its 32 keys x 256 B): 16-byte chunk c of key row r; the low
-// three chunk bits are XOR-ed with the row, so the 8 rows an ldmatrix reads hit distinct banks.
-__device__ __forceinline__ uint32_t kpriv_addr(uint32_t buf, int r, int c) {
-  return buf + r * 256 + (((c & 8) | ((c & 7) ^ (r & 7))) << 4);
-}
 // Private fp16 V buffer of a warp (128 keys x its 32 dimensions = 64 B): chunk c (0..3) of key
 // row r, XOR-ed with bits 1..2 of the row (8 consecutive rows then cover all 32 banks).
 __device__ __forceinline__ uint32_t vpriv_addr(uint32_t buf, int r, int c) {
@@ -652,7 +649,7 @@ __global__ void __launch_bounds__(160, 1)
   // ------------------------------ compute warps 1..4 ------------------------------
   const int w = warp - 1;
   const int gid = lane >> 2, tq = lane & 3;
-  const uint32_t kp = base + Lay::kPriv + w * Lay::kPrivWarp, vp = kp + 8192;  // e4m3 only
+  const uint32_t vp = base + Lay::kPriv + w * Lay::kPrivWarp;  // e4m3 only
   uint32_t qa[8][4];
   int cur_sg = -1;
   int p = 0;
@@ -668,12 +665,24 @@ __global__ void __launch_bounds__(160, 1)
     if (sg != cur_sg) {  // query fragments of this (sequence, group), straight from global
       const uint32_t* q32 = reinterpret_cast<const uint32_t*>(a.q + static_cast<size_t>(sg) *
                                                                         kHeads * kDim);
+      if (kKV8) {
+        // fp16, with k elements 2tq, 2tq+1, 2tq+8, 2tq+9 of each k-step taken from dimensions
+        // 4tq .. 4tq+3 (the K fragments below use the same permutation)
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        qa[kk][0] = q32[(gid * kDim + kk * 16 + tq * 2) >> 1];
-        qa[kk][1] = q32[((gid + 8) * kDim + kk * 16 + tq * 2) >> 1];
-        qa[kk][2] = q32[(gid * kDim + kk * 16 + 8 + tq * 2) >> 1];
-        qa[kk][3] = q32[((gid + 8) * kDim + kk * 16 + 8 + tq * 2) >> 1];
+        for (int kk = 0; kk < 8; ++kk) {
+          qa[kk][0] = bf16x2_to_f16x2(q32[(gid * kDim + kk * 16 + tq * 4) >> 1]);
+          qa[kk][1] = bf16x2_to_f16x2(q32[((gid + 8) * kDim + kk * 16 + tq * 4) >> 1]);
+          qa[kk][2] = bf16x2_to_f16x2(q32[(gid * kDim + kk * 16 + tq * 4 + 2) >> 1]);
+          qa[kk][3] = bf16x2_to_f16x2(q32[((gid + 8) * kDim + kk * 16 + tq * 4 + 2) >> 1]);
+        }
+      } else {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          qa[kk][0] = q32[(gid * kDim + kk * 16 + tq * 2) >> 1];
+          qa[kk][1] = q32[((gid + 8) * kDim + kk * 16 + tq * 2) >> 1];
+          qa[kk][2] = q32[(gid * kDim + kk * 16 + 8 + tq * 2) >> 1];
+          qa[kk][3] = q32[((gid + 8) * kDim + kk * 16 + 8 + tq * 2) >> 1];
+        }
       }
       cur_sg = sg;
     }
@@ -686,16 +695,6 @@ __global__ void __launch_bounds__(160, 1)
     }
     const uint32_t kt = base + st * Lay::kStage, vt = kt + Lay::kTile;
     if (kKV8) {
-      // K rows [32w, 32w+32): lane takes bytes [4 lane, 4 lane + 4) of each row
-#pragma unroll 4
-      for (int it = 0; it < 32; ++it) {
-        const int r = 32 * w + it;
-        const uint32_t src = kt + r * 128 + (((lane >> 2) ^ (r & 7)) << 4) + (lane & 3) * 4;
-        uint32_t h0, h1;
-        e4m3x4_to_f16x4(ld_shared_u32(src), h0, h1);
-        st_shared_v2(kpriv_addr(kp, it, lane >> 1) + (lane & 1) * 8, f16x2_to_bf16x2(h0),
-                     f16x2_to_bf16x2(h1));
-      }
       // V columns [32w, 32w+32) of all 128 keys: 4 keys per step, 8 lanes per key
 #pragma unroll 4
       for (int it = 0; it < 32; ++it) {
@@ -707,7 +706,6 @@ __global__ void __launch_bounds__(160, 1)
         st_shared_v2(vpriv_addr(vp, r, (lane & 7) >> 1) + (lane & 1) * 8, h0, h1);
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(empty(st));  // the stage is no longer read
     }
     const int par = p & 1;
     const uint32_t pt = base + Lay::kP + par * Lay::kPBytes;  // this unit's P tile
@@ -719,16 +717,31 @@ __global__ void __launch_bounds__(160, 1)
     for (int j = 0; j < 4; ++j) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) sacc[j][e] = 0.f;
-      const int key = w * 32 + j * 8 + (lane & 7);
+      if (kKV8) {
+        // B fragment of key w*32 + 8j + gid: bytes [4tq, 4tq + 4) of k-step kk's 16-byte chunk
+        // (the 8 keys' rows hit 8 distinct chunks of the swizzle: no bank conflicts)
+        const int kr = w * 32 + j * 8 + gid;
 #pragma unroll
-      for (int kk = 0; kk < 8; kk += 2) {
-        uint32_t r[4];
-        ldmatrix_x4(kKV8 ? kpriv_addr(kp, j * 8 + (lane & 7), 2 * kk + (lane >> 3))
-                         : swz(kt, key, 2 * kk + (lane >> 3)),
-                    r);
-        mma_m16n8k16_bf16(sacc[j], qa[kk], r[0], r[1]);
-        mma_m16n8k16_bf16(sacc[j], qa[kk + 1], r[2], r[3]);
+        for (int kk = 0; kk < 8; ++kk) {
+          uint32_t b0, b1;
+          e4m3x4_to_f16x4(ld_shared_u32(kt + kr * 128 + ((kk ^ (kr & 7)) << 4) + tq * 4), b0,
+                          b1);
+          mma_m16n8k16_f16(sacc[j], qa[kk], b0, b1);
+        }
+      } else {
+        const int key = w * 32 + j * 8 + (lane & 7);
+#pragma unroll
+        for (int kk = 0; kk < 8; kk += 2) {
+          uint32_t r[4];
+          ldmatrix_x4(swz(kt, key, 2 * kk + (lane >> 3)), r);
+          mma_m16n8k16_bf16(sacc[j], qa[kk], r[0], r[1]);
+          mma_m16n8k16_bf16(sacc[j], qa[kk + 1], r[2], r[3]);
+        }
       }
+    }
+    if (kKV8) {  // K and V of the stage have been read
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty(st));
     }
     // scale, causal limit, this warp's row maxima (rows gid and gid+8) over its 32 keys
     float m0 = ninf, m1 = ninf;

@@ -488,10 +488,12 @@ __global__ void __launch_bounds__(128) decode_topk_kernel(TopkArgs a) {
 
 // ------------------------------------------------------------------------------------------
 // Decode attention: one unit per (sequence, group, slot).  A persistent CTA takes a contiguous
-// range of units; warp 0 stages each unit's K and V page tiles (TMA, 128-byte swizzle), warps
-// 1-4 each score 32 keys (S = q K^T with m16n8k16 MMAs, M = the group's 16 heads), exchange row
-// maxima, sums and their slice of P through shared memory, and then each computes O = P V for 32
-// of the 128 output dimensions over all the page's keys, written straight to the partial.
+// range of units; warp 0 stages each unit's K and V page tiles (TMA, 128-byte swizzle).  The
+// staged units alternate between two groups of four compute warps (warps 1-4, 5-8); in a group
+// each warp scores 32 keys (S = q K^T with m16n8k16 MMAs, M = the group's 16 heads), the four
+// exchange row maxima, sums and their slice of P through shared memory, and then each computes
+// O = P V for 32 of the 128 output dimensions over all the page's keys, written straight to the
+// partial.
 // With an e4m3 K/V cache (kKV8) the pages arrive as 16 KiB e4m3 tiles and both products run in
 // fp16 (every e4m3 value is an fp16 value; q is rounded to fp16 once per (sequence, group),
 // which is exact for |q| >= 2^-17).  For S each thread loads its B fragments straight from the
@@ -515,6 +517,11 @@ struct DecAttnArgs {
 };
 
 // Shared-memory layout of the decode attention kernel, by K/V storage type.
+// Two groups of four compute warps take alternate staged units, so every SM sub-partition has
+// two warps to interleave.
+constexpr int kDecGroups = 2;
+constexpr int kDecThreads = 32 + kDecGroups * 128;
+
 template <bool kKV8>
 struct DecLayout {
   static constexpr int kStages = kKV8 ? 4 : 3;
@@ -523,13 +530,14 @@ struct DecLayout {
   // e4m3: per compute warp, V of its 32 dimensions in fp16 (128 rows x 64 B)
   static constexpr uint32_t kPriv = kStages * kStage;
   static constexpr uint32_t kPrivWarp = 8192;
-  static constexpr uint32_t kP = kPriv + (kKV8 ? 4 * kPrivWarp : 0);
-  // Per unit the four warps exchange their row maxima and row sums and the P tile (16 rows x
-  // 128 keys, 128-byte swizzled panels); two copies, by unit parity, so a warp may start the
-  // next unit while another still reads this one's.
+  static constexpr uint32_t kP = kPriv + (kKV8 ? 4 * kDecGroups * kPrivWarp : 0);
+  // Per unit the four warps of a group exchange their row maxima and row sums and the P tile (16
+  // rows x 128 keys, 128-byte swizzled panels); two copies per group, by the parity of the
+  // group's units, so a warp may start the next unit while another still reads this one's.
   static constexpr uint32_t kPBytes = kHeads * kBlock * 2;
-  static constexpr uint32_t kML = kP + 2 * kPBytes;  // 2 x (max, sum) x 4 warps x 16 rows fp32
-  static constexpr uint32_t kBar = kML + 2 * 2 * 4 * kHeads * 4;
+  static constexpr uint32_t kML = kP + kDecGroups * 2 * kPBytes;
+  static constexpr uint32_t kMLGroup = 2 * 2 * 4 * kHeads * 4;  // 2 x (max, sum) x 4 warps x 16
+  static constexpr uint32_t kBar = kML + kDecGroups * kMLGroup;
   static constexpr uint32_t kSmem = kBar + 128 + 1024;
 };
 constexpr int kDecMaxStages = 4;
@@ -583,7 +591,7 @@ __device__ __forceinline__ uint32_t vpriv_addr(uint32_t buf, int r, int c) {
 }
 
 template <bool kKV8>
-__global__ void __launch_bounds__(160, 1)
+__global__ void __launch_bounds__(kDecThreads, 1)
     decode_attn_kernel(const __grid_constant__ CUtensorMap map_kp,
                        const __grid_constant__ CUtensorMap map_vp, DecAttnArgs a) {
   using Lay = DecLayout<kKV8>;
@@ -646,21 +654,23 @@ __global__ void __launch_bounds__(160, 1)
     return;  // the producer takes no part in the compute warps' named barriers
   }
 
-  // ------------------------------ compute warps 1..4 ------------------------------
-  const int w = warp - 1;
+  // ---------------- compute warps 1..8: group gr takes the staged units p with p % 2 == gr ----
+  const int gr = (warp - 1) >> 2, w = (warp - 1) & 3;
+  const uint32_t bar_id = 1 + gr;  // the group's named barrier
   const int gid = lane >> 2, tq = lane & 3;
-  const uint32_t vp = base + Lay::kPriv + w * Lay::kPrivWarp;  // e4m3 only
+  const uint32_t vp = base + Lay::kPriv + (gr * 4 + w) * Lay::kPrivWarp;  // e4m3 only
   uint32_t qa[8][4];
   int cur_sg = -1;
-  int p = 0;
+  int p = -1;  // staged units seen so far, minus one
   const float ninf = -__int_as_float(0x7f800000);
   for (int u = u0; u < u1; ++u) {
     const UnitInfo x = unit_info(a, u, false);
     if (!x.valid) {
-      if (w == 0 && lane < kHeads)
+      if (gr == 0 && w == 0 && lane < kHeads)
         a.plse[static_cast<size_t>(u) * kHeads + lane] = ninf;
       continue;
     }
+    if ((++p & 1) != gr) continue;  // the other group's unit
     const int sg = x.s * a.G + x.g;
     if (sg != cur_sg) {  // query fragments of this (sequence, group), straight from global
       const uint32_t* q32 = reinterpret_cast<const uint32_t*>(a.q + static_cast<size_t>(sg) *
@@ -687,7 +697,14 @@ __global__ void __launch_bounds__(160, 1)
       cur_sg = sg;
     }
     const int st = p % kDecStages;
-    bool ok = !*abort_flag && mbar_wait(full(st), (p / kDecStages) & 1, a.wait_ns);
+    // The stage's previous unit (p - kDecStages) belongs to the other group: wait until it has
+    // been released, as the producer does before refilling it, so that the full barrier is at
+    // most one phase ahead of this wait (a group skips every other unit, and a parity test on a
+    // barrier two phases behind would pass on the stale phase).
+    bool ok = !*abort_flag &&
+              (p < kDecStages ||
+               mbar_wait(empty(st), ((p / kDecStages) & 1) ^ 1, a.wait_ns)) &&
+              mbar_wait(full(st), (p / kDecStages) & 1, a.wait_ns);
     if (!__all_sync(0xffffffffu, ok)) {
       if (lane == 0) report_status(a.status, kStatusTimeout);
       *abort_flag = 1;  // keep going with whatever is in the buffer: every warp still meets
@@ -707,10 +724,10 @@ __global__ void __launch_bounds__(160, 1)
       }
       __syncwarp();
     }
-    const int par = p & 1;
-    const uint32_t pt = base + Lay::kP + par * Lay::kPBytes;  // this unit's P tile
-    float* mx = mlx + par * (2 * 4 * kHeads);              // [4 warps][16] maxima
-    float* ls = mx + 4 * kHeads;                           // [4 warps][16] sums
+    const int par = (p >> 1) & 1;                          // parity of the group's units
+    const uint32_t pt = base + Lay::kP + (gr * 2 + par) * Lay::kPBytes;  // this unit's P tile
+    float* mx = mlx + gr * (Lay::kMLGroup / 4) + par * (2 * 4 * kHeads);  // [4 warps][16] maxima
+    float* ls = mx + 4 * kHeads;                                          // [4 warps][16] sums
     // S = q K^T over this warp's 32 keys: 4 n-tiles of 8 keys
     float sacc[4][4];
 #pragma unroll
@@ -764,7 +781,7 @@ __global__ void __launch_bounds__(160, 1)
       mx[w * kHeads + gid] = m0;
       mx[w * kHeads + gid + 8] = m1;
     }
-    named_barrier(1, 128);
+    named_barrier(bar_id, 128);
     // row maxima over the page (key 0 is always in range, so they are finite)
     float M0 = mx[gid], M1 = mx[gid + 8];
 #pragma unroll
@@ -795,7 +812,7 @@ __global__ void __launch_bounds__(160, 1)
       ls[w * kHeads + gid] = l0;
       ls[w * kHeads + gid + 8] = l1;
     }
-    named_barrier(1, 128);
+    named_barrier(bar_id, 128);
     const float L0 = ls[gid] + ls[kHeads + gid] + ls[2 * kHeads + gid] + ls[3 * kHeads + gid];
     const float L1 = ls[gid + 8] + ls[kHeads + gid + 8] + ls[2 * kHeads + gid + 8] +
                      ls[3 * kHeads + gid + 8];
@@ -827,7 +844,6 @@ __global__ void __launch_bounds__(160, 1)
     }
     __syncwarp();
     if (!kKV8 && lane == 0) mbar_arrive(empty(st));
-    ++p;
     const float i0 = 1.f / L0, i1 = 1.f / L1;
     float* dst = a.po + static_cast<size_t>(u) * kHeads * kDim;
 #pragma unroll
@@ -989,14 +1005,14 @@ cudaError_t launch_decode_attn(const CUtensorMap& map_kp, const CUtensorMap& map
                                   cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) !=
         cudaSuccess)
       return e;
-    decode_attn_kernel<true><<<grid, 160, smem, stream>>>(map_kp, map_vp, a);
+    decode_attn_kernel<true><<<grid, kDecThreads, smem, stream>>>(map_kp, map_vp, a);
   } else {
     constexpr uint32_t smem = DecLayout<false>::kSmem;
     if ((e = cudaFuncSetAttribute(decode_attn_kernel<false>,
                                   cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) !=
         cudaSuccess)
       return e;
-    decode_attn_kernel<false><<<grid, 160, smem, stream>>>(map_kp, map_vp, a);
+    decode_attn_kernel<false><<<grid, kDecThreads, smem, stream>>>(map_kp, map_vp, a);
   }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   DecCombineArgs c{a.po, a.plse, batch, G, k, static_cast<__nv_bfloat16*>(o), lse};

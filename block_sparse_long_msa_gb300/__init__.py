@@ -138,10 +138,24 @@ def _check(st: int, where: str):
         raise MsaError(st, where)
 
 
-def _workspace(nbytes: int, device, ws):
+# Workspaces of the calls made without one: one per (device, stream), grown as needed.  Calls on
+# one stream run in order, so they may share it; its status word is cleared before each reuse.
+_ws_cache: dict = {}
+
+
+def _workspace(nbytes: int, device, ws, stream=None):
     import torch
     if ws is None:
-        ws = torch.zeros(max(nbytes, WS_HEADER_BYTES), dtype=torch.uint8, device=device)
+        s = torch.cuda.current_stream(device) if stream is None else stream
+        key = (str(device), s.cuda_stream)
+        ws = _ws_cache.get(key)
+        if ws is None or ws.numel() < nbytes:
+            with torch.cuda.stream(s):  # allocated (and zeroed) in the order of the stream it serves
+                ws = torch.zeros(max(nbytes, WS_HEADER_BYTES), dtype=torch.uint8, device=device)
+            _ws_cache[key] = ws
+        else:
+            _check(lib().msa_reset_device_status(_ptr(ws), ctypes.c_void_p(s.cuda_stream)),
+                   "msa_reset_device_status")
     if ws.numel() * ws.element_size() < nbytes:
         raise MsaError(MSA_ERR_WORKSPACE, "workspace")
     return ws
@@ -185,7 +199,7 @@ def msa_index_select(cfg: MsaConfig, q_idx, k_idx=None, paged: MsaPagedKV | None
         sel = torch.empty((G, T, k), dtype=torch.int32, device=q_idx.device)
     if want_score and sel_score is None:
         sel_score = torch.empty((G, T, k), dtype=torch.float32, device=q_idx.device)
-    ws = _workspace(msa_index_select_workspace(cfg, T, L, paged), q_idx.device, ws)
+    ws = _workspace(msa_index_select_workspace(cfg, T, L, paged), q_idx.device, ws, stream)
     st = lib().msa_index_select(ctypes.byref(cfg), _ptr(q_idx), _ptr(k_idx), L,
                                 ctypes.byref(paged) if paged is not None else None, _ptr(sel),
                                 _ptr(sel_score), _ptr(ws), ws.numel(), _stream(stream))
@@ -211,7 +225,7 @@ def msa_index_select_scores(cfg: MsaConfig, q_idx, k_idx=None, paged: MsaPagedKV
     elif (block_scores.dtype != torch.float32 or tuple(block_scores.shape) != (G, T, nb)
           or not block_scores.is_contiguous()):
         raise MsaError(MSA_ERR_INVALID_ARG, f"block_scores must be contiguous fp32 {(G, T, nb)}")
-    ws = _workspace(msa_index_select_workspace(cfg, T, L, paged), q_idx.device, ws)
+    ws = _workspace(msa_index_select_workspace(cfg, T, L, paged), q_idx.device, ws, stream)
     st = lib().msa_index_select_scores(ctypes.byref(cfg), _ptr(q_idx), _ptr(k_idx), L,
                                        ctypes.byref(paged) if paged is not None else None,
                                        _ptr(sel), None, _ptr(block_scores), _ptr(ws), ws.numel(),
@@ -240,7 +254,7 @@ def msa_index_candidates(cfg: MsaConfig, q_idx, k_idx=None, L: int | None = None
         cand_score = torch.empty((G, T, w), dtype=torch.float32, device=q_idx.device)
     if cand_block is None:
         cand_block = torch.empty((G, T, w), dtype=torch.int32, device=q_idx.device)
-    ws = _workspace(msa_index_select_workspace(cfg, T, Lc, paged), q_idx.device, ws)
+    ws = _workspace(msa_index_select_workspace(cfg, T, Lc, paged), q_idx.device, ws, stream)
     st = lib().msa_index_candidates(ctypes.byref(cfg), _ptr(q_idx), _ptr(k_idx), Lc,
                                     ctypes.byref(paged) if paged is not None else None,
                                     block_begin, block_end, _ptr(cand_score), _ptr(cand_block),
@@ -259,7 +273,7 @@ def msa_index_merge(cfg: MsaConfig, cand_score, cand_block, seq_lens=None, sel=N
         sel = torch.empty((G, T, cfg.topk), dtype=torch.int32, device=cand_block.device)
     if want_score and sel_score is None:
         sel_score = torch.empty((G, T, cfg.topk), dtype=torch.float32, device=cand_block.device)
-    ws = _workspace(WS_HEADER_BYTES, cand_block.device, ws)
+    ws = _workspace(WS_HEADER_BYTES, cand_block.device, ws, stream)
     st = lib().msa_index_merge(ctypes.byref(cfg), R, _ptr(cand_score), _ptr(cand_block), T,
                                _ptr(seq_lens), _ptr(sel), _ptr(sel_score), _ptr(ws), ws.numel(),
                                _stream(stream))
@@ -292,7 +306,7 @@ def msa_attn_prefill(cfg: MsaConfig, q, k, v, sel, o=None, lse=None, ws=None, st
         o = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((Hq, L), dtype=torch.float32, device=q.device)
-    ws = _workspace(msa_attn_prefill_workspace(cfg, L), q.device, ws)
+    ws = _workspace(msa_attn_prefill_workspace(cfg, L), q.device, ws, stream)
     if marks:
         arr = (ctypes.c_void_p * len(marks))(*[m.cuda_event for m in marks])
         st = lib().msa_attn_prefill_marked(ctypes.byref(cfg), _ptr(q), _ptr(k), _ptr(v), L,
@@ -318,7 +332,7 @@ def msa_attn_decode(cfg: MsaConfig, q, paged: MsaPagedKV, sel, o=None, lse=None,
         o = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((Hq, batch), dtype=torch.float32, device=q.device)
-    ws = _workspace(msa_attn_decode_workspace(cfg, paged), q.device, ws)
+    ws = _workspace(msa_attn_decode_workspace(cfg, paged), q.device, ws, stream)
     st = lib().msa_attn_decode(ctypes.byref(cfg), _ptr(q), ctypes.byref(paged), _ptr(sel),
                                _ptr(o), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream))
     _check(st, "msa_attn_decode")

@@ -28,7 +28,9 @@
  *   - Host-side argument errors return before anything is enqueued.  Launch failures return
  *     MSA_ERR_CUDA.
  *   - v1 supports head_dim = index_dim = block_size = 128, 1 <= topk <= 16, num_groups <= 4 for
- *     prefill index selection; other values return MSA_ERR_UNSUPPORTED.
+ *     the index branch, heads_per_group = 16 for the main branch (prefill and decode: a group's
+ *     16 query heads are the rows of its tensor-core tiles), prefill lengths up to 1,572,864;
+ *     other values return MSA_ERR_UNSUPPORTED.
  */
 #ifndef MSA_H_
 #define MSA_H_

@@ -206,12 +206,12 @@ NCU_TRAFFIC = {
                 {"bytes_per_launch": 18935632640, "workload": "prefill_L1M_hot@1048576",
                  "sources_sha256": "d98350c3d0d851f10cfb97ed7e8e492b5174a6df8014fa897331e73b48970534"}],
     # decode, 64 sequences of 16K-256K tokens
-    "decode_scan": [{"bytes_per_launch": 2087746304,
+    "decode_scan": [{"bytes_per_launch": 2087661824,
                      "workload": "decode_b64_16K_256K@64x262144",
-                     "sources_sha256": "0575040a09534ddf37df1b7229e2c7493631706ebd9c3c5bb1c7b56f0c5279d9"}],
-    "decode_scan_e4m3": [{"bytes_per_launch": 1047515904,
+                     "sources_sha256": "ea2ceaeb42364f74df04a1a52e6916a5665e459083da5f93f30443f5175b71fd"}],
+    "decode_scan_e4m3": [{"bytes_per_launch": 1047573248,
                           "workload": "decode_b64_16K_256K@64x262144",
-                          "sources_sha256": "0575040a09534ddf37df1b7229e2c7493631706ebd9c3c5bb1c7b56f0c5279d9"}],
+                          "sources_sha256": "ea2ceaeb42364f74df04a1a52e6916a5665e459083da5f93f30443f5175b71fd"}],
 }
 # Tensor-pipe activity from the same captures (sm__pipe_tensor_cycles_active, % of elapsed
 # cycles: a fraction of the part's nominal tensor rate at the clock of the moment).

@@ -143,8 +143,21 @@ struct PageWalk {
   }
 };
 
+// Maximum of v over the 32 lanes of the (converged) warp, in one instruction (redux.sync with
+// .f32, sm_100 family); a NaN operand is ignored as in fmaxf.
+__device__ __forceinline__ float warp_max_f32(float v) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
+}
+
+// Warps: 0 TMA producer, 1 MMA issuer (and TMEM owner), 2 finds the CTA's page range, 4-11 two
+// epilogue groups taking alternate pages (a page's 128 keys are the 128 TMEM lanes, one warp per
+// quarter), so two pages' reductions are in flight.
+constexpr int kScanThreads = 384;
+
 template <bool kF8>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(kScanThreads, 1)
     decode_scan_kernel(const __grid_constant__ CUtensorMap map_k,
                        const __grid_constant__ CUtensorMap map_q, ScanArgs a) {
   using T = ScanTiles<kF8>;
@@ -297,13 +310,17 @@ __global__ void __launch_bounds__(256, 1)
       mbar_wait(drain_bar, 0, kDefaultWaitNs);
     }
   } else if (warp >= 4) {
-    // epilogue: thread = key of the page; the warp's max over its 32 keys per group
-    const int ew = warp - 4;
+    // epilogue: thread = key of the page; the warp's max over its 32 keys per group.  Group eg
+    // takes the pages p with p % 2 == eg; an even number of slots keeps every slot with one
+    // group, which therefore sees each of its slot's phases in order.
+    static_assert(kScanSlots % 2 == 0, "scan slots per epilogue group");
+    const int eg = (warp - 4) >> 2, ew = (warp - 4) & 3;
     const uint32_t lane_base = static_cast<uint32_t>(ew * 32) << 16;
     PageWalk w;
     w.init(a, walk);
     int p = 0;
     for (int b = w.next(a); b >= 0; b = w.next(a), ++p) {
+      if ((p & 1) != eg) continue;
       const int slot = p % kScanSlots;
       if (!__all_sync(0xffffffffu, mbar_wait(acc_full(slot), (p / kScanSlots) & 1, a.wait_ns))) {
         report_status(a.status, kStatusTimeout);
@@ -318,11 +335,7 @@ __global__ void __launch_bounds__(256, 1)
       mbar_arrive(acc_empty(slot));
       float m[4];
 #pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        m[g] = __uint_as_float(v[g]);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m[g] = fmaxf(m[g], __shfl_xor_sync(0xffffffffu, m[g], o));
-      }
+      for (int g = 0; g < 4; ++g) m[g] = warp_max_f32(__uint_as_float(v[g]));
       if (lane < a.G) {
         float* dst = reinterpret_cast<float*>(
             a.scores + (static_cast<size_t>(w.s) * a.G + lane) * a.max_pages + b);
@@ -941,13 +954,15 @@ cudaError_t launch_decode_select(const CUtensorMap& map_k, const CUtensorMap& ma
                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   scan_smem<true>())) != cudaSuccess)
       return e;
-    decode_scan_kernel<true><<<grid, 256, scan_smem<true>(), stream>>>(map_k, map_q, a);
+    decode_scan_kernel<true><<<grid, kScanThreads, scan_smem<true>(), stream>>>(map_k, map_q,
+                                                                                 a);
   } else {
     if ((e = cudaFuncSetAttribute(decode_scan_kernel<false>,
                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   scan_smem<false>())) != cudaSuccess)
       return e;
-    decode_scan_kernel<false><<<grid, 256, scan_smem<false>(), stream>>>(map_k, map_q, a);
+    decode_scan_kernel<false><<<grid, kScanThreads, scan_smem<false>(), stream>>>(map_k, map_q,
+                                                                                  a);
   }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   TopkArgs t{};

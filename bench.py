@@ -183,46 +183,48 @@ KERNEL_SOURCES = {
 }
 NCU_TRAFFIC = {
     # index kernel: L=1,048,576 hot blocks and L=32,768 (profile_case, second launch)
-    "index": [{"bytes_per_launch": 22924614912, "workload": "prefill_L1M_hot@1048576",
-               "sources_sha256": "5349d3312bd0bf376d0903be3af3814f85f37ca024e6f34f29091bdabf43b274"},
-              {"bytes_per_launch": 41905664, "workload": "prefill_L32K@32768",
-               "sources_sha256": "5349d3312bd0bf376d0903be3af3814f85f37ca024e6f34f29091bdabf43b274"}],
-    "index_e4m3": [{"bytes_per_launch": 7807967232, "workload": "prefill_L1M_hot@1048576",
-                    "sources_sha256": "5349d3312bd0bf376d0903be3af3814f85f37ca024e6f34f29091bdabf43b274"},
-                   {"bytes_per_launch": 20997632, "workload": "prefill_L32K@32768",
-                    "sources_sha256": "5349d3312bd0bf376d0903be3af3814f85f37ca024e6f34f29091bdabf43b274"}],
+    "index": [{"bytes_per_launch": 23000039424, "workload": "prefill_L1M_hot@1048576",
+               "sources_sha256": "bdca6e914cb6ff0dc7fa7af84499fe692bfa4272dc855bff19fa35591b172626"},
+              {"bytes_per_launch": 41904640, "workload": "prefill_L32K@32768",
+               "sources_sha256": "bdca6e914cb6ff0dc7fa7af84499fe692bfa4272dc855bff19fa35591b172626"}],
+    "index_e4m3": [{"bytes_per_launch": 7784805632, "workload": "prefill_L1M_hot@1048576",
+                    "sources_sha256": "bdca6e914cb6ff0dc7fa7af84499fe692bfa4272dc855bff19fa35591b172626"},
+                   {"bytes_per_launch": 20997376, "workload": "prefill_L32K@32768",
+                    "sources_sha256": "bdca6e914cb6ff0dc7fa7af84499fe692bfa4272dc855bff19fa35591b172626"}],
     # attention and combine per launch (one query chunk): L=32,768 (its one chunk); L=131,072
     # (second chunk); L=1,048,576 (8th of 16 chunks, a middle one)
-    "attention": [{"bytes_per_launch": 9906456320, "workload": "prefill_L32K@32768",
-                   "sources_sha256": "d98350c3d0d851f10cfb97ed7e8e492b5174a6df8014fa897331e73b48970534"},
-                  {"bytes_per_launch": 20751655168, "workload": "prefill_L128K_clustered@131072",
-                   "sources_sha256": "d98350c3d0d851f10cfb97ed7e8e492b5174a6df8014fa897331e73b48970534"},
-                  {"bytes_per_launch": 33448929280, "workload": "prefill_L1M_hot@1048576",
-                   "sources_sha256": "d98350c3d0d851f10cfb97ed7e8e492b5174a6df8014fa897331e73b48970534"}],
-    "combine": [{"bytes_per_launch": 9193131776, "workload": "prefill_L32K@32768",
-                 "sources_sha256": "d98350c3d0d851f10cfb97ed7e8e492b5174a6df8014fa897331e73b48970534"},
-                {"bytes_per_launch": 18668413440, "workload": "prefill_L128K_clustered@131072",
-                 "sources_sha256": "d98350c3d0d851f10cfb97ed7e8e492b5174a6df8014fa897331e73b48970534"},
-                {"bytes_per_launch": 18935632640, "workload": "prefill_L1M_hot@1048576",
-                 "sources_sha256": "d98350c3d0d851f10cfb97ed7e8e492b5174a6df8014fa897331e73b48970534"}],
+    "attention": [{"bytes_per_launch": 9905228544, "workload": "prefill_L32K@32768",
+                   "sources_sha256": "55d1c77b924afda7453fd25713a809c2454a115dd07a1f391499b611b2f32625"},
+                  {"bytes_per_launch": 20745970176, "workload": "prefill_L128K_clustered@131072",
+                   "sources_sha256": "55d1c77b924afda7453fd25713a809c2454a115dd07a1f391499b611b2f32625"},
+                  {"bytes_per_launch": 33456025088, "workload": "prefill_L1M_hot@1048576",
+                   "sources_sha256": "55d1c77b924afda7453fd25713a809c2454a115dd07a1f391499b611b2f32625"}],
+    "combine": [{"bytes_per_launch": 9192910080, "workload": "prefill_L32K@32768",
+                 "sources_sha256": "55d1c77b924afda7453fd25713a809c2454a115dd07a1f391499b611b2f32625"},
+                {"bytes_per_launch": 18668071936, "workload": "prefill_L128K_clustered@131072",
+                 "sources_sha256": "55d1c77b924afda7453fd25713a809c2454a115dd07a1f391499b611b2f32625"},
+                {"bytes_per_launch": 18934947584, "workload": "prefill_L1M_hot@1048576",
+                 "sources_sha256": "55d1c77b924afda7453fd25713a809c2454a115dd07a1f391499b611b2f32625"}],
     # decode, 64 sequences of 16K-256K tokens
-    "decode_scan": [{"bytes_per_launch": 2087661824,
-                     "workload": "decode_b64_16K_256K@64x262144",
-                     "sources_sha256": "ea2ceaeb42364f74df04a1a52e6916a5665e459083da5f93f30443f5175b71fd"}],
-    "decode_scan_e4m3": [{"bytes_per_launch": 1047573248,
-                          "workload": "decode_b64_16K_256K@64x262144",
-                          "sources_sha256": "ea2ceaeb42364f74df04a1a52e6916a5665e459083da5f93f30443f5175b71fd"}],
+    "decode_scan": [{"bytes_per_launch": 2087945216, "workload": "decode_b64_16K_256K@64x262144",
+                     "sources_sha256": "c6ba85d779f7de1ce06e7602971fdd5baebd6cc7b9d388c22c0b1b5894dff508"}],
+    "decode_scan_e4m3": [{"bytes_per_launch": 1047191296, "workload": "decode_b64_16K_256K@64x262144",
+                          "sources_sha256": "c6ba85d779f7de1ce06e7602971fdd5baebd6cc7b9d388c22c0b1b5894dff508"}],
 }
 # Tensor-pipe activity from the same captures (sm__pipe_tensor_cycles_active, % of elapsed
 # cycles: a fraction of the part's nominal tensor rate at the clock of the moment).
 NCU_TENSOR_PIPE = {
-    "index": [{"pct": 69.23, "workload": "prefill_L1M_hot@1048576", "sources_sha256": "5349d3312bd0bf376d0903be3af3814f85f37ca024e6f34f29091bdabf43b274"},
-              {"pct": 57.04, "workload": "prefill_L32K@32768", "sources_sha256": "5349d3312bd0bf376d0903be3af3814f85f37ca024e6f34f29091bdabf43b274"}],
+    "index": [{"pct": 69.23, "workload": "prefill_L1M_hot@1048576",
+               "sources_sha256": "bdca6e914cb6ff0dc7fa7af84499fe692bfa4272dc855bff19fa35591b172626"},
+              {"pct": 57.11, "workload": "prefill_L32K@32768",
+               "sources_sha256": "bdca6e914cb6ff0dc7fa7af84499fe692bfa4272dc855bff19fa35591b172626"}],
     "index_e4m3": [{"pct": 45.18, "workload": "prefill_L1M_hot@1048576",
-                    "sources_sha256": "5349d3312bd0bf376d0903be3af3814f85f37ca024e6f34f29091bdabf43b274"},
-                   {"pct": 32.15, "workload": "prefill_L32K@32768", "sources_sha256": "5349d3312bd0bf376d0903be3af3814f85f37ca024e6f34f29091bdabf43b274"}],
+                    "sources_sha256": "bdca6e914cb6ff0dc7fa7af84499fe692bfa4272dc855bff19fa35591b172626"},
+                   {"pct": 32.22, "workload": "prefill_L32K@32768",
+                    "sources_sha256": "bdca6e914cb6ff0dc7fa7af84499fe692bfa4272dc855bff19fa35591b172626"}],
     # attention: ncu --set full at L=8,192 (the 32K kernel at a capture-sized length)
-    "attention": [{"pct": 42.02, "workload": "prefill_L32K@8192", "sources_sha256": "d98350c3d0d851f10cfb97ed7e8e492b5174a6df8014fa897331e73b48970534"}],
+    "attention": [{"pct": 42.22, "workload": "prefill_L32K@8192",
+                   "sources_sha256": "55d1c77b924afda7453fd25713a809c2454a115dd07a1f391499b611b2f32625"}],
 }
 
 

@@ -3,6 +3,11 @@
 Argument marshalling only: every step of the operator runs in the CUDA kernels of libmsa.so.
 torch supplies device memory (outputs, workspace) and the current stream.  If the library has
 not been built, every call raises; there is no CPU fallback.
+
+With the environment variable MSA_DEBUG_CHECKS set (to anything but "" or "0") when the library
+is first loaded, the checked build libmsa_debug.so is loaded instead: the same calls, with
+bounds checks in the kernels and validation of the caller's index tensors (include/msa.h,
+"Checked build"); debug_record() reads its record of the first failed check.
 """
 from __future__ import annotations
 
@@ -12,6 +17,7 @@ import os
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libmsa.so")
+DEBUG_LIB_PATH = os.path.join(_HERE, "_build", "libmsa_debug.so")
 
 MSA_OK, MSA_ERR_INVALID_ARG, MSA_ERR_UNSUPPORTED, MSA_ERR_WORKSPACE = 0, 1, 2, 3
 MSA_ERR_CUDA, MSA_ERR_DEVICE_TIMEOUT, MSA_ERR_DEVICE_BOUNDS = 4, 5, 6
@@ -23,7 +29,13 @@ EXPORTS = ("msa_index_select_workspace", "msa_index_select", "msa_index_select_s
            "msa_attn_prefill", "msa_attn_prefill_marked", "msa_prefill_chunk_tokens",
            "msa_attn_prefill_launches",
            "msa_attn_decode_workspace", "msa_attn_decode",
-           "msa_get_device_status", "msa_reset_device_status", "msa_status_string")
+           "msa_get_device_status", "msa_reset_device_status", "msa_status_string",
+           "msa_debug_checks", "msa_get_debug_record")
+
+# msa_debug_site_t
+DEBUG_SITES = {0: "none", 1: "sel_range", 2: "sel_order", 3: "sel_local", 4: "seq_len",
+               5: "page_id", 16: "sched_list", 17: "sched_item", 18: "attn_item",
+               19: "attn_token", 20: "combine_pos", 21: "decode_page", 22: "index_row"}
 
 
 class MsaConfig(ctypes.Structure):
@@ -42,6 +54,11 @@ class MsaPagedKV(ctypes.Structure):
                 ("kv_dtype", ctypes.c_int32)]
 
 
+class MsaDebugRecord(ctypes.Structure):
+    _fields_ = [("site", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("value", ctypes.c_int64), ("bound", ctypes.c_int64), ("row", ctypes.c_int64)]
+
+
 class MsaError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
@@ -51,14 +68,21 @@ class MsaError(RuntimeError):
 _lib = None
 
 
+def checked_build_requested() -> bool:
+    v = os.environ.get("MSA_DEBUG_CHECKS", "")
+    return v not in ("", "0")
+
+
 def lib() -> ctypes.CDLL:
-    """The loaded libmsa.so; raises if it has not been built (no fallback exists)."""
+    """The loaded libmsa.so (libmsa_debug.so when MSA_DEBUG_CHECKS is set); raises if it has not
+    been built (no fallback exists)."""
     global _lib
     if _lib is None:
-        if not os.path.exists(LIB_PATH):
-            raise RuntimeError(f"libmsa.so is not built ({LIB_PATH}); run "
+        path = DEBUG_LIB_PATH if checked_build_requested() else LIB_PATH
+        if not os.path.exists(path):
+            raise RuntimeError(f"{os.path.basename(path)} is not built ({path}); run "
                                "`python -m block_sparse_long_msa_gb300.build`")
-        L = ctypes.CDLL(LIB_PATH)
+        L = ctypes.CDLL(path)
         P, i64, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t
         cfgp, pagedp = ctypes.POINTER(MsaConfig), ctypes.POINTER(MsaPagedKV)
         L.msa_index_select_workspace.argtypes = [cfgp, i64, i64, pagedp]
@@ -84,11 +108,15 @@ def lib() -> ctypes.CDLL:
         L.msa_reset_device_status.argtypes = [P, P]
         L.msa_status_string.argtypes = [ctypes.c_int]
         L.msa_status_string.restype = ctypes.c_char_p
+        L.msa_debug_checks.argtypes = []
+        L.msa_debug_checks.restype = ctypes.c_int32
+        L.msa_get_debug_record.argtypes = [P, ctypes.POINTER(MsaDebugRecord), P]
         for name in ("msa_index_select", "msa_index_select_scores", "msa_index_candidates",
                      "msa_index_merge", "msa_attn_prefill",
                      "msa_attn_prefill_marked",
                      "msa_attn_decode",
-                     "msa_get_device_status", "msa_reset_device_status"):
+                     "msa_get_device_status", "msa_reset_device_status",
+                     "msa_get_debug_record"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -345,3 +373,20 @@ def msa_get_device_status(ws, stream=None) -> int:
 
 def msa_reset_device_status(ws, stream=None) -> None:
     _check(lib().msa_reset_device_status(_ptr(ws), _stream(stream)), "msa_reset_device_status")
+
+
+def msa_debug_checks() -> int:
+    """0 for the release build; bit 0: the checked build; bit 1: input validation is on."""
+    return int(lib().msa_debug_checks())
+
+
+def debug_record(ws, stream=None) -> dict | None:
+    """The checked build's record of the first failed check in ws ({"site", "value", "bound",
+    "row"}; site "none" if no check failed); None for the release build."""
+    rec = MsaDebugRecord()
+    st = int(lib().msa_get_debug_record(_ptr(ws), ctypes.byref(rec), _stream(stream)))
+    if st == MSA_ERR_UNSUPPORTED:
+        return None
+    _check(st, "msa_get_debug_record")
+    return {"site": DEBUG_SITES.get(rec.site, str(rec.site)), "value": rec.value,
+            "bound": rec.bound, "row": rec.row}

@@ -58,6 +58,8 @@ struct SchedArgs {
   int4* items;         // {g, b, start, count}
   int32_t* list;       // (token << 4) | slot
   int32_t* pos;        // [(il*G + g)*k + s]: list position of the slot's unit, -1 if none
+  int64_t units;       // capacity of list / pos: chunk * G * k
+  int64_t max_items;   // capacity of items
   int32_t* status;
 };
 
@@ -216,8 +218,10 @@ __global__ void sched_items_kernel(SchedArgs a) {
   const int gb = idx % (a.G * a.nbk);
   const int g = gb / a.nbk, b = gb % a.nbk;
   const int c = a.rcnt[idx], base = a.list_base[gb] + a.rstart[idx], ib = a.item_base[idx];
-  for (int q = 0; q * kItemTokens < c; ++q)
+  for (int q = 0; q * kItemTokens < c; ++q) {
+    if (!MSA_IN_RANGE(a.status, kSiteSchedItem, ib + q, a.max_items, idx)) break;
     a.items[ib + q] = make_int4(g, b, base + q * kItemTokens, min(kItemTokens, c - q * kItemTokens));
+  }
 }
 
 __global__ void sched_fill_kernel(SchedArgs a) {
@@ -242,6 +246,10 @@ __global__ void sched_fill_kernel(SchedArgs a) {
     for (int q = 0; q < w; ++q) rank += __popc(mask[b * 4 + q]);
     const int gb = g * a.nbk + b;
     const int pos = a.list_base[gb] + a.hist[static_cast<size_t>(gb) * a.nbq + qbl] + rank;
+    if (!MSA_IN_RANGE(a.status, kSiteSchedList, pos, a.units, i)) {
+      a.pos[u0 + s] = -1;
+      continue;
+    }
     a.list[pos] = static_cast<int32_t>((i << 4) | s);
     a.pos[u0 + s] = pos;
   }
@@ -274,6 +282,8 @@ struct AttnArgs {
   int32_t* next_item;     // work counter: each CTA takes the next item when it has room
   const int32_t* list;
   int32_t G, k, q0;
+  int32_t q1, nbk;        // end of the chunk's queries, key blocks the chunk can select
+  int64_t units, max_items;  // capacities of list / partials and of items
   float scale_log2;       // softmax scale * log2(e)
   __half* po;             // [list position][16][128] unnormalised partial O (fp16)
   float* pm;              // [list position][16] row max (natural-log units)
@@ -366,7 +376,9 @@ __global__ void __launch_bounds__(512, 1)
   ItemMeta* meta = reinterpret_cast<ItemMeta*>(smem + kSmemMeta);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_items = *a.n_items;
+  int n_items = *a.n_items;
+  if (!MSA_IN_RANGE(a.status, kSiteSchedItem, n_items, a.max_items + 1, -1))
+    n_items = static_cast<int>(a.max_items);
 
   if (threadIdx.x == 0) {
     for (int r = 0; r < kMetaRing; ++r) {
@@ -429,8 +441,22 @@ __global__ void __launch_bounds__(512, 1)
         }
         break;
       }
-      const int4 item = a.items[it];
-      for (int j = lane; j < item.w; j += 32) m.tok[j] = a.list[item.z + j];
+      int4 item = a.items[it];
+      // checked build: a malformed item or token is clamped into range (the status word then
+      // marks the results invalid) so that every role still sees a consistent item
+      if (!MSA_IN_RANGE(a.status, kSiteAttnItem, item.x, a.G, it)) item.x = 0;
+      if (!MSA_IN_RANGE(a.status, kSiteAttnItem, item.y, a.nbk, it)) item.y = 0;
+      if (!MSA_IN_RANGE(a.status, kSiteAttnItem, item.w - 1, kItemTokens, it)) item.w = 1;
+      if (!MSA_IN_RANGE(a.status, kSiteAttnItem, item.z, a.units - item.w + 1, it)) item.z = 0;
+      for (int j = lane; j < item.w; j += 32) {
+        int32_t e = a.list[item.z + j];
+        // a token of the chunk, at or after the first token of the item's block; a slot < k
+        const int lo = max(a.q0, item.y * kBlock);
+        if (!MSA_IN_RANGE(a.status, kSiteAttnToken, (e >> 4) - lo, a.q1 - lo, it) ||
+            !MSA_IN_RANGE(a.status, kSiteAttnToken, e & 15, a.k, it))
+          e = lo << 4;
+        m.tok[j] = e;
+      }
       if (lane == 0) {
         m.g = item.x;
         m.b = item.y;
@@ -841,6 +867,8 @@ struct CombineArgs {
   int32_t G, k, q0, nrows;     // rows q0 .. q0+nrows-1
   __nv_bfloat16* o;            // [L][G*16][128]
   float* lse;                  // [G*16][L]
+  int64_t units;               // capacity of the partials
+  int32_t* status;
 };
 
 __global__ void __launch_bounds__(128) combine_kernel(CombineArgs a) {
@@ -848,9 +876,17 @@ __global__ void __launch_bounds__(128) combine_kernel(CombineArgs a) {
   const int64_t i = static_cast<int64_t>(a.q0) + il;
   const int t = threadIdx.x, hh = t >> 3, d0 = (t & 7) * 16;
   const int32_t* prow = a.pos + (static_cast<size_t>(il) * a.G + g) * a.k;
+  // a slot's list position: -1 (padding, or an id that was flagged) or below units; the checked
+  // build treats a position past the partials as padding
+  auto slot_pos = [&](int s) {
+    const int32_t p = prow[s];
+    return p >= 0 && MSA_IN_RANGE(a.status, kSiteCombinePos, p, a.units, i * a.G + g) ? p : -1;
+  };
   float M = -__int_as_float(0x7f800000);
-  for (int s = 0; s < a.k; ++s)
-    if (prow[s] >= 0) M = fmaxf(M, a.plse[static_cast<size_t>(prow[s]) * kHeadsPerGroup + hh]);
+  for (int s = 0; s < a.k; ++s) {
+    const int32_t p = slot_pos(s);
+    if (p >= 0) M = fmaxf(M, a.plse[static_cast<size_t>(p) * kHeadsPerGroup + hh]);
+  }
   float acc[16];
 #pragma unroll
   for (int q = 0; q < 16; ++q) acc[q] = 0.f;
@@ -859,8 +895,9 @@ __global__ void __launch_bounds__(128) combine_kernel(CombineArgs a) {
   // the sums is unchanged)
 #pragma unroll 4
   for (int s = 0; s < a.k; ++s) {
-    if (prow[s] < 0) continue;  // padding (and out-of-range ids, which were flagged)
-    const size_t r = static_cast<size_t>(prow[s]) * kHeadsPerGroup + hh;
+    const int32_t p = slot_pos(s);
+    if (p < 0) continue;  // padding (and out-of-range ids, which were flagged)
+    const size_t r = static_cast<size_t>(p) * kHeadsPerGroup + hh;
     den += __expf(a.plse[r] - M);
     const float w = __expf(a.pm[r] - M);
     const uint4* src = reinterpret_cast<const uint4*>(a.po + r * kDim + d0);
@@ -967,6 +1004,8 @@ cudaError_t launch_attn_prefill_chunk(const CUtensorMap& map_q, const CUtensorMa
   s.items = reinterpret_cast<int4*>(ws + w.items);
   s.list = reinterpret_cast<int32_t*>(ws + w.list);
   s.pos = reinterpret_cast<int32_t*>(ws + w.pos);
+  s.units = w.chunk * G * k;
+  s.max_items = w.max_items;
   s.status = reinterpret_cast<int32_t*>(ws);
   const size_t mask_smem = static_cast<size_t>(s.nbk) * 16;
   cudaError_t e;
@@ -996,6 +1035,10 @@ cudaError_t launch_attn_prefill_chunk(const CUtensorMap& map_q, const CUtensorMa
   a.G = G;
   a.k = k;
   a.q0 = s.q0;
+  a.q1 = static_cast<int32_t>(q1);
+  a.nbk = s.nbk;
+  a.units = s.units;
+  a.max_items = s.max_items;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.po = reinterpret_cast<__half*>(ws + w.po);
   a.pm = reinterpret_cast<float*>(ws + w.pm);
@@ -1037,6 +1080,8 @@ cudaError_t launch_attn_prefill_chunk(const CUtensorMap& map_q, const CUtensorMa
   c.nrows = static_cast<int32_t>(q1 - q0);
   c.o = reinterpret_cast<__nv_bfloat16*>(o);
   c.lse = lse;
+  c.units = s.units;
+  c.status = s.status;
   if (marks && marks[2]) cudaEventRecord(marks[2], stream);
   combine_kernel<<<dim3(c.nrows, G), 128, 0, stream>>>(c);
   return cudaGetLastError();

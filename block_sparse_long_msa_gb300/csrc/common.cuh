@@ -16,6 +16,47 @@ constexpr int kListMax = 15;    // non-local slots kept while scanning (k - 1 <=
 
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;  // 2 s
 
+// Checked build (compiled with MSA_DEBUG_CHECKS): the workspace header holds, next to the status
+// word, a record of the first failed bounds check: int32 site at byte 16, then int64 value,
+// bound and row at bytes 24, 32, 40 (msa_debug_record_t in include/msa.h).  Codes of the sites
+// checked inside the kernels (msa_debug_site_t):
+enum : int32_t {
+  kSiteSchedList = 16,   // a (token, slot) list position past the chunk's units
+  kSiteSchedItem = 17,   // a work item past the workspace's item capacity
+  kSiteAttnItem = 18,    // a work item's group, block, token count or list range
+  kSiteAttnToken = 19,   // a listed token outside the chunk or before the item's block
+  kSiteCombinePos = 20,  // a slot's list position past the chunk's units
+  kSiteDecodePage = 21,  // a scanned (sequence, logical page) outside [0, batch) x [0, max_pages)
+  kSiteIndexRow = 22,    // a selection or candidate row past the query count
+};
+
+#if defined(MSA_DEBUG_CHECKS)
+// Record a failed check (the first one wins) and flag MSA_ERR_DEVICE_BOUNDS; returns false so
+// that the caller skips or clamps the access.
+static __device__ __noinline__ bool debug_fail(int32_t* status, int32_t site, long long value,
+                                               long long bound, long long row) {
+  if (status) {
+    if (atomicCAS(status + 4, 0, site) == 0) {
+      long long* rec = reinterpret_cast<long long*>(status + 6);
+      rec[0] = value;
+      rec[1] = bound;
+      rec[2] = row;
+    }
+    report_status(status, kStatusBounds);
+  }
+  return false;
+}
+// True when 0 <= value < bound; otherwise records the failure.  The release build compiles the
+// check out entirely (the expression is the constant true and its operands are not evaluated).
+#define MSA_IN_RANGE(status, site, value, bound, row)                                   \
+  ((static_cast<long long>(value) >= 0 &&                                               \
+    static_cast<long long>(value) < static_cast<long long>(bound)) ||                   \
+   ::msa::debug_fail((status), (site), static_cast<long long>(value),                   \
+                     static_cast<long long>(bound), static_cast<long long>(row)))
+#else
+#define MSA_IN_RANGE(status, site, value, bound, row) true
+#endif
+
 // (score desc, block asc): does (sa, ba) rank before (sb, bb)?
 __device__ __forceinline__ bool ranks_before(float sa, int32_t ba, float sb, int32_t bb) {
   return sa > sb || (sa == sb && ba < bb);

@@ -137,6 +137,10 @@ struct PageWalk {
     while (b >= ns) {  // on to the next sequence that has pages
       ++s;
       b = 0;
+      if (!MSA_IN_RANGE(a.status, kSiteDecodePage, s, a.batch, s)) {  // checked build only
+        left = 0;
+        return -1;
+      }
       ns = scan_pages(a, s);
     }
     return a.kb0 + b;
@@ -336,7 +340,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
       float m[4];
 #pragma unroll
       for (int g = 0; g < 4; ++g) m[g] = warp_max_f32(__uint_as_float(v[g]));
-      if (lane < a.G) {
+      if (lane < a.G && MSA_IN_RANGE(a.status, kSiteDecodePage, b, a.max_pages, w.s)) {
         float* dst = reinterpret_cast<float*>(
             a.scores + (static_cast<size_t>(w.s) * a.G + lane) * a.max_pages + b);
         dst[ew] = lane == 0 ? m[0] : lane == 1 ? m[1] : lane == 2 ? m[2] : m[3];

@@ -293,6 +293,14 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
     if ((gpc == 2 || e == 0) && ok && !*abort_flag && i < a.L) {
       const int n = min(a.k - 1, nkey);
       const int g = g0 + (gpc == 2 ? e : 0);
+#if defined(MSA_DEBUG_CHECKS)
+      // checked build: the kept blocks are blocks this CTA scored (at most one failure recorded
+      // per row), and the row belongs to a group of the call
+      MSA_IN_RANGE(a.status, kSiteIndexRow, g, a.G, i);
+#pragma unroll
+      for (int p = 0; p < kListMax; ++p)
+        if (p < n && !MSA_IN_RANGE(a.status, kSiteIndexRow, list.b[p] - a.kb0, nkey, i)) break;
+#endif
       if (a.cand_block) {  // the list is in rank order
         const size_t off = (static_cast<size_t>(g) * a.L + i) * (a.k - 1);
         write_cand_row(list, n, a.k - 1, a.cand_score + off, a.cand_block + off);

@@ -71,4 +71,15 @@ cudaError_t launch_decode_attn(const CUtensorMap& map_kp, const CUtensorMap& map
                                int32_t* status, uint64_t wait_ns, int num_sms,
                                cudaStream_t stream, bool kv_fp8 = false);
 
+// Checked build (MSA_DEBUG_CHECKS): validation of the caller's index tensors, run before the
+// kernels when debug_checks_enabled() (the environment variable MSA_DEBUG_CHECKS is set to a
+// value other than "" or "0").  The release build compiles these to no-ops returning success.
+bool debug_checks_enabled();
+cudaError_t debug_check_prefill_sel(const int32_t* sel, int64_t L, int G, int k,
+                                    int32_t* status, cudaStream_t stream);
+cudaError_t debug_check_paged(const int32_t* page_table, const int32_t* seq_lens, int batch,
+                              int max_pages, int num_pages, int32_t* status, cudaStream_t stream);
+cudaError_t debug_check_decode_sel(const int32_t* sel, const int32_t* seq_lens, int batch, int G,
+                                   int k, int max_pages, int32_t* status, cudaStream_t stream);
+
 }  // namespace msa

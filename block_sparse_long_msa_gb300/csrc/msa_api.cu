@@ -5,6 +5,7 @@
 #include "common.cuh"
 #include "launch.h"
 #include "tmap.h"
+#include "trace.h"
 
 namespace {
 
@@ -116,6 +117,10 @@ msa_status_t index_select_paged(const msa_config_t* cfg, const void* q_idx,
   }
   int sms = 0;
   if (!sm_count(&sms)) return MSA_ERR_CUDA;
+  if (msa::debug_checks_enabled() &&
+      msa::debug_check_paged(paged->page_table, paged->seq_lens, paged->batch, paged->max_pages,
+                             paged->num_pages, status_word(ws), stream) != cudaSuccess)
+    return MSA_ERR_CUDA;
   float* scores = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + MSA_WS_HEADER_BYTES);
   cudaError_t e = msa::launch_decode_select(mk, mq, paged->page_table, paged->seq_lens,
                                             paged->batch, paged->max_pages, paged->num_pages, G,
@@ -141,12 +146,43 @@ const char* msa_status_string(msa_status_t s) {
   return "unknown status";
 }
 
+// The status word and the checked build's record: bytes [0, 48) of the header.
+constexpr size_t kStatusBytes = 48;
+
 msa_status_t msa_reset_device_status(void* ws, cudaStream_t stream) {
+  MSA_RANGE("msa_reset_device_status");
   if (!ws) return MSA_ERR_INVALID_ARG;
-  return cudaMemsetAsync(ws, 0, sizeof(int32_t), stream) == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+  return cudaMemsetAsync(ws, 0, kStatusBytes, stream) == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+}
+
+int32_t msa_debug_checks(void) {
+#if defined(MSA_DEBUG_CHECKS)
+  return 1 | (msa::debug_checks_enabled() ? 2 : 0);
+#else
+  return 0;
+#endif
+}
+
+msa_status_t msa_get_debug_record(const void* ws, msa_debug_record_t* record,
+                                  cudaStream_t stream) {
+  MSA_RANGE("msa_get_debug_record");
+  if (!ws || !record) return MSA_ERR_INVALID_ARG;
+  *record = msa_debug_record_t{};
+#if defined(MSA_DEBUG_CHECKS)
+  static_assert(sizeof(msa_debug_record_t) == 32, "record layout");
+  if (cudaMemcpyAsync(record, static_cast<const uint8_t*>(ws) + 16, sizeof *record,
+                      cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess)
+    return MSA_ERR_CUDA;
+  return MSA_OK;
+#else
+  (void)stream;
+  return MSA_ERR_UNSUPPORTED;
+#endif
 }
 
 msa_status_t msa_get_device_status(const void* ws, cudaStream_t stream) {
+  MSA_RANGE("msa_get_device_status");
   if (!ws) return MSA_ERR_INVALID_ARG;
   int32_t v = 0;
   if (cudaMemcpyAsync(&v, ws, sizeof v, cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
@@ -219,6 +255,7 @@ extern "C" {
 msa_status_t msa_index_select(const msa_config_t* cfg, const void* q_idx, const void* k_idx,
                               int64_t L, const msa_paged_kv_t* paged, int32_t* sel,
                               float* sel_score, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  MSA_RANGE("msa_index_select");
   return index_select(cfg, q_idx, k_idx, L, paged, sel, sel_score, nullptr, ws, ws_bytes, stream);
 }
 
@@ -226,6 +263,7 @@ msa_status_t msa_index_select_scores(const msa_config_t* cfg, const void* q_idx,
                                      const void* k_idx, int64_t L, const msa_paged_kv_t* paged,
                                      int32_t* sel, float* sel_score, float* block_scores,
                                      void* ws, size_t ws_bytes, cudaStream_t stream) {
+  MSA_RANGE("msa_index_select_scores");
   if (!block_scores) return MSA_ERR_INVALID_ARG;
   return index_select(cfg, q_idx, k_idx, L, paged, sel, sel_score, block_scores, ws, ws_bytes,
                       stream);
@@ -235,6 +273,7 @@ msa_status_t msa_index_candidates(const msa_config_t* cfg, const void* q_idx, co
                                   int64_t L, const msa_paged_kv_t* paged, int32_t block_begin,
                                   int32_t block_end, float* cand_score, int32_t* cand_block,
                                   void* ws, size_t ws_bytes, cudaStream_t stream) {
+  MSA_RANGE("msa_index_candidates");
   msa_status_t st = check_config(cfg);
   if (st != MSA_OK) return st;
   if (!q_idx || !ws || !aligned16(q_idx) || block_begin < 0 || block_end < block_begin)
@@ -265,6 +304,11 @@ msa_status_t msa_index_candidates(const msa_config_t* cfg, const void* q_idx, co
       if (!make_index_map(&mq, fp8, q_idx, 2, dims, strides, box)) return MSA_ERR_CUDA;
     }
     if (!sm_count(&sms)) return MSA_ERR_CUDA;
+    if (msa::debug_checks_enabled() &&
+        msa::debug_check_paged(paged->page_table, paged->seq_lens, paged->batch,
+                               paged->max_pages, paged->num_pages, status_word(ws),
+                               stream) != cudaSuccess)
+      return MSA_ERR_CUDA;
     const int kb1 = block_end < paged->max_pages ? block_end : paged->max_pages;
     float* scores = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + MSA_WS_HEADER_BYTES);
     cudaError_t e = msa::launch_decode_select(
@@ -306,6 +350,7 @@ msa_status_t msa_index_merge(const msa_config_t* cfg, int32_t num_shards,
                              const float* cand_score, const int32_t* cand_block, int64_t T,
                              const int32_t* seq_lens, int32_t* sel, float* sel_score, void* ws,
                              size_t ws_bytes, cudaStream_t stream) {
+  MSA_RANGE("msa_index_merge");
   msa_status_t st = check_config(cfg);
   if (st != MSA_OK) return st;
   if (num_shards < 1 || T < 0 || !sel || !ws) return MSA_ERR_INVALID_ARG;
@@ -336,16 +381,14 @@ int32_t msa_attn_prefill_launches(const msa_config_t* cfg, int64_t L) {
   return static_cast<int32_t>((L + chunk - 1) / chunk) * msa::prefill_chunk_launches();
 }
 
-msa_status_t msa_attn_prefill(const msa_config_t* cfg, const void* q, const void* k,
-                              const void* v, int64_t L, const int32_t* sel, void* o, float* lse,
-                              void* ws, size_t ws_bytes, cudaStream_t stream) {
-  return msa_attn_prefill_marked(cfg, q, k, v, L, sel, o, lse, ws, ws_bytes, stream, nullptr, 0);
-}
+}  // extern "C"
 
-msa_status_t msa_attn_prefill_marked(const msa_config_t* cfg, const void* q, const void* k,
-                                     const void* v, int64_t L, const int32_t* sel, void* o,
-                                     float* lse, void* ws, size_t ws_bytes, cudaStream_t stream,
-                                     cudaEvent_t* marks, int32_t n_marks) {
+namespace {
+
+msa_status_t attn_prefill(const msa_config_t* cfg, const void* q, const void* k, const void* v,
+                          int64_t L, const int32_t* sel, void* o, float* lse, void* ws,
+                          size_t ws_bytes, cudaStream_t stream, cudaEvent_t* marks,
+                          int32_t n_marks) {
   msa_status_t st = check_config(cfg);
   if (st != MSA_OK) return st;
   if (!q || !k || !v || !sel || !o || !lse || !ws || L < 0) return MSA_ERR_INVALID_ARG;
@@ -376,8 +419,12 @@ msa_status_t msa_attn_prefill_marked(const msa_config_t* cfg, const void* q, con
     return MSA_ERR_CUDA;
   const int64_t chunk = prefill_chunk(L);
   const msa::PrefillWorkspace w = msa::prefill_workspace_layout(L, G, cfg->topk, chunk);
+  if (msa::debug_checks_enabled() &&
+      msa::debug_check_prefill_sel(sel, L, G, cfg->topk, status_word(ws), stream) != cudaSuccess)
+    return MSA_ERR_CUDA;
   int32_t c = 0;
   for (int64_t q0 = 0; q0 < L; q0 += chunk, ++c) {
+    MSA_RANGE("prefill_chunk");
     const int64_t q1 = q0 + chunk < L ? q0 + chunk : L;
     cudaEvent_t m3[3] = {nullptr, nullptr, nullptr};
     for (int j = 0; j < 3; ++j)
@@ -394,6 +441,25 @@ msa_status_t msa_attn_prefill_marked(const msa_config_t* cfg, const void* q, con
   return MSA_OK;
 }
 
+}  // namespace
+
+extern "C" {
+
+msa_status_t msa_attn_prefill(const msa_config_t* cfg, const void* q, const void* k,
+                              const void* v, int64_t L, const int32_t* sel, void* o, float* lse,
+                              void* ws, size_t ws_bytes, cudaStream_t stream) {
+  MSA_RANGE("msa_attn_prefill");
+  return attn_prefill(cfg, q, k, v, L, sel, o, lse, ws, ws_bytes, stream, nullptr, 0);
+}
+
+msa_status_t msa_attn_prefill_marked(const msa_config_t* cfg, const void* q, const void* k,
+                                     const void* v, int64_t L, const int32_t* sel, void* o,
+                                     float* lse, void* ws, size_t ws_bytes, cudaStream_t stream,
+                                     cudaEvent_t* marks, int32_t n_marks) {
+  MSA_RANGE("msa_attn_prefill_marked");
+  return attn_prefill(cfg, q, k, v, L, sel, o, lse, ws, ws_bytes, stream, marks, n_marks);
+}
+
 size_t msa_attn_decode_workspace(const msa_config_t* cfg, const msa_paged_kv_t* paged) {
   if (check_config(cfg) != MSA_OK || !paged || paged->batch < 0) return 0;
   return MSA_WS_HEADER_BYTES +
@@ -404,6 +470,7 @@ size_t msa_attn_decode_workspace(const msa_config_t* cfg, const msa_paged_kv_t* 
 msa_status_t msa_attn_decode(const msa_config_t* cfg, const void* q, const msa_paged_kv_t* paged,
                              const int32_t* sel, void* o, float* lse, void* ws, size_t ws_bytes,
                              cudaStream_t stream) {
+  MSA_RANGE("msa_attn_decode");
   msa_status_t st = check_config(cfg);
   if (st != MSA_OK) return st;
   if ((st = check_paged(paged, true)) != MSA_OK) return st;
@@ -427,6 +494,12 @@ msa_status_t msa_attn_decode(const msa_config_t* cfg, const void* q, const msa_p
   }
   int sms = 0;
   if (!sm_count(&sms)) return MSA_ERR_CUDA;
+  if (msa::debug_checks_enabled() &&
+      (msa::debug_check_paged(paged->page_table, paged->seq_lens, paged->batch, paged->max_pages,
+                              paged->num_pages, status_word(ws), stream) != cudaSuccess ||
+       msa::debug_check_decode_sel(sel, paged->seq_lens, paged->batch, G, cfg->topk,
+                                   paged->max_pages, status_word(ws), stream) != cudaSuccess))
+    return MSA_ERR_CUDA;
   cudaError_t e = msa::launch_decode_attn(
       mk, mv, q, sel, paged->page_table, paged->seq_lens, paged->batch, paged->max_pages,
       paged->num_pages, G, cfg->topk, cfg->softmax_scale,

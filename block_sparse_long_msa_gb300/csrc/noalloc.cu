@@ -7,6 +7,7 @@
 #include "common.cuh"
 #include "launch.h"
 #include "tmap.h"
+#include "trace.h"
 
 namespace {
 
@@ -63,6 +64,7 @@ extern "C" msa_status_t msa_attn_prefill_noalloc(const msa_config_t* cfg, const 
                                                  const void* k, const void* v, int64_t L,
                                                  const int32_t* sel, void* o, float* lse,
                                                  int32_t* device_status, cudaStream_t stream) {
+  MSA_RANGE("msa_attn_prefill_noalloc");
   if (!cfg || cfg->num_groups < 1 || cfg->heads_per_group < 1 || cfg->topk < 1 ||
       (cfg->index_dtype != MSA_INDEX_BF16 && cfg->index_dtype != MSA_INDEX_E4M3) ||
       cfg->wait_limit_ns < 0 || !(cfg->softmax_scale == cfg->softmax_scale))
@@ -101,6 +103,10 @@ extern "C" msa_status_t msa_attn_prefill_noalloc(const msa_config_t* cfg, const 
   const uint64_t wait_ns = cfg->wait_limit_ns > 0 ? static_cast<uint64_t>(cfg->wait_limit_ns)
                                                   : msa::kDefaultWaitNs;
   const msa::PrefillWorkspace w = msa::prefill_workspace_layout(L, G, topk, chunk);
+  if (msa::debug_checks_enabled() &&
+      msa::debug_check_prefill_sel(sel, L, G, topk, reinterpret_cast<int32_t*>(scratch),
+                                   stream) != cudaSuccess)
+    return MSA_ERR_CUDA;
   for (int64_t q0 = 0; q0 < L; q0 += chunk) {
     const int64_t q1 = q0 + chunk < L ? q0 + chunk : L;
     cudaEvent_t none[3] = {nullptr, nullptr, nullptr};

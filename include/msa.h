@@ -27,6 +27,19 @@
  *     skips the offending access and finishes.
  *   - Host-side argument errors return before anything is enqueued.  Launch failures return
  *     MSA_ERR_CUDA.
+ *   - Tracing: a library built with MSA_NVTX (the default build) wraps every call that enqueues
+ *     work in an NVTX range named after the call (and each 64K-query pass of the prefill main
+ *     branch in a nested range "prefill_chunk"), so profilers can select one call's kernels.
+ *   - Checked build: libmsa_debug.so, compiled with MSA_DEBUG_CHECKS, exports the same calls.
+ *     Its kernels check the indices they derive (schedule positions, work items, listed tokens,
+ *     scanned pages, written rows) before each access, clamp or skip a failing one, flag
+ *     MSA_ERR_DEVICE_BOUNDS and record the first failure (msa_get_debug_record).  With the
+ *     environment variable MSA_DEBUG_CHECKS set (to anything but "" or "0") it also validates
+ *     the caller's index tensors before the kernels run: selection rows in the form
+ *     msa_index_select writes them (ascending, within the query's causal range, the query's own
+ *     block present, -1 only as trailing padding), sequence lengths in [1, max_pages * 128] and
+ *     every page-table entry of a used page in [0, num_pages).  Results are bit-identical to the
+ *     release build's when no check fails.
  *   - v1 supports head_dim = index_dim = block_size = 128, 1 <= topk <= 16, num_groups <= 4 for
  *     the index branch, heads_per_group = 16 for the main branch (prefill and decode: a group's
  *     16 query heads are the rows of its tensor-core tiles), prefill lengths up to 1,572,864;
@@ -44,6 +57,8 @@
 extern "C" {
 #endif
 
+/* Workspace header: bytes [0, 4) the device status word; bytes [16, 48) the checked build's
+ * msa_debug_record_t; the rest is reserved. */
 #define MSA_WS_HEADER_BYTES 256
 
 typedef enum {
@@ -264,8 +279,50 @@ msa_status_t msa_attn_decode(const msa_config_t* cfg, const void* q,
 /* Synchronizes `stream`, then returns the device status recorded in ws (MSA_OK if none). */
 msa_status_t msa_get_device_status(const void* ws, cudaStream_t stream);
 
-/* Enqueues a clear of the device status word in ws on `stream`. */
+/* Enqueues a clear of the device status word in ws, and of the checked build's record, on
+ * `stream`. */
 msa_status_t msa_reset_device_status(void* ws, cudaStream_t stream);
+
+/* The checks of the checked build (libmsa_debug.so), each named by the site that failed. */
+typedef enum {
+  MSA_SITE_NONE = 0,
+  /* the caller's index tensors (validated when MSA_DEBUG_CHECKS is set in the environment) */
+  MSA_SITE_SEL_RANGE = 1,    /* a selected id outside [-1, block of the query]:
+                                value = the id, bound = that block + 1 */
+  MSA_SITE_SEL_ORDER = 2,    /* ids not strictly ascending, or an id after -1 padding:
+                                value = the slot, bound = k */
+  MSA_SITE_SEL_LOCAL = 3,    /* the query's own block missing: value = the row's last id */
+  MSA_SITE_SEQ_LEN = 4,      /* seq_lens[s] outside [1, max_pages * 128]: row = s */
+  MSA_SITE_PAGE_ID = 5,      /* a used page's page-table entry outside [0, num_pages): row = s */
+  /* indices the kernels derive, checked before each access */
+  MSA_SITE_SCHED_LIST = 16,  /* a (token, slot) list position past the pass's units */
+  MSA_SITE_SCHED_ITEM = 17,  /* a work item past the workspace's item capacity */
+  MSA_SITE_ATTN_ITEM = 18,   /* a work item's group, block, token count or list range */
+  MSA_SITE_ATTN_TOKEN = 19,  /* a listed token outside the pass or before the item's block */
+  MSA_SITE_COMBINE_POS = 20, /* a slot's list position past the pass's units */
+  MSA_SITE_DECODE_PAGE = 21, /* a scanned (sequence, logical page) outside the batch's range */
+  MSA_SITE_INDEX_ROW = 22    /* a selection row's group, or a kept block the row did not score */
+} msa_debug_site_t;
+
+/* The first failed check since the last reset.  row names what the failure concerns: g * T + t
+ * for a selection row of query t in group g (T = L or batch), the sequence for paged input, the
+ * query or work item for the kernels' own checks. */
+typedef struct {
+  int32_t site;     /* msa_debug_site_t; MSA_SITE_NONE if no check failed */
+  int32_t reserved;
+  int64_t value;    /* the offending value */
+  int64_t bound;    /* the exclusive upper bound of the check */
+  int64_t row;
+} msa_debug_record_t;
+
+/* 0 for the release build; in the checked build bit 0 is set, and bit 1 when the caller's index
+ * tensors are validated (MSA_DEBUG_CHECKS set in the environment). */
+int32_t msa_debug_checks(void);
+
+/* Synchronizes `stream`, then copies the record of the first failed check from ws.  The release
+ * build keeps no record: it zeroes *record and returns MSA_ERR_UNSUPPORTED. */
+msa_status_t msa_get_debug_record(const void* ws, msa_debug_record_t* record,
+                                  cudaStream_t stream);
 
 /* Static description of a status code. */
 const char* msa_status_string(msa_status_t status);

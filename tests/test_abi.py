@@ -28,15 +28,29 @@ def _declared():
 
 
 def test_every_declared_symbol_is_exported(lib):
+    import block_sparse_long_msa_gb300 as msa
     declared = _declared()
     assert len(declared) >= 9
-    out = subprocess.run(["nm", "-D", "--defined-only", lib._name], capture_output=True,
-                         text=True, check=True).stdout
-    exported = set(re.findall(r"\bT\s+(msa_\w+)", out))
-    missing = [n for n in declared if n not in exported]
-    assert not missing, missing
+    # the release build and the checked build export the same calls
+    for path in (lib._name, msa.DEBUG_LIB_PATH):
+        out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True,
+                             text=True, check=True).stdout
+        exported = set(re.findall(r"\bT\s+(msa_\w+)", out))
+        missing = [n for n in declared if n not in exported]
+        assert not missing, (path, missing)
+        assert set(msa.EXPORTS) <= exported
+
+
+def test_checked_build_describes_itself_without_a_gpu(lib):
     import block_sparse_long_msa_gb300 as msa
-    assert set(msa.EXPORTS) <= exported
+    assert lib.msa_debug_checks() == 0
+    rec = msa.MsaDebugRecord()
+    assert lib.msa_get_debug_record(None, ctypes.byref(rec), None) == msa.MSA_ERR_INVALID_ARG
+    dbg = ctypes.CDLL(msa.DEBUG_LIB_PATH)
+    dbg.msa_debug_checks.restype = ctypes.c_int32
+    # bit 0: the checked build; bit 1 follows MSA_DEBUG_CHECKS in this process's environment
+    assert dbg.msa_debug_checks() & 1 == 1
+    assert (dbg.msa_debug_checks() >> 1) == int(msa.checked_build_requested())
 
 
 def test_status_strings(lib):

@@ -36,7 +36,7 @@ struct ScanTiles {
   static constexpr uint32_t kStage = kKeys + kQRows;
   static constexpr int kPanels = kF8 ? 1 : 2;
   static constexpr int kSteps = kF8 ? 4 : 8;
-  static constexpr int kStages = kF8 ? 11 : 6;                 // about 200 KB in flight
+  static constexpr int kStages = kF8 ? 6 : 3;                  // 108 KB per CTA, two per SM
   static constexpr uint32_t kIdesc = kF8 ? idesc_e4m3_f32(128, 16)
                                          : idesc_bf16_f32(128, 16, false, false);
 };
@@ -61,6 +61,12 @@ static_assert(ScanTiles<false>::kStages <= kScanMaxStages && scan_smem<false>() 
               "scan shared memory");
 static_assert(ScanTiles<true>::kStages <= kScanMaxStages && scan_smem<true>() <= 232448,
               "scan shared memory");
+// two scan CTAs share an SM (233,472 bytes of shared memory, 1 KB of it reserved per CTA), so
+// each SM runs two independent page pipelines
+constexpr int kScanCtasPerSm = 2;
+static_assert(kScanCtasPerSm * (scan_smem<false>() + 1024) <= 233472 &&
+                  kScanCtasPerSm * (scan_smem<true>() + 1024) <= 233472,
+              "two scan CTAs per SM");
 
 struct ScanArgs {
   const int32_t* page_table;
@@ -161,7 +167,7 @@ __device__ __forceinline__ float warp_max_f32(float v) {
 constexpr int kScanThreads = 384;
 
 template <bool kF8>
-__global__ void __launch_bounds__(kScanThreads, 1)
+__global__ void __launch_bounds__(kScanThreads, kScanCtasPerSm)
     decode_scan_kernel(const __grid_constant__ CUtensorMap map_k,
                        const __grid_constant__ CUtensorMap map_q, ScanArgs a) {
   using T = ScanTiles<kF8>;
@@ -951,7 +957,8 @@ cudaError_t launch_decode_select(const CUtensorMap& map_k, const CUtensorMap& ma
   a.status = status;
   a.wait_ns = wait_ns;
   const int grid = static_cast<int>(
-      std::max<int64_t>(1, std::min<int64_t>(num_sms, static_cast<int64_t>(batch) * max_pages)));
+      std::max<int64_t>(1, std::min<int64_t>(static_cast<int64_t>(kScanCtasPerSm) * num_sms,
+                                             static_cast<int64_t>(batch) * max_pages)));
   cudaError_t e;
   if (fp8) {
     if ((e = cudaFuncSetAttribute(decode_scan_kernel<true>,

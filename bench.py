@@ -206,10 +206,10 @@ NCU_TRAFFIC = {
                 {"bytes_per_launch": 18934947584, "workload": "prefill_L1M_hot@1048576",
                  "sources_sha256": "55d1c77b924afda7453fd25713a809c2454a115dd07a1f391499b611b2f32625"}],
     # decode, 64 sequences of 16K-256K tokens
-    "decode_scan": [{"bytes_per_launch": 2087945216, "workload": "decode_b64_16K_256K@64x262144",
-                     "sources_sha256": "c6ba85d779f7de1ce06e7602971fdd5baebd6cc7b9d388c22c0b1b5894dff508"}],
-    "decode_scan_e4m3": [{"bytes_per_launch": 1047191296, "workload": "decode_b64_16K_256K@64x262144",
-                          "sources_sha256": "c6ba85d779f7de1ce06e7602971fdd5baebd6cc7b9d388c22c0b1b5894dff508"}],
+    "decode_scan": [{"bytes_per_launch": 2088344832, "workload": "decode_b64_16K_256K@64x262144",
+                     "sources_sha256": "4fa089e411d05e1478e45e648c8a0f4df982c50a01db26b715de010610f4a19f"}],
+    "decode_scan_e4m3": [{"bytes_per_launch": 1047283712, "workload": "decode_b64_16K_256K@64x262144",
+                          "sources_sha256": "4fa089e411d05e1478e45e648c8a0f4df982c50a01db26b715de010610f4a19f"}],
 }
 # Tensor-pipe activity from the same captures (sm__pipe_tensor_cycles_active, % of elapsed
 # cycles: a fraction of the part's nominal tensor rate at the clock of the moment).

@@ -575,7 +575,7 @@ def e2e_leg(msa, case, dc, steps, world, stream):
     (prefill and decode) are double-buffered on the device, and every copy runs on one of two
     copy streams, so step s+1's inputs arrive and step s-1's results leave while step s
     computes, and no copy waits in a copy engine's queue in front of the compute stream.
-    Returns (ms, h2d bytes, d2h bytes)."""
+    Returns (ms, h2d bytes, d2h bytes, clocks sampled over the timed steps)."""
     names_in = ("q", "k", "v", "q_idx", "k_idx")
     dnames = ("q", "q_idx", "seq_lens", "page_table")
     inp = case.inp
@@ -605,21 +605,32 @@ def e2e_leg(msa, case, dc, steps, world, stream):
     ev_out = [torch.cuda.Event() for _ in range(2)]
     cfg = case.cfg
 
-    def e2e_step(i):
+    c_marks = []  # per timed step: compute start and end on the compute stream
+    h_marks, d_marks = [], []  # per timed step: its copies in, its copies out
+
+    def e2e_step(i, mark=False):
         b = i % 2
         with torch.cuda.stream(s_h2d):
             if i >= 2:
                 s_h2d.wait_event(ev_used[b])
+            if mark:
+                h_marks.append((_event(s_h2d), _event(s_h2d)))
+                h_marks[-1][0].record(s_h2d)
             for k_, t in dhost_in.items():
                 dev_in[b]["d_" + k_].copy_(t, non_blocking=True)
             for k_, t in host_in.items():
                 dev_in[b][k_].copy_(t, non_blocking=True)
+            if mark:
+                h_marks[-1][1].record(s_h2d)
             ev_in[b].record(s_h2d)
         stream.wait_event(ev_in[b])
         if i >= 2:
             stream.wait_event(ev_out[b])
         ob, lb, sb, dob, dlb, dsb = dev_out[b]
         di = dev_in[b]
+        if mark:
+            c_marks.append((_event(stream), _event(stream)))
+            c_marks[-1][0].record(stream)
         msa.msa_index_select(cfg, di["q_idx"], di["k_idx"], sel=sb, ws=case.ws, stream=stream)
         msa.msa_attn_prefill(cfg, di["q"], di["k"], di["v"], sb, o=ob, lse=lb, ws=case.ws,
                              stream=stream)
@@ -627,11 +638,18 @@ def e2e_leg(msa, case, dc, steps, world, stream):
                              stream=stream)
         msa.msa_attn_decode(dc.cfg, di["d_q"], pagedb[b], dsb, o=dob, lse=dlb, ws=dc.ws,
                             stream=stream)
+        if mark:
+            c_marks[-1][1].record(stream)
         ev_used[b].record(stream)
         with torch.cuda.stream(s_d2h):
             s_d2h.wait_event(ev_used[b])
+            if mark:
+                d_marks.append((_event(s_d2h), _event(s_d2h)))
+                d_marks[-1][0].record(s_d2h)
             for hd, t in zip(host_out, dev_out[b]):
                 hd.copy_(t, non_blocking=True)
+            if mark:
+                d_marks[-1][1].record(s_d2h)
             ev_out[b].record(s_d2h)
 
     ref_sel, ref_dsel = case.sel.clone(), dc.sel.clone()  # the resident-input step's selections
@@ -639,21 +657,35 @@ def e2e_leg(msa, case, dc, steps, world, stream):
         e2e_step(i)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.__enter__()
     barrier(world)
     torch.cuda.synchronize()
     e0.record(s_h2d)  # the first operation of the timed region
     for i in range(steps):
-        e2e_step(i)
+        e2e_step(i, mark=True)
     s_d2h.wait_stream(stream)
     e1.record(s_d2h)  # after the last copy out, which follows everything else
     torch.cuda.synchronize()
+    sampler.__exit__(None, None, None)
     ms = max_over_ranks(e0.elapsed_time(e1), world)
+    compute_ms = [a.elapsed_time(b) for a, b in c_marks]
+    starts = [e0.elapsed_time(a) for a, _ in c_marks]
     check_status(msa, case.ws, dc.ws)
     # the pipelined steps computed the same selections as the resident-input step
     assert torch.equal(host_out[2], ref_sel.cpu()), "end-to-end selection differs"
     assert torch.equal(host_out[5], ref_dsel.cpu()), "end-to-end decode selection differs"
     del host_in, host_out, dev_in, dev_out, dhost_in
-    return ms, h2d, d2h
+    h2d_ms = [a.elapsed_time(b) for a, b in h_marks]
+    d2h_ms = [a.elapsed_time(b) for a, b in d_marks]
+    detail = {"clocks": sampler.summary(),
+              "compute_ms_per_step": statistics.median(compute_ms),
+              "h2d_ms_per_step": [round(x, 1) for x in h2d_ms],
+              "d2h_ms_per_step": [round(x, 1) for x in d2h_ms],
+              "first_compute_start_ms": starts[0],
+              "compute_start_spacing_ms": statistics.median(
+                  [b - a for a, b in zip(starts, starts[1:])]) if len(starts) > 1 else None}
+    return ms, h2d, d2h, detail
 
 
 def timed_alone(fn, n, warmup, stream):
@@ -699,10 +731,11 @@ def run_msa(args, world, rank):
                    "skipped": f"host memory available {avail / 2**30:.0f} GiB < "
                               f"{need / 2**30:.0f} GiB"}
         else:
-            ms, h2d, d2h = e2e_leg(msa, case, dc, args.e2e_steps, world, stream)
+            ms, h2d, d2h, e2e_detail = e2e_leg(msa, case, dc, args.e2e_steps, world, stream)
             e2e = {"value": world * w.L * args.e2e_steps / (ms * 1e-3), "unit": "tokens/s",
                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                    "steps": args.e2e_steps, "ms_per_step": ms / args.e2e_steps,
+                   **e2e_detail,
                    "note": "prefill tokens over the whole step (prefill + decode) with every "
                            "step's inputs copied from pinned host memory and its outputs copied "
                            "back, on copy streams of their own (device buffers doubled, so the "

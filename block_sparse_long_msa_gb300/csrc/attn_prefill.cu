@@ -87,6 +87,7 @@ __device__ __forceinline__ void build_block_mask(const SchedArgs& a, int g, int 
 }
 
 __global__ void sched_hist_kernel(SchedArgs a) {
+  pdl_enter();  // before any global memory access (launch_pdl)
   extern __shared__ uint32_t mask[];
   const int qbl = blockIdx.x, g = blockIdx.y;
   const int qb = a.q0 / kBlock + qbl;
@@ -100,6 +101,7 @@ __global__ void sched_hist_kernel(SchedArgs a) {
 
 // One warp per (group, block): exclusive prefix over the query blocks that can choose b.
 __global__ void sched_scan_kernel(SchedArgs a) {
+  pdl_enter();  // before any global memory access (launch_pdl)
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (warp >= a.G * a.nbk) return;
   const int b = warp % a.nbk;
@@ -197,6 +199,7 @@ __device__ int block_exclusive_scan(int n, F val, int32_t* out, int32_t* warp_su
 
 // One CTA: list offsets over (group, block), item offsets over (range, group, block).
 __global__ void __launch_bounds__(1024) sched_bases_kernel(SchedArgs a) {
+  pdl_enter();  // before any global memory access (launch_pdl)
   __shared__ int32_t warp_sums[32];
   __shared__ int32_t carry;
   const int32_t* cnt = a.cnt;
@@ -213,6 +216,7 @@ __global__ void __launch_bounds__(1024) sched_bases_kernel(SchedArgs a) {
 }
 
 __global__ void sched_items_kernel(SchedArgs a) {
+  pdl_enter();  // before any global memory access (launch_pdl)
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= a.nr * a.G * a.nbk) return;
   const int gb = idx % (a.G * a.nbk);
@@ -225,6 +229,7 @@ __global__ void sched_items_kernel(SchedArgs a) {
 }
 
 __global__ void sched_fill_kernel(SchedArgs a) {
+  pdl_enter();  // before any global memory access (launch_pdl)
   extern __shared__ uint32_t mask[];
   const int qbl = blockIdx.x, g = blockIdx.y;
   const int qb = a.q0 / kBlock + qbl;
@@ -352,6 +357,7 @@ __global__ void __launch_bounds__(512, 1)
                          const __grid_constant__ CUtensorMap map_v,
                          const __grid_constant__ CUtensorMap map_po,
                          const __grid_constant__ CUtensorMap map_po_tok, AttnArgs a) {
+  pdl_enter();  // before any global memory access (launch_pdl)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw;
   const uint32_t base = smem_u32(smem);
@@ -872,6 +878,7 @@ struct CombineArgs {
 };
 
 __global__ void __launch_bounds__(128) combine_kernel(CombineArgs a) {
+  pdl_enter();  // before any global memory access (launch_pdl)
   const int il = blockIdx.x, g = blockIdx.y;
   const int64_t i = static_cast<int64_t>(a.q0) + il;
   const int t = threadIdx.x, hh = t >> 3, d0 = (t & 7) * 16;
@@ -1019,13 +1026,17 @@ cudaError_t launch_attn_prefill_chunk(const CUtensorMap& map_q, const CUtensorMa
   }
   const dim3 qgrid(s.nbq, G);
   if (marks && marks[0]) cudaEventRecord(marks[0], stream);
-  sched_hist_kernel<<<qgrid, kBlock, mask_smem, stream>>>(s);
   const int pairs = G * s.nbk;
-  sched_scan_kernel<<<(pairs * 32 + 255) / 256, 256, 0, stream>>>(s);
-  sched_bases_kernel<<<1, 1024, 0, stream>>>(s);
-  sched_items_kernel<<<(s.nr * pairs + 255) / 256, 256, 0, stream>>>(s);
-  sched_fill_kernel<<<qgrid, kBlock, mask_smem, stream>>>(s);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = launch_pdl(sched_hist_kernel, qgrid, dim3(kBlock), mask_smem, stream, s)) !=
+          cudaSuccess ||
+      (e = launch_pdl(sched_scan_kernel, dim3((pairs * 32 + 255) / 256), dim3(256), 0, stream,
+                      s)) != cudaSuccess ||
+      (e = launch_pdl(sched_bases_kernel, dim3(1), dim3(1024), 0, stream, s)) != cudaSuccess ||
+      (e = launch_pdl(sched_items_kernel, dim3((s.nr * pairs + 255) / 256), dim3(256), 0, stream,
+                      s)) != cudaSuccess ||
+      (e = launch_pdl(sched_fill_kernel, qgrid, dim3(kBlock), mask_smem, stream, s)) !=
+          cudaSuccess)
+    return e;
 
   AttnArgs a{};
   a.items = s.items;
@@ -1064,9 +1075,9 @@ cudaError_t launch_attn_prefill_chunk(const CUtensorMap& map_q, const CUtensorMa
   }
   const int grid = static_cast<int>(std::min<int64_t>(w.max_items, num_sms));
   if (marks && marks[1]) cudaEventRecord(marks[1], stream);
-  attn_kv_outer_kernel<<<grid, 512, kAttnSmem, stream>>>(map_q, map_k, map_v, map_po,
-                                                          map_po_tok, a);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = launch_pdl(attn_kv_outer_kernel, dim3(grid), dim3(512), kAttnSmem, stream, map_q,
+                      map_k, map_v, map_po, map_po_tok, a)) != cudaSuccess)
+    return e;
 
   CombineArgs c{};
   c.pos = s.pos;
@@ -1083,8 +1094,7 @@ cudaError_t launch_attn_prefill_chunk(const CUtensorMap& map_q, const CUtensorMa
   c.units = s.units;
   c.status = s.status;
   if (marks && marks[2]) cudaEventRecord(marks[2], stream);
-  combine_kernel<<<dim3(c.nrows, G), 128, 0, stream>>>(c);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel, dim3(c.nrows, G), dim3(128), 0, stream, c);
 }
 
 }  // namespace msa

@@ -170,6 +170,7 @@ template <bool kF8>
 __global__ void __launch_bounds__(kScanThreads, kScanCtasPerSm)
     decode_scan_kernel(const __grid_constant__ CUtensorMap map_k,
                        const __grid_constant__ CUtensorMap map_q, ScanArgs a) {
+  pdl_enter();  // before any global memory access (launch_pdl)
   using T = ScanTiles<kF8>;
   constexpr int kScanStages = T::kStages;
   constexpr uint32_t kScanStage = T::kStage;
@@ -382,6 +383,7 @@ struct TopkArgs {
 };
 
 __global__ void __launch_bounds__(128) decode_topk_kernel(TopkArgs a) {
+  pdl_enter();  // before any global memory access (launch_pdl)
   __shared__ float cand_s[4][kListMax];
   __shared__ int32_t cand_b[4][kListMax];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -617,6 +619,7 @@ template <bool kKV8>
 __global__ void __launch_bounds__(kDecThreads, 1)
     decode_attn_kernel(const __grid_constant__ CUtensorMap map_kp,
                        const __grid_constant__ CUtensorMap map_vp, DecAttnArgs a) {
+  pdl_enter();  // before any global memory access (launch_pdl)
   using Lay = DecLayout<kKV8>;
   constexpr int kDecStages = Lay::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -895,6 +898,7 @@ struct DecCombineArgs {
 };
 
 __global__ void __launch_bounds__(128) decode_combine_kernel(DecCombineArgs a) {
+  pdl_enter();  // before any global memory access (launch_pdl)
   const int s = blockIdx.x, g = blockIdx.y, t = threadIdx.x, hh = t >> 3, d0 = (t & 7) * 16;
   const size_t u0 = (static_cast<size_t>(s) * a.G + g) * a.k;
   float M = -__int_as_float(0x7f800000);
@@ -965,15 +969,17 @@ cudaError_t launch_decode_select(const CUtensorMap& map_k, const CUtensorMap& ma
                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   scan_smem<true>())) != cudaSuccess)
       return e;
-    decode_scan_kernel<true><<<grid, kScanThreads, scan_smem<true>(), stream>>>(map_k, map_q,
-                                                                                 a);
+    if ((e = launch_pdl(decode_scan_kernel<true>, dim3(grid), dim3(kScanThreads),
+                        scan_smem<true>(), stream, map_k, map_q, a)) != cudaSuccess)
+      return e;
   } else {
     if ((e = cudaFuncSetAttribute(decode_scan_kernel<false>,
                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   scan_smem<false>())) != cudaSuccess)
       return e;
-    decode_scan_kernel<false><<<grid, kScanThreads, scan_smem<false>(), stream>>>(map_k, map_q,
-                                                                                  a);
+    if ((e = launch_pdl(decode_scan_kernel<false>, dim3(grid), dim3(kScanThreads),
+                        scan_smem<false>(), stream, map_k, map_q, a)) != cudaSuccess)
+      return e;
   }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   TopkArgs t{};
@@ -991,8 +997,7 @@ cudaError_t launch_decode_select(const CUtensorMap& map_k, const CUtensorMap& ma
   t.cand_score = cand_score;
   t.cand_block = cand_block;
   t.status = status;
-  decode_topk_kernel<<<batch * G, 128, 0, stream>>>(t);
-  return cudaGetLastError();
+  return launch_pdl(decode_topk_kernel, dim3(batch * G), dim3(128), 0, stream, t);
 }
 
 size_t decode_attn_workspace_bytes(int batch, int G, int k) {
@@ -1031,18 +1036,24 @@ cudaError_t launch_decode_attn(const CUtensorMap& map_kp, const CUtensorMap& map
                                   cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) !=
         cudaSuccess)
       return e;
-    decode_attn_kernel<true><<<grid, kDecThreads, smem, stream>>>(map_kp, map_vp, a);
+    if ((e = launch_pdl(decode_attn_kernel<true>, dim3(grid), dim3(kDecThreads), smem, stream,
+                        map_kp, map_vp, a)) != cudaSuccess)
+      return e;
   } else {
     constexpr uint32_t smem = DecLayout<false>::kSmem;
     if ((e = cudaFuncSetAttribute(decode_attn_kernel<false>,
                                   cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) !=
         cudaSuccess)
       return e;
-    decode_attn_kernel<false><<<grid, kDecThreads, smem, stream>>>(map_kp, map_vp, a);
+    if ((e = launch_pdl(decode_attn_kernel<false>, dim3(grid), dim3(kDecThreads), smem, stream,
+                        map_kp, map_vp, a)) != cudaSuccess)
+      return e;
   }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   DecCombineArgs c{a.po, a.plse, batch, G, k, static_cast<__nv_bfloat16*>(o), lse};
-  decode_combine_kernel<<<dim3(batch, G), 128, 0, stream>>>(c);
+  if ((e = launch_pdl(decode_combine_kernel, dim3(batch, G), dim3(128), 0, stream, c)) !=
+      cudaSuccess)
+    return e;
   return cudaGetLastError();
 }
 

@@ -25,6 +25,7 @@ struct MergeArgs {
 
 // One thread per (group, query) row: a register top-(k-1) over the R x (k-1) candidates.
 __global__ void __launch_bounds__(128) index_merge_kernel(MergeArgs a) {
+  pdl_enter();  // before any global memory access (launch_pdl)
   const int64_t r = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (r >= a.G * a.T) return;
   const int g = static_cast<int>(r / a.T);
@@ -78,8 +79,7 @@ cudaError_t launch_index_merge(const float* cand_score, const int32_t* cand_bloc
   MergeArgs a{cand_score, cand_block, num_shards, G, k, T, seq_lens, sel, sel_score, status};
   const int64_t rows = static_cast<int64_t>(G) * T;
   const unsigned grid = static_cast<unsigned>((rows + 127) / 128);
-  index_merge_kernel<<<grid, 128, 0, stream>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(index_merge_kernel, dim3(grid), dim3(128), 0, stream, a);
 }
 
 }  // namespace msa

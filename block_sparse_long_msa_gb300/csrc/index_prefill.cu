@@ -85,6 +85,7 @@ template <bool kF8>
 __global__ void __launch_bounds__(kIndexThreads, 1)
     index_select_prefill_kernel(const __grid_constant__ CUtensorMap map_q,
                                 const __grid_constant__ CUtensorMap map_k, IndexPrefillArgs a) {
+  pdl_enter();  // before any global memory access (launch_pdl)
   using T = IdxTiles<kF8>;
   constexpr uint32_t kQTile = T::kQTile, kQPanel = T::kQPanel, kKTile = T::kKTile,
                      kKPanel = T::kKPanel;
@@ -353,9 +354,8 @@ cudaError_t launch(const CUtensorMap& map_q, const CUtensorMap& map_k, int64_t L
   IndexPrefillArgs a{L,       G,       gpc,  k,   nb,         ns,         sel,
                      sel_score, block_scores, status, wait_ns, kb0, kb1, cand_score,
                      cand_block};
-  index_select_prefill_kernel<kF8><<<nb * (G / gpc), kIndexThreads, smem, stream>>>(map_q, map_k,
-                                                                                   a);
-  return cudaGetLastError();
+  return launch_pdl(index_select_prefill_kernel<kF8>, dim3(nb * (G / gpc)), dim3(kIndexThreads),
+                    smem, stream, map_q, map_k, a);
 }
 
 }  // namespace

@@ -9,6 +9,25 @@
 
 namespace msa {
 
+// Launch with programmatic stream serialization: the kernel may begin while the previous kernel
+// on the stream drains (its CTAs wait in pdl_enter, ptx.cuh, before touching global memory),
+// which hides the launch latency between the back-to-back kernels of a call and between calls.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 // Keys per tile of the prefill index kernel (two blocks): the box height of its key tensor map.
 constexpr int kIndexKeyTile = 256;
 // fp8: index vectors are e4m3 (else bf16); the tensor maps' element type must match.

@@ -23,6 +23,17 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+// Programmatic dependent launch.  The kernels are launched so that a kernel's launch is
+// processed while the previous kernel on the stream still runs (launch_pdl in launch.h); its CTAs
+// are dispatched as the previous grid's CTAs exit.  Every CTA first waits until all prerequisite
+// grids have completed and their memory is visible, so nothing a kernel reads or writes in global
+// memory can race with its predecessors.  No kernel signals its dependents early
+// (griddepcontrol.launch_dependents): waiting CTAs of the next kernel sharing an SM with a running
+// one cost the decode attention 33 us.  Without a programmatic predecessor the wait is a no-op.
+__device__ __forceinline__ void pdl_enter() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // Record the first error of a launch in the caller's status word (sticky: first writer wins).
 __device__ __forceinline__ void report_status(int32_t* status, int32_t code) {
   if (status) atomicCAS(status, 0, code);

@@ -183,48 +183,48 @@ KERNEL_SOURCES = {
 }
 NCU_TRAFFIC = {
     # index kernel: L=1,048,576 hot blocks and L=32,768 (profile_case, second launch)
-    "index": [{"bytes_per_launch": 23000039424, "workload": "prefill_L1M_hot@1048576",
-               "sources_sha256": "bdca6e914cb6ff0dc7fa7af84499fe692bfa4272dc855bff19fa35591b172626"},
-              {"bytes_per_launch": 41904640, "workload": "prefill_L32K@32768",
-               "sources_sha256": "bdca6e914cb6ff0dc7fa7af84499fe692bfa4272dc855bff19fa35591b172626"}],
-    "index_e4m3": [{"bytes_per_launch": 7784805632, "workload": "prefill_L1M_hot@1048576",
-                    "sources_sha256": "bdca6e914cb6ff0dc7fa7af84499fe692bfa4272dc855bff19fa35591b172626"},
-                   {"bytes_per_launch": 20997376, "workload": "prefill_L32K@32768",
-                    "sources_sha256": "bdca6e914cb6ff0dc7fa7af84499fe692bfa4272dc855bff19fa35591b172626"}],
+    "index": [{"bytes_per_launch": 22795514624, "workload": "prefill_L1M_hot@1048576",
+               "sources_sha256": "b28d96647c45d57b7721afcbbb039567f773384b7cd3af90bacf3c24d339f568"},
+              {"bytes_per_launch": 41906688, "workload": "prefill_L32K@32768",
+               "sources_sha256": "b28d96647c45d57b7721afcbbb039567f773384b7cd3af90bacf3c24d339f568"}],
+    "index_e4m3": [{"bytes_per_launch": 7374747136, "workload": "prefill_L1M_hot@1048576",
+                    "sources_sha256": "b28d96647c45d57b7721afcbbb039567f773384b7cd3af90bacf3c24d339f568"},
+                   {"bytes_per_launch": 20997632, "workload": "prefill_L32K@32768",
+                    "sources_sha256": "b28d96647c45d57b7721afcbbb039567f773384b7cd3af90bacf3c24d339f568"}],
     # attention and combine per launch (one query chunk): L=32,768 (its one chunk); L=131,072
     # (second chunk); L=1,048,576 (8th of 16 chunks, a middle one)
-    "attention": [{"bytes_per_launch": 9905228544, "workload": "prefill_L32K@32768",
-                   "sources_sha256": "55d1c77b924afda7453fd25713a809c2454a115dd07a1f391499b611b2f32625"},
-                  {"bytes_per_launch": 20745970176, "workload": "prefill_L128K_clustered@131072",
-                   "sources_sha256": "55d1c77b924afda7453fd25713a809c2454a115dd07a1f391499b611b2f32625"},
-                  {"bytes_per_launch": 33456025088, "workload": "prefill_L1M_hot@1048576",
-                   "sources_sha256": "55d1c77b924afda7453fd25713a809c2454a115dd07a1f391499b611b2f32625"}],
-    "combine": [{"bytes_per_launch": 9192910080, "workload": "prefill_L32K@32768",
-                 "sources_sha256": "55d1c77b924afda7453fd25713a809c2454a115dd07a1f391499b611b2f32625"},
-                {"bytes_per_launch": 18668071936, "workload": "prefill_L128K_clustered@131072",
-                 "sources_sha256": "55d1c77b924afda7453fd25713a809c2454a115dd07a1f391499b611b2f32625"},
-                {"bytes_per_launch": 18934947584, "workload": "prefill_L1M_hot@1048576",
-                 "sources_sha256": "55d1c77b924afda7453fd25713a809c2454a115dd07a1f391499b611b2f32625"}],
+    "attention": [{"bytes_per_launch": 9905374976, "workload": "prefill_L32K@32768",
+                   "sources_sha256": "84ab03f2e25f4dd9d37d61e2b5542f122c47fa1f87940be0e387cd2c896d3008"},
+                  {"bytes_per_launch": 20752672768, "workload": "prefill_L128K_clustered@131072",
+                   "sources_sha256": "84ab03f2e25f4dd9d37d61e2b5542f122c47fa1f87940be0e387cd2c896d3008"},
+                  {"bytes_per_launch": 33455269120, "workload": "prefill_L1M_hot@1048576",
+                   "sources_sha256": "84ab03f2e25f4dd9d37d61e2b5542f122c47fa1f87940be0e387cd2c896d3008"}],
+    "combine": [{"bytes_per_launch": 9193360896, "workload": "prefill_L32K@32768",
+                 "sources_sha256": "84ab03f2e25f4dd9d37d61e2b5542f122c47fa1f87940be0e387cd2c896d3008"},
+                {"bytes_per_launch": 18667236096, "workload": "prefill_L128K_clustered@131072",
+                 "sources_sha256": "84ab03f2e25f4dd9d37d61e2b5542f122c47fa1f87940be0e387cd2c896d3008"},
+                {"bytes_per_launch": 18936193792, "workload": "prefill_L1M_hot@1048576",
+                 "sources_sha256": "84ab03f2e25f4dd9d37d61e2b5542f122c47fa1f87940be0e387cd2c896d3008"}],
     # decode, 64 sequences of 16K-256K tokens
-    "decode_scan": [{"bytes_per_launch": 2088344832, "workload": "decode_b64_16K_256K@64x262144",
-                     "sources_sha256": "4fa089e411d05e1478e45e648c8a0f4df982c50a01db26b715de010610f4a19f"}],
-    "decode_scan_e4m3": [{"bytes_per_launch": 1047283712, "workload": "decode_b64_16K_256K@64x262144",
-                          "sources_sha256": "4fa089e411d05e1478e45e648c8a0f4df982c50a01db26b715de010610f4a19f"}],
+    "decode_scan": [{"bytes_per_launch": 2088251904, "workload": "decode_b64_16K_256K@64x262144",
+                     "sources_sha256": "411af29b796fe96db34caf8db506ac6dfb453f42c5b252cd5e0f7a3f05400475"}],
+    "decode_scan_e4m3": [{"bytes_per_launch": 1047264256, "workload": "decode_b64_16K_256K@64x262144",
+                          "sources_sha256": "411af29b796fe96db34caf8db506ac6dfb453f42c5b252cd5e0f7a3f05400475"}],
 }
 # Tensor-pipe activity from the same captures (sm__pipe_tensor_cycles_active, % of elapsed
 # cycles: a fraction of the part's nominal tensor rate at the clock of the moment).
 NCU_TENSOR_PIPE = {
-    "index": [{"pct": 69.23, "workload": "prefill_L1M_hot@1048576",
-               "sources_sha256": "bdca6e914cb6ff0dc7fa7af84499fe692bfa4272dc855bff19fa35591b172626"},
-              {"pct": 57.11, "workload": "prefill_L32K@32768",
-               "sources_sha256": "bdca6e914cb6ff0dc7fa7af84499fe692bfa4272dc855bff19fa35591b172626"}],
-    "index_e4m3": [{"pct": 45.18, "workload": "prefill_L1M_hot@1048576",
-                    "sources_sha256": "bdca6e914cb6ff0dc7fa7af84499fe692bfa4272dc855bff19fa35591b172626"},
+    "index": [{"pct": 69.09, "workload": "prefill_L1M_hot@1048576",
+               "sources_sha256": "b28d96647c45d57b7721afcbbb039567f773384b7cd3af90bacf3c24d339f568"},
+              {"pct": 57.01, "workload": "prefill_L32K@32768",
+               "sources_sha256": "b28d96647c45d57b7721afcbbb039567f773384b7cd3af90bacf3c24d339f568"}],
+    "index_e4m3": [{"pct": 45.31, "workload": "prefill_L1M_hot@1048576",
+                    "sources_sha256": "b28d96647c45d57b7721afcbbb039567f773384b7cd3af90bacf3c24d339f568"},
                    {"pct": 32.22, "workload": "prefill_L32K@32768",
-                    "sources_sha256": "bdca6e914cb6ff0dc7fa7af84499fe692bfa4272dc855bff19fa35591b172626"}],
+                    "sources_sha256": "b28d96647c45d57b7721afcbbb039567f773384b7cd3af90bacf3c24d339f568"}],
     # attention: ncu --set full at L=8,192 (the 32K kernel at a capture-sized length)
-    "attention": [{"pct": 42.22, "workload": "prefill_L32K@8192",
-                   "sources_sha256": "55d1c77b924afda7453fd25713a809c2454a115dd07a1f391499b611b2f32625"}],
+    "attention": [{"pct": 42.12, "workload": "prefill_L32K@8192",
+                   "sources_sha256": "84ab03f2e25f4dd9d37d61e2b5542f122c47fa1f87940be0e387cd2c896d3008"}],
 }
 
 

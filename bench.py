@@ -183,14 +183,14 @@ KERNEL_SOURCES = {
 }
 NCU_TRAFFIC = {
     # index kernel: L=1,048,576 hot blocks and L=32,768 (profile_case, second launch)
-    "index": [{"bytes_per_launch": 22795514624, "workload": "prefill_L1M_hot@1048576",
-               "sources_sha256": "b28d96647c45d57b7721afcbbb039567f773384b7cd3af90bacf3c24d339f568"},
-              {"bytes_per_launch": 41906688, "workload": "prefill_L32K@32768",
-               "sources_sha256": "b28d96647c45d57b7721afcbbb039567f773384b7cd3af90bacf3c24d339f568"}],
-    "index_e4m3": [{"bytes_per_launch": 7374747136, "workload": "prefill_L1M_hot@1048576",
-                    "sources_sha256": "b28d96647c45d57b7721afcbbb039567f773384b7cd3af90bacf3c24d339f568"},
-                   {"bytes_per_launch": 20997632, "workload": "prefill_L32K@32768",
-                    "sources_sha256": "b28d96647c45d57b7721afcbbb039567f773384b7cd3af90bacf3c24d339f568"}],
+    "index": [{"bytes_per_launch": 19651720704, "workload": "prefill_L1M_hot@1048576",
+               "sources_sha256": "37fa83146405eb38b128c6634872835c4bf94e255327951c2cb9722643be3d7f"},
+              {"bytes_per_launch": 41905920, "workload": "prefill_L32K@32768",
+               "sources_sha256": "37fa83146405eb38b128c6634872835c4bf94e255327951c2cb9722643be3d7f"}],
+    "index_e4m3": [{"bytes_per_launch": 6326164224, "workload": "prefill_L1M_hot@1048576",
+                    "sources_sha256": "37fa83146405eb38b128c6634872835c4bf94e255327951c2cb9722643be3d7f"},
+                   {"bytes_per_launch": 21001216, "workload": "prefill_L32K@32768",
+                    "sources_sha256": "37fa83146405eb38b128c6634872835c4bf94e255327951c2cb9722643be3d7f"}],
     # attention and combine per launch (one query chunk): L=32,768 (its one chunk); L=131,072
     # (second chunk); L=1,048,576 (8th of 16 chunks, a middle one)
     "attention": [{"bytes_per_launch": 9905374976, "workload": "prefill_L32K@32768",
@@ -214,14 +214,14 @@ NCU_TRAFFIC = {
 # Tensor-pipe activity from the same captures (sm__pipe_tensor_cycles_active, % of elapsed
 # cycles: a fraction of the part's nominal tensor rate at the clock of the moment).
 NCU_TENSOR_PIPE = {
-    "index": [{"pct": 69.09, "workload": "prefill_L1M_hot@1048576",
-               "sources_sha256": "b28d96647c45d57b7721afcbbb039567f773384b7cd3af90bacf3c24d339f568"},
-              {"pct": 57.01, "workload": "prefill_L32K@32768",
-               "sources_sha256": "b28d96647c45d57b7721afcbbb039567f773384b7cd3af90bacf3c24d339f568"}],
-    "index_e4m3": [{"pct": 45.31, "workload": "prefill_L1M_hot@1048576",
-                    "sources_sha256": "b28d96647c45d57b7721afcbbb039567f773384b7cd3af90bacf3c24d339f568"},
-                   {"pct": 32.22, "workload": "prefill_L32K@32768",
-                    "sources_sha256": "b28d96647c45d57b7721afcbbb039567f773384b7cd3af90bacf3c24d339f568"}],
+    "index": [{"pct": 71.59, "workload": "prefill_L1M_hot@1048576",
+               "sources_sha256": "37fa83146405eb38b128c6634872835c4bf94e255327951c2cb9722643be3d7f"},
+              {"pct": 58.15, "workload": "prefill_L32K@32768",
+               "sources_sha256": "37fa83146405eb38b128c6634872835c4bf94e255327951c2cb9722643be3d7f"}],
+    "index_e4m3": [{"pct": 46.5, "workload": "prefill_L1M_hot@1048576",
+                    "sources_sha256": "37fa83146405eb38b128c6634872835c4bf94e255327951c2cb9722643be3d7f"},
+                   {"pct": 31.96, "workload": "prefill_L32K@32768",
+                    "sources_sha256": "37fa83146405eb38b128c6634872835c4bf94e255327951c2cb9722643be3d7f"}],
     # attention: ncu --set full at L=8,192 (the 32K kernel at a capture-sized length)
     "attention": [{"pct": 42.12, "workload": "prefill_L32K@8192",
                    "sources_sha256": "84ab03f2e25f4dd9d37d61e2b5542f122c47fa1f87940be0e387cd2c896d3008"}],

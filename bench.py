@@ -184,56 +184,84 @@ KERNEL_SOURCES = {
 NCU_TRAFFIC = {
     # index kernel: L=1,048,576 hot blocks and L=32,768 (profile_case, second launch)
     "index": [{"bytes_per_launch": 19651720704, "workload": "prefill_L1M_hot@1048576",
-               "sources_sha256": "37fa83146405eb38b128c6634872835c4bf94e255327951c2cb9722643be3d7f"},
+               "sources_sha256": "d543ec92396d5af3486dfe63ef914722bf2b38e8e2b854aa29aaafaf2933c155"},
               {"bytes_per_launch": 41905920, "workload": "prefill_L32K@32768",
-               "sources_sha256": "37fa83146405eb38b128c6634872835c4bf94e255327951c2cb9722643be3d7f"}],
+               "sources_sha256": "d543ec92396d5af3486dfe63ef914722bf2b38e8e2b854aa29aaafaf2933c155"}],
     "index_e4m3": [{"bytes_per_launch": 6326164224, "workload": "prefill_L1M_hot@1048576",
-                    "sources_sha256": "37fa83146405eb38b128c6634872835c4bf94e255327951c2cb9722643be3d7f"},
+                    "sources_sha256": "d543ec92396d5af3486dfe63ef914722bf2b38e8e2b854aa29aaafaf2933c155"},
                    {"bytes_per_launch": 21001216, "workload": "prefill_L32K@32768",
-                    "sources_sha256": "37fa83146405eb38b128c6634872835c4bf94e255327951c2cb9722643be3d7f"}],
+                    "sources_sha256": "d543ec92396d5af3486dfe63ef914722bf2b38e8e2b854aa29aaafaf2933c155"}],
     # attention and combine per launch (one query chunk): L=32,768 (its one chunk); L=131,072
     # (second chunk); L=1,048,576 (8th of 16 chunks, a middle one)
     "attention": [{"bytes_per_launch": 9905374976, "workload": "prefill_L32K@32768",
-                   "sources_sha256": "84ab03f2e25f4dd9d37d61e2b5542f122c47fa1f87940be0e387cd2c896d3008"},
+                   "sources_sha256": "91d4a0294468ac4a7479d9901505ceeb2e709ad276433f41e0b9e4dac012cbdb"},
                   {"bytes_per_launch": 20752672768, "workload": "prefill_L128K_clustered@131072",
-                   "sources_sha256": "84ab03f2e25f4dd9d37d61e2b5542f122c47fa1f87940be0e387cd2c896d3008"},
+                   "sources_sha256": "91d4a0294468ac4a7479d9901505ceeb2e709ad276433f41e0b9e4dac012cbdb"},
                   {"bytes_per_launch": 33455269120, "workload": "prefill_L1M_hot@1048576",
-                   "sources_sha256": "84ab03f2e25f4dd9d37d61e2b5542f122c47fa1f87940be0e387cd2c896d3008"}],
+                   "sources_sha256": "91d4a0294468ac4a7479d9901505ceeb2e709ad276433f41e0b9e4dac012cbdb"}],
     "combine": [{"bytes_per_launch": 9193360896, "workload": "prefill_L32K@32768",
-                 "sources_sha256": "84ab03f2e25f4dd9d37d61e2b5542f122c47fa1f87940be0e387cd2c896d3008"},
+                 "sources_sha256": "91d4a0294468ac4a7479d9901505ceeb2e709ad276433f41e0b9e4dac012cbdb"},
                 {"bytes_per_launch": 18667236096, "workload": "prefill_L128K_clustered@131072",
-                 "sources_sha256": "84ab03f2e25f4dd9d37d61e2b5542f122c47fa1f87940be0e387cd2c896d3008"},
+                 "sources_sha256": "91d4a0294468ac4a7479d9901505ceeb2e709ad276433f41e0b9e4dac012cbdb"},
                 {"bytes_per_launch": 18936193792, "workload": "prefill_L1M_hot@1048576",
-                 "sources_sha256": "84ab03f2e25f4dd9d37d61e2b5542f122c47fa1f87940be0e387cd2c896d3008"}],
+                 "sources_sha256": "91d4a0294468ac4a7479d9901505ceeb2e709ad276433f41e0b9e4dac012cbdb"}],
     # decode, 64 sequences of 16K-256K tokens
     "decode_scan": [{"bytes_per_launch": 2088251904, "workload": "decode_b64_16K_256K@64x262144",
-                     "sources_sha256": "411af29b796fe96db34caf8db506ac6dfb453f42c5b252cd5e0f7a3f05400475"}],
+                     "sources_sha256": "6812ee3a8e0a2bd0b910288aa039843c7817de62d0791d770e2e8a15f71de36f"}],
     "decode_scan_e4m3": [{"bytes_per_launch": 1047264256, "workload": "decode_b64_16K_256K@64x262144",
-                          "sources_sha256": "411af29b796fe96db34caf8db506ac6dfb453f42c5b252cd5e0f7a3f05400475"}],
+                          "sources_sha256": "6812ee3a8e0a2bd0b910288aa039843c7817de62d0791d770e2e8a15f71de36f"}],
 }
 # Tensor-pipe activity from the same captures (sm__pipe_tensor_cycles_active, % of elapsed
 # cycles: a fraction of the part's nominal tensor rate at the clock of the moment).
 NCU_TENSOR_PIPE = {
     "index": [{"pct": 71.59, "workload": "prefill_L1M_hot@1048576",
-               "sources_sha256": "37fa83146405eb38b128c6634872835c4bf94e255327951c2cb9722643be3d7f"},
+               "sources_sha256": "d543ec92396d5af3486dfe63ef914722bf2b38e8e2b854aa29aaafaf2933c155"},
               {"pct": 58.15, "workload": "prefill_L32K@32768",
-               "sources_sha256": "37fa83146405eb38b128c6634872835c4bf94e255327951c2cb9722643be3d7f"}],
+               "sources_sha256": "d543ec92396d5af3486dfe63ef914722bf2b38e8e2b854aa29aaafaf2933c155"}],
     "index_e4m3": [{"pct": 46.5, "workload": "prefill_L1M_hot@1048576",
-                    "sources_sha256": "37fa83146405eb38b128c6634872835c4bf94e255327951c2cb9722643be3d7f"},
+                    "sources_sha256": "d543ec92396d5af3486dfe63ef914722bf2b38e8e2b854aa29aaafaf2933c155"},
                    {"pct": 31.96, "workload": "prefill_L32K@32768",
-                    "sources_sha256": "37fa83146405eb38b128c6634872835c4bf94e255327951c2cb9722643be3d7f"}],
+                    "sources_sha256": "d543ec92396d5af3486dfe63ef914722bf2b38e8e2b854aa29aaafaf2933c155"}],
     # attention: ncu --set full at L=8,192 (the 32K kernel at a capture-sized length)
     "attention": [{"pct": 42.12, "workload": "prefill_L32K@8192",
-                   "sources_sha256": "84ab03f2e25f4dd9d37d61e2b5542f122c47fa1f87940be0e387cd2c896d3008"}],
+                   "sources_sha256": "91d4a0294468ac4a7479d9901505ceeb2e709ad276433f41e0b9e4dac012cbdb"}],
 }
 
 
+def code_text(src: str) -> str:
+    """The code of a C++/CUDA source without its comments and blank space, so that a change to
+    the comments alone does not count as a change of the kernel.  String and character literals
+    are kept whole (a // inside one is not a comment)."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    lines = (" ".join(line.split()) for line in "".join(out).split("\n"))
+    return "\n".join(line for line in lines if line)
+
+
 def sources_sha256(kernel: str) -> str:
+    """Hash of the code (comments left out) of the sources a kernel is built from."""
     import hashlib
     h = hashlib.sha256()
     for f in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(CSRC, f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(CSRC, f), encoding="utf-8") as fh:
+            h.update(code_text(fh.read()).encode())
     return h.hexdigest()
 
 

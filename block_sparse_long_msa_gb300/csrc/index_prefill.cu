@@ -8,18 +8,18 @@
 // One CTA owns one query block qb (128 queries) for gpc groups (two when G is even, else one).
 // The gpc index-query tiles stay in shared memory; the keys of blocks 0..qb-1 stream through a
 // TMA ring in tiles of 256 keys (two blocks), so every MMA is M=128 x N=256 (x K=16 in bf16,
-// K=32 in e4m3): the tensor core runs an N=256 step in about the time of an N=128 one.  Score tiles go to two 256-column
-// TMEM accumulators; work unit u = (key tile u / gpc, group u % gpc) takes slot u & 1, so with
-// two groups each slot belongs to one group and each group's MMAs overlap the other group's
-// epilogue.  Roles:
+// K=32 in e4m3): the tensor core runs an N=256 step in about the time of an N=128 one.  Score
+// tiles go to two 256-column TMEM accumulators; work unit u = (key tile u / gpc, group u % gpc)
+// takes slot u & 1, so with two groups each slot belongs to one group and each group's MMAs
+// overlap the other group's epilogue.  Roles:
 //   warps 0..7  two epilogue warpgroups; warpgroup e drains slot e: thread r owns query row r and
 //               takes the two block maxima of its 256 scores straight from the TMEM loads
 //               (tcgen05.ld.red), then keeps a register top-15
 //   warp 8      TMA producer (index-query tiles once, then key tiles)
-//   warp 9      TMEM owner + single-thread tcgen05.mma issuer
-// A slot is MMA'd, then drained, then MMA'd again, so the drain (four waves of two 32-column TMEM
-// loads, each wave bound by the load latency) is on the critical path once the MMA runs at the
-// fp8 rate.
+//   warp 9      TMEM owner + single-thread tcgen05.mma issuer, which polls its barriers
+// A slot is MMA'd, then drained, then MMA'd again, so each slot's round trip (MMAs done, commit,
+// drain, release, the next MMAs issued) must hide behind the other slot's MMAs; at the fp8 rate
+// four MMA steps do not cover it.
 // With one group per CTA the two warpgroups see alternate key tiles and merge their lists at the
 // end; the full (score desc, block asc) comparison of the list keeps the tie rule.
 #include "common.cuh"

@@ -96,6 +96,25 @@ def test_host_argument_checks(lib):
     assert lib.msa_index_select_workspace(ctypes.byref(bad), 1, 1, None) == 0
 
 
+def test_prefill_length_limit_is_checked_on_the_host(lib):
+    """The main branch supports L up to 1,572,864 tokens (the schedule keeps a 16-byte token mask
+    per key block in shared memory); one token more is refused before any GPU work, with
+    aligned stand-in pointers that are never dereferenced."""
+    import block_sparse_long_msa_gb300 as msa
+    cfg = msa.config(4, 16, 16)
+    L_MAX = 1572864
+    P = [ctypes.c_void_p(0x10000 * (i + 1)) for i in range(8)]
+
+    def call(L):
+        return lib.msa_attn_prefill(ctypes.byref(cfg), P[0], P[1], P[2], L, P[3], P[4], P[5],
+                                    P[6], 1 << 62, None)
+
+    assert call(L_MAX + 1) == msa.MSA_ERR_UNSUPPORTED
+    assert msa.msa_attn_prefill_launches(cfg, L_MAX) == 24 * 7  # 24 passes of 65,536 queries
+    assert msa.msa_attn_prefill_launches(cfg, L_MAX + 1) == 0
+    assert msa.msa_attn_prefill_workspace(cfg, L_MAX) > 0
+
+
 def test_launch_count_and_index_dtype_config(lib):
     """The prefill launch count is host arithmetic (seven kernels per 65,536-token chunk); an
     index_dtype other than bf16 (0) or e4m3 (1) is an invalid config."""

@@ -13,7 +13,7 @@ import synthetic
 
 pytestmark = pytest.mark.gpu
 
-MAX_ABS, MEAN_ABS = 1e-2, 1e-3
+from parity_bar import MAX_ABS, MEAN_ABS, o_bar
 
 
 @pytest.fixture(scope="module")
@@ -47,7 +47,7 @@ def compare(w, inp, sel, o, lse, rows=None):
     lerr = np.abs(lse - r_lse)
     msg = (f"O max {err.max():.3g} mean {err.mean():.3g}; LSE max {lerr.max():.3g} "
            f"mean {lerr.mean():.3g}")
-    assert err.max() <= MAX_ABS and err.mean() <= MEAN_ABS, msg
+    assert (err <= o_bar(r_o)).all() and err.mean() <= MEAN_ABS, msg
     assert lerr.max() <= MAX_ABS and lerr.mean() <= MEAN_ABS, msg
     assert np.isfinite(o).all() and np.isfinite(lse).all()
     print(f"[parity {w.name} L={w.L}] {msg}")
@@ -92,7 +92,7 @@ def test_full_budget_matches_sdpa_on_gpu(msa):
     ref = F.scaled_dot_product_attention(Q, K, V, is_causal=True, scale=w.scale,
                                          enable_gqa=True)[0].permute(1, 0, 2).cpu().numpy()
     err = np.abs(o - ref)
-    assert err.max() <= MAX_ABS and err.mean() <= MEAN_ABS, (err.max(), err.mean())
+    assert (err <= o_bar(ref)).all() and err.mean() <= MEAN_ABS, (err.max(), err.mean())
 
 
 def test_full_size_32k_sampled_rows(msa):
@@ -143,7 +143,42 @@ def test_full_size_1m_hot_sampled_rows(msa):
     err, lerr = np.abs(g_o - r_o), np.abs(g_lse - r_lse)
     msg = (f"O max {err.max():.3g} mean {err.mean():.3g}; LSE max {lerr.max():.3g} "
            f"mean {lerr.mean():.3g}; hot fraction {hot:.3f}")
-    assert err.max() <= MAX_ABS and err.mean() <= MEAN_ABS, msg
+    assert (err <= o_bar(r_o)).all() and err.mean() <= MEAN_ABS, msg
+    assert lerr.max() <= MAX_ABS and lerr.mean() <= MEAN_ABS, msg
+    print(f"[parity {w.name} L={w.L}] {msg}")
+
+
+def test_maximum_length_sampled_rows(msa):
+    """L = 1,572,864, the longest prefill the library takes: 24 query passes, and the schedule's
+    token mask of 12,288 key blocks fills 192 KiB of shared memory.  The hot-block key bias of the
+    1M workload; the selection and the main branch on sampled rows against the oracle, the last
+    rows included."""
+    w = synthetic.Workload(**{**synthetic.WORKLOADS["prefill_L1M_hot"].__dict__, "L": 1572864,
+                              "name": "prefill_Lmax_hot", "seed": 1571})
+    inp = synthetic.prefill_inputs(w, device="cuda")
+    cfg = msa.config(w.G, w.hpg, w.k, w.scale)
+    assert msa.msa_attn_prefill_launches(cfg, w.L) == 24 * 7
+    sel = msa.msa_index_select(cfg, inp["q_idx"], inp["k_idx"])
+    ws = torch.zeros(msa.msa_attn_prefill_workspace(cfg, w.L), dtype=torch.uint8, device="cuda")
+    o, lse = msa.msa_attn_prefill(cfg, inp["q"], inp["k"], inp["v"], sel, ws=ws)
+    torch.cuda.synchronize()
+    assert msa.msa_get_device_status(ws) == 0
+    rows = _rows(w.L, 20, 8)
+    ridx = torch.tensor(rows, device="cuda")
+    g_sel = sel[:, ridx].cpu().numpy()
+    g_o = o[ridx].float().cpu().numpy()
+    g_lse = lse[:, ridx].cpu().numpy()
+    del o, lse, ws
+    r_sel = oracle.select_prefill(inp["q_idx"].cpu(), inp["k_idx"].cpu(), w.B, w.k, rows=rows)
+    np.testing.assert_array_equal(g_sel, r_sel)
+    r_o, r_lse = oracle.attn_prefill(inp["q"][ridx].cpu(), inp["k"].cpu(), inp["v"].cpu(), r_sel,
+                                     w.B, w.k, w.scale, rows=rows, q_compact=True)
+    err, lerr = np.abs(g_o - r_o), np.abs(g_lse - r_lse)
+    wide = np.abs(r_o) >= 4.0  # bf16 spacing 1/32 there: the output must round faithfully
+    msg = (f"O max {err.max():.3g} (below |o| = 4: {err[~wide].max():.3g}; {int(wide.sum())} "
+           f"elements at |o| >= 4) mean {err.mean():.3g}; LSE max {lerr.max():.3g} "
+           f"mean {lerr.mean():.3g}")
+    assert (err <= o_bar(r_o)).all() and err.mean() <= MEAN_ABS, msg
     assert lerr.max() <= MAX_ABS and lerr.mean() <= MEAN_ABS, msg
     print(f"[parity {w.name} L={w.L}] {msg}")
 

@@ -150,8 +150,9 @@ def test_decode_equals_last_prefill_row(msa):
     o_d, lse_d = msa.msa_attn_decode(cfg, inp["q"][n - 1:n].contiguous(), paged, sel_d)
     torch.cuda.synchronize()
     assert torch.equal(sel_d[:, 0], sel_p[:, n - 1])
-    err = (o_d[0].float() - o_p[n - 1].float()).abs()
-    assert err.max().item() <= MAX_ABS
+    ref = o_p[n - 1].float().cpu().numpy()
+    err = np.abs(o_d[0].float().cpu().numpy() - ref)
+    assert (err <= o_bar(ref)).all(), err.max()  # two bf16 roundings of nearly the same value
     assert (lse_d[:, 0] - lse_p[:, n - 1]).abs().max().item() <= 1e-4
 
 

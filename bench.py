@@ -206,10 +206,10 @@ NCU_TRAFFIC = {
                 {"bytes_per_launch": 18936193792, "workload": "prefill_L1M_hot@1048576",
                  "sources_sha256": "91d4a0294468ac4a7479d9901505ceeb2e709ad276433f41e0b9e4dac012cbdb"}],
     # decode, 64 sequences of 16K-256K tokens
-    "decode_scan": [{"bytes_per_launch": 2088251904, "workload": "decode_b64_16K_256K@64x262144",
-                     "sources_sha256": "6812ee3a8e0a2bd0b910288aa039843c7817de62d0791d770e2e8a15f71de36f"}],
-    "decode_scan_e4m3": [{"bytes_per_launch": 1047264256, "workload": "decode_b64_16K_256K@64x262144",
-                          "sources_sha256": "6812ee3a8e0a2bd0b910288aa039843c7817de62d0791d770e2e8a15f71de36f"}],
+    "decode_scan": [{"bytes_per_launch": 2087903488, "workload": "decode_b64_16K_256K@64x262144",
+                     "sources_sha256": "7f1a8671298ab06678201ffad395c79bb54caa2e99123835f0c9af03751614d5"}],
+    "decode_scan_e4m3": [{"bytes_per_launch": 1047261696, "workload": "decode_b64_16K_256K@64x262144",
+                          "sources_sha256": "7f1a8671298ab06678201ffad395c79bb54caa2e99123835f0c9af03751614d5"}],
 }
 # Tensor-pipe activity from the same captures (sm__pipe_tensor_cycles_active, % of elapsed
 # cycles: a fraction of the part's nominal tensor rate at the clock of the moment).

@@ -514,7 +514,8 @@ __global__ void __launch_bounds__(128) decode_topk_kernel(TopkArgs a) {
 // ------------------------------------------------------------------------------------------
 // Decode attention: one unit per (sequence, group, slot).  A persistent CTA takes a contiguous
 // range of units; warp 0 stages each unit's K and V page tiles (TMA, 128-byte swizzle).  The
-// staged units alternate between two groups of four compute warps (warps 1-4, 5-8); in a group
+// staged units go in turn to groups of four compute warps (warps 1-4, 5-8, 9-12: three groups
+// with bf16 pages, two with e4m3 pages; DecLayout::kGroups); in a group
 // each warp scores 32 keys (S = q K^T with m16n8k16 MMAs, M = the group's 16 heads), the four
 // exchange row maxima, sums and their slice of P through shared memory, and then each computes
 // O = P V for 32 of the 128 output dimensions over all the page's keys, written straight to the
@@ -542,27 +543,27 @@ struct DecAttnArgs {
 };
 
 // Shared-memory layout of the decode attention kernel, by K/V storage type.
-// Two groups of four compute warps take alternate staged units, so every SM sub-partition has
-// two warps to interleave.
-constexpr int kDecGroups = 2;
-constexpr int kDecThreads = 32 + kDecGroups * 128;
-
+// kGroups groups of four compute warps take the staged units in turn, so every SM sub-partition
+// has kGroups warps to interleave: three with bf16 pages, two with e4m3 pages (whose warps need
+// 168 registers, so a third group would not fit the register file).
 template <bool kKV8>
 struct DecLayout {
+  static constexpr int kGroups = kKV8 ? 2 : 3;
+  static constexpr int kThreads = 32 + kGroups * 128;
   static constexpr int kStages = kKV8 ? 4 : 3;
   static constexpr uint32_t kTile = kKV8 ? 16384 : 32768;  // one K or V page tile
   static constexpr uint32_t kStage = 2 * kTile;
   // e4m3: per compute warp, V of its 32 dimensions in fp16 (128 rows x 64 B)
   static constexpr uint32_t kPriv = kStages * kStage;
   static constexpr uint32_t kPrivWarp = 8192;
-  static constexpr uint32_t kP = kPriv + (kKV8 ? 4 * kDecGroups * kPrivWarp : 0);
+  static constexpr uint32_t kP = kPriv + (kKV8 ? 4 * kGroups * kPrivWarp : 0);
   // Per unit the four warps of a group exchange their row maxima and row sums and the P tile (16
   // rows x 128 keys, 128-byte swizzled panels); two copies per group, by the parity of the
   // group's units, so a warp may start the next unit while another still reads this one's.
   static constexpr uint32_t kPBytes = kHeads * kBlock * 2;
-  static constexpr uint32_t kML = kP + kDecGroups * 2 * kPBytes;
+  static constexpr uint32_t kML = kP + kGroups * 2 * kPBytes;
   static constexpr uint32_t kMLGroup = 2 * 2 * 4 * kHeads * 4;  // 2 x (max, sum) x 4 warps x 16
-  static constexpr uint32_t kBar = kML + kDecGroups * kMLGroup;
+  static constexpr uint32_t kBar = kML + kGroups * kMLGroup;
   static constexpr uint32_t kSmem = kBar + 128 + 1024;
 };
 constexpr int kDecMaxStages = 4;
@@ -616,7 +617,7 @@ __device__ __forceinline__ uint32_t vpriv_addr(uint32_t buf, int r, int c) {
 }
 
 template <bool kKV8>
-__global__ void __launch_bounds__(kDecThreads, 1)
+__global__ void __launch_bounds__(DecLayout<kKV8>::kThreads, 1)
     decode_attn_kernel(const __grid_constant__ CUtensorMap map_kp,
                        const __grid_constant__ CUtensorMap map_vp, DecAttnArgs a) {
   pdl_enter();  // before any global memory access (launch_pdl)
@@ -696,7 +697,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         a.plse[static_cast<size_t>(u) * kHeads + lane] = ninf;
       continue;
     }
-    if ((++p & 1) != gr) continue;  // the other group's unit
+    if (++p % Lay::kGroups != gr) continue;  // another group's unit
     const int sg = x.s * a.G + x.g;
     if (sg != cur_sg) {  // query fragments of this (sequence, group), straight from global
       const uint32_t* q32 = reinterpret_cast<const uint32_t*>(a.q + static_cast<size_t>(sg) *
@@ -723,10 +724,11 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       cur_sg = sg;
     }
     const int st = p % kDecStages;
-    // The stage's previous unit (p - kDecStages) belongs to the other group: wait until it has
-    // been released, as the producer does before refilling it, so that the full barrier is at
-    // most one phase ahead of this wait (a group skips every other unit, and a parity test on a
-    // barrier two phases behind would pass on the stale phase).
+    // The stage's previous unit (p - kDecStages) may belong to another group (two groups, three
+    // or four stages): wait until it has been released, as the producer does before refilling
+    // it, so that the full barrier is at most one phase ahead of this wait (a group skips the
+    // other groups' units, and a parity test on a barrier two phases behind would pass on the
+    // stale phase).  With three groups and three stages it is this group's own previous unit.
     bool ok = !*abort_flag &&
               (p < kDecStages ||
                mbar_wait(empty(st), ((p / kDecStages) & 1) ^ 1, a.wait_ns)) &&
@@ -750,7 +752,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       }
       __syncwarp();
     }
-    const int par = (p >> 1) & 1;                          // parity of the group's units
+    const int par = (p / Lay::kGroups) & 1;                // parity of the group's units
     const uint32_t pt = base + Lay::kP + (gr * 2 + par) * Lay::kPBytes;  // this unit's P tile
     float* mx = mlx + gr * (Lay::kMLGroup / 4) + par * (2 * 4 * kHeads);  // [4 warps][16] maxima
     float* ls = mx + 4 * kHeads;                                          // [4 warps][16] sums
@@ -1036,8 +1038,8 @@ cudaError_t launch_decode_attn(const CUtensorMap& map_kp, const CUtensorMap& map
                                   cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) !=
         cudaSuccess)
       return e;
-    if ((e = launch_pdl(decode_attn_kernel<true>, dim3(grid), dim3(kDecThreads), smem, stream,
-                        map_kp, map_vp, a)) != cudaSuccess)
+    if ((e = launch_pdl(decode_attn_kernel<true>, dim3(grid), dim3(DecLayout<true>::kThreads),
+                        smem, stream, map_kp, map_vp, a)) != cudaSuccess)
       return e;
   } else {
     constexpr uint32_t smem = DecLayout<false>::kSmem;
@@ -1045,8 +1047,8 @@ cudaError_t launch_decode_attn(const CUtensorMap& map_kp, const CUtensorMap& map
                                   cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) !=
         cudaSuccess)
       return e;
-    if ((e = launch_pdl(decode_attn_kernel<false>, dim3(grid), dim3(kDecThreads), smem, stream,
-                        map_kp, map_vp, a)) != cudaSuccess)
+    if ((e = launch_pdl(decode_attn_kernel<false>, dim3(grid), dim3(DecLayout<false>::kThreads),
+                        smem, stream, map_kp, map_vp, a)) != cudaSuccess)
       return e;
   }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;

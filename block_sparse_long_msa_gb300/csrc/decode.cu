@@ -36,7 +36,7 @@ struct ScanTiles {
   static constexpr uint32_t kStage = kKeys + kQRows;
   static constexpr int kPanels = kF8 ? 1 : 2;
   static constexpr int kSteps = kF8 ? 4 : 8;
-  static constexpr int kStages = kF8 ? 6 : 3;                  // 108 KB per CTA, two per SM
+  static constexpr int kStages = kF8 ? 4 : 3;  // 72 KiB (e4m3) or 108 KiB (bf16) per CTA
   static constexpr uint32_t kIdesc = kF8 ? idesc_e4m3_f32(128, 16)
                                          : idesc_bf16_f32(128, 16, false, false);
 };
@@ -61,12 +61,14 @@ static_assert(ScanTiles<false>::kStages <= kScanMaxStages && scan_smem<false>() 
               "scan shared memory");
 static_assert(ScanTiles<true>::kStages <= kScanMaxStages && scan_smem<true>() <= 232448,
               "scan shared memory");
-// two scan CTAs share an SM (233,472 bytes of shared memory, 1 KB of it reserved per CTA), so
-// each SM runs two independent page pipelines
-constexpr int kScanCtasPerSm = 2;
-static_assert(kScanCtasPerSm * (scan_smem<false>() + 1024) <= 233472 &&
-                  kScanCtasPerSm * (scan_smem<true>() + 1024) <= 233472,
-              "two scan CTAs per SM");
+// Several scan CTAs share an SM (233,472 bytes of shared memory, 1 KB of it reserved per CTA), so
+// each SM runs independent page pipelines: two with bf16 pages, three with the half-size e4m3
+// pages (at 56 registers a thread, the register file's share of three CTAs).
+template <bool kF8>
+constexpr int scan_ctas_per_sm() { return kF8 ? 3 : 2; }
+static_assert(scan_ctas_per_sm<false>() * (scan_smem<false>() + 1024) <= 233472 &&
+                  scan_ctas_per_sm<true>() * (scan_smem<true>() + 1024) <= 233472,
+              "scan CTAs per SM");
 
 struct ScanArgs {
   const int32_t* page_table;
@@ -167,7 +169,7 @@ __device__ __forceinline__ float warp_max_f32(float v) {
 constexpr int kScanThreads = 384;
 
 template <bool kF8>
-__global__ void __launch_bounds__(kScanThreads, kScanCtasPerSm)
+__global__ void __launch_bounds__(kScanThreads, scan_ctas_per_sm<kF8>())
     decode_scan_kernel(const __grid_constant__ CUtensorMap map_k,
                        const __grid_constant__ CUtensorMap map_q, ScanArgs a) {
   pdl_enter();  // before any global memory access (launch_pdl)
@@ -963,7 +965,9 @@ cudaError_t launch_decode_select(const CUtensorMap& map_k, const CUtensorMap& ma
   a.status = status;
   a.wait_ns = wait_ns;
   const int grid = static_cast<int>(
-      std::max<int64_t>(1, std::min<int64_t>(static_cast<int64_t>(kScanCtasPerSm) * num_sms,
+      std::max<int64_t>(1, std::min<int64_t>(static_cast<int64_t>(fp8 ? scan_ctas_per_sm<true>()
+                                                                     : scan_ctas_per_sm<false>()) *
+                                                 num_sms,
                                              static_cast<int64_t>(batch) * max_pages)));
   cudaError_t e;
   if (fp8) {

@@ -206,10 +206,10 @@ NCU_TRAFFIC = {
                 {"bytes_per_launch": 18936193792, "workload": "prefill_L1M_hot@1048576",
                  "sources_sha256": "91d4a0294468ac4a7479d9901505ceeb2e709ad276433f41e0b9e4dac012cbdb"}],
     # decode, 64 sequences of 16K-256K tokens
-    "decode_scan": [{"bytes_per_launch": 2087903488, "workload": "decode_b64_16K_256K@64x262144",
-                     "sources_sha256": "7f1a8671298ab06678201ffad395c79bb54caa2e99123835f0c9af03751614d5"}],
-    "decode_scan_e4m3": [{"bytes_per_launch": 1047261696, "workload": "decode_b64_16K_256K@64x262144",
-                          "sources_sha256": "7f1a8671298ab06678201ffad395c79bb54caa2e99123835f0c9af03751614d5"}],
+    "decode_scan": [{"bytes_per_launch": 2088358144, "workload": "decode_b64_16K_256K@64x262144",
+                     "sources_sha256": "fdef8822de34f56d0f5805addf2ceab9949d70a6bebb62f0fa937bc425cd58be"}],
+    "decode_scan_e4m3": [{"bytes_per_launch": 1047622656, "workload": "decode_b64_16K_256K@64x262144",
+                          "sources_sha256": "fdef8822de34f56d0f5805addf2ceab9949d70a6bebb62f0fa937bc425cd58be"}],
 }
 # Tensor-pipe activity from the same captures (sm__pipe_tensor_cycles_active, % of elapsed
 # cycles: a fraction of the part's nominal tensor rate at the clock of the moment).

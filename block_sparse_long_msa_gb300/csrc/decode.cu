@@ -516,9 +516,8 @@ __global__ void __launch_bounds__(128) decode_topk_kernel(TopkArgs a) {
 // ------------------------------------------------------------------------------------------
 // Decode attention: one unit per (sequence, group, slot).  A persistent CTA takes a contiguous
 // range of units; warp 0 stages each unit's K and V page tiles (TMA, 128-byte swizzle).  The
-// staged units go in turn to groups of four compute warps (warps 1-4, 5-8, 9-12: three groups
-// with bf16 pages, two with e4m3 pages; DecLayout::kGroups); in a group
-// each warp scores 32 keys (S = q K^T with m16n8k16 MMAs, M = the group's 16 heads), the four
+// staged units go in turn to three groups of four compute warps (warps 1-4, 5-8, 9-12); in a
+// group each warp scores 32 keys (S = q K^T with m16n8k16 MMAs, M = the group's 16 heads), the four
 // exchange row maxima, sums and their slice of P through shared memory, and then each computes
 // O = P V for 32 of the 128 output dimensions over all the page's keys, written straight to the
 // partial.
@@ -545,14 +544,16 @@ struct DecAttnArgs {
 };
 
 // Shared-memory layout of the decode attention kernel, by K/V storage type.
-// kGroups groups of four compute warps take the staged units in turn, so every SM sub-partition
-// has kGroups warps to interleave: three with bf16 pages, two with e4m3 pages (whose warps need
-// 168 registers, so a third group would not fit the register file).
+// Three groups of four compute warps take the staged units in turn, so every SM sub-partition has
+// three warps to interleave (each unit's chain of products, exchanges and barriers is latency-
+// bound; two groups: e4m3 0.0662 -> 0.0621 ms per step with three).  416 threads leave a thread
+// 152 registers: the bf16 instance uses 127, the e4m3 one 128.  Three stages of pages fit beside
+// the e4m3 instance's private fp16 V buffers (12 warps x 8 KiB).
 template <bool kKV8>
 struct DecLayout {
-  static constexpr int kGroups = kKV8 ? 2 : 3;
+  static constexpr int kGroups = 3;
   static constexpr int kThreads = 32 + kGroups * 128;
-  static constexpr int kStages = kKV8 ? 4 : 3;
+  static constexpr int kStages = 3;
   static constexpr uint32_t kTile = kKV8 ? 16384 : 32768;  // one K or V page tile
   static constexpr uint32_t kStage = 2 * kTile;
   // e4m3: per compute warp, V of its 32 dimensions in fp16 (128 rows x 64 B)
@@ -726,11 +727,11 @@ __global__ void __launch_bounds__(DecLayout<kKV8>::kThreads, 1)
       cur_sg = sg;
     }
     const int st = p % kDecStages;
-    // The stage's previous unit (p - kDecStages) may belong to another group (two groups, three
-    // or four stages): wait until it has been released, as the producer does before refilling
-    // it, so that the full barrier is at most one phase ahead of this wait (a group skips the
-    // other groups' units, and a parity test on a barrier two phases behind would pass on the
-    // stale phase).  With three groups and three stages it is this group's own previous unit.
+    // The stage's previous unit (p - kDecStages) is this group's own previous unit when there
+    // are as many stages as groups; with more stages it would belong to another group, whose
+    // release must be waited for (as the producer does before refilling the stage) so that the
+    // full barrier is at most one phase ahead of this wait: a group skips the other groups' units,
+    // and a parity test on a barrier two phases behind would pass on the stale phase.
     bool ok = !*abort_flag &&
               (p < kDecStages ||
                mbar_wait(empty(st), ((p / kDecStages) & 1) ^ 1, a.wait_ns)) &&

@@ -206,10 +206,10 @@ NCU_TRAFFIC = {
                 {"bytes_per_launch": 18936193792, "workload": "prefill_L1M_hot@1048576",
                  "sources_sha256": "91d4a0294468ac4a7479d9901505ceeb2e709ad276433f41e0b9e4dac012cbdb"}],
     # decode, 64 sequences of 16K-256K tokens
-    "decode_scan": [{"bytes_per_launch": 2088358144, "workload": "decode_b64_16K_256K@64x262144",
-                     "sources_sha256": "fdef8822de34f56d0f5805addf2ceab9949d70a6bebb62f0fa937bc425cd58be"}],
-    "decode_scan_e4m3": [{"bytes_per_launch": 1047622656, "workload": "decode_b64_16K_256K@64x262144",
-                          "sources_sha256": "fdef8822de34f56d0f5805addf2ceab9949d70a6bebb62f0fa937bc425cd58be"}],
+    "decode_scan": [{"bytes_per_launch": 2088173056, "workload": "decode_b64_16K_256K@64x262144",
+                     "sources_sha256": "0f603e9e75afd96b62e8e789f25800aae524b40c7454c08370937806f2b45de6"}],
+    "decode_scan_e4m3": [{"bytes_per_launch": 1047312896, "workload": "decode_b64_16K_256K@64x262144",
+                          "sources_sha256": "0f603e9e75afd96b62e8e789f25800aae524b40c7454c08370937806f2b45de6"}],
 }
 # Tensor-pipe activity from the same captures (sm__pipe_tensor_cycles_active, % of elapsed
 # cycles: a fraction of the part's nominal tensor rate at the clock of the moment).

@@ -41,9 +41,9 @@
  *     every page-table entry of a used page in [0, num_pages).  Results are bit-identical to the
  *     release build's when no check fails.
  *   - v1 supports head_dim = index_dim = block_size = 128, 1 <= topk <= 16, num_groups <= 4 for
- *     the index branch, heads_per_group = 16 for the main branch (prefill and decode: a group's
- *     16 query heads are the rows of its tensor-core tiles), prefill lengths up to 1,572,864;
- *     other values return MSA_ERR_UNSUPPORTED.
+ *     the index branch (any number of groups for the main branch), heads_per_group = 16 for the
+ *     main branch (prefill and decode: a group's 16 query heads are the rows of its tensor-core
+ *     tiles), prefill lengths up to 1,572,864; other values return MSA_ERR_UNSUPPORTED.
  */
 #ifndef MSA_H_
 #define MSA_H_

@@ -183,6 +183,32 @@ def test_maximum_length_sampled_rows(msa):
     print(f"[parity {w.name} L={w.L}] {msg}")
 
 
+@pytest.mark.parametrize("L,k", [(700, 5), (1300, 12)])
+def test_more_than_four_groups_with_the_oracle_selection(msa, L, k):
+    """The main branch takes any number of GQA groups (the index branch stops at four): G = 8,
+    128 query heads, fed the oracle's selection; every row against the oracle."""
+    w = synthetic.Workload("g8", "prefill", L=L, Hq=128, G=8, k=k, seed=808 + L)
+    inp = synthetic.prefill_inputs(w)
+    r_sel = oracle.select_prefill(inp["q_idx"], inp["k_idx"], w.B, w.k)
+    cfg = msa.config(w.G, w.hpg, w.k, w.scale)
+    dev = torch.device("cuda")
+    d = {name: t.to(dev) for name, t in inp.items() if isinstance(t, torch.Tensor)}
+    with pytest.raises(msa.MsaError):  # the index branch refuses more than four groups
+        msa.msa_index_select(cfg, d["q_idx"], d["k_idx"])
+    ws = torch.zeros(msa.msa_attn_prefill_workspace(cfg, w.L), dtype=torch.uint8, device=dev)
+    o, lse = msa.msa_attn_prefill(cfg, d["q"], d["k"], d["v"], torch.from_numpy(r_sel).to(dev),
+                                  ws=ws)
+    torch.cuda.synchronize()
+    assert msa.msa_get_device_status(ws) == 0
+    r_o, r_lse = oracle.attn_prefill(inp["q"], inp["k"], inp["v"], r_sel, w.B, w.k, w.scale)
+    got_o, got_lse = o.float().cpu().numpy(), lse.cpu().numpy()
+    err, lerr = np.abs(got_o - r_o), np.abs(got_lse - r_lse)
+    msg = f"O max {err.max():.3g} mean {err.mean():.3g}; LSE max {lerr.max():.3g}"
+    assert (err <= o_bar(r_o)).all() and err.mean() <= MEAN_ABS, msg
+    assert lerr.max() <= MAX_ABS and lerr.mean() <= MEAN_ABS, msg
+    print(f"[parity G=8 L={L} k={k}] {msg}")
+
+
 def _random_shapes(n, seed):
     """n seeded (L, G, k) draws: L in [130, 2600] (ragged tails), G in {1, 2, 4}, k in [1, 16]."""
     Ls = synthetic.uniform_int(seed, 81, n, 130, 2600).tolist()

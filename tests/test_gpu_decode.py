@@ -109,6 +109,28 @@ def test_group_and_k_variants(msa, G, k):
     check(w, inp, gpu_decode(msa, w, inp))
 
 
+def test_more_than_four_groups_with_the_oracle_selection(msa):
+    """Decode attention takes any number of GQA groups (the index branch stops at four): G = 8,
+    128 query heads, fed the oracle's selection; every sequence against the oracle."""
+    w, inp = _custom([1, 129, 700, 3000, 5000], seed=31, G=8, k=6)
+    r_sel, _, r_o, r_lse = oracle_decode(w, inp)
+    dev = torch.device("cuda")
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    cfg = msa.config(w.G, w.hpg, w.k, w.scale)
+    paged = msa.paged_kv(d["k_idx_pool"], d["k_pool"], d["v_pool"], d["page_table"],
+                         d["seq_lens"])
+    ws = torch.zeros(msa.msa_attn_decode_workspace(cfg, paged), dtype=torch.uint8, device=dev)
+    with pytest.raises(msa.MsaError):  # the index branch refuses more than four groups
+        msa.msa_index_select(cfg, d["q_idx"], paged=paged, ws=ws)
+    o, lse = msa.msa_attn_decode(cfg, d["q"], paged, torch.from_numpy(r_sel).to(dev), ws=ws)
+    torch.cuda.synchronize()
+    assert msa.msa_get_device_status(ws) == 0
+    got_o, got_lse = o.float().cpu().numpy(), lse.cpu().numpy()
+    err, lerr = np.abs(got_o - r_o), np.abs(got_lse - r_lse)
+    assert (err <= o_bar(r_o)).all() and err.mean() <= MEAN_ABS, err.max()
+    assert lerr.max() <= MAX_ABS and lerr.mean() <= MEAN_ABS, lerr.max()
+
+
 def test_mid_size_batch(msa):
     w, inp = _custom([16384, 20000, 40000, 65536, 17000, 33333, 50001, 16385], seed=12)
     check(w, inp, gpu_decode(msa, w, inp))
